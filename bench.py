@@ -1,0 +1,370 @@
+"""Benchmark of the sparse-attention decode step (metadata -> indexer logits ->
+top-k + slot transform -> sparse MLA) on the DeepSeek-V3.2-shaped bf16-KV
+decode workload: 32 requests, seqlens U{4096..32768}, page 64, indexer
+64 heads x 128 e4m3, topk 2048, MLA 128 heads d_qk 576 / d_v 512.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs an independent
+replica of the workload on its own GPU (replicas only: the path has no
+exchange step) and `value` is all ranks' rows / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "sparse-MLA decode tokens/s + indexer/top-k µs per step; % of HBM/TC roofline"
+WORKLOAD = "v32_decode_bf16"
+WORKLOAD_DESC = ("DeepSeek-V3.2-shaped decode, bf16 KV: batch 32, seqlens U{4096..32768}, page 64 in random "
+                 "order, indexer 64x128 e4m3 + fp32 row scale, weights N(0,1)/8, topk 2048, MLA 128 heads "
+                 "d_qk 576 (512+64) d_v 512 bf16, sm_scale 192^-0.5")
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ---------------------------------------------------------------- algorithmic work per stage
+
+def algorithmic_work(wl, seqlens_expanded: np.ndarray):
+    """Bytes each stage must move and flops it must do, from the shapes alone."""
+    L = seqlens_expanded.astype(np.int64)
+    Lsum = int(L.sum())
+    nsel = np.minimum(L, wl.topk)
+    ps = wl.page_size
+    idx_elem = 1 if wl.idx_dtype == W.DT_E4M3 else 4
+    row_bytes = wl.kv_row_bytes
+    qb = 2 if wl.q_dtype == W.DT_BF16 else 4
+    dq = wl.d_latent + wl.d_rope
+    w = {}
+    w["metadata"] = dict(bytes=wl.B * wl.W * 4 * 2 + wl.B * ((wl.W + ps - 1) // ps) * 4 + 40 * (wl.B + wl.R), flops=0)
+    w["indexer"] = dict(bytes=Lsum * (wl.Di * idx_elem + 4 + 4) + wl.R * wl.Hi * (wl.Di * idx_elem + 4)
+                        + int(((L + ps - 1) // ps).sum()) * 4, flops=2 * wl.Hi * wl.Di * Lsum)
+    w["topk"] = dict(bytes=Lsum * 4 + wl.R * wl.topk * 4 + int(nsel.sum()) * 4, flops=0)
+    w["sparse_mla"] = dict(bytes=int(nsel.sum()) * row_bytes + wl.R * wl.H * (dq + wl.d_latent) * qb
+                           + wl.R * wl.H * 4 + wl.R * wl.topk * 4,
+                           flops=2 * wl.H * int(nsel.sum()) * (dq + wl.d_latent))
+    return w
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock / throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"], samples=0)
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(mx) if mx else None,
+                    reasons=sorted(reasons), samples=len(sm))
+
+
+# ---------------------------------------------------------------- replicas
+
+def replica_seed(rank: int) -> int:
+    """Each rank draws an independent batch of the same workload."""
+    return 2 + 1000 * rank
+
+
+def max_over_ranks(values, world: int):
+    """Element-wise max of per-rank timings (the slowest rank sets the pace)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def replica_throughput(rows_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Rows of all ranks per second of the slowest rank's step."""
+    return rows_per_rank * world / (ms_per_step * 1e-3)
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import deepseek_sparse_mla_indexer_gb300 as nsa
+    from deepseek_sparse_mla_indexer_gb300.step import SparseAttentionStep
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    nsa.load()
+    wl = W.config(WORKLOAD, seed=replica_seed(rank))  # an independent replica per rank
+    step = SparseAttentionStep(wl, dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    stages = ["metadata", "indexer", "topk", "sparse_mla"]
+    calls = [step.metadata, step.indexer, step.topk_transform, step.attention]
+
+    def one_step(evs=None):
+        for i, fn in enumerate(calls):
+            if evs is not None:
+                evs[i].record(stream)
+            fn(stream)
+        if evs is not None:
+            evs[len(calls)].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        one_step()
+    torch.cuda.synchronize(dev)
+    if step.status_code() != 0:
+        raise RuntimeError(f"device status {step.status_code()} after warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    for k in range(args.steps):
+        flush.zero_()  # L2 flush between steps, outside the timed events
+        one_step(ev[k])
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+
+    per_stage = {s: [] for s in stages}
+    totals = []
+    for k in range(args.steps):
+        for i, s in enumerate(stages):
+            per_stage[s].append(ev[k][i].elapsed_time(ev[k][i + 1]))
+        totals.append(ev[k][0].elapsed_time(ev[k][len(calls)]))
+    ms_step = float(np.mean(totals))
+
+    # end to end through the public API with host buffers: per step the
+    # per-request inputs go host->device from pinned memory, the outputs come back.
+    h_in = {k: torch.from_numpy(np.ascontiguousarray(getattr(wl, k))).pin_memory()
+            for k in ["seq_lens", "req_pool_indices", "q_idx", "weights"]}
+    h_q = {"q_nope": torch.from_numpy(wl.q_nope.view(np.int16)).pin_memory(),
+           "q_rope": torch.from_numpy(wl.q_rope.view(np.int16)).pin_memory()}
+    h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h_lse = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in list(h_in.values()) + list(h_q.values()))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * 4
+
+    def e2e_step():
+        step.seq_lens.copy_(h_in["seq_lens"], non_blocking=True)
+        step.req_pool_indices.copy_(h_in["req_pool_indices"], non_blocking=True)
+        step.q_idx.copy_(h_in["q_idx"], non_blocking=True)
+        step.weights.copy_(h_in["weights"], non_blocking=True)
+        step.q_nope.view(torch.int16).copy_(h_q["q_nope"], non_blocking=True)
+        step.q_rope.view(torch.int16).copy_(h_q["q_rope"], non_blocking=True)
+        one_step()
+        h_out.copy_(step.out, non_blocking=True)
+        h_lse.copy_(step.lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.zero_()
+        e2e_ev[k][0].record(stream)
+        e2e_step()
+        e2e_ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e2e_ev]))
+    if step.status_code() != 0:
+        raise RuntimeError(f"device status {step.status_code()} after the timed steps")
+
+    ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], world)
+
+    md_len = step.md["seqlens_expanded"].cpu().numpy()
+    work = algorithmic_work(wl, md_len)
+    peaks = load_peaks()
+    stage_ms = {s: float(np.mean(v)) for s, v in per_stage.items()}
+    stage_info = {}
+    for s in stages:
+        sec = stage_ms[s] * 1e-3
+        gbs = work[s]["bytes"] / sec / 1e9
+        tfl = work[s]["flops"] / sec / 1e12
+        stage_info[s] = dict(us=round(stage_ms[s] * 1e3, 2), gbs=round(gbs, 1), tflops=round(tfl, 2),
+                             hbm_frac=round(gbs / peaks["hbm_gbs"], 4))
+    dom = max(stages, key=lambda s: stage_ms[s])
+    dom_sec = stage_ms[dom] * 1e-3
+    achieved = work[dom]["bytes"] / dom_sec / 1e9
+    roof = dict(kernel=dom, bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
+                frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None,
+                algorithmic_bytes=work[dom]["bytes"], peak_source=peaks["source"])
+
+    rows_total = wl.R * world
+    line = dict(metric=METRIC, value=round(replica_throughput(wl.R, world, ms_step), 1), unit="tokens/s", n_gpus=world,
+                steps=args.steps, warmup=args.warmup, ms_per_step=round(ms_step, 5), higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="bf16+e4m3 (f32 accumulate)",
+                data="synthetic (seeded; random pages; see workloads/)",
+                config=dict(workload=WORKLOAD_DESC, global_batch=rows_total,
+                            seq_len=int(np.mean(wl.seq_lens)), parallelism=f"replicas x{world}",
+                            l2="flushed between steps (512 MB write outside the timed events)"),
+                stages=stage_info, roofline=roof,
+                e2e=dict(value=round(rows_total / (e2e_ms * 1e-3), 1), unit="tokens/s",
+                         h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
+                         note="per-request inputs host->device and out+lse device->host each step; "
+                              "KV / indexer-K caches and the req_to_token pool stay resident"),
+                gpu_launches=len(calls) * args.steps,
+                clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"]))
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows)
+    return line
+
+
+# ---------------------------------------------------------------- CPU baseline (the oracle)
+
+def oracle_rows_time(wl, rows):
+    """Seconds for the oracle to run metadata (whole batch) plus indexer,
+    top-k and sparse MLA for the given rows."""
+    import oracle
+    t0 = time.perf_counter()
+    md = oracle.metadata(wl.mode, wl.seq_lens, wl.req_to_token, wl.req_pool_indices, W=wl.W, topk=wl.topk,
+                         page_size=wl.page_size, extend_lens=wl.extend_lens, n_draft=wl.n_draft)
+    t_md = time.perf_counter() - t0
+    t1 = time.perf_counter()
+    lg = oracle.indexer_logits(wl.idx_dtype, wl.q_idx, wl.weights, wl.k_cache, wl.k_scale, md["real_page_table"],
+                               md["row_to_req"], md["seqlens_expanded"], rows=rows, width=wl.W)
+    idx = oracle.topk_transform(lg, md["seqlens_expanded"], md["row_to_req"], md["page_table_1"], wl.topk,
+                                rows=rows, logits_rows_are_subset=True)
+    oracle.sparse_mla(wl.q_dtype, wl.kv_dtype, wl.q_nope, wl.q_rope, wl.kv, idx, wl.sm_scale, rows=rows,
+                      indices_rows_are_subset=True)
+    t_rows = time.perf_counter() - t1
+    return t_md, t_rows
+
+
+def cpu_baseline(wl, nrows):
+    rows = list(range(min(nrows, wl.R)))
+    t_md, t_rows = oracle_rows_time(wl, rows)
+    # whole-step time extrapolated from the sampled rows; metadata timed in full
+    per_row = t_rows / len(rows)
+    step_s = t_md + per_row * wl.R
+    return dict(value=round(wl.R / step_s, 3), unit="tokens/s", cores=1, kind="oracle",
+                sample=f"metadata for all {wl.B} requests + indexer/top-k/sparse MLA for rows {rows[0]}..{rows[-1]} "
+                       f"({len(rows)} of {wl.R}); per-row time scaled to the full step; single-threaded C, fp64")
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    wl = W.config(WORKLOAD, seed=2)
+    rows_per_step = 1
+    for k in range(args.warmup):
+        oracle_rows_time(wl, [k % wl.R])
+    t = []
+    for k in range(args.steps):
+        t_md, t_rows = oracle_rows_time(wl, [(args.warmup + k) % wl.R])
+        t.append(t_md + t_rows)
+    s = float(np.mean(t))
+    v = round(rows_per_step / s, 4)
+    sample = (f"each step: oracle metadata for the whole batch + indexer/top-k/sparse MLA for 1 of {wl.R} rows "
+              "(single-threaded C, fp64)")
+    return dict(impl="reference", metric=METRIC, value=v, unit="tokens/s", n_gpus=world, steps=args.steps,
+                warmup=args.warmup, ms_per_step=round(s * 1e3, 3), higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype="f64", data="synthetic (seeded; random pages; see workloads/)",
+                config=dict(workload=WORKLOAD_DESC, global_batch=wl.R, seq_len=int(np.mean(wl.seq_lens)),
+                            parallelism="oracle on rank 0"),
+                cpu_baseline=dict(value=v, unit="tokens/s", cores=1, kind="oracle", sample=sample),
+                e2e=dict(value=v, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,231 @@
+"""Python binding of the sparse-attention C ABI (include/nsa.h).
+
+Argument marshalling only: every computation runs in libnsa.so's CUDA
+kernels (the local virtual-batch builder runs in its host C++).  Device
+buffers are torch CUDA tensors; work is enqueued on the current torch stream
+unless `stream` is given.  There is no CPU fallback: if the library cannot be
+loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+
+from . import _build
+
+__all__ = [
+    "NsaError", "load", "MODE_DECODE", "MODE_EXTEND", "MODE_TARGET_VERIFY", "DT_F32", "DT_BF16",
+    "DT_E4M3", "nsa_metadata", "alloc_metadata", "nsa_local_virtual_batches", "nsa_effective_chunk_size",
+    "nsa_indexer_logits", "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes",
+    "nsa_status_read", "nsa_status_string", "nsa_abi_version", "EXPORTED_SYMBOLS",
+]
+
+MODE_DECODE, MODE_EXTEND, MODE_TARGET_VERIFY = 0, 1, 2
+DT_F32, DT_BF16, DT_E4M3 = 0, 1, 2
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_BOUNDS, ERR_TIMEOUT = range(6)
+
+EXPORTED_SYMBOLS = [
+    "nsa_status_string", "nsa_abi_version", "nsa_status_read", "nsa_metadata",
+    "nsa_effective_chunk_size", "nsa_local_virtual_batches", "nsa_indexer_logits",
+    "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes",
+]
+
+_lib = None
+
+
+class NsaError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {nsa_status_string(code)} ({code})")
+
+
+def load(build_if_missing: bool = True):
+    """Load libnsa.so (building it with nvcc when missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing:
+        path = _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libnsa.so is missing ({path}); run __graft_entry__.build()")
+    lib = C.CDLL(path)
+    P, I, L, F, S = C.c_void_p, C.c_int, C.c_int64, C.c_float, C.c_size_t
+    sig = {
+        "nsa_status_string": ([I], C.c_char_p),
+        "nsa_abi_version": ([], I),
+        "nsa_status_read": ([P, P, P], I),
+        "nsa_metadata": ([I, I, I, I, I, I, I, P, P, P, L, L, P, P, P, P], I),
+        "nsa_effective_chunk_size": ([I, I, I], I),
+        "nsa_local_virtual_batches": ([I, I, I, P, P, P, L, L, I, P, P, P, P, P, P], I),
+        "nsa_indexer_logits": ([I, P, P, P, P, L, I, I, I, P, L, P, P, I, I, P, L, P, P], I),
+        "nsa_topk_transform": ([P, L, P, P, P, L, I, I, I, P, L, P, P], I),
+        "nsa_sparse_mla": ([I, I, P, L, L, P, L, L, P, L, P, L, I, I, I, I, I, F, P, P, P, S, P, P], I),
+        "nsa_sparse_mla_workspace_bytes": ([I, I, I, I, I, I, I], S),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes, fn.restype = args, res
+    _lib = lib
+    return lib
+
+
+class _MetadataOut(C.Structure):
+    _fields_ = [("cache_seqlens", C.c_void_p), ("cu_seqlens_k", C.c_void_p), ("cu_seqlens_q", C.c_void_p),
+                ("seqlens_expanded", C.c_void_p), ("nsa_cache_seqlens", C.c_void_p),
+                ("nsa_cu_seqlens_k", C.c_void_p), ("nsa_cu_seqlens_q", C.c_void_p),
+                ("row_to_req", C.c_void_p), ("page_table_1", C.c_void_p), ("page_table_1_ld", C.c_int64),
+                ("real_page_table", C.c_void_p), ("real_page_table_ld", C.c_int64),
+                ("indexer_ks", C.c_void_p), ("indexer_ke", C.c_void_p)]
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(fn: str, code: int):
+    if code != OK:
+        raise NsaError(fn, code)
+
+
+def nsa_status_string(code: int) -> str:
+    return load().nsa_status_string(code).decode()
+
+
+def nsa_abi_version() -> int:
+    return load().nsa_abi_version()
+
+
+def nsa_status_read(status: torch.Tensor, stream=None) -> int:
+    """Synchronize `stream` and return the device status word."""
+    v = C.c_int32(0)
+    _check("nsa_status_read", load().nsa_status_read(_ptr(status), C.byref(v), _stream(stream)))
+    return int(v.value)
+
+
+# ------------------------------------------------------------------ metadata
+
+def alloc_metadata(mode: int, B: int, R: int, W: int, page_size: int, device="cuda",
+                   with_ks_ke: bool = False) -> Dict[str, torch.Tensor]:
+    """Device buffers for nsa_metadata's outputs."""
+    i32 = dict(dtype=torch.int32, device=device)
+    nq = R + 1 if mode == MODE_TARGET_VERIFY else B + 1
+    npg = (W + page_size - 1) // page_size
+    out = dict(cache_seqlens=torch.empty(B, **i32), cu_seqlens_k=torch.empty(B + 1, **i32),
+               cu_seqlens_q=torch.empty(nq, **i32), seqlens_expanded=torch.empty(R, **i32),
+               nsa_cache_seqlens=torch.empty(R, **i32), nsa_cu_seqlens_k=torch.empty(R + 1, **i32),
+               nsa_cu_seqlens_q=torch.empty(R + 1, **i32), row_to_req=torch.empty(R, **i32),
+               page_table_1=torch.empty((B, max(W, 1)), **i32),
+               real_page_table=torch.empty((B, max(npg, 1)), **i32))
+    if with_ks_ke:
+        out["indexer_ks"] = torch.empty(R, **i32)
+        out["indexer_ke"] = torch.empty(R, **i32)
+    return out
+
+
+def nsa_metadata(mode: int, B: int, R: int, W: int, n_draft: int, topk: int, page_size: int,
+                 seq_lens: torch.Tensor, extend_lens: Optional[torch.Tensor], req_to_token: torch.Tensor,
+                 req_pool_indices: torch.Tensor, out: Dict[str, torch.Tensor],
+                 status: Optional[torch.Tensor] = None, stream=None) -> None:
+    o = _MetadataOut(*(_ptr(out[k]) for k in ["cache_seqlens", "cu_seqlens_k", "cu_seqlens_q",
+                                              "seqlens_expanded", "nsa_cache_seqlens", "nsa_cu_seqlens_k",
+                                              "nsa_cu_seqlens_q", "row_to_req", "page_table_1"]),
+                     out["page_table_1"].stride(0), _ptr(out["real_page_table"]),
+                     out["real_page_table"].stride(0), _ptr(out.get("indexer_ks")), _ptr(out.get("indexer_ke")))
+    rc = load().nsa_metadata(mode, B, R, W, n_draft, topk, page_size, _ptr(seq_lens), _ptr(extend_lens),
+                             _ptr(req_to_token), req_to_token.stride(0), req_to_token.shape[0],
+                             _ptr(req_pool_indices), C.byref(o), _ptr(status), _stream(stream))
+    _check("nsa_metadata", rc)
+
+
+# ------------------------------------------------------------------ local attention (host)
+
+def nsa_effective_chunk_size(attn_chunk_size: int, max_seq_len: int, page_size: int) -> int:
+    v = load().nsa_effective_chunk_size(attn_chunk_size, max_seq_len, page_size)
+    if v < 0:
+        raise NsaError("nsa_effective_chunk_size", ERR_INVALID_ARG)
+    return v
+
+
+def nsa_local_virtual_batches(attn_chunk_size: int, page_size: int, cu_seqlens_q, seq_lens, block_table):
+    """Host call.  Returns numpy arrays (seqlens_q_local, cu_seqlens_q_local,
+    seqlens_k_local, k_seqstarts_absolute, block_table_local)."""
+    lib = load()
+    cq = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    B = len(sl)
+    n = C.c_int(0)
+    P = lambda a: a.ctypes.data_as(C.c_void_p)
+    _check("nsa_local_virtual_batches",
+           lib.nsa_local_virtual_batches(attn_chunk_size, page_size, B, P(cq), P(sl), P(bt), bt.shape[1],
+                                         bt.shape[1], 0, C.byref(n), None, None, None, None, None))
+    V, ppl = n.value, attn_chunk_size // page_size
+    sq, cu, sk = np.zeros(V, np.int32), np.zeros(V + 1, np.int32), np.zeros(V, np.int32)
+    st, btl = np.zeros(V, np.int32), np.zeros((V, ppl), np.int32)
+    _check("nsa_local_virtual_batches",
+           lib.nsa_local_virtual_batches(attn_chunk_size, page_size, B, P(cq), P(sl), P(bt), bt.shape[1],
+                                         bt.shape[1], V, C.byref(n), P(sq), P(cu), P(sk), P(st), P(btl)))
+    return sq, cu, sk, st, btl
+
+
+# ------------------------------------------------------------------ indexer / top-k / attention
+
+def nsa_indexer_logits(dtype: int, q_idx: torch.Tensor, weights: torch.Tensor, k_cache: torch.Tensor,
+                       k_scale: torch.Tensor, real_page_table: torch.Tensor, row_to_req: torch.Tensor,
+                       row_len: torch.Tensor, max_row_len: int, logits: torch.Tensor,
+                       status: Optional[torch.Tensor] = None, stream=None) -> None:
+    R, Hi, Di = q_idx.shape
+    num_pages, ps = k_cache.shape[0], k_cache.shape[1]
+    assert q_idx.is_contiguous() and k_cache.is_contiguous() and weights.is_contiguous() and k_scale.is_contiguous()
+    rc = load().nsa_indexer_logits(dtype, _ptr(q_idx), _ptr(weights), _ptr(k_cache), _ptr(k_scale), num_pages,
+                                   ps, Hi, Di, _ptr(real_page_table), real_page_table.stride(0),
+                                   _ptr(row_to_req), _ptr(row_len), R, max_row_len, _ptr(logits),
+                                   logits.stride(0), _ptr(status), _stream(stream))
+    _check("nsa_indexer_logits", rc)
+
+
+def nsa_topk_transform(logits: torch.Tensor, row_len: torch.Tensor, row_to_req: torch.Tensor,
+                       page_table_1: torch.Tensor, topk: int, max_row_len: int, indices: torch.Tensor,
+                       status: Optional[torch.Tensor] = None, stream=None) -> None:
+    R = row_len.shape[0]
+    rc = load().nsa_topk_transform(_ptr(logits), logits.stride(0), _ptr(row_len), _ptr(row_to_req),
+                                   _ptr(page_table_1), page_table_1.stride(0), R, topk, max_row_len,
+                                   _ptr(indices), indices.stride(0), _ptr(status), _stream(stream))
+    _check("nsa_topk_transform", rc)
+
+
+def nsa_sparse_mla_workspace_bytes(q_dtype: int, kv_dtype: int, R: int, H: int, d_latent: int, d_rope: int,
+                                   topk: int) -> int:
+    return int(load().nsa_sparse_mla_workspace_bytes(q_dtype, kv_dtype, R, H, d_latent, d_rope, topk))
+
+
+def nsa_sparse_mla(q_dtype: int, kv_dtype: int, q_nope: torch.Tensor, q_rope: torch.Tensor, kv: torch.Tensor,
+                   indices: torch.Tensor, sm_scale: float, out: torch.Tensor, lse: torch.Tensor,
+                   workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                   stream=None, num_slots: Optional[int] = None) -> None:
+    """q_nope [R,H,d_latent] and q_rope [R,H,d_rope] (any row / head strides,
+    unit stride in the last dim); kv [slots, row]; indices [R, topk]."""
+    R, H, d_latent = q_nope.shape
+    d_rope = q_rope.shape[2]
+    topk = indices.shape[1]
+    assert q_nope.stride(2) == 1 and q_rope.stride(2) == 1 and out.is_contiguous() and lse.is_contiguous()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().nsa_sparse_mla(q_dtype, kv_dtype, _ptr(q_nope), q_nope.stride(0), q_nope.stride(1), _ptr(q_rope),
+                               q_rope.stride(0), q_rope.stride(1), _ptr(kv),
+                               kv.shape[0] if num_slots is None else num_slots, _ptr(indices),
+                               indices.stride(0), R, H, d_latent, d_rope, topk, float(sm_scale), _ptr(out),
+                               _ptr(lse), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
+    _check("nsa_sparse_mla", rc)

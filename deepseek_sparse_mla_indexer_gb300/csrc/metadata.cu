@@ -1,0 +1,183 @@
+// nsa_metadata: the per-step metadata of the sparse-attention backend in one
+// launch.  Block 0 builds every length / offset array (they are O(B + R)
+// and need block-wide prefix sums); the other blocks copy the page table
+// rows out of req_to_token and derive the page-granular table on the fly.
+//
+// Follows [DSA] DeepseekSparseAttnBackend.init_forward_metadata (decode,
+// target-verify and extend branches), _cal_indexer_k_start_end and
+// compute_cu_seqlens; [NSA-diff] the target-verify branch.
+#include "nsa_internal.cuh"
+
+namespace nsa {
+namespace {
+
+constexpr int kRowThreads = 1024;
+
+struct MetaParams {
+    int mode, B, R, W, n_draft, topk, ps;
+    const int32_t *seq_lens, *extend_lens, *r2t, *rpi;
+    int64_t r2t_ld, pool_rows;
+    nsa_metadata_out out;
+    int32_t *status;
+};
+
+// out[0] = 0, out[i + 1] = f(0) + ... + f(i) for i < n, with the whole block.
+template <class F>
+__device__ void block_cumsum_pad(int n, F f, int32_t *out)
+{
+    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t carry;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    if (threadIdx.x == 0) { carry = 0; out[0] = 0; }
+    __syncthreads();
+    for (int base = 0; base < n; base += blockDim.x) {
+        int i = base + threadIdx.x;
+        int x = i < n ? f(i) : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_tot[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int w = lane < nwarps ? warp_tot[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            warp_tot[lane] = w;
+        }
+        __syncthreads();
+        int incl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x;
+        if (i < n) out[i + 1] = incl;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = incl;
+        __syncthreads();
+    }
+}
+
+__device__ void build_rows(const MetaParams &p)
+{
+    const nsa_metadata_out &o = p.out;
+    const int draft = p.mode == NSA_MODE_TARGET_VERIFY ? p.n_draft : 0;
+
+    // cache_seqlens and cu_seqlens_k
+    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+        int c = p.seq_lens[b] + draft;
+        if (c < 0 || c > p.W) set_status(p.status, NSA_ERR_BOUNDS);
+        o.cache_seqlens[b] = c;
+    }
+    block_cumsum_pad(p.B, [&](int b) { return p.seq_lens[b] + draft; }, o.cu_seqlens_k);
+
+    // cu_seqlens_q
+    if (p.mode == NSA_MODE_EXTEND) {
+        block_cumsum_pad(p.B, [&](int b) { return p.extend_lens[b]; }, o.cu_seqlens_q);
+    } else {
+        const int n = p.mode == NSA_MODE_DECODE ? p.B : p.R;
+        for (int i = threadIdx.x; i <= n; i += blockDim.x) o.cu_seqlens_q[i] = i;
+    }
+    __syncthreads();
+
+    // per-row arrays
+    for (int r = threadIdx.x; r < p.R; r += blockDim.x) {
+        int b, q, i;
+        if (p.mode == NSA_MODE_DECODE) {
+            b = r; q = 1; i = 0;
+        } else if (p.mode == NSA_MODE_TARGET_VERIFY) {
+            b = r / p.n_draft; q = p.n_draft; i = r - b * p.n_draft;
+        } else {
+            int lo = 0, hi = p.B - 1;  // largest b with cu_seqlens_q[b] <= r
+            while (lo < hi) {
+                int mid = (lo + hi + 1) >> 1;
+                if (o.cu_seqlens_q[mid] <= r) lo = mid; else hi = mid - 1;
+            }
+            b = lo; q = p.extend_lens[b]; i = r - o.cu_seqlens_q[b];
+            if (i >= q) set_status(p.status, NSA_ERR_BOUNDS);  // R exceeds sum(extend_lens)
+        }
+        const int L = p.seq_lens[b] + draft - q + 1 + i;  // arange(kv - q + 1, kv + 1)[i]
+        o.seqlens_expanded[r] = L;
+        o.nsa_cache_seqlens[r] = L < p.topk ? L : p.topk;
+        o.row_to_req[r] = b;
+        if (p.mode == NSA_MODE_EXTEND && o.indexer_ks) {
+            const int ks = o.cu_seqlens_k[b];
+            o.indexer_ks[r] = ks;
+            o.indexer_ke[r] = ks + L;
+        }
+    }
+    __syncthreads();
+    block_cumsum_pad(p.R, [&](int r) { return o.nsa_cache_seqlens[r]; }, o.nsa_cu_seqlens_k);
+    for (int i = threadIdx.x; i <= p.R; i += blockDim.x) o.nsa_cu_seqlens_q[i] = i;
+}
+
+__device__ void copy_tables(const MetaParams &p, int64_t first, int64_t stride)
+{
+    const nsa_metadata_out &o = p.out;
+    const int64_t total = (int64_t)p.B * p.W;
+    for (int64_t e = first; e < total; e += stride) {
+        const int b = (int)(e / p.W);
+        const int t = (int)(e - (int64_t)b * p.W);
+        const int32_t row = p.rpi[b];
+        if (row < 0 || row >= p.pool_rows) {
+            if (t == 0) set_status(p.status, NSA_ERR_BOUNDS);
+            continue;
+        }
+        const int32_t v = p.r2t[(int64_t)row * p.r2t_ld + t];
+        o.page_table_1[(int64_t)b * o.page_table_1_ld + t] = v;
+        if (t % p.ps == 0) o.real_page_table[(int64_t)b * o.real_page_table_ld + t / p.ps] = floor_div(v, p.ps);
+    }
+}
+
+__global__ void __launch_bounds__(kRowThreads) metadata_kernel(MetaParams p)
+{
+    if (blockIdx.x == 0) {
+        build_rows(p);
+    } else {
+        copy_tables(p, (int64_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x,
+                    (int64_t)(gridDim.x - 1) * blockDim.x);
+    }
+}
+
+}  // namespace
+}  // namespace nsa
+
+extern "C" nsa_status nsa_metadata(nsa_mode mode, int B, int R, int W, int n_draft, int topk,
+                                   int page_size, const int32_t *seq_lens_dev,
+                                   const int32_t *extend_lens_dev, const int32_t *req_to_token_dev,
+                                   int64_t req_to_token_ld, int64_t pool_rows,
+                                   const int32_t *req_pool_indices_dev, const nsa_metadata_out *out,
+                                   int32_t *status_dev, nsa_stream_t stream)
+{
+    using namespace nsa;
+    if (!out || B < 0 || R < 0 || W < 0 || topk < 1 || page_size < 1) return NSA_ERR_INVALID_ARG;
+    if (mode != NSA_MODE_DECODE && mode != NSA_MODE_EXTEND && mode != NSA_MODE_TARGET_VERIFY)
+        return NSA_ERR_INVALID_ARG;
+    if (mode == NSA_MODE_DECODE && R != B) return NSA_ERR_INVALID_ARG;
+    if (mode == NSA_MODE_TARGET_VERIFY && (n_draft < 1 || (int64_t)R != (int64_t)B * n_draft))
+        return NSA_ERR_INVALID_ARG;
+    if (mode == NSA_MODE_EXTEND && B > 0 && !extend_lens_dev) return NSA_ERR_INVALID_ARG;
+    if (mode == NSA_MODE_EXTEND && B == 0 && R != 0) return NSA_ERR_INVALID_ARG;
+    if (B > 0 && (!seq_lens_dev || !req_to_token_dev || !req_pool_indices_dev)) return NSA_ERR_INVALID_ARG;
+    if (B > 0 && (req_to_token_ld < W || pool_rows < 1)) return NSA_ERR_INVALID_ARG;
+    if (!out->cache_seqlens || !out->cu_seqlens_k || !out->cu_seqlens_q || !out->seqlens_expanded ||
+        !out->nsa_cache_seqlens || !out->nsa_cu_seqlens_k || !out->nsa_cu_seqlens_q ||
+        !out->row_to_req || !out->page_table_1 || !out->real_page_table)
+        return NSA_ERR_INVALID_ARG;
+    if (out->page_table_1_ld < W || out->real_page_table_ld < ceil_div(W, page_size))
+        return NSA_ERR_INVALID_ARG;
+    if ((out->indexer_ks == nullptr) != (out->indexer_ke == nullptr)) return NSA_ERR_INVALID_ARG;
+
+    MetaParams p;
+    p.mode = mode; p.B = B; p.R = R; p.W = W; p.n_draft = n_draft; p.topk = topk; p.ps = page_size;
+    p.seq_lens = seq_lens_dev; p.extend_lens = extend_lens_dev; p.r2t = req_to_token_dev;
+    p.rpi = req_pool_indices_dev; p.r2t_ld = req_to_token_ld; p.pool_rows = pool_rows;
+    p.out = *out; p.status = status_dev;
+
+    const int64_t total = (int64_t)B * W;
+    int64_t copy_blocks = ceil_div(total, (int64_t)kRowThreads * 4);
+    if (copy_blocks > 152 * 8) copy_blocks = 152 * 8;
+    if (copy_blocks < 1) copy_blocks = 1;
+    metadata_kernel<<<(unsigned)(1 + copy_blocks), kRowThreads, 0, (cudaStream_t)stream>>>(p);
+    return launch_status();
+}

@@ -1,0 +1,51 @@
+// Internal helpers shared by the CUDA sources of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "../../include/nsa.h"
+
+#define NSA_CUDA_TRY(expr)                                   \
+    do {                                                     \
+        cudaError_t _e = (expr);                             \
+        if (_e != cudaSuccess) return NSA_ERR_CUDA;          \
+    } while (0)
+
+namespace nsa {
+
+// Record the first device-side error in the caller's status word (if any).
+__device__ __forceinline__ void set_status(int32_t *status, int32_t code)
+{
+    if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint8_t b)
+{
+    __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3);
+    return __half2float(__half(h));
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b)
+{
+    return __uint_as_float(((uint32_t)b) << 16);
+}
+
+__host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Python floor division for the page-table transform (ids are non-negative
+// in practice; negative ids keep the pages' `//` meaning).
+__device__ __forceinline__ int32_t floor_div(int32_t a, int32_t b)
+{
+    int32_t q = a / b, r = a % b;
+    return (r != 0 && ((r < 0) != (b < 0))) ? q - 1 : q;
+}
+
+inline nsa_status launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
+}
+
+}  // namespace nsa

@@ -1,0 +1,289 @@
+/*
+ * nsa.h -- C ABI of the DeepSeek sparse-attention (NSA / DSA) decode and
+ * extend hot path on one GPU:
+ *
+ *   nsa_metadata        per-step sequence-length and page-table metadata
+ *   nsa_local_virtual_batches   chunk-local attention virtual batches (host)
+ *   nsa_indexer_logits  lightning-indexer scores  sum_h w * ReLU(q . k)
+ *   nsa_topk_transform  per-row top-k of the scores, mapped to KV slots
+ *   nsa_sparse_mla      MLA attention over only the selected KV rows
+ *
+ * Sources, cited by page title and the function shown on the page:
+ *   [NSA-diff] "sglang 0.5.3rc2 -> 0.5.4 diff: sglang/srt/layers/attention/nsa_backend.py"
+ *   [FA3-diff] "sglang 0.4.4.post3 -> 0.4.5 diff: sglang/srt/layers/attention/flashattention_backend.py"
+ *   [NSA]      "sglang/python/sglang/srt/layers/attention/nsa_backend.py"
+ *   [DSA]      "sgl-project--sglang/python/sglang/srt/layers/attention/dsa_backend.py"
+ *
+ * General rules
+ *  - Ownership: the caller allocates every buffer.  The library never
+ *    allocates device or host memory, keeps no state between calls and holds
+ *    no pointer after a call returns.
+ *  - Pointers named *_dev (or documented "device") are device pointers; all
+ *    work is enqueued asynchronously on `stream` (NULL = the legacy default
+ *    stream).  Host pointers are read before the call returns.
+ *  - Errors: arguments are validated on the host before any launch; a bad
+ *    argument returns NSA_ERR_INVALID_ARG / NSA_ERR_UNSUPPORTED and nothing is
+ *    launched.  A failed launch returns NSA_ERR_CUDA.  Problems that only the
+ *    device can see (a page id or slot outside the cache, a length beyond the
+ *    table) are recorded in the optional device status word `status_dev`
+ *    (int32, caller-zeroed; the first error code written wins) and the
+ *    offending element is skipped -- kernels never trap.  Read it with
+ *    nsa_status_read() when convenient.
+ *  - Integers are int32 unless stated; leading dimensions (`*_ld`) count
+ *    elements, not bytes.
+ *  - -1 is the "no index" sentinel in index rows ([DSA] _pad_topk_indices).
+ */
+#ifndef NSA_H
+#define NSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *nsa_stream_t; /* same type as cudaStream_t */
+
+typedef enum nsa_status {
+    NSA_OK = 0,
+    NSA_ERR_INVALID_ARG = 1, /* host-detected bad argument; nothing launched */
+    NSA_ERR_UNSUPPORTED = 2, /* valid but not supported (dtype / shape combination) */
+    NSA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    NSA_ERR_BOUNDS = 4,      /* device-detected index, page id or length out of range */
+    NSA_ERR_TIMEOUT = 5      /* a bounded device wait gave up */
+} nsa_status;
+
+typedef enum nsa_mode {
+    NSA_MODE_DECODE = 0,        /* one query row per request */
+    NSA_MODE_EXTEND = 1,        /* extend_lens[b] new query rows per request (chunked prefill) */
+    NSA_MODE_TARGET_VERIFY = 2  /* n_draft query rows per request (speculative verify) */
+} nsa_mode;
+
+typedef enum nsa_dtype {
+    NSA_DT_F32 = 0,
+    NSA_DT_BF16 = 1,
+    NSA_DT_E4M3 = 2 /* OCP float8 e4m3fn */
+} nsa_dtype;
+
+/* Human-readable name of a status code (static storage). */
+const char *nsa_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int nsa_abi_version(void);
+
+/* Copy the device status word to *host_value after synchronizing `stream`.
+ * Returns NSA_OK if the copy worked, NSA_ERR_CUDA otherwise. */
+nsa_status nsa_status_read(const int32_t *status_dev, int32_t *host_value, nsa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* nsa_metadata                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* Output arrays of nsa_metadata: device pointers, all caller-allocated.
+ * R = number of query rows (decode: B; target-verify: B * n_draft;
+ * extend: sum(extend_lens)). */
+typedef struct nsa_metadata_out {
+    int32_t *cache_seqlens;     /* [B]    seq_lens (+ n_draft in target-verify) */
+    int32_t *cu_seqlens_k;      /* [B+1]  [0, cumsum(cache_seqlens)] */
+    int32_t *cu_seqlens_q;      /* decode [B+1] arange; extend [B+1] [0, cumsum(extend_lens)];
+                                   target-verify [R+1] arange */
+    int32_t *seqlens_expanded;  /* [R]    tokens visible to each row (unclipped) */
+    int32_t *nsa_cache_seqlens; /* [R]    min(seqlens_expanded, topk) */
+    int32_t *nsa_cu_seqlens_k;  /* [R+1]  [0, cumsum(nsa_cache_seqlens)] */
+    int32_t *nsa_cu_seqlens_q;  /* [R+1]  arange(R+1) */
+    int32_t *row_to_req;        /* [R]    request of each row */
+    int32_t *page_table_1;      /* [B, page_table_1_ld]; columns 0..W-1 written */
+    int64_t page_table_1_ld;    /* >= W */
+    int32_t *real_page_table;   /* [B, real_page_table_ld]; columns 0..ceil(W/ps)-1 written */
+    int64_t real_page_table_ld; /* >= ceil(W / page_size) */
+    int32_t *indexer_ks;        /* [R] extend only (may be NULL): first key of the row's request
+                                   in the ragged key space */
+    int32_t *indexer_ke;        /* [R] extend only (may be NULL): indexer_ks + seqlens_expanded */
+} nsa_metadata_out;
+
+/*
+ * Per-step metadata of the sparse-attention backend, in one launch.
+ * [DSA] DeepseekSparseAttnBackend.init_forward_metadata (decode, target-verify
+ * and extend branches) and _cal_indexer_k_start_end; [NSA] NSAMetadata,
+ * compute_cu_seqlens; [NSA-diff] the target-verify branch.
+ *
+ *   mode               decode / extend / target-verify
+ *   B                  requests in the step (>= 0)
+ *   R                  query rows (must equal the value implied by mode; host-known)
+ *   W                  page-table width = max_seqlen_k (host-known, >= every cache_seqlens)
+ *   n_draft            draft tokens per request (target-verify; else ignored)
+ *   topk               top-k of the indexer (clips nsa_cache_seqlens)
+ *   page_size          tokens per KV page (>= 1)
+ *   seq_lens_dev       [B] committed tokens per request (extend: including new tokens)
+ *   extend_lens_dev    [B] new tokens per request (extend only; else may be NULL)
+ *   req_to_token_dev   [pool_rows, req_to_token_ld] token slot of each request position
+ *   req_pool_indices_dev [B] row of each request in req_to_token
+ *   out                host struct of device output pointers
+ *
+ * Differences from the pages: the page table is kept per request in every
+ * mode (target-verify rows reach it through row_to_req instead of an n-times
+ * repeated copy), and row_to_req is always produced.
+ * Device errors: a cache length outside [0, W] or a pool index outside
+ * [0, pool_rows) sets NSA_ERR_BOUNDS in *status_dev (that request's table
+ * row is skipped).
+ */
+nsa_status nsa_metadata(nsa_mode mode, int B, int R, int W, int n_draft, int topk, int page_size,
+                        const int32_t *seq_lens_dev, const int32_t *extend_lens_dev,
+                        const int32_t *req_to_token_dev, int64_t req_to_token_ld,
+                        int64_t pool_rows, const int32_t *req_pool_indices_dev,
+                        const nsa_metadata_out *out, int32_t *status_dev, nsa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* nsa_local_virtual_batches (host)                                         */
+/* ------------------------------------------------------------------------ */
+
+/* Effective local-attention chunk: min(chunk, max_seq_len) floored to a
+ * multiple of page_size, and at least page_size.  [FA3-diff]
+ * FlashAttentionBackend.init_forward_metadata.  Returns -1 on bad input. */
+int nsa_effective_chunk_size(int attn_chunk_size, int max_seq_len, int page_size);
+
+/*
+ * Chunk-local attention as independent "virtual" requests.
+ * [FA3-diff] make_local_attention_virtual_batches: every request's query
+ * rows are cut where the key axis crosses a multiple of attn_chunk_size, and
+ * each piece attends (causally, bottom-right aligned) to the keys of its own
+ * chunk only.
+ *
+ * All pointers are HOST pointers (the pages build this on the host too).
+ *   cu_seqlens_q   [B+1] query start of each request (every request has >= 1 query)
+ *   seq_lens       [B]   key length of each request
+ *   block_table    [B, block_table_ld] page ids of each request
+ *   block_table_cols  valid columns of block_table (bounds check)
+ * Outputs (V = number of virtual batches, P = attn_chunk_size / page_size):
+ *   seqlens_q_local [V], cu_seqlens_q_local [V+1], seqlens_k_local [V],
+ *   k_seqstarts_absolute [V], block_table_local [V, P]
+ * With any output pointer NULL the call only counts: *num_virtual_batches = V.
+ * Returns NSA_ERR_INVALID_ARG if attn_chunk_size is not a positive multiple of
+ * page_size, V exceeds max_virtual_batches, or a block_table read would fall
+ * outside block_table_cols.
+ */
+nsa_status nsa_local_virtual_batches(int attn_chunk_size, int page_size, int B,
+                                     const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                                     const int32_t *block_table, int64_t block_table_ld,
+                                     int64_t block_table_cols, int max_virtual_batches,
+                                     int *num_virtual_batches, int32_t *seqlens_q_local,
+                                     int32_t *cu_seqlens_q_local, int32_t *seqlens_k_local,
+                                     int32_t *k_seqstarts_absolute, int32_t *block_table_local);
+
+/* ------------------------------------------------------------------------ */
+/* nsa_indexer_logits                                                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Lightning-indexer scores over the paged indexer-key cache:
+ *   logits[r, s] = k_scale[slot] * sum_h w[r, h] * ReLU(sum_d q[r, h, d] * k[slot, d])
+ *   slot        = real_page_table[row_to_req[r], s / page_size] * page_size + s % page_size
+ * for 0 <= s < row_len[r].  This is the score the pages hand to top-k
+ * ([NSA] NSAIndexerMetadata: get_page_table_64, get_seqlens_int32; [DSA]
+ * the paged MQA logits call); with k_scale >= 0 it equals
+ * sum_h w * ReLU(q . (k * k_scale)).  Entries at s >= row_len[r] are not written.
+ *
+ *   dtype              NSA_DT_E4M3 (q and k e4m3) or NSA_DT_F32 (q and k float32)
+ *   q_dev              [R, Hi, Di] row-major
+ *   weights_dev        [R, Hi] float32
+ *   k_cache_dev        [num_pages, page_size, Di] (slot-major rows of Di)
+ *   k_scale_dev        [num_pages, page_size] float32, >= 0 (one scale per key row)
+ *   real_page_table_dev [*, rpt_ld] page ids per request (from nsa_metadata)
+ *   row_to_req_dev     [R], row_len_dev [R] (seqlens_expanded)
+ *   max_row_len        host-known upper bound of row_len (sizes the grid)
+ *   logits_dev         [R, logits_ld] float32, logits_ld >= max_row_len
+ * Supported: Hi*Di <= 8192, Di % 16 == 0.  The tensor-core path is used for
+ * e4m3 with Hi == 64, Di == 128, page_size % 64 == 0... and the SIMT path
+ * otherwise.
+ * Device errors: a page id outside [0, num_pages) sets NSA_ERR_BOUNDS and the
+ * affected logits are written as -inf.
+ */
+nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, const float *weights_dev,
+                              const void *k_cache_dev, const float *k_scale_dev, int64_t num_pages,
+                              int page_size, int Hi, int Di, const int32_t *real_page_table_dev,
+                              int64_t rpt_ld, const int32_t *row_to_req_dev,
+                              const int32_t *row_len_dev, int R, int max_row_len,
+                              float *logits_dev, int64_t logits_ld, int32_t *status_dev,
+                              nsa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* nsa_topk_transform                                                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Per-row top-k of the indexer scores, transformed to KV slots
+ * ([NSA] NSAIndexerMetadata.topk_transform, fused variant that "returns a
+ * transformed page table directly"; [DSA] transform_index_page_table_decode /
+ * _prefill with page size 1 and _pad_topk_indices):
+ *   row r with L = row_len[r]:
+ *     L <= topk : every position 0..L-1
+ *     L >  topk : the topk positions with the largest logits; equal logits
+ *                 prefer the lower position; -0 equals +0; NaN ranks lowest
+ *   the chosen positions are listed in ascending order, each replaced by
+ *   page_table_1[row_to_req[r], s], and the row is padded with -1.
+ *
+ *   logits_dev       [R, logits_ld] float32 (only s < row_len[r] is read)
+ *   row_len_dev      [R] (seqlens_expanded), row_to_req_dev [R]
+ *   page_table_1_dev [*, pt_ld] token slots per request (from nsa_metadata)
+ *   max_row_len      host-known upper bound of row_len
+ *   indices_dev      [R, indices_ld] int32, indices_ld >= topk
+ * Supported: 1 <= topk <= 4096.
+ * Device errors: row_len[r] > max_row_len sets NSA_ERR_BOUNDS and that row is
+ * written as all -1.
+ */
+nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits_ld, const int32_t *row_len_dev,
+                              const int32_t *row_to_req_dev, const int32_t *page_table_1_dev,
+                              int64_t pt_ld, int R, int topk, int max_row_len, int32_t *indices_dev,
+                              int64_t indices_ld, int32_t *status_dev, nsa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* nsa_sparse_mla                                                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Sparse MLA attention over only the selected KV rows ([DSA]
+ * _forward_flashmla_sparse / _forward_flashmla_kv call contract; [NSA]
+ * "here, we use page size = 1": indices are rows of the flat KV view).
+ * Keys and values share the latent: K_j = KV[idx_j, 0:d_latent+d_rope],
+ * V_j = KV[idx_j, 0:d_latent].  For each row r and head h:
+ *   s_j      = sm_scale * (q_nope[r,h] . K_j[0:d_latent] + q_rope[r,h] . K_j[d_latent:])
+ *   lse[r,h] = ln sum_j exp(s_j)        (natural log; -inf if no valid index)
+ *   out[r,h] = sum_j exp(s_j - lse) V_j (0 if no valid index)
+ * over the valid entries j of indices[r, 0:topk] (-1 entries are skipped).
+ *
+ *   q_dtype           NSA_DT_BF16 or NSA_DT_F32; `out` has the same dtype
+ *   kv_dtype          NSA_DT_BF16 rows of d_latent+d_rope bf16,
+ *                     NSA_DT_F32 rows of d_latent+d_rope float32, or
+ *                     NSA_DT_E4M3 rows of d_latent e4m3 codes, then one float32
+ *                     scale per 128 latent elements, then d_rope bf16
+ *                     (656 bytes for 512 + 64); requires d_latent % 128 == 0
+ *   q_nope_dev        element (r, h, d) at r*nope_ld_r + h*nope_ld_h + d
+ *   q_rope_dev        element (r, h, d) at r*rope_ld_r + rope_ld_h*h + d
+ *   kv_dev            [num_slots, row] as above
+ *   indices_dev       [R, indices_ld] int32 slots or -1
+ *   out_dev           [R, H, d_latent] contiguous, dtype = q_dtype
+ *   lse_dev           [R, H] float32
+ *   workspace_dev     scratch of nsa_sparse_mla_workspace_bytes(...) bytes
+ *                     (16-byte aligned; may be NULL if that size is 0)
+ * q_dtype F32 requires kv_dtype F32; BF16 q takes BF16 or E4M3 KV.
+ * Device errors: an index outside [-1, num_slots) sets NSA_ERR_BOUNDS and is
+ * treated as -1.
+ */
+nsa_status nsa_sparse_mla(nsa_dtype q_dtype, nsa_dtype kv_dtype, const void *q_nope_dev,
+                          int64_t nope_ld_r, int64_t nope_ld_h, const void *q_rope_dev,
+                          int64_t rope_ld_r, int64_t rope_ld_h, const void *kv_dev,
+                          int64_t num_slots, const int32_t *indices_dev, int64_t indices_ld, int R,
+                          int H, int d_latent, int d_rope, int topk, float sm_scale, void *out_dev,
+                          float *lse_dev, void *workspace_dev, size_t workspace_bytes,
+                          int32_t *status_dev, nsa_stream_t stream);
+
+/* Scratch bytes nsa_sparse_mla needs for this problem (0 if none). */
+size_t nsa_sparse_mla_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int H,
+                                      int d_latent, int d_rope, int topk);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NSA_H */

@@ -1,0 +1,85 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every entry
+point the header declares, and its host-side calls (local virtual batches,
+effective chunk size, status strings) match the oracle and the pages'
+worked example."""
+import re
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.golden import load as load_golden
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def nsa():
+    import deepseek_sparse_mla_indexer_gb300 as m
+    m.load()
+    return m
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(nsa_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_library_exports_every_declared_entry_point(nsa):
+    declared = _declared_functions()
+    assert declared >= set(nsa.EXPORTED_SYMBOLS)
+    lib = nsa.load()
+    for name in sorted(declared):
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_status_strings(nsa):
+    assert nsa.nsa_status_string(0) == "ok"
+    assert "out of range" in nsa.nsa_status_string(4)
+    assert nsa.nsa_abi_version() >= 100
+
+
+def test_local_virtual_batches_worked_example(nsa):
+    g = load_golden("local_virtual_batches_worked_example.txt")
+    bt = g["block_table"].reshape(int(g["block_table_rows"][0]), int(g["block_table_cols"][0]))
+    sq, cu, sk, st, btl = nsa.nsa_local_virtual_batches(int(g["attn_chunk_size"][0]), int(g["page_size"][0]),
+                                                        g["query_start_loc"], g["seq_lens"], bt)
+    assert np.array_equal(sq, g["seqlens_q_local"])
+    assert np.array_equal(cu, g["cu_seqlens_q_local"])
+    assert np.array_equal(sk, g["seqlens_k_local"])
+    assert np.array_equal(st, g["k_seqstarts_absolute"])
+    assert np.array_equal(btl.reshape(-1), g["block_table_local"])
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_local_virtual_batches_match_oracle(nsa, seed):
+    rng = np.random.default_rng(1000 + seed)
+    ps = int(rng.choice([1, 2, 16, 64]))
+    c = ps * int(rng.integers(1, 6))
+    B = int(rng.integers(1, 9))
+    kv = rng.integers(1, 600, size=B)
+    q = np.array([int(rng.integers(1, k + 1)) for k in kv])
+    cq = np.concatenate([[0], np.cumsum(q)])
+    cols = (int(kv.max()) + c) // ps + 2
+    bt = rng.integers(0, 10 ** 6, size=(B, cols)).astype(np.int32)
+    got = nsa.nsa_local_virtual_batches(c, ps, cq, kv, bt)
+    exp = oracle.local_virtual_batches(c, ps, cq, kv, bt)
+    for a, b in zip(got, exp):
+        assert np.array_equal(a, b)
+
+
+def test_local_virtual_batches_rejects_chunk_not_multiple_of_page(nsa):
+    with pytest.raises(nsa.NsaError):
+        nsa.nsa_local_virtual_batches(6, 4, np.array([0, 3]), np.array([5]), np.zeros((1, 8), np.int32))
+
+
+def test_effective_chunk_size_matches_oracle(nsa):
+    for c, m, ps in [(8192, 100000, 64), (8192, 1000, 64), (8192, 10, 64), (100, 1000, 64), (4, 17, 2)]:
+        assert nsa.nsa_effective_chunk_size(c, m, ps) == oracle.effective_chunk_size(c, m, ps)

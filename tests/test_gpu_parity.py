@@ -1,0 +1,137 @@
+"""CUDA path vs oracle, element by element, through the C ABI (GPU only).
+
+Small cases run every row; the five named workloads at full size are checked
+on sampled rows in the same launch configuration the benchmark uses.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests import _harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import deepseek_sparse_mla_indexer_gb300 as nsa
+    nsa.load()
+
+
+def _step(wl):
+    from deepseek_sparse_mla_indexer_gb300.step import SparseAttentionStep
+    return SparseAttentionStep(wl, "cuda")
+
+
+def _mk(name, **kw):
+    base = dict(mode=W.MODE_DECODE, topk=2048, page_size=64, Hi=64, Di=128, idx_dtype=W.DT_E4M3, H=128,
+                d_latent=512, d_rope=64, q_dtype=W.DT_BF16, kv_dtype=W.DT_BF16, sm_scale=W.SM_SCALE_V32,
+                seed=17)
+    base.update(kw)
+    return W.make_workload(name, **base)
+
+
+SMALL = {
+    # tiny float32 decode exactly as named (topk 32 < L: the selection is exercised)
+    "tiny_fp32_decode": lambda: W.config("tiny_fp32_decode"),
+    # tiny with topk >= L (sparse covers the whole sequence)
+    "tiny_fp32_topk_covers": lambda: W.make_workload(
+        "tiny_cover", mode=W.MODE_DECODE, seq_lens=[64, 100], topk=128, page_size=16, Hi=4, Di=32,
+        idx_dtype=W.DT_F32, H=4, d_latent=64, d_rope=16, q_dtype=W.DT_F32, kv_dtype=W.DT_F32,
+        sm_scale=80 ** -0.5, seed=1, weight_dist="uniform"),
+    # bf16 decode, ragged lengths around topk and page boundaries
+    "decode_bf16_ragged": lambda: _mk("dec", seq_lens=[1, 63, 2048, 2049, 3001], seed=21),
+    # fp8 KV decode, 16 heads, with outliers
+    "decode_fp8kv_h16": lambda: _mk("f8", seq_lens=[64, 2100, 3000, 130], H=16, kv_dtype=W.DT_E4M3,
+                                    kv_outliers=0.01, seed=22),
+    # chunked extend: rows cross topk inside one request
+    "extend_bf16": lambda: _mk("ext", mode=W.MODE_EXTEND, seq_lens=[2100, 300], extend_lens=[80, 20], seed=23),
+    # target-verify with fp8 KV
+    "verify_fp8kv": lambda: _mk("ver", mode=W.MODE_VERIFY, seq_lens=[2040, 2046, 5000], n_draft=4,
+                                kv_dtype=W.DT_E4M3, seed=24),
+    # e4m3 indexer with a small page size and few heads (SIMT indexer path)
+    "decode_small_heads_ps16": lambda: _mk("ps16", seq_lens=[33, 700, 129], page_size=16, Hi=8, Di=32,
+                                           topk=256, H=16, seed=25),
+}
+
+
+@pytest.mark.parametrize("case", list(SMALL))
+def test_small_case_all_rows(case):
+    wl = SMALL[case]()
+    step = _step(wl)
+    rows = None if wl.R <= 8 else H.sample_rows(wl, 8, seed=1)
+    H.full_parity(step, wl, rows=rows)
+
+
+@pytest.mark.parametrize("name,nrows", [("v32_decode_bf16", 3), ("fp8kv_decode_h16", 3),
+                                        ("chunked_extend", 3), ("verify_long_fp8kv", 3)])
+def test_named_workload_full_size_sampled(name, nrows):
+    wl = W.config(name)
+    step = _step(wl)
+    H.full_parity(step, wl, rows=H.sample_rows(wl, nrows, seed=2))
+
+
+def test_empty_batch_is_a_no_op():
+    import deepseek_sparse_mla_indexer_gb300 as nsa
+    d = "cuda"
+    md = nsa.alloc_metadata(nsa.MODE_DECODE, 0, 0, 0, 64, d)
+    z = torch.zeros(0, dtype=torch.int32, device=d)
+    r2t = torch.zeros((1, 64), dtype=torch.int32, device=d)
+    nsa.nsa_metadata(nsa.MODE_DECODE, 0, 0, 0, 0, 2048, 64, z, None, r2t, z, md)
+    logits = torch.zeros((0, 64), device=d)
+    idx = torch.zeros((0, 2048), dtype=torch.int32, device=d)
+    nsa.nsa_topk_transform(logits, z, z, md["page_table_1"], 2048, 0, idx)
+    torch.cuda.synchronize()
+    assert int(md["cu_seqlens_k"][0]) == 0 and int(md["nsa_cu_seqlens_k"][0]) == 0
+
+
+def test_topk_ties_nan_and_signed_zero_bit_exact():
+    import deepseek_sparse_mla_indexer_gb300 as nsa
+    import oracle
+    rng = np.random.default_rng(5)
+    R, Wd, k = 6, 70000, 2048
+    lg = rng.integers(-3, 4, size=(R, Wd)).astype(np.float32)  # massive ties
+    lg[1] = rng.standard_normal(Wd).astype(np.float32)
+    lg[1, ::7] = -0.0
+    lg[1, 5::11] = 0.0
+    lg[2, ::3] = np.nan
+    lg[3] = 1.0  # all equal: the first k positions win
+    L = np.array([Wd, 60000, 50001, 2049, 2048, 4000], np.int32)
+    pt = rng.integers(0, 2 ** 31 - 1, size=(R, Wd)).astype(np.int32)
+    r2q = np.arange(R, dtype=np.int32)
+    exp = oracle.topk_transform(lg, L, r2q, pt, k)
+    d = "cuda"
+    idx = torch.empty((R, k), dtype=torch.int32, device=d)
+    nsa.nsa_topk_transform(torch.from_numpy(lg).to(d), torch.from_numpy(L).to(d), torch.from_numpy(r2q).to(d),
+                           torch.from_numpy(pt).to(d), k, Wd, idx)
+    assert np.array_equal(idx.cpu().numpy(), exp)
+
+
+def test_out_of_range_index_sets_bounds_status():
+    import deepseek_sparse_mla_indexer_gb300 as nsa
+    wl = SMALL["decode_fp8kv_h16"]()
+    step = _step(wl)
+    idx = torch.full((wl.R, wl.topk), -1, dtype=torch.int32, device="cuda")
+    idx[:, 0] = 5
+    idx[0, 1] = step.num_slots  # one past the end
+    step.status.zero_()
+    step.attention(indices=idx)
+    assert step.status_code() == nsa.ERR_BOUNDS
+    assert torch.isfinite(step.lse).all()
+
+
+def test_host_rejects_bad_arguments_without_launch():
+    import deepseek_sparse_mla_indexer_gb300 as nsa
+    wl = SMALL["tiny_fp32_decode"]()
+    step = _step(wl)
+    with pytest.raises(nsa.NsaError) as e:
+        nsa.nsa_topk_transform(step.logits, step.md["seqlens_expanded"], step.md["row_to_req"],
+                               step.md["page_table_1"], 0, wl.W, step.indices)
+    assert e.value.code == nsa.ERR_INVALID_ARG
+    with pytest.raises(nsa.NsaError) as e:  # f32 query with bf16 KV is not a supported pair
+        nsa.nsa_sparse_mla(nsa.DT_F32, nsa.DT_BF16, step.q_nope, step.q_rope, step.kv, step.indices,
+                           1.0, step.out, step.lse)
+    assert e.value.code == nsa.ERR_UNSUPPORTED
