@@ -160,10 +160,13 @@ extern "C" nsa_status nsa_metadata(nsa_mode mode, int B, int R, int W, int n_dra
     if (mode == NSA_MODE_EXTEND && B == 0 && R != 0) return NSA_ERR_INVALID_ARG;
     if (B > 0 && (!seq_lens_dev || !req_to_token_dev || !req_pool_indices_dev)) return NSA_ERR_INVALID_ARG;
     if (B > 0 && (req_to_token_ld < W || pool_rows < 1)) return NSA_ERR_INVALID_ARG;
-    if (!out->cache_seqlens || !out->cu_seqlens_k || !out->cu_seqlens_q || !out->seqlens_expanded ||
-        !out->nsa_cache_seqlens || !out->nsa_cu_seqlens_k || !out->nsa_cu_seqlens_q ||
-        !out->row_to_req || !out->page_table_1 || !out->real_page_table)
+    // arrays of length >= 1 must exist; per-request / per-row arrays only when non-empty
+    if (!out->cu_seqlens_k || !out->cu_seqlens_q || !out->nsa_cu_seqlens_k || !out->nsa_cu_seqlens_q)
         return NSA_ERR_INVALID_ARG;
+    if (B > 0 && !out->cache_seqlens) return NSA_ERR_INVALID_ARG;
+    if (R > 0 && (!out->seqlens_expanded || !out->nsa_cache_seqlens || !out->row_to_req))
+        return NSA_ERR_INVALID_ARG;
+    if (B > 0 && W > 0 && (!out->page_table_1 || !out->real_page_table)) return NSA_ERR_INVALID_ARG;
     if (out->page_table_1_ld < W || out->real_page_table_ld < ceil_div(W, page_size))
         return NSA_ERR_INVALID_ARG;
     if ((out->indexer_ks == nullptr) != (out->indexer_ke == nullptr)) return NSA_ERR_INVALID_ARG;
