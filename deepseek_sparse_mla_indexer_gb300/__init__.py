@@ -62,7 +62,7 @@ def load(build_if_missing: bool = True):
         "nsa_metadata": ([I, I, I, I, I, I, I, P, P, P, L, L, P, P, P, P], I),
         "nsa_effective_chunk_size": ([I, I, I], I),
         "nsa_local_virtual_batches": ([I, I, I, P, P, P, L, L, I, P, P, P, P, P, P], I),
-        "nsa_indexer_logits": ([I, P, P, P, P, L, I, I, I, P, L, P, P, I, I, P, L, P, P], I),
+        "nsa_indexer_logits": ([I, P, P, P, P, L, I, I, I, P, L, P, P, I, I, I, P, L, P, P], I),
         "nsa_topk_transform": ([P, L, P, P, P, L, I, I, I, P, L, P, P], I),
         "nsa_sparse_mla": ([I, I, P, L, L, P, L, L, P, L, P, L, I, I, I, I, I, F, P, P, P, S, P, P], I),
         "nsa_sparse_mla_workspace_bytes": ([I, I, I, I, I, I, I], S),
@@ -186,13 +186,13 @@ def nsa_local_virtual_batches(attn_chunk_size: int, page_size: int, cu_seqlens_q
 def nsa_indexer_logits(dtype: int, q_idx: torch.Tensor, weights: torch.Tensor, k_cache: torch.Tensor,
                        k_scale: torch.Tensor, real_page_table: torch.Tensor, row_to_req: torch.Tensor,
                        row_len: torch.Tensor, max_row_len: int, logits: torch.Tensor,
-                       status: Optional[torch.Tensor] = None, stream=None) -> None:
+                       status: Optional[torch.Tensor] = None, stream=None, rows_per_group: int = 1) -> None:
     R, Hi, Di = q_idx.shape
     num_pages, ps = k_cache.shape[0], k_cache.shape[1]
     assert q_idx.is_contiguous() and k_cache.is_contiguous() and weights.is_contiguous() and k_scale.is_contiguous()
     rc = load().nsa_indexer_logits(dtype, _ptr(q_idx), _ptr(weights), _ptr(k_cache), _ptr(k_scale), num_pages,
                                    ps, Hi, Di, _ptr(real_page_table), real_page_table.stride(0),
-                                   _ptr(row_to_req), _ptr(row_len), R, max_row_len, _ptr(logits),
+                                   _ptr(row_to_req), _ptr(row_len), R, rows_per_group, max_row_len, _ptr(logits),
                                    logits.stride(0), _ptr(status), _stream(stream))
     _check("nsa_indexer_logits", rc)
 

@@ -48,7 +48,9 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     def compile_one(src):
         obj = os.path.join(OUT, os.path.basename(src) + ".o")
         if src.endswith(".cpp"):
-            cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-I", os.path.join(ROOT, "include"), "-c", src, "-o", obj]
+            cuda_inc = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "include")
+            cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+                   "-c", src, "-o", obj]
         else:
             cmd = [nvcc] + NVCC_FLAGS + list(extra_flags) + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)

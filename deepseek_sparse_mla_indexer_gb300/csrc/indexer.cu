@@ -102,12 +102,12 @@ extern "C" nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, con
                                          int64_t num_pages, int page_size, int Hi, int Di,
                                          const int32_t *real_page_table_dev, int64_t rpt_ld,
                                          const int32_t *row_to_req_dev, const int32_t *row_len_dev,
-                                         int R, int max_row_len, float *logits_dev,
+                                         int R, int rows_per_group, int max_row_len, float *logits_dev,
                                          int64_t logits_ld, int32_t *status_dev, nsa_stream_t stream)
 {
     using namespace nsa;
     if (dtype != NSA_DT_E4M3 && dtype != NSA_DT_F32) return NSA_ERR_UNSUPPORTED;
-    if (R < 0 || Hi < 1 || Di < 1 || page_size < 1 || num_pages < 0 || max_row_len < 0)
+    if (R < 0 || Hi < 1 || Di < 1 || page_size < 1 || num_pages < 0 || max_row_len < 0 || rows_per_group < 1)
         return NSA_ERR_INVALID_ARG;
     if (Hi * Di > kMaxQ || Di % 16 != 0) return NSA_ERR_UNSUPPORTED;
     if (logits_ld < max_row_len || rpt_ld < ceil_div(max_row_len, page_size)) return NSA_ERR_INVALID_ARG;
@@ -120,7 +120,7 @@ extern "C" nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, con
     nsa_status st = indexer_tc_try_launch(dtype, q_dev, weights_dev, k_cache_dev, k_scale_dev,
                                           num_pages, page_size, Hi, Di, real_page_table_dev, rpt_ld,
                                           row_to_req_dev, row_len_dev, R, max_row_len, logits_dev,
-                                          logits_ld, status_dev, (cudaStream_t)stream);
+                                          logits_ld, status_dev, (cudaStream_t)stream, rows_per_group);
     if (st != NSA_ERR_UNSUPPORTED) return st;
 
     const size_t smem = sizeof(float) * ((size_t)(Hi + kTok) * (Di + 1) + Hi + kTok);

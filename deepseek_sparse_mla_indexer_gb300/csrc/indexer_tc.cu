@@ -1,11 +1,335 @@
-// Tensor-core indexer (placeholder until the tcgen05 kernel lands).
+// Tensor-core lightning indexer for e4m3 q / K with 64 heads x 128 dims.
+//
+//   logits[r, s] = k_scale[slot] * sum_h w[r,h] * ReLU(q[r,h,:] . k[slot,:])
+//
+// The score of the DeepSeek sparse-attention pages ([NSA] NSAIndexerMetadata,
+// [DSA] the paged MQA logits call) computed as a dense fp8 contraction:
+// for a tile of 128 consecutive positions of one request (two 64-token halves,
+// each a contiguous run of one KV page) and the c <= 4 query rows of that
+// request handled by the CTA,
+//
+//   D[128 tokens, 64*c] = K_tile[128, 128] (e4m3) x Q[64*c, 128]^T (e4m3)
+//
+// accumulates in TMEM (fp32) via tcgen05.mma kind::f8f6f4.  The epilogue
+// (one thread per token) applies ReLU, the per-head weights, the head sum and
+// the key's scale, and stores one fp32 logit per (row, token).
+//
+// Roles (192 threads): warp 0 issues TMA loads of K pages and q rows into
+// 128B-swizzled shared memory; warp 1 owns TMEM and issues the MMAs; warps
+// 2..5 are the epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
+// Stages are tracked with mbarriers; every wait is bounded and reports
+// NSA_ERR_TIMEOUT instead of hanging.
 #include "indexer_tc.cuh"
+#include "sm100.cuh"
+#include "tma_host.h"
 
 namespace nsa {
-nsa_status indexer_tc_try_launch(nsa_dtype, const void *, const float *, const void *, const float *, int64_t,
-                                 int, int, int, const int32_t *, int64_t, const int32_t *, const int32_t *, int,
-                                 int, float *, int64_t, int32_t *, cudaStream_t)
+namespace {
+
+using namespace sm100;
+
+constexpr int kTileTok = 128;
+constexpr int kHalf = 64;
+constexpr int kDi = 128;
+constexpr int kHi = 64;
+constexpr int kStages = 4;
+constexpr int kThreadsTc = 192;
+constexpr int kMaxG = 4;
+constexpr int kTilesPerCta = 16;
+constexpr uint32_t kTileBytes = kTileTok * kDi;    // 16 KB of e4m3
+constexpr uint32_t kHalfBytes = kHalf * kDi;       // 8 KB
+constexpr uint32_t kQRowBytes = kHi * kDi;         // 8 KB per query row
+constexpr long long kWaitBudget = 2000000000LL;    // ~1 s at 2 GHz
+
+struct TcParams {
+    const float *w;
+    const float *k_scale;
+    const int32_t *rpt;
+    int64_t rpt_ld;
+    const int32_t *row_to_req;
+    const int32_t *row_len;
+    int R, G, max_row_len, ps;
+    int64_t num_pages;
+    float *logits;
+    int64_t logits_ld;
+    int32_t *status;
+    uint32_t acc_stride;  // TMEM columns per accumulator buffer
+    uint32_t tmem_cols;
+};
+
+struct Bars {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t q_full;
+    uint64_t q_empty;
+    uint64_t done;
+    uint32_t tmem_base;
+    volatile int abort;
+    float w[kMaxG * kHi];
+};
+
+// Sub-group n of the CTA's row group: the n-th maximal run of rows sharing a request.
+struct SubGroup {
+    int r0, c, b, lmax;
+};
+
+__device__ __forceinline__ int clamp_len(const TcParams &p, int r)
 {
-    return NSA_ERR_UNSUPPORTED;
+    int L = p.row_len[r];
+    return L < 0 ? 0 : (L > p.max_row_len ? p.max_row_len : L);
 }
+
+__device__ __forceinline__ bool next_subgroup(const TcParams &p, int g_end, int &r, SubGroup &sg)
+{
+    if (r >= g_end) return false;
+    sg.r0 = r;
+    sg.b = p.row_to_req[r];
+    sg.lmax = 0;
+    int c = 0;
+    while (r < g_end && p.row_to_req[r] == sg.b) {
+        int L = clamp_len(p, r);
+        sg.lmax = L > sg.lmax ? L : sg.lmax;
+        ++c;
+        ++r;
+    }
+    sg.c = c;
+    return true;
+}
+
+__device__ __forceinline__ void fail(Bars *bars, int32_t *status)
+{
+    bars->abort = 1;
+    set_status(status, NSA_ERR_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(kThreadsTc)
+indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *a_ring = smem;                              // kStages x 16 KB
+    uint8_t *q_smem = a_ring + kStages * kTileBytes;     // G x 8 KB
+    Bars *bars = (Bars *)(q_smem + p.G * kQRowBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g_begin = blockIdx.y * p.G;
+    const int g_end = min(g_begin + p.G, p.R);
+    const int t_begin = blockIdx.x * kTilesPerCta;
+    const int t_end = t_begin + kTilesPerCta;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&bars->full[i], 1);
+            mbar_init(&bars->empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->acc_full[i], 1);
+            mbar_init(&bars->acc_empty[i], 128);
+        }
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_empty, 1);
+        mbar_init(&bars->done, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&qmap);
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, p.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            uint32_t it = 0, qi = 0;
+            uint32_t issued_mask = 0, last_parity = 0;
+            int r = g_begin;
+            SubGroup sg;
+            while (!bars->abort && next_subgroup(p, g_end, r, sg)) {
+                const int nt = (int)ceil_div(sg.lmax, kTileTok);
+                const int te = min(t_end, nt);
+                if (t_begin >= te) continue;
+                if (!mbar_wait(&bars->q_empty, (qi & 1) ^ 1, kWaitBudget)) { fail(bars, p.status); break; }
+                mbar_arrive_expect_tx(&bars->q_full, sg.c * kQRowBytes);
+                for (int i = 0; i < sg.c; ++i)
+                    tma_load_2d(q_smem + i * kQRowBytes, &qmap, 0, (sg.r0 + i) * kHi, &bars->q_full);
+                ++qi;
+                for (int t = t_begin; t < te; ++t, ++it) {
+                    const int st = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
+                    if (!mbar_wait(&bars->empty[st], ph ^ 1, kWaitBudget)) { fail(bars, p.status); break; }
+                    int64_t row0[2];
+                    uint32_t bytes = 0;
+                    for (int h = 0; h < 2; ++h) {
+                        const int s = t * kTileTok + h * kHalf;
+                        row0[h] = -1;
+                        if (s < sg.lmax) {
+                            const int64_t page = p.rpt[(int64_t)sg.b * p.rpt_ld + s / p.ps];
+                            if (page >= 0 && page < p.num_pages) {
+                                row0[h] = page * p.ps + s % p.ps;
+                                bytes += kHalfBytes;
+                            }
+                        }
+                    }
+                    mbar_arrive_expect_tx(&bars->full[st], bytes);
+                    for (int h = 0; h < 2; ++h)
+                        if (row0[h] >= 0)
+                            tma_load_2d(a_ring + st * kTileBytes + h * kHalfBytes, &kmap, 0, (int)row0[h],
+                                        &bars->full[st]);
+                    issued_mask |= 1u << st;
+                    last_parity = (last_parity & ~(1u << st)) | (ph << st);
+                }
+            }
+            // drain: never leave with copies in flight
+            for (int st = 0; st < kStages; ++st)
+                if (issued_mask & (1u << st)) mbar_wait(&bars->full[st], (last_parity >> st) & 1, kWaitBudget);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, ai = 0, qi = 0;
+            int r = g_begin;
+            SubGroup sg;
+            while (!bars->abort && next_subgroup(p, g_end, r, sg)) {
+                const int nt = (int)ceil_div(sg.lmax, kTileTok);
+                const int te = min(t_end, nt);
+                if (t_begin >= te) continue;
+                const uint32_t N = kHi * sg.c;
+                const uint32_t idesc = instr_desc(0, 0, 0, 0, kTileTok, N);
+                if (!mbar_wait(&bars->q_full, qi & 1, kWaitBudget)) { fail(bars, p.status); break; }
+                ++qi;
+                for (int t = t_begin; t < te; ++t, ++it, ++ai) {
+                    const int st = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
+                    const int ab = ai & 1;
+                    const uint32_t aph = (ai >> 1) & 1;
+                    if (!mbar_wait(&bars->full[st], ph, kWaitBudget)) { fail(bars, p.status); break; }
+                    if (!mbar_wait(&bars->acc_empty[ab], aph ^ 1, kWaitBudget)) { fail(bars, p.status); break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(a_ring + st * kTileBytes);
+                    const uint32_t b_addr = smem_u32(q_smem);
+                    const uint32_t d = tmem + ab * p.acc_stride;
+#pragma unroll
+                    for (int k = 0; k < kDi / 32; ++k) {
+                        const uint64_t ad = smem_desc(a_addr + k * 32, 16, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(b_addr + k * 32, 16, 1024, kSwizzle128B);
+                        mma_f8(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bars->empty[st]);
+                    mma_commit(&bars->acc_full[ab]);
+                }
+                mma_commit(&bars->q_empty);
+            }
+            // all MMAs retired before TMEM is released
+            mma_commit(&bars->done);
+            mbar_wait(&bars->done, 0, kWaitBudget);
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int et = threadIdx.x - 64;          // 0..127
+        const int quad = warp & 3;                // TMEM lane quadrant of this warp
+        const int tok = quad * 32 + lane;         // token within the tile
+        uint32_t ai = 0;
+        int r = g_begin;
+        SubGroup sg;
+        while (!bars->abort && next_subgroup(p, g_end, r, sg)) {
+            const int nt = (int)ceil_div(sg.lmax, kTileTok);
+            const int te = min(t_end, nt);
+            if (t_begin >= te) continue;
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            for (int i = et; i < sg.c * kHi; i += 128) bars->w[i] = p.w[(int64_t)sg.r0 * kHi + i];
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            int Lrow[kMaxG];
+#pragma unroll
+            for (int i = 0; i < kMaxG; ++i) Lrow[i] = i < sg.c ? clamp_len(p, sg.r0 + i) : 0;
+            for (int t = t_begin; t < te; ++t, ++ai) {
+                const int ab = ai & 1;
+                const uint32_t aph = (ai >> 1) & 1;
+                if (!mbar_wait(&bars->acc_full[ab], aph, kWaitBudget)) { fail(bars, p.status); break; }
+                tc_fence_after();
+                const int s = t * kTileTok + tok;
+                float scale = 0.f;
+                bool valid_page = false;
+                if (s < sg.lmax) {
+                    const int64_t page = p.rpt[(int64_t)sg.b * p.rpt_ld + s / p.ps];
+                    valid_page = page >= 0 && page < p.num_pages;
+                    if (valid_page) scale = p.k_scale[page * p.ps + s % p.ps];
+                    else set_status(p.status, NSA_ERR_BOUNDS);
+                }
+                const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + ab * p.acc_stride;
+                for (int i = 0; i < sg.c; ++i) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(tbase + i * kHi, v0);
+                    tmem_ld32(tbase + i * kHi + 32, v1);
+                    tmem_ld_wait();
+                    const float *wr = bars->w + i * kHi;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) acc = fmaf(wr[h], fmaxf(__uint_as_float(v0[h]), 0.f), acc);
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) acc = fmaf(wr[32 + h], fmaxf(__uint_as_float(v1[h]), 0.f), acc);
+                    if (s < Lrow[i])
+                        p.logits[(int64_t)(sg.r0 + i) * p.logits_ld + s] = valid_page ? acc * scale : -INFINITY;
+                }
+                tc_fence_before();
+                mbar_arrive(&bars->acc_empty[ab]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, p.tmem_cols);
+    }
+}
+
+}  // namespace
+
+nsa_status indexer_tc_try_launch(nsa_dtype dtype, const void *q, const float *w, const void *k_cache,
+                                 const float *k_scale, int64_t num_pages, int page_size, int Hi, int Di,
+                                 const int32_t *rpt, int64_t rpt_ld, const int32_t *row_to_req,
+                                 const int32_t *row_len, int R, int max_row_len, float *logits,
+                                 int64_t logits_ld, int32_t *status, cudaStream_t stream, int rows_per_group)
+{
+    if (dtype != NSA_DT_E4M3 || Hi != kHi || Di != kDi || page_size % kHalf != 0) return NSA_ERR_UNSUPPORTED;
+    if (((uintptr_t)q & 15) || ((uintptr_t)k_cache & 15)) return NSA_ERR_UNSUPPORTED;
+    if (num_pages * page_size > 2147483647LL || (int64_t)R * kHi > 2147483647LL) return NSA_ERR_UNSUPPORTED;
+    const int G = rows_per_group < 1 ? 1 : (rows_per_group > kMaxG ? kMaxG : rows_per_group);
+
+    CUtensorMap kmap, qmap;
+    if (!make_tma_2d(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_cache, kDi, (uint64_t)num_pages * page_size, kDi,
+                     kDi, kHalf, CU_TENSOR_MAP_SWIZZLE_128B))
+        return NSA_ERR_CUDA;
+    if (!make_tma_2d(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, kDi, (uint64_t)R * kHi, kDi, kDi, kHi,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+        return NSA_ERR_CUDA;
+
+    TcParams p;
+    p.w = w; p.k_scale = k_scale; p.rpt = rpt; p.rpt_ld = rpt_ld; p.row_to_req = row_to_req; p.row_len = row_len;
+    p.R = R; p.G = G; p.max_row_len = max_row_len; p.ps = page_size; p.num_pages = num_pages;
+    p.logits = logits; p.logits_ld = logits_ld; p.status = status;
+    p.acc_stride = (uint32_t)(kHi * G);
+    uint32_t cols = 32;
+    while (cols < 2 * p.acc_stride) cols <<= 1;
+    p.tmem_cols = cols;
+
+    const size_t smem = 1024 + (size_t)kStages * kTileBytes + (size_t)G * kQRowBytes + sizeof(Bars);
+    auto kern = indexer_tc_kernel;
+    NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    const int tiles = (int)ceil_div(max_row_len, kTileTok);
+    dim3 grid((unsigned)ceil_div(tiles, kTilesPerCta), (unsigned)ceil_div(R, G));
+    if (grid.y > 65535) return NSA_ERR_UNSUPPORTED;
+    kern<<<grid, kThreadsTc, smem, stream>>>(kmap, qmap, p);
+    return launch_status();
+}
+
 }  // namespace nsa

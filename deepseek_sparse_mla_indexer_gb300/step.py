@@ -43,6 +43,8 @@ class SparseAttentionStep:
         self.topk, self.ps, self.n_draft = host.topk, host.page_size, host.n_draft
         self.idx_dtype, self.q_dtype, self.kv_dtype = host.idx_dtype, host.q_dtype, host.kv_dtype
         self.sm_scale = float(host.sm_scale)
+        # rows sharing a request are scored together (decode 1, verify n_draft, extend 4)
+        self.rows_per_group = {0: 1, 1: 4, 2: max(1, min(4, self.n_draft))}[self.mode]
         self.seq_lens = _dev(host.seq_lens.astype(np.int32), d)
         self.extend_lens = None if host.extend_lens is None else _dev(host.extend_lens.astype(np.int32), d)
         self.req_to_token = _dev(host.req_to_token, d)
@@ -77,7 +79,7 @@ class SparseAttentionStep:
     def indexer(self, stream=None):
         nsa_indexer_logits(self.idx_dtype, self.q_idx, self.weights, self.k_cache, self.k_scale,
                            self.md["real_page_table"], self.md["row_to_req"], self.md["seqlens_expanded"],
-                           self.W, self.logits, self.status, stream)
+                           self.W, self.logits, self.status, stream, rows_per_group=self.rows_per_group)
 
     def topk_transform(self, stream=None, logits: Optional[torch.Tensor] = None):
         nsa_topk_transform(self.logits if logits is None else logits, self.md["seqlens_expanded"],

@@ -191,11 +191,16 @@ nsa_status nsa_local_virtual_batches(int attn_chunk_size, int page_size, int B,
  *   k_scale_dev        [num_pages, page_size] float32, >= 0 (one scale per key row)
  *   real_page_table_dev [*, rpt_ld] page ids per request (from nsa_metadata)
  *   row_to_req_dev     [R], row_len_dev [R] (seqlens_expanded)
+ *   rows_per_group     >= 1: up to this many (at most 4) consecutive rows are
+ *                      scored together so that rows of one request share each
+ *                      K tile: 1 for decode, n_draft for target-verify, 4 for
+ *                      extend.  Rows of a group that belong to different
+ *                      requests are handled separately, so any value is correct.
  *   max_row_len        host-known upper bound of row_len (sizes the grid)
  *   logits_dev         [R, logits_ld] float32, logits_ld >= max_row_len
- * Supported: Hi*Di <= 8192, Di % 16 == 0.  The tensor-core path is used for
- * e4m3 with Hi == 64, Di == 128, page_size % 64 == 0... and the SIMT path
- * otherwise.
+ * Supported: Hi*Di <= 8192, Di % 16 == 0.  e4m3 with Hi == 64, Di == 128 and
+ * page_size % 64 == 0 runs on the tensor cores (tcgen05, fp8); every other
+ * shape runs on the CUDA cores.
  * Device errors: a page id outside [0, num_pages) sets NSA_ERR_BOUNDS and the
  * affected logits are written as -inf.
  */
@@ -203,7 +208,7 @@ nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, const float *w
                               const void *k_cache_dev, const float *k_scale_dev, int64_t num_pages,
                               int page_size, int Hi, int Di, const int32_t *real_page_table_dev,
                               int64_t rpt_ld, const int32_t *row_to_req_dev,
-                              const int32_t *row_len_dev, int R, int max_row_len,
+                              const int32_t *row_len_dev, int R, int rows_per_group, int max_row_len,
                               float *logits_dev, int64_t logits_ld, int32_t *status_dev,
                               nsa_stream_t stream);
 
