@@ -1,12 +1,475 @@
-// Tensor-core sparse MLA (placeholder until the tcgen05 kernel lands).
+// Tensor-core sparse MLA for d_qk = 576 (512 latent + 64 rope), d_v = 512,
+// bf16 query and bf16 KV rows.
+//
+// [DSA] _forward_flashmla_sparse / _forward_flashmla_kv call contract: for
+// each query row r and head h, attention over the KV rows listed in
+// indices[r, :] (slots of the flat KV view, -1 = none); keys and values share
+// the latent (V = first 512 columns of the same row).
+//
+// One CTA = one query row x 64 heads x one split of the top-k list.  Per tile
+// of 128 selected KV rows:
+//   1. warp 0 gathers the 128 rows into shared memory with TMA tile::gather4
+//      (9 column blocks of 64 bf16, 128-byte swizzled, K-major);
+//   2. warp 1 issues S^T[128 tok, 64 heads] = KV_tile . Q^T on tcgen05 (TMEM);
+//   3. warps 2..5 (one thread per token) run the online softmax over the
+//      token axis: a lazily refreshed running max per head (refreshed only
+//      when a score exceeds it by 2^8; the accumulator is rescaled then), the
+//      per-thread partial sums of the probabilities, and P^T written as bf16
+//      into the rope block (free once S^T is done) in the MN-major layout;
+//   4. warp 1 issues O^T[512 d, 64 heads] += V^T . P^T, reading the latent
+//      tile a second time as an MN-major operand (4 blocks of 128 d rows,
+//      256 TMEM columns).
+// At the end warps 2..5 normalise O^T by the head sums and write the output
+// (one split) or fp32 partials plus their log-sum-exp (several splits, merged
+// by sparse_mla_combine_kernel).
 #include "sparse_mla_tc.cuh"
+#include "sm100.cuh"
+#include "tma_host.h"
 
 namespace nsa {
-size_t sparse_mla_tc_workspace_bytes(nsa_dtype, nsa_dtype, int, int, int, int, int) { return 0; }
-nsa_status sparse_mla_tc_try_launch(nsa_dtype, nsa_dtype, const void *, int64_t, int64_t, const void *, int64_t,
-                                    int64_t, const void *, int64_t, const int32_t *, int64_t, int, int, int, int,
-                                    int, float, void *, float *, void *, int32_t *, cudaStream_t)
+namespace {
+
+using namespace sm100;
+
+constexpr int kTok = 128;
+constexpr int kHc = 64;
+constexpr int kDl = 512;
+constexpr int kDr = 64;
+constexpr int kBlocks = 9;
+constexpr uint32_t kQBlk = kHc * 128;
+constexpr uint32_t kKvBlk = kTok * 128;
+constexpr uint32_t kQBytes = kBlocks * kQBlk;
+constexpr uint32_t kKvBytes = kBlocks * kKvBlk;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 256;
+constexpr float kRescale = 8.0f;  // log2 units
+constexpr long long kWaitBudget = 2000000000LL;
+constexpr int kNumSms = 152;
+
+struct MlaParams {
+    const int32_t *indices;
+    int64_t indices_ld;
+    int R, H, topk, nsplit, tiles_per_split;
+    int64_t num_slots;
+    float scale_log2;
+    __nv_bfloat16 *out;
+    float *lse;
+    float *o_part;
+    float *lse_part;
+    int32_t *status;
+};
+
+struct MlaShared {
+    uint64_t q_full, kv_full, s_full, p_full, kv_empty, done;
+    uint32_t tmem_base;
+    volatile int abort;
+    int idx[kTok];
+    float m_used[kHc];
+    float alpha[kHc];
+    float red[4][kHc];
+};
+
+__device__ __forceinline__ void fail(MlaShared *sm, int32_t *status)
 {
-    return NSA_ERR_UNSUPPORTED;
+    sm->abort = 1;
+    set_status(status, NSA_ERR_TIMEOUT);
 }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_constant__ CUtensorMap qr_map,
+                     const __grid_constant__ CUtensorMap kv_map, MlaParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *q_s = base;
+    uint8_t *kv_s = base + kQBytes;
+    uint8_t *p_s = kv_s + 8 * kKvBlk;  // P^T reuses the rope block
+    MlaShared *sm = (MlaShared *)(kv_s + kKvBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hg = blockIdx.x, sp = blockIdx.y, r = blockIdx.z;
+    const int ntiles_all = (p.topk + kTok - 1) / kTok;
+    const int t0 = sp * p.tiles_per_split;
+    const int nt = max(0, min(t0 + p.tiles_per_split, ntiles_all) - t0);
+
+    if (threadIdx.x == 0) {
+        mbar_init(&sm->q_full, 1);
+        mbar_init(&sm->kv_full, 1);
+        mbar_init(&sm->s_full, 1);
+        mbar_init(&sm->p_full, 128);
+        mbar_init(&sm->kv_empty, 1);
+        mbar_init(&sm->done, 1);
+        sm->abort = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&qn_map);
+        prefetch_tensormap(&qr_map);
+        prefetch_tensormap(&kv_map);
+    }
+    if (threadIdx.x >= 64 && threadIdx.x < 128) sm->m_used[threadIdx.x - 64] = -INFINITY;
+    if (warp == 1) {
+        tmem_alloc(&sm->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm->tmem_base;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&sm->q_full, kQBytes);
+            for (int c = 0; c < 8; ++c) tma_load_3d(q_s + c * kQBlk, &qn_map, c * 64, hg * kHc, r, &sm->q_full);
+            tma_load_3d(q_s + 8 * kQBlk, &qr_map, 0, hg * kHc, r, &sm->q_full);
+        }
+        const int32_t *irow = p.indices + (int64_t)r * p.indices_ld;
+        int issued = 0;
+        for (int i = 0; i < nt && !sm->abort; ++i) {
+            if (i > 0) {
+                bool ok = mbar_wait(&sm->kv_empty, (i - 1) & 1, kWaitBudget);
+                if (!__all_sync(0xffffffffu, ok)) { if (lane == 0) fail(sm, p.status); break; }
+            }
+            int y[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int pos = (t0 + i) * kTok + lane * 4 + j;
+                int s = pos < p.topk ? irow[pos] : -1;
+                if (s < -1 || s >= p.num_slots) {
+                    set_status(p.status, NSA_ERR_BOUNDS);
+                    s = -1;
+                }
+                sm->idx[lane * 4 + j] = s;
+                y[j] = s < 0 ? 0 : s;  // masked rows read slot 0; the softmax zeroes them
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(&sm->kv_full, kKvBytes);
+#pragma unroll 1
+            for (int c = 0; c < kBlocks; ++c)
+                tma_gather4(kv_s + c * kKvBlk + lane * 4 * 128, &kv_map, c * 64, y[0], y[1], y[2], y[3],
+                            &sm->kv_full);
+            issued = i + 1;
+        }
+        // never leave with copies in flight
+        if (issued > 0) mbar_wait(&sm->kv_full, (issued - 1) & 1, kWaitBudget);
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = instr_desc(1, 1, 0, 0, kTok, kHc);  // bf16, K-major A and B
+            const uint32_t idesc_o = instr_desc(1, 1, 1, 1, 128, kHc);   // bf16, MN-major A and B
+            const uint32_t q_addr = smem_u32(q_s), kv_addr = smem_u32(kv_s), p_addr = smem_u32(p_s);
+            bool ok = mbar_wait(&sm->q_full, 0, kWaitBudget);
+            if (!ok) fail(sm, p.status);
+            for (int i = 0; i < nt && ok && !sm->abort; ++i) {
+                if (!mbar_wait(&sm->kv_full, i & 1, kWaitBudget)) { fail(sm, p.status); break; }
+                tc_fence_after();
+                // S^T = KV (128 x 576) . Q^T (576 x 64)
+#pragma unroll 1
+                for (int c = 0; c < kBlocks; ++c) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t ad = smem_desc(kv_addr + c * kKvBlk + ks * 32, 16, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(q_addr + c * kQBlk + ks * 32, 16, 1024, kSwizzle128B);
+                        mma_f16(tmem + kColS, ad, bd, idesc_s, (c | ks) != 0);
+                    }
+                }
+                mma_commit(&sm->s_full);
+                if (!mbar_wait(&sm->p_full, i & 1, kWaitBudget)) { fail(sm, p.status); break; }
+                tc_fence_after();
+                // O^T[d, h] += sum_t V[t, d] P[t, h]: A = V^T (MN-major), B = P^T (MN-major)
+#pragma unroll 1
+                for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                    for (int k = 0; k < kTok / 16; ++k) {
+                        const uint64_t ad =
+                            smem_desc(kv_addr + 2 * m * kKvBlk + k * 2048, kKvBlk, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(p_addr + k * 2048, kKvBlk, 1024, kSwizzle128B);
+                        mma_f16(tmem + m * kHc, ad, bd, idesc_o, (i > 0 || k > 0) ? 1u : 0u);
+                    }
+                }
+                mma_commit(&sm->kv_empty);
+            }
+            mma_commit(&sm->done);
+            mbar_wait(&sm->done, 0, kWaitBudget);
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax / epilogue
+        const int quad = warp & 3;
+        const int t = quad * 32 + lane;  // token row of S^T; d row of each O^T block
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        float l_part[kHc];
+#pragma unroll
+        for (int h = 0; h < kHc; ++h) l_part[h] = 0.f;
+        int done_tiles = 0;
+        for (int i = 0; i < nt; ++i) {
+            bool ok = mbar_wait(&sm->kv_full, i & 1, kWaitBudget) && mbar_wait(&sm->s_full, i & 1, kWaitBudget);
+            if (bar_red_or(1, 128, !ok || sm->abort)) { if (!ok) fail(sm, p.status); break; }
+            tc_fence_after();
+            uint32_t sv[kHc];
+            tmem_ld32(lane_base + kColS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+            tmem_ld32(lane_base + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+            tmem_ld_wait();
+            const bool valid = sm->idx[t] >= 0;
+            float *s = reinterpret_cast<float *>(sv);  // scores in log2 units, in place
+            bool exceed = false;
+#pragma unroll
+            for (int h = 0; h < kHc; ++h) {
+                s[h] = valid ? __uint_as_float(sv[h]) * p.scale_log2 : -INFINITY;
+                exceed |= s[h] > sm->m_used[h] + kRescale;
+            }
+            if (bar_red_or(1, 128, exceed)) {
+                // refresh the running max of every head from this tile's column maxima
+#pragma unroll
+                for (int h = 0; h < kHc; ++h) {
+                    float v = s[h];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+                    if (lane == 0) sm->red[quad][h] = v;
+                }
+                bar_sync(1, 128);
+                if (t < kHc) {
+                    const float cm = fmaxf(fmaxf(sm->red[0][t], sm->red[1][t]), fmaxf(sm->red[2][t], sm->red[3][t]));
+                    const float mo = sm->m_used[t];
+                    const float mn = fmaxf(mo, cm);
+                    sm->alpha[t] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
+                    sm->m_used[t] = mn;
+                }
+                bar_sync(1, 128);
+#pragma unroll
+                for (int h = 0; h < kHc; ++h) l_part[h] *= sm->alpha[h];
+                if (i > 0) {
+                    // the previous tile's O^T must be complete before it is rescaled
+                    if (!mbar_wait(&sm->kv_empty, (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int m = 0; m < 4; ++m) {
+#pragma unroll 1
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t v[32];
+                            const uint32_t a = lane_base + m * kHc + half * 32;
+                            tmem_ld32(a, v);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                v[j] = __float_as_uint(__uint_as_float(v[j]) * sm->alpha[half * 32 + j]);
+                            tmem_st32(a, v);
+                        }
+                    }
+                    tmem_st_wait();
+                }
+            }
+            // probabilities (relative to the running max), partial sums, P^T row t
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // heads 8c .. 8c+7 -> one 16-byte chunk of row t
+                uint32_t pk[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int h = 8 * c + 2 * j;
+                    const float p0 = s[h] == -INFINITY ? 0.f : exp2f(s[h] - sm->m_used[h]);
+                    const float p1 = s[h + 1] == -INFINITY ? 0.f : exp2f(s[h + 1] - sm->m_used[h + 1]);
+                    l_part[h] += p0;
+                    l_part[h + 1] += p1;
+                    pk[j] = pack_bf16x2(p0, p1);
+                }
+                *reinterpret_cast<uint4 *>(p_s + sw128_offset(t, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm->p_full);
+            done_tiles = i + 1;
+        }
+
+        // ------------------------------------------------------------ epilogue
+        // head sums: reduce the per-thread partials over the 128 token threads
+#pragma unroll
+        for (int h = 0; h < kHc; ++h) {
+            float v = l_part[h];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) sm->red[quad][h] = v;
+        }
+        bar_sync(1, 128);
+        if (t < kHc) sm->alpha[t] = sm->red[0][t] + sm->red[1][t] + sm->red[2][t] + sm->red[3][t];
+        bar_sync(1, 128);
+        const int hv = min(kHc, p.H - hg * kHc);  // real heads of this CTA
+        const bool have_o = done_tiles > 0 && !sm->abort &&
+                            mbar_wait(&sm->kv_empty, (done_tiles - 1) & 1, kWaitBudget);
+        tc_fence_after();
+#pragma unroll 1
+        for (int m = 0; m < 4; ++m) {
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                uint32_t v[32];
+                if (have_o) {
+                    tmem_ld32(lane_base + m * kHc + half * 32, v);
+                    tmem_ld_wait();
+                }
+                const int d = m * 128 + t;
+#pragma unroll 4
+                for (int j = 0; j < 32; ++j) {
+                    const int h = half * 32 + j;
+                    if (h >= hv) break;
+                    const float l = sm->alpha[h];
+                    const float o = (have_o && l > 0.f) ? __uint_as_float(v[j]) / l : 0.f;
+                    const int64_t row = (int64_t)r * p.H + hg * kHc + h;
+                    if (p.nsplit == 1)
+                        p.out[row * kDl + d] = __float2bfloat16_rn(o);
+                    else
+                        p.o_part[((int64_t)sp * p.R * p.H + row) * kDl + d] = o;
+                }
+            }
+        }
+        if (t < hv) {
+            const float l = sm->alpha[t];
+            const float lse = l > 0.f ? (sm->m_used[t] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            const int64_t row = (int64_t)r * p.H + hg * kHc + t;
+            if (p.nsplit == 1)
+                p.lse[row] = lse;
+            else
+                p.lse_part[(int64_t)sp * p.R * p.H + row] = lse;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// out[r, h, :] = sum_s exp(lse_s - lse) * o_s,  lse = ln sum_s exp(lse_s)
+__global__ void __launch_bounds__(128)
+sparse_mla_combine_kernel(const float *o_part, const float *lse_part, int nsplit, int64_t rows,
+                          __nv_bfloat16 *out, float *lse)
+{
+    const int64_t row = blockIdx.x;
+    float mx = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, lse_part[s * rows + row]);
+    float wsum = 0.f;
+    float w[16];
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+        w[s] = 0.f;
+        if (s < nsplit && mx != -INFINITY) w[s] = __expf(lse_part[s * rows + row] - mx);
+        wsum += w[s];
+    }
+    const int d = threadIdx.x * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < nsplit; ++s) {
+        const float4 v = *reinterpret_cast<const float4 *>(o_part + (s * rows + row) * kDl + d);
+        const float ws = wsum > 0.f ? w[s] / wsum : 0.f;
+        acc.x += ws * v.x; acc.y += ws * v.y; acc.z += ws * v.z; acc.w += ws * v.w;
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+    *reinterpret_cast<__nv_bfloat162 *>(out + row * kDl + d) = lo;
+    *reinterpret_cast<__nv_bfloat162 *>(out + row * kDl + d + 2) = hi;
+    if (threadIdx.x == 0) lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+}
+
+int num_sms()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return kNumSms;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return kNumSms;
+    return n;
+}
+
+// Splits of the top-k list per (row, head group): the fewest splits that give
+// the shortest schedule of CTA-tiles over the SMs (one CTA per SM).
+void choose_split(int R, int H, int topk, int &nsplit, int &tiles_per_split)
+{
+    const int tiles = (topk + kTok - 1) / kTok;
+    const int64_t base = (int64_t)R * ((H + kHc - 1) / kHc);
+    const int sms = num_sms();
+    int best_ns = 1;
+    int64_t best_cost = -1;
+    for (int ns = 1; ns <= 16 && ns <= tiles; ++ns) {
+        const int tps = (tiles + ns - 1) / ns;
+        const int ns_eff = (tiles + tps - 1) / tps;
+        if (ns_eff != ns) continue;
+        const int64_t units = base * ns;
+        const int64_t cost = ((units + sms - 1) / sms) * tps;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best_ns = ns;
+        }
+    }
+    nsplit = best_ns;
+    tiles_per_split = (tiles + best_ns - 1) / best_ns;
+}
+
+bool tc_applicable(nsa_dtype q_dtype, nsa_dtype kv_dtype, int H, int d_latent, int d_rope)
+{
+    return q_dtype == NSA_DT_BF16 && kv_dtype == NSA_DT_BF16 && d_latent == kDl && d_rope == kDr &&
+           (H % kHc == 0 || H < kHc) && H % 16 == 0;
+}
+
+}  // namespace
+
+size_t sparse_mla_tc_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int H, int d_latent, int d_rope,
+                                     int topk)
+{
+    if (!tc_applicable(q_dtype, kv_dtype, H, d_latent, d_rope) || R <= 0 || topk <= 0) return 0;
+    int ns, tps;
+    choose_split(R, H, topk, ns, tps);
+    if (ns <= 1) return 0;
+    return (size_t)ns * R * H * (kDl + 1) * sizeof(float);
+}
+
+nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const void *q_nope, int64_t nope_ld_r,
+                                    int64_t nope_ld_h, const void *q_rope, int64_t rope_ld_r, int64_t rope_ld_h,
+                                    const void *kv, int64_t num_slots, const int32_t *indices, int64_t indices_ld,
+                                    int R, int H, int d_latent, int d_rope, int topk, float sm_scale, void *out,
+                                    float *lse, void *workspace, int32_t *status, cudaStream_t stream)
+{
+    if (!tc_applicable(q_dtype, kv_dtype, H, d_latent, d_rope)) return NSA_ERR_UNSUPPORTED;
+    if (num_slots < 1 || num_slots > 2147483647LL) return NSA_ERR_UNSUPPORTED;
+    if (((uintptr_t)q_nope & 15) || ((uintptr_t)q_rope & 15) || ((uintptr_t)kv & 15)) return NSA_ERR_UNSUPPORTED;
+    if ((nope_ld_h * 2) % 16 || (nope_ld_r * 2) % 16 || (rope_ld_h * 2) % 16 || (rope_ld_r * 2) % 16)
+        return NSA_ERR_UNSUPPORTED;
+    if (R > 65535) return NSA_ERR_UNSUPPORTED;
+
+    CUtensorMap qn_map, qr_map, kv_map;
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!make_tma_3d(&qn_map, bf, q_nope, kDl, (uint64_t)H, (uint64_t)R, nope_ld_h * 2, nope_ld_r * 2, 64, kHc, 1,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tma_3d(&qr_map, bf, q_rope, kDr, (uint64_t)H, (uint64_t)R, rope_ld_h * 2, rope_ld_r * 2, 64, kHc, 1,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tma_2d(&kv_map, bf, kv, kDl + kDr, (uint64_t)num_slots, (kDl + kDr) * 2, 64, 1,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+        return NSA_ERR_CUDA;
+
+    MlaParams p;
+    p.indices = indices; p.indices_ld = indices_ld; p.R = R; p.H = H; p.topk = topk; p.num_slots = num_slots;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    choose_split(R, H, topk, p.nsplit, p.tiles_per_split);
+    p.out = (__nv_bfloat16 *)out; p.lse = lse; p.status = status;
+    p.o_part = nullptr; p.lse_part = nullptr;
+    if (p.nsplit > 1) {
+        if (!workspace) return NSA_ERR_INVALID_ARG;
+        p.o_part = (float *)workspace;
+        p.lse_part = p.o_part + (size_t)p.nsplit * R * H * kDl;
+    }
+    const size_t smem = 1024 + kQBytes + kKvBytes + sizeof(MlaShared);
+    auto kern = sparse_mla_tc_kernel;
+    NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    dim3 grid((unsigned)((H + kHc - 1) / kHc), (unsigned)p.nsplit, (unsigned)R);
+    kern<<<grid, kThreads, smem, stream>>>(qn_map, qr_map, kv_map, p);
+    NSA_CUDA_TRY(cudaGetLastError());
+    if (p.nsplit > 1) {
+        const int64_t rows = (int64_t)R * H;
+        sparse_mla_combine_kernel<<<(unsigned)rows, 128, 0, stream>>>(p.o_part, p.lse_part, p.nsplit, rows,
+                                                                     (__nv_bfloat16 *)out, lse);
+        NSA_CUDA_TRY(cudaGetLastError());
+    }
+    return NSA_OK;
+}
+
 }  // namespace nsa
