@@ -111,21 +111,53 @@ __device__ void build_rows(const MetaParams &p)
     for (int i = threadIdx.x; i <= p.R; i += blockDim.x) o.nsa_cu_seqlens_q[i] = i;
 }
 
-__device__ void copy_tables(const MetaParams &p, int64_t first, int64_t stride)
+constexpr int kSeg = 8192;  // page-table entries per copy segment
+
+// page_table_1[b, 0:W] = req_to_token[rpi[b], 0:W], and every page start also
+// lands in real_page_table.  Segments of kSeg entries are spread over the copy
+// blocks; 16-byte vector accesses when both rows are 16-byte aligned.
+__device__ void copy_tables(const MetaParams &p, int first_seg, int seg_stride)
 {
     const nsa_metadata_out &o = p.out;
-    const int64_t total = (int64_t)p.B * p.W;
-    for (int64_t e = first; e < total; e += stride) {
-        const int b = (int)(e / p.W);
-        const int t = (int)(e - (int64_t)b * p.W);
+    const int segs_per_row = (int)ceil_div(p.W, kSeg);
+    const int64_t total = (int64_t)p.B * segs_per_row;
+    for (int64_t g = first_seg; g < total; g += seg_stride) {
+        const int b = (int)(g / segs_per_row);
+        const int t0 = (int)(g - (int64_t)b * segs_per_row) * kSeg;
+        const int t1 = min(p.W, t0 + kSeg);
         const int32_t row = p.rpi[b];
         if (row < 0 || row >= p.pool_rows) {
-            if (t == 0) set_status(p.status, NSA_ERR_BOUNDS);
+            if (threadIdx.x == 0 && t0 == 0) set_status(p.status, NSA_ERR_BOUNDS);
             continue;
         }
-        const int32_t v = p.r2t[(int64_t)row * p.r2t_ld + t];
-        o.page_table_1[(int64_t)b * o.page_table_1_ld + t] = v;
-        if (t % p.ps == 0) o.real_page_table[(int64_t)b * o.real_page_table_ld + t / p.ps] = floor_div(v, p.ps);
+        const int32_t *src = p.r2t + (int64_t)row * p.r2t_ld;
+        int32_t *dst = o.page_table_1 + (int64_t)b * o.page_table_1_ld;
+        int32_t *real = o.real_page_table + (int64_t)b * o.real_page_table_ld;
+        const bool vec = (((uintptr_t)src | (uintptr_t)dst) & 15) == 0;
+        if (vec) {
+            for (int t = t0 + 4 * (int)threadIdx.x; t < t1; t += 4 * blockDim.x) {
+                if (t + 4 <= t1) {
+                    const int4 v = *reinterpret_cast<const int4 *>(src + t);
+                    *reinterpret_cast<int4 *>(dst + t) = v;
+                    const int32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if ((t + j) % p.ps == 0) real[(t + j) / p.ps] = floor_div(e[j], p.ps);
+                } else {
+                    for (int j = t; j < t1; ++j) {
+                        const int32_t v = src[j];
+                        dst[j] = v;
+                        if (j % p.ps == 0) real[j / p.ps] = floor_div(v, p.ps);
+                    }
+                }
+            }
+        } else {
+            for (int t = t0 + (int)threadIdx.x; t < t1; t += blockDim.x) {
+                const int32_t v = src[t];
+                dst[t] = v;
+                if (t % p.ps == 0) real[t / p.ps] = floor_div(v, p.ps);
+            }
+        }
     }
 }
 
@@ -134,8 +166,7 @@ __global__ void __launch_bounds__(kRowThreads) metadata_kernel(MetaParams p)
     if (blockIdx.x == 0) {
         build_rows(p);
     } else {
-        copy_tables(p, (int64_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x,
-                    (int64_t)(gridDim.x - 1) * blockDim.x);
+        copy_tables(p, (int)blockIdx.x - 1, (int)gridDim.x - 1);
     }
 }
 
@@ -177,9 +208,9 @@ extern "C" nsa_status nsa_metadata(nsa_mode mode, int B, int R, int W, int n_dra
     p.rpi = req_pool_indices_dev; p.r2t_ld = req_to_token_ld; p.pool_rows = pool_rows;
     p.out = *out; p.status = status_dev;
 
-    const int64_t total = (int64_t)B * W;
-    int64_t copy_blocks = ceil_div(total, (int64_t)kRowThreads * 4);
-    if (copy_blocks > 152 * 8) copy_blocks = 152 * 8;
+    const int64_t segs = (int64_t)B * ceil_div(W, kSeg);
+    int64_t copy_blocks = segs;
+    if (copy_blocks > 152 * 4) copy_blocks = 152 * 4;
     if (copy_blocks < 1) copy_blocks = 1;
     metadata_kernel<<<(unsigned)(1 + copy_blocks), kRowThreads, 0, (cudaStream_t)stream>>>(p);
     return launch_status();

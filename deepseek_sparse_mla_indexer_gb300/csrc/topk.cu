@@ -4,39 +4,44 @@
 // transformed page table directly"), [DSA] transform_index_page_table_* with
 // page size 1 and _pad_topk_indices (-1 padding).
 //
-// One block per row.  Scores are mapped to order-preserving 32-bit keys
-// (-0 folded onto +0, NaN below every number) and the exact k-th largest key
-// T is found by a most-significant-digit radix select (4 passes of 8 bits,
-// warp-aggregated shared-memory histograms).  A final ordered pass keeps
-// every key > T and the first (k - #{key > T}) keys == T in position order,
-// so ties go to the lower position and the output comes out sorted by
-// position without a sort.  Rows up to kCacheCap scores are read from HBM
-// once and kept in shared memory for the remaining passes.
+// One block of 1024 threads per row.  Scores become order-preserving 32-bit
+// keys (-0 folded onto +0, NaN below every number).  The k-th largest key is
+// located by a most-significant-digit radix select with 11/11/10-bit digits:
+// each pass histograms the keys that still match the chosen prefix (eight
+// replicated shared-memory histograms to spread atomic traffic), and a block
+// scan over the bins, largest digit first, picks the digit holding the k-th
+// key.  A pass stops the search early when the whole bin is selected.  A
+// final ordered pass keeps every key above the threshold and the first
+// (k - #above) keys equal to it, in position order, so ties go to the lower
+// position and the output comes out sorted without a sort.  Rows up to
+// kCacheCap scores are read from HBM once and kept in shared memory.
 #include "nsa_internal.cuh"
 
 namespace nsa {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kCacheCap = 48 * 1024;  // scores cached in shared memory (192 KB)
+constexpr int kBins = 2048;
+constexpr int kCopies = 8;
+constexpr int kCacheCap = 36 * 1024;  // 144 KB of keys
+constexpr int kItems = 4;             // consecutive elements per thread in the ordered pass
 
 __device__ __forceinline__ uint32_t order_key(float x)
 {
     uint32_t u = __float_as_uint(x);
-    if (x != x) return 0u;            // NaN ranks lowest
-    if ((u << 1) == 0u) u = 0u;       // -0 == +0
+    if (x != x) return 0u;       // NaN ranks lowest
+    if ((u << 1) == 0u) u = 0u;  // -0 == +0
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive block scan of one int per thread; returns the exclusive prefix and
-// writes the block total to *total (all threads see it after the call).
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_buf, uint32_t *total)
+// Inclusive block scan of one value per thread; *total receives the block sum.
+__device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *warp_buf, uint32_t *total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
     if (lane == 31) warp_buf[warp] = x;
@@ -45,16 +50,16 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_b
         uint32_t w = warp_buf[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
         warp_buf[lane] = w;
         if (lane == 31) *total = w;
     }
     __syncthreads();
-    uint32_t excl = x - v + (warp > 0 ? warp_buf[warp - 1] : 0u);
+    const uint32_t incl = x + (warp > 0 ? warp_buf[warp - 1] : 0u);
     __syncthreads();
-    return excl;
+    return incl;
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -63,11 +68,12 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
                       int max_row_len, int cache_cap, int32_t *indices, int64_t indices_ld,
                       int32_t *status)
 {
-    extern __shared__ uint32_t cache[];
-    __shared__ uint32_t hist[256];
+    extern __shared__ uint32_t dyn[];
+    uint32_t *hist = dyn;                      // [kCopies][kBins]
+    uint32_t *cache = dyn + kCopies * kBins;   // [cache_cap]
     __shared__ uint32_t warp_buf[32];
-    __shared__ uint32_t chunk_total;
-    __shared__ uint32_t sel_digit, sel_remaining;
+    __shared__ uint32_t total;
+    __shared__ uint32_t sel_digit, sel_need, sel_exact;
 
     const int r = blockIdx.x;
     const int L = row_len[r];
@@ -75,103 +81,106 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
     int32_t *out = indices + (int64_t)r * indices_ld;
     const int32_t *ptr = pt + (int64_t)b * pt_ld;
     const float *lg = logits + (int64_t)r * logits_ld;
+    const int tid = threadIdx.x;
 
     if (L < 0 || L > max_row_len) {
-        if (threadIdx.x == 0) set_status(status, NSA_ERR_BOUNDS);
-        for (int i = threadIdx.x; i < topk; i += kThreads) out[i] = -1;
+        if (tid == 0) set_status(status, NSA_ERR_BOUNDS);
+        for (int i = tid; i < topk; i += kThreads) out[i] = -1;
         return;
     }
     if (L <= topk) {
-        for (int i = threadIdx.x; i < topk; i += kThreads) out[i] = i < L ? ptr[i] : -1;
+        for (int i = tid; i < topk; i += kThreads) out[i] = i < L ? ptr[i] : -1;
         return;
     }
 
     const bool cached = L <= cache_cap;
-    if (cached) {
-        for (int i = threadIdx.x; i < L; i += kThreads) cache[i] = order_key(lg[i]);
-    }
+    if (cached)
+        for (int i = tid; i < L; i += kThreads) cache[i] = order_key(lg[i]);
     auto key_at = [&](int i) -> uint32_t { return cached ? cache[i] : order_key(lg[i]); };
 
-    uint32_t prefix = 0u, mask = 0u, remaining = (uint32_t)topk;
-    const int lane = threadIdx.x & 31;
+    // radix select: find the resolution shift S, value V and count `need`
+    // such that keys with (key >> S) > V are all selected and `need` of the
+    // keys with (key >> S) == V are selected (the lowest positions).
+    uint32_t prefix = 0u, need = (uint32_t)topk;
+    int S = 32;
+    uint32_t *myhist = hist + (size_t)((tid >> 5) % kCopies) * kBins;
 #pragma unroll 1
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < 256; i += kThreads) hist[i] = 0u;
+    for (int pass = 0; pass < 3; ++pass) {
+        const int width = pass < 2 ? 11 : 10;
+        const int shift = S - width;
+        const uint32_t dmask = (1u << width) - 1u;
+        for (int i = tid; i < kCopies * kBins; i += kThreads) hist[i] = 0u;
         __syncthreads();
-        for (int base = 0; base < L; base += kThreads) {
-            const int i = base + threadIdx.x;
-            bool in = false;
-            uint32_t digit = 0u;
-            if (i < L) {
-                const uint32_t k = key_at(i);
-                in = (k & mask) == prefix;
-                digit = (k >> shift) & 0xFFu;
-            }
-            // warp-aggregated histogram update: one atomic per distinct digit
-            const uint32_t active = __ballot_sync(0xffffffffu, in);
-            if (in) {
-                const uint32_t peers = __match_any_sync(active, digit);
-                if (lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+        for (int i = tid; i < L; i += kThreads) {
+            const uint32_t k = key_at(i);
+            if (S == 32 || (k >> S) == prefix) atomicAdd(&myhist[(k >> shift) & dmask], 1u);
+        }
+        __syncthreads();
+        // thread t owns digits (2047 - 2t) and (2046 - 2t): largest digits first
+        const int d_hi = kBins - 1 - 2 * tid, d_lo = d_hi - 1;
+        uint32_t c_hi = 0u, c_lo = 0u;
+        if (d_hi <= (int)dmask) {
+#pragma unroll
+            for (int c = 0; c < kCopies; ++c) c_hi += hist[c * kBins + d_hi];
+        }
+        if (d_lo >= 0 && d_lo <= (int)dmask) {
+#pragma unroll
+            for (int c = 0; c < kCopies; ++c) c_lo += hist[c * kBins + d_lo];
+        }
+        const uint32_t incl = block_incl_scan(c_hi + c_lo, warp_buf, &total);
+        const uint32_t excl = incl - c_hi - c_lo;
+        if (excl < need && need <= incl) {
+            if (excl + c_hi >= need) {
+                sel_digit = (uint32_t)d_hi;
+                sel_need = need - excl;
+                sel_exact = (c_hi == need - excl);
+            } else {
+                sel_digit = (uint32_t)d_lo;
+                sel_need = need - excl - c_hi;
+                sel_exact = (c_lo == need - excl - c_hi);
             }
         }
         __syncthreads();
-        if (threadIdx.x < 32) {
-            // lane l owns bins 255-8l .. 248-8l (largest digits first)
-            const int top = 255 - 8 * lane;
-            uint32_t c[8], s = 0u;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) { c[j] = hist[top - j]; s += c[j]; }
-            uint32_t incl = s;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const uint32_t excl = incl - s;
-            if (excl < remaining && remaining <= incl) {
-                uint32_t cum = excl;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (cum + c[j] >= remaining) {
-                        sel_digit = (uint32_t)(top - j);
-                        sel_remaining = remaining - cum;
-                        break;
-                    }
-                    cum += c[j];
-                }
-            }
-        }
+        prefix = (S == 32 ? 0u : (prefix << width)) | sel_digit;
+        need = sel_need;
+        S = shift;
+        const bool exact = sel_exact != 0u;
         __syncthreads();
-        prefix |= sel_digit << shift;
-        mask |= 0xFFu << shift;
-        remaining = sel_remaining;
-        __syncthreads();
+        if (exact) break;
     }
 
-    // Ordered selection: keys > T, then the first `remaining` keys == T.
-    const uint32_t T = prefix, need_eq = remaining;
+    // ordered selection: kItems consecutive positions per thread per round
     uint32_t gt_run = 0u, eq_run = 0u;
-    for (int base = 0; base < L; base += kThreads) {
-        const int i = base + threadIdx.x;
-        uint32_t k = 0u;
-        bool gt = false, eq = false;
-        if (i < L) {
-            k = key_at(i);
-            gt = k > T;
-            eq = k == T;
+    for (int base = 0; base < L; base += kThreads * kItems) {
+        const int i0 = base + tid * kItems;
+        uint32_t cls[kItems];  // 2 = above, 1 = equal, 0 = below / past the row
+        uint32_t n_gt = 0u, n_eq = 0u;
+#pragma unroll
+        for (int j = 0; j < kItems; ++j) {
+            cls[j] = 0u;
+            if (i0 + j < L) {
+                const uint32_t v = key_at(i0 + j) >> S;
+                cls[j] = v > prefix ? 2u : (v == prefix ? 1u : 0u);
+            }
+            n_gt += cls[j] == 2u;
+            n_eq += cls[j] == 1u;
         }
-        const uint32_t packed = (gt ? 1u : 0u) | (eq ? (1u << 16) : 0u);
-        const uint32_t excl = block_excl_scan(packed, warp_buf, &chunk_total);
-        const uint32_t gt_before = gt_run + (excl & 0xFFFFu);
-        const uint32_t eq_before = eq_run + (excl >> 16);
-        if (gt || (eq && eq_before < need_eq)) {
-            const uint32_t pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
-            out[pos] = ptr[i];
+        const uint32_t packed = n_gt | (n_eq << 16);
+        const uint32_t incl = block_incl_scan(packed, warp_buf, &total);
+        uint32_t gt_before = gt_run + ((incl - packed) & 0xFFFFu);
+        uint32_t eq_before = eq_run + ((incl - packed) >> 16);
+#pragma unroll
+        for (int j = 0; j < kItems; ++j) {
+            if (cls[j] == 2u) {
+                out[gt_before + (eq_before < need ? eq_before : need)] = ptr[i0 + j];
+                ++gt_before;
+            } else if (cls[j] == 1u) {
+                if (eq_before < need) out[gt_before + eq_before] = ptr[i0 + j];
+                ++eq_before;
+            }
         }
-        const uint32_t tot = chunk_total;
-        gt_run += tot & 0xFFFFu;
-        eq_run += tot >> 16;
-        __syncthreads();
+        gt_run += total & 0xFFFFu;
+        eq_run += total >> 16;
     }
 }
 
@@ -190,8 +199,8 @@ extern "C" nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits
     if (R == 0) return NSA_OK;
     if (!logits_dev || !row_len_dev || !row_to_req_dev || !page_table_1_dev || !indices_dev)
         return NSA_ERR_INVALID_ARG;
-    int cap = max_row_len > topk ? (max_row_len < kCacheCap ? max_row_len : kCacheCap) : 0;
-    const size_t smem = (size_t)cap * sizeof(uint32_t);
+    const int cap = max_row_len > topk ? (max_row_len < kCacheCap ? max_row_len : kCacheCap) : 0;
+    const size_t smem = (size_t)(kCopies * kBins + cap) * sizeof(uint32_t);
     NSA_CUDA_TRY(cudaFuncSetAttribute(topk_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)smem));
     topk_transform_kernel<<<(unsigned)R, kThreads, smem, (cudaStream_t)stream>>>(
