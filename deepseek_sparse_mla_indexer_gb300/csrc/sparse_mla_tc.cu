@@ -1,5 +1,5 @@
 // Tensor-core sparse MLA for d_qk = 576 (512 latent + 64 rope), d_v = 512,
-// bf16 query and bf16 KV rows.
+// bf16 query, bf16 or fp8 (e4m3 + per-128 fp32 scale + bf16 rope) KV rows.
 //
 // [DSA] _forward_flashmla_sparse / _forward_flashmla_kv call contract: for
 // each query row r and head h, attention over the KV rows listed in
@@ -8,23 +8,24 @@
 //
 // One CTA = one query row x 64 heads x one split of the top-k list.  Per tile
 // of 128 selected KV rows:
-//   1. warp 0 gathers the 128 rows into shared memory with TMA tile::gather4
-//      (9 column blocks of 64 bf16, 128-byte swizzled, K-major);
+//   1. loader warps (0, 2, 3) copy the 128 rows into shared memory with 16-byte
+//      cp.async (fp8 rows: loaded, dequantised to bf16 and stored), laid out as
+//      9 column blocks of 64 bf16, 128-byte swizzled, K-major -- and prefetch
+//      the next tile's rows into L2 so HBM keeps streaming during compute;
 //   2. warp 1 issues S^T[128 tok, 64 heads] = KV_tile . Q^T on tcgen05 (TMEM);
-//   3. warps 2..5 (one thread per token) run the online softmax over the
+//   3. warps 4..7 (one thread per token) run the online softmax over the
 //      token axis: a lazily refreshed running max per head (refreshed only
-//      when a score exceeds it by 2^8; the accumulator is rescaled then), the
+//      when a score exceeds it by 2^8; the TMEM accumulator is rescaled then),
 //      per-thread partial sums of the probabilities, and P^T written as bf16
 //      into the rope block (free once S^T is done) in the MN-major layout;
 //   4. warp 1 issues O^T[512 d, 64 heads] += V^T . P^T, reading the latent
 //      tile a second time as an MN-major operand (4 blocks of 128 d rows,
 //      256 TMEM columns).
-// At the end warps 2..5 normalise O^T by the head sums and write the output
+// At the end warps 4..7 normalise O^T by the head sums and write the output
 // (one split) or fp32 partials plus their log-sum-exp (several splits, merged
-// by sparse_mla_combine_kernel).
+// by sparse_mla_combine_kernel in a fixed order).
 #include "sparse_mla_tc.cuh"
 #include "sm100.cuh"
-#include "tma_host.h"
 
 namespace nsa {
 namespace {
@@ -40,14 +41,21 @@ constexpr uint32_t kQBlk = kHc * 128;
 constexpr uint32_t kKvBlk = kTok * 128;
 constexpr uint32_t kQBytes = kBlocks * kQBlk;
 constexpr uint32_t kKvBytes = kBlocks * kKvBlk;
-constexpr int kThreads = 192;
+constexpr int kThreads = 256;
+constexpr int kLoaders = 96;          // warps 0, 2, 3
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 256;
-constexpr float kRescale = 8.0f;  // log2 units
+constexpr float kRescale = 8.0f;      // log2 units
 constexpr long long kWaitBudget = 2000000000LL;
 constexpr int kNumSms = 152;
+constexpr int kBf16RowBytes = (kDl + kDr) * 2;        // 1152
+constexpr int kFp8RowBytes = kDl + 4 * (kDl / 128) + 2 * kDr;  // 656
 
 struct MlaParams {
+    const uint8_t *kv;
+    const uint16_t *q_nope;
+    const uint16_t *q_rope;
+    int64_t nope_ld_r, nope_ld_h, rope_ld_r, rope_ld_h;
     const int32_t *indices;
     int64_t indices_ld;
     int R, H, topk, nsplit, tiles_per_split;
@@ -82,9 +90,27 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_constant__ CUtensorMap qr_map,
-                     const __grid_constant__ CUtensorMap kv_map, MlaParams p)
+// Eight e4m3 codes (a 64-bit word) times `sc` -> four packed bf16 pairs.
+__device__ __forceinline__ void dequant8(uint2 w, float sc, uint32_t *dst4)
+{
+    const uint32_t words[2] = {w.x, w.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((words[i] >> (16 * j)) & 0xFFFFu);
+            const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+            dst4[2 * i + j] = pack_bf16x2(f.x * sc, f.y * sc);
+        }
+    }
+}
+
+// Loader-group barrier (warps 0, 2, 3).
+__device__ __forceinline__ void loader_sync() { bar_sync(2, kLoaders); }
+
+template <bool FP8>
+__global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -98,21 +124,19 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_co
     const int ntiles_all = (p.topk + kTok - 1) / kTok;
     const int t0 = sp * p.tiles_per_split;
     const int nt = max(0, min(t0 + p.tiles_per_split, ntiles_all) - t0);
+    const int64_t row_bytes = FP8 ? kFp8RowBytes : kBf16RowBytes;
 
     if (threadIdx.x == 0) {
-        mbar_init(&sm->q_full, 1);
-        mbar_init(&sm->kv_full, 1);
+        mbar_init(&sm->q_full, kLoaders);
+        mbar_init(&sm->kv_full, kLoaders);
         mbar_init(&sm->s_full, 1);
         mbar_init(&sm->p_full, 128);
         mbar_init(&sm->kv_empty, 1);
         mbar_init(&sm->done, 1);
         sm->abort = 0;
         fence_mbar_init();
-        prefetch_tensormap(&qn_map);
-        prefetch_tensormap(&qr_map);
-        prefetch_tensormap(&kv_map);
     }
-    if (threadIdx.x >= 64 && threadIdx.x < 128) sm->m_used[threadIdx.x - 64] = -INFINITY;
+    if (threadIdx.x >= 128 && threadIdx.x < 128 + kHc) sm->m_used[threadIdx.x - 128] = -INFINITY;
     if (warp == 1) {
         tmem_alloc(&sm->tmem_base, kTmemCols);
         tmem_relinquish();
@@ -122,42 +146,106 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_co
     tc_fence_after();
     const uint32_t tmem = sm->tmem_base;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- producer
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&sm->q_full, kQBytes);
-            for (int c = 0; c < 8; ++c) tma_load_3d(q_s + c * kQBlk, &qn_map, c * 64, hg * kHc, r, &sm->q_full);
-            tma_load_3d(q_s + 8 * kQBlk, &qr_map, 0, hg * kHc, r, &sm->q_full);
-        }
-        const int32_t *irow = p.indices + (int64_t)r * p.indices_ld;
-        int issued = 0;
-        for (int i = 0; i < nt && !sm->abort; ++i) {
-            if (i > 0) {
-                bool ok = mbar_wait(&sm->kv_empty, (i - 1) & 1, kWaitBudget);
-                if (!__all_sync(0xffffffffu, ok)) { if (lane == 0) fail(sm, p.status); break; }
+    if (warp == 0 || warp == 2 || warp == 3) {
+        // ---------------------------------------------------------------- loaders
+        const int lid = (warp == 0 ? 0 : warp - 1) * 32 + lane;  // 0 .. 95
+        // Q of this head group: 64 heads x (64 latent + 8 rope) 16-byte chunks
+        for (int q = lid; q < kHc * 72; q += kLoaders) {
+            const int h = q / 72, c = q - h * 72;
+            uint8_t *dst = q_s + (c >> 3) * kQBlk + sw128_offset(h, c & 7);
+            const int hh = hg * kHc + h;
+            if (hh < p.H) {
+                const uint16_t *src = c < 64 ? p.q_nope + r * p.nope_ld_r + hh * p.nope_ld_h + c * 8
+                                             : p.q_rope + r * p.rope_ld_r + hh * p.rope_ld_h + (c - 64) * 8;
+                cp_async16(dst, src);
+            } else {
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);  // padded head
             }
-            int y[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int pos = (t0 + i) * kTok + lane * 4 + j;
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        mbar_arrive(&sm->q_full);
+
+        const int32_t *irow = p.indices + (int64_t)r * p.indices_ld;
+        for (int i = 0; i < nt; ++i) {
+            if (i > 0) {
+                const bool ok = mbar_wait(&sm->kv_empty, (i - 1) & 1, kWaitBudget);
+                if (!ok) fail(sm, p.status);
+            }
+            if (bar_red_or(2, kLoaders, sm->abort != 0)) break;  // uniform over the loaders
+            for (int j = lid; j < kTok; j += kLoaders) {
+                const int pos = (t0 + i) * kTok + j;
                 int s = pos < p.topk ? irow[pos] : -1;
                 if (s < -1 || s >= p.num_slots) {
                     set_status(p.status, NSA_ERR_BOUNDS);
                     s = -1;
                 }
-                sm->idx[lane * 4 + j] = s;
-                y[j] = s < 0 ? 0 : s;  // masked rows read slot 0; the softmax zeroes them
+                sm->idx[j] = s;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(&sm->kv_full, kKvBytes);
+            loader_sync();
+            if (!FP8) {
+                for (int q = lid; q < kTok * 72; q += kLoaders) {
+                    const int row = q / 72, c = q - row * 72;
+                    const int s = sm->idx[row];
+                    const uint8_t *src = p.kv + (int64_t)(s < 0 ? 0 : s) * row_bytes + c * 16;
+                    cp_async16(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7), src);
+                }
+                cp_async_commit();
+            } else {
+                // rope: 8 chunks of bf16 per row, copied as is
+                for (int q = lid; q < kTok * 8; q += kLoaders) {
+                    const int row = q >> 3, c = q & 7;
+                    const int s = sm->idx[row];
+                    const uint8_t *src = p.kv + (int64_t)(s < 0 ? 0 : s) * row_bytes + kDl + 16 + c * 16;
+                    cp_async16(kv_s + 8 * kKvBlk + sw128_offset(row, c), src);
+                }
+                cp_async_commit();
+                // latent: 64 groups of 8 codes per row -> 64 bf16 chunks
 #pragma unroll 1
-            for (int c = 0; c < kBlocks; ++c)
-                tma_gather4(kv_s + c * kKvBlk + lane * 4 * 128, &kv_map, c * 64, y[0], y[1], y[2], y[3],
-                            &sm->kv_full);
-            issued = i + 1;
+                for (int q0 = lid; q0 < kTok * 64; q0 += 4 * kLoaders) {
+                    uint2 w[4];
+                    float sc[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int q = q0 + u * kLoaders;
+                        w[u] = make_uint2(0u, 0u);
+                        sc[u] = 0.f;
+                        if (q < kTok * 64) {
+                            const int row = q >> 6, c = q & 63;
+                            const int s = sm->idx[row];
+                            const uint8_t *rowp = p.kv + (int64_t)(s < 0 ? 0 : s) * row_bytes;
+                            w[u] = __ldg(reinterpret_cast<const uint2 *>(rowp + c * 8));
+                            sc[u] = __ldg(reinterpret_cast<const float *>(rowp + kDl) + (c >> 4));
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int q = q0 + u * kLoaders;
+                        if (q < kTok * 64) {
+                            const int row = q >> 6, c = q & 63;  // bf16 chunk c of the latent
+                            uint32_t d4[4];
+                            dequant8(w[u], sc[u], d4);
+                            *reinterpret_cast<uint4 *>(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7)) =
+                                make_uint4(d4[0], d4[1], d4[2], d4[3]);
+                        }
+                    }
+                }
+            }
+            // bring the next tile's rows into L2 while this one is consumed
+            if (i + 1 < nt) {
+                for (int j = lid; j < kTok; j += kLoaders) {
+                    const int pos = (t0 + i + 1) * kTok + j;
+                    if (pos < p.topk) {
+                        const int s = irow[pos];
+                        if (s >= 0 && s < p.num_slots) prefetch_l2_bulk(p.kv + (int64_t)s * row_bytes, (uint32_t)row_bytes);
+                    }
+                }
+            }
+            cp_async_wait_all();
+            fence_proxy_async_smem();
+            mbar_arrive(&sm->kv_full);
         }
-        // never leave with copies in flight
-        if (issued > 0) mbar_wait(&sm->kv_full, (issued - 1) & 1, kWaitBudget);
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -202,21 +290,25 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_co
         // ---------------------------------------------------------------- softmax / epilogue
         const int quad = warp & 3;
         const int t = quad * 32 + lane;  // token row of S^T; d row of each O^T block
+        const int et = threadIdx.x - 128;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         float l_part[kHc];
 #pragma unroll
         for (int h = 0; h < kHc; ++h) l_part[h] = 0.f;
         int done_tiles = 0;
         for (int i = 0; i < nt; ++i) {
-            bool ok = mbar_wait(&sm->kv_full, i & 1, kWaitBudget) && mbar_wait(&sm->s_full, i & 1, kWaitBudget);
-            if (bar_red_or(1, 128, !ok || sm->abort)) { if (!ok) fail(sm, p.status); break; }
+            const bool ok = mbar_wait(&sm->kv_full, i & 1, kWaitBudget) && mbar_wait(&sm->s_full, i & 1, kWaitBudget);
+            if (bar_red_or(1, 128, !ok || sm->abort)) {
+                if (!ok) fail(sm, p.status);
+                break;
+            }
             tc_fence_after();
             uint32_t sv[kHc];
             tmem_ld32(lane_base + kColS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
             tmem_ld32(lane_base + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
             tmem_ld_wait();
             const bool valid = sm->idx[t] >= 0;
-            float *s = reinterpret_cast<float *>(sv);  // scores in log2 units, in place
+            float s[kHc];
             bool exceed = false;
 #pragma unroll
             for (int h = 0; h < kHc; ++h) {
@@ -233,12 +325,12 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_co
                     if (lane == 0) sm->red[quad][h] = v;
                 }
                 bar_sync(1, 128);
-                if (t < kHc) {
-                    const float cm = fmaxf(fmaxf(sm->red[0][t], sm->red[1][t]), fmaxf(sm->red[2][t], sm->red[3][t]));
-                    const float mo = sm->m_used[t];
+                if (et < kHc) {
+                    const float cm = fmaxf(fmaxf(sm->red[0][et], sm->red[1][et]), fmaxf(sm->red[2][et], sm->red[3][et]));
+                    const float mo = sm->m_used[et];
                     const float mn = fmaxf(mo, cm);
-                    sm->alpha[t] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
-                    sm->m_used[t] = mn;
+                    sm->alpha[et] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
+                    sm->m_used[et] = mn;
                 }
                 bar_sync(1, 128);
 #pragma unroll
@@ -295,7 +387,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_co
             if (lane == 0) sm->red[quad][h] = v;
         }
         bar_sync(1, 128);
-        if (t < kHc) sm->alpha[t] = sm->red[0][t] + sm->red[1][t] + sm->red[2][t] + sm->red[3][t];
+        if (et < kHc) sm->alpha[et] = sm->red[0][et] + sm->red[1][et] + sm->red[2][et] + sm->red[3][et];
         bar_sync(1, 128);
         const int hv = min(kHc, p.H - hg * kHc);  // real heads of this CTA
         const bool have_o = done_tiles > 0 && !sm->abort &&
@@ -325,10 +417,10 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_co
                 }
             }
         }
-        if (t < hv) {
-            const float l = sm->alpha[t];
-            const float lse = l > 0.f ? (sm->m_used[t] + log2f(l)) * 0.69314718055994531f : -INFINITY;
-            const int64_t row = (int64_t)r * p.H + hg * kHc + t;
+        if (et < hv) {
+            const float l = sm->alpha[et];
+            const float lse = l > 0.f ? (sm->m_used[et] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            const int64_t row = (int64_t)r * p.H + hg * kHc + et;
             if (p.nsplit == 1)
                 p.lse[row] = lse;
             else
@@ -353,18 +445,14 @@ sparse_mla_combine_kernel(const float *o_part, const float *lse_part, int nsplit
     float mx = -INFINITY;
     for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, lse_part[s * rows + row]);
     float wsum = 0.f;
-    float w[16];
-#pragma unroll
-    for (int s = 0; s < 16; ++s) {
-        w[s] = 0.f;
-        if (s < nsplit && mx != -INFINITY) w[s] = __expf(lse_part[s * rows + row] - mx);
-        wsum += w[s];
-    }
+    for (int s = 0; s < nsplit; ++s)
+        if (mx != -INFINITY) wsum += __expf(lse_part[s * rows + row] - mx);
     const int d = threadIdx.x * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < nsplit; ++s) {
+        const float ls = lse_part[s * rows + row];
+        const float ws = (wsum > 0.f && ls != -INFINITY) ? __expf(ls - mx) / wsum : 0.f;
         const float4 v = *reinterpret_cast<const float4 *>(o_part + (s * rows + row) * kDl + d);
-        const float ws = wsum > 0.f ? w[s] / wsum : 0.f;
         acc.x += ws * v.x; acc.y += ws * v.y; acc.z += ws * v.z; acc.w += ws * v.w;
     }
     __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
@@ -381,22 +469,22 @@ int num_sms()
     return n;
 }
 
-// Splits of the top-k list per (row, head group): the fewest splits that give
-// the shortest schedule of CTA-tiles over the SMs (one CTA per SM).
+// Splits of the top-k list per (row, head group), one CTA per SM: minimise
+// waves x (tiles per split + per-CTA overhead), the overhead (Q load, TMEM
+// set-up, epilogue, partial write) counted as about one and a half tiles.
 void choose_split(int R, int H, int topk, int &nsplit, int &tiles_per_split)
 {
     const int tiles = (topk + kTok - 1) / kTok;
     const int64_t base = (int64_t)R * ((H + kHc - 1) / kHc);
     const int sms = num_sms();
     int best_ns = 1;
-    int64_t best_cost = -1;
+    double best_cost = -1.0;
     for (int ns = 1; ns <= 16 && ns <= tiles; ++ns) {
         const int tps = (tiles + ns - 1) / ns;
-        const int ns_eff = (tiles + tps - 1) / tps;
-        if (ns_eff != ns) continue;
+        if ((tiles + tps - 1) / tps != ns) continue;
         const int64_t units = base * ns;
-        const int64_t cost = ((units + sms - 1) / sms) * tps;
-        if (best_cost < 0 || cost < best_cost) {
+        const double cost = (double)((units + sms - 1) / sms) * (tps + (ns > 1 ? 1.5 : 1.0));
+        if (best_cost < 0.0 || cost < best_cost - 1e-9) {
             best_cost = cost;
             best_ns = ns;
         }
@@ -407,8 +495,8 @@ void choose_split(int R, int H, int topk, int &nsplit, int &tiles_per_split)
 
 bool tc_applicable(nsa_dtype q_dtype, nsa_dtype kv_dtype, int H, int d_latent, int d_rope)
 {
-    return q_dtype == NSA_DT_BF16 && kv_dtype == NSA_DT_BF16 && d_latent == kDl && d_rope == kDr &&
-           (H % kHc == 0 || H < kHc) && H % 16 == 0;
+    return q_dtype == NSA_DT_BF16 && (kv_dtype == NSA_DT_BF16 || kv_dtype == NSA_DT_E4M3) && d_latent == kDl &&
+           d_rope == kDr && (H % kHc == 0 || H < kHc) && H % 16 == 0;
 }
 
 }  // namespace
@@ -432,21 +520,14 @@ nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const
     if (!tc_applicable(q_dtype, kv_dtype, H, d_latent, d_rope)) return NSA_ERR_UNSUPPORTED;
     if (num_slots < 1 || num_slots > 2147483647LL) return NSA_ERR_UNSUPPORTED;
     if (((uintptr_t)q_nope & 15) || ((uintptr_t)q_rope & 15) || ((uintptr_t)kv & 15)) return NSA_ERR_UNSUPPORTED;
-    if ((nope_ld_h * 2) % 16 || (nope_ld_r * 2) % 16 || (rope_ld_h * 2) % 16 || (rope_ld_r * 2) % 16)
-        return NSA_ERR_UNSUPPORTED;
+    if (nope_ld_h % 8 || nope_ld_r % 8 || rope_ld_h % 8 || rope_ld_r % 8) return NSA_ERR_UNSUPPORTED;
     if (R > 65535) return NSA_ERR_UNSUPPORTED;
 
-    CUtensorMap qn_map, qr_map, kv_map;
-    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    if (!make_tma_3d(&qn_map, bf, q_nope, kDl, (uint64_t)H, (uint64_t)R, nope_ld_h * 2, nope_ld_r * 2, 64, kHc, 1,
-                     CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tma_3d(&qr_map, bf, q_rope, kDr, (uint64_t)H, (uint64_t)R, rope_ld_h * 2, rope_ld_r * 2, 64, kHc, 1,
-                     CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tma_2d(&kv_map, bf, kv, kDl + kDr, (uint64_t)num_slots, (kDl + kDr) * 2, 64, 1,
-                     CU_TENSOR_MAP_SWIZZLE_128B))
-        return NSA_ERR_CUDA;
-
     MlaParams p;
+    p.kv = (const uint8_t *)kv;
+    p.q_nope = (const uint16_t *)q_nope;
+    p.q_rope = (const uint16_t *)q_rope;
+    p.nope_ld_r = nope_ld_r; p.nope_ld_h = nope_ld_h; p.rope_ld_r = rope_ld_r; p.rope_ld_h = rope_ld_h;
     p.indices = indices; p.indices_ld = indices_ld; p.R = R; p.H = H; p.topk = topk; p.num_slots = num_slots;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     choose_split(R, H, topk, p.nsplit, p.tiles_per_split);
@@ -458,10 +539,16 @@ nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const
         p.lse_part = p.o_part + (size_t)p.nsplit * R * H * kDl;
     }
     const size_t smem = 1024 + kQBytes + kKvBytes + sizeof(MlaShared);
-    auto kern = sparse_mla_tc_kernel;
-    NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     dim3 grid((unsigned)((H + kHc - 1) / kHc), (unsigned)p.nsplit, (unsigned)R);
-    kern<<<grid, kThreads, smem, stream>>>(qn_map, qr_map, kv_map, p);
+    if (kv_dtype == NSA_DT_E4M3) {
+        auto kern = sparse_mla_tc_kernel<true>;
+        NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        kern<<<grid, kThreads, smem, stream>>>(p);
+    } else {
+        auto kern = sparse_mla_tc_kernel<false>;
+        NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        kern<<<grid, kThreads, smem, stream>>>(p);
+    }
     NSA_CUDA_TRY(cudaGetLastError());
     if (p.nsplit > 1) {
         const int64_t rows = (int64_t)R * H;
