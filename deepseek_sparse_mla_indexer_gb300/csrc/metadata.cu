@@ -135,19 +135,31 @@ __device__ void copy_tables(const MetaParams &p, int first_seg, int seg_stride)
         int32_t *real = o.real_page_table + (int64_t)b * o.real_page_table_ld;
         const bool vec = (((uintptr_t)src | (uintptr_t)dst) & 15) == 0;
         if (vec) {
-            for (int t = t0 + 4 * (int)threadIdx.x; t < t1; t += 4 * blockDim.x) {
-                if (t + 4 <= t1) {
-                    const int4 v = *reinterpret_cast<const int4 *>(src + t);
-                    *reinterpret_cast<int4 *>(dst + t) = v;
-                    const int32_t e[4] = {v.x, v.y, v.z, v.w};
+            // 4 independent 16-byte loads in flight per thread
+            constexpr int kU = 4;
+            for (int tb = t0 + 4 * (int)threadIdx.x; tb < t1; tb += 4 * kU * blockDim.x) {
+                int4 v[kU];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if ((t + j) % p.ps == 0) real[(t + j) / p.ps] = floor_div(e[j], p.ps);
-                } else {
-                    for (int j = t; j < t1; ++j) {
-                        const int32_t v = src[j];
-                        dst[j] = v;
-                        if (j % p.ps == 0) real[j / p.ps] = floor_div(v, p.ps);
+                for (int u = 0; u < kU; ++u) {
+                    const int t = tb + u * 4 * blockDim.x;
+                    if (t + 4 <= t1) v[u] = *reinterpret_cast<const int4 *>(src + t);
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int t = tb + u * 4 * blockDim.x;
+                    if (t + 4 <= t1) {
+                        *reinterpret_cast<int4 *>(dst + t) = v[u];
+                        const int32_t e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                        const int first = (p.ps - t % p.ps) % p.ps;  // offset of the first page start in t..t+3
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (j >= first && (j - first) % p.ps == 0) real[(t + j) / p.ps] = floor_div(e[j], p.ps);
+                    } else {
+                        for (int j = t; j < t1; ++j) {
+                            const int32_t x = src[j];
+                            dst[j] = x;
+                            if (j % p.ps == 0) real[j / p.ps] = floor_div(x, p.ps);
+                        }
                     }
                 }
             }

@@ -44,7 +44,8 @@ constexpr uint32_t kKvBytes = kBlocks * kKvBlk;
 constexpr int kThreads = 256;
 constexpr int kLoaders = 96;          // warps 0, 2, 3
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 256;
+constexpr uint32_t kColL = 256;   // ones . P^T: every lane holds the running head sums
+constexpr uint32_t kColS = 320;   // S^T accumulator
 constexpr float kRescale = 8.0f;      // log2 units
 constexpr long long kWaitBudget = 2000000000LL;
 constexpr int kNumSms = 152;
@@ -73,9 +74,9 @@ struct MlaShared {
     uint32_t tmem_base;
     volatile int abort;
     int idx[kTok];
-    float m_used[kHc];
-    float alpha[kHc];
     float red[4][kHc];
+    float alpha[kHc];
+    float m_run[kHc];  // running max per head, log2 units
 };
 
 __device__ __forceinline__ void fail(MlaShared *sm, int32_t *status)
@@ -117,7 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
     uint8_t *q_s = base;
     uint8_t *kv_s = base + kQBytes;
     uint8_t *p_s = kv_s + 8 * kKvBlk;  // P^T reuses the rope block
-    MlaShared *sm = (MlaShared *)(kv_s + kKvBytes);
+    uint8_t *ones_s = kv_s + kKvBytes;  // 1 KB of bf16 1.0: an all-ones MN-major operand atom
+    MlaShared *sm = (MlaShared *)(ones_s + 1024);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hg = blockIdx.x, sp = blockIdx.y, r = blockIdx.z;
@@ -136,7 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         sm->abort = 0;
         fence_mbar_init();
     }
-    if (threadIdx.x >= 128 && threadIdx.x < 128 + kHc) sm->m_used[threadIdx.x - 128] = -INFINITY;
+    if (threadIdx.x < 64) reinterpret_cast<uint4 *>(ones_s)[threadIdx.x] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
     if (warp == 1) {
         tmem_alloc(&sm->tmem_base, kTmemCols);
         tmem_relinquish();
@@ -168,21 +171,36 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         mbar_arrive(&sm->q_full);
 
         const int32_t *irow = p.indices + (int64_t)r * p.indices_ld;
+        // the indices of a tile are read one tile ahead (lanes own j = lid, lid + 96)
+        auto fetch_idx = [&](int tile, int (&v)[2]) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int j = lid + u * kLoaders;
+                const int pos = tile * kTok + j;
+                v[u] = (j < kTok && tile < t0 + nt && pos < p.topk) ? __ldg(irow + pos) : -1;
+            }
+        };
+        int cur[2], nxt[2];
+        fetch_idx(t0, cur);
         for (int i = 0; i < nt; ++i) {
             if (i > 0) {
                 const bool ok = mbar_wait(&sm->kv_empty, (i - 1) & 1, kWaitBudget);
                 if (!ok) fail(sm, p.status);
             }
             if (bar_red_or(2, kLoaders, sm->abort != 0)) break;  // uniform over the loaders
-            for (int j = lid; j < kTok; j += kLoaders) {
-                const int pos = (t0 + i) * kTok + j;
-                int s = pos < p.topk ? irow[pos] : -1;
-                if (s < -1 || s >= p.num_slots) {
-                    set_status(p.status, NSA_ERR_BOUNDS);
-                    s = -1;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int j = lid + u * kLoaders;
+                if (j < kTok) {
+                    int v = cur[u];
+                    if (v < -1 || v >= p.num_slots) {
+                        set_status(p.status, NSA_ERR_BOUNDS);
+                        v = -1;
+                    }
+                    sm->idx[j] = v;
                 }
-                sm->idx[j] = s;
             }
+            fetch_idx(t0 + i + 1, nxt);
             loader_sync();
             if (!FP8) {
                 for (int q = lid; q < kTok * 72; q += kLoaders) {
@@ -233,15 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                 }
             }
             // bring the next tile's rows into L2 while this one is consumed
-            if (i + 1 < nt) {
-                for (int j = lid; j < kTok; j += kLoaders) {
-                    const int pos = (t0 + i + 1) * kTok + j;
-                    if (pos < p.topk) {
-                        const int s = irow[pos];
-                        if (s >= 0 && s < p.num_slots) prefetch_l2_bulk(p.kv + (int64_t)s * row_bytes, (uint32_t)row_bytes);
-                    }
-                }
-            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (nxt[u] >= 0 && nxt[u] < p.num_slots)
+                    prefetch_l2_bulk(p.kv + (int64_t)nxt[u] * row_bytes, (uint32_t)row_bytes);
+            cur[0] = nxt[0];
+            cur[1] = nxt[1];
             cp_async_wait_all();
             fence_proxy_async_smem();
             mbar_arrive(&sm->kv_full);
@@ -281,6 +296,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                         mma_f16(tmem + m * kHc, ad, bd, idesc_o, (i > 0 || k > 0) ? 1u : 0u);
                     }
                 }
+                // head sums l[h] = sum_t P[t, h] in every lane: A = all-ones (one atom, zero strides)
+                const uint64_t ones_d = smem_desc(smem_u32(ones_s), 0, 0, kSwizzle128B);
+#pragma unroll
+                for (int k = 0; k < kTok / 16; ++k) {
+                    const uint64_t bd = smem_desc(p_addr + k * 2048, kKvBlk, 1024, kSwizzle128B);
+                    mma_f16(tmem + kColL, ones_d, bd, idesc_o, (i > 0 || k > 0) ? 1u : 0u);
+                }
                 mma_commit(&sm->kv_empty);
             }
             mma_commit(&sm->done);
@@ -292,9 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         const int t = quad * 32 + lane;  // token row of S^T; d row of each O^T block
         const int et = threadIdx.x - 128;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        float l_part[kHc];
-#pragma unroll
-        for (int h = 0; h < kHc; ++h) l_part[h] = 0.f;
+        if (et < kHc) sm->m_run[et] = -INFINITY;
+        bar_sync(1, 128);
+        const float4 *m_run4 = reinterpret_cast<const float4 *>(sm->m_run);
         int done_tiles = 0;
         for (int i = 0; i < nt; ++i) {
             const bool ok = mbar_wait(&sm->kv_full, i & 1, kWaitBudget) && mbar_wait(&sm->s_full, i & 1, kWaitBudget);
@@ -303,17 +325,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                 break;
             }
             tc_fence_after();
-            uint32_t sv[kHc];
-            tmem_ld32(lane_base + kColS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-            tmem_ld32(lane_base + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+            uint32_t sa[32], sb[32];
+            tmem_ld32(lane_base + kColS, sa);
+            tmem_ld32(lane_base + kColS + 32, sb);
             tmem_ld_wait();
             const bool valid = sm->idx[t] >= 0;
             float s[kHc];
             bool exceed = false;
 #pragma unroll
-            for (int h = 0; h < kHc; ++h) {
-                s[h] = valid ? __uint_as_float(sv[h]) * p.scale_log2 : -INFINITY;
-                exceed |= s[h] > sm->m_used[h] + kRescale;
+            for (int c = 0; c < kHc / 4; ++c) {
+                const float4 mr = m_run4[c];
+                const float mv[4] = {mr.x, mr.y, mr.z, mr.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int h = 4 * c + j;
+                    const uint32_t raw = h < 32 ? sa[h] : sb[h - 32];
+                    s[h] = valid ? __uint_as_float(raw) * p.scale_log2 : -INFINITY;
+                    exceed |= s[h] > mv[j] + kRescale;
+                }
             }
             if (bar_red_or(1, 128, exceed)) {
                 // refresh the running max of every head from this tile's column maxima
@@ -326,21 +355,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                 }
                 bar_sync(1, 128);
                 if (et < kHc) {
-                    const float cm = fmaxf(fmaxf(sm->red[0][et], sm->red[1][et]), fmaxf(sm->red[2][et], sm->red[3][et]));
-                    const float mo = sm->m_used[et];
+                    const int h = et;
+                    const float cm = fmaxf(fmaxf(sm->red[0][h], sm->red[1][h]), fmaxf(sm->red[2][h], sm->red[3][h]));
+                    const float mo = sm->m_run[h];
                     const float mn = fmaxf(mo, cm);
-                    sm->alpha[et] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
-                    sm->m_used[et] = mn;
+                    sm->alpha[h] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
+                    sm->m_run[h] = mn;
                 }
-                bar_sync(1, 128);
-#pragma unroll
-                for (int h = 0; h < kHc; ++h) l_part[h] *= sm->alpha[h];
+                bar_sync(1, 128);  // alpha[] and m_run[] complete; red[] free for the next refresh
                 if (i > 0) {
-                    // the previous tile's O^T must be complete before it is rescaled
+                    // the previous tile's O^T and head sums must be complete before they are rescaled
                     if (!mbar_wait(&sm->kv_empty, (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
                     tc_fence_after();
 #pragma unroll 1
-                    for (int m = 0; m < 4; ++m) {
+                    for (int m = 0; m < 5; ++m) {  // 4 O^T blocks + the head-sum block
 #pragma unroll 1
                         for (int half = 0; half < 2; ++half) {
                             uint32_t v[32];
@@ -356,17 +384,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                     tmem_st_wait();
                 }
             }
-            // probabilities (relative to the running max), partial sums, P^T row t
+            // probabilities relative to the running max, written as P^T row t (bf16)
 #pragma unroll
             for (int c = 0; c < 8; ++c) {  // heads 8c .. 8c+7 -> one 16-byte chunk of row t
+                const float4 ma = m_run4[2 * c], mb = m_run4[2 * c + 1];
+                const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
                 uint32_t pk[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int h = 8 * c + 2 * j;
-                    const float p0 = s[h] == -INFINITY ? 0.f : exp2f(s[h] - sm->m_used[h]);
-                    const float p1 = s[h + 1] == -INFINITY ? 0.f : exp2f(s[h + 1] - sm->m_used[h + 1]);
-                    l_part[h] += p0;
-                    l_part[h + 1] += p1;
+                    const float p0 = s[h] == -INFINITY ? 0.f : exp2f(s[h] - mv[2 * j]);
+                    const float p1 = s[h + 1] == -INFINITY ? 0.f : exp2f(s[h + 1] - mv[2 * j + 1]);
                     pk[j] = pack_bf16x2(p0, p1);
                 }
                 *reinterpret_cast<uint4 *>(p_s + sw128_offset(t, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -378,24 +406,19 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         }
 
         // ------------------------------------------------------------ epilogue
-        // head sums: reduce the per-thread partials over the 128 token threads
-#pragma unroll
-        for (int h = 0; h < kHc; ++h) {
-            float v = l_part[h];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) sm->red[quad][h] = v;
-        }
-        bar_sync(1, 128);
-        if (et < kHc) sm->alpha[et] = sm->red[0][et] + sm->red[1][et] + sm->red[2][et] + sm->red[3][et];
-        bar_sync(1, 128);
         const int hv = min(kHc, p.H - hg * kHc);  // real heads of this CTA
         const bool have_o = done_tiles > 0 && !sm->abort &&
                             mbar_wait(&sm->kv_empty, (done_tiles - 1) & 1, kWaitBudget);
         tc_fence_after();
+        uint32_t la[32], lb[32];  // head sums (identical in every lane)
+        if (have_o) {
+            tmem_ld32(lane_base + kColL, la);
+            tmem_ld32(lane_base + kColL + 32, lb);
+            tmem_ld_wait();
+        }
 #pragma unroll 1
         for (int m = 0; m < 4; ++m) {
-#pragma unroll 1
+#pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t v[32];
                 if (have_o) {
@@ -403,23 +426,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                     tmem_ld_wait();
                 }
                 const int d = m * 128 + t;
-#pragma unroll 4
+#pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int h = half * 32 + j;
-                    if (h >= hv) break;
-                    const float l = sm->alpha[h];
-                    const float o = (have_o && l > 0.f) ? __uint_as_float(v[j]) / l : 0.f;
-                    const int64_t row = (int64_t)r * p.H + hg * kHc + h;
-                    if (p.nsplit == 1)
-                        p.out[row * kDl + d] = __float2bfloat16_rn(o);
-                    else
-                        p.o_part[((int64_t)sp * p.R * p.H + row) * kDl + d] = o;
+                    if (h < hv) {
+                        const float l = have_o ? __uint_as_float(half ? lb[j] : la[j]) : 0.f;
+                        const float o = l > 0.f ? __uint_as_float(v[j]) / l : 0.f;
+                        const int64_t row = (int64_t)r * p.H + hg * kHc + h;
+                        if (p.nsplit == 1)
+                            p.out[row * kDl + d] = __float2bfloat16_rn(o);
+                        else
+                            p.o_part[((int64_t)sp * p.R * p.H + row) * kDl + d] = o;
+                    }
                 }
             }
         }
         if (et < hv) {
-            const float l = sm->alpha[et];
-            const float lse = l > 0.f ? (sm->m_used[et] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            const float mm = sm->m_run[et];
+            float l = 0.f;
+#pragma unroll
+            for (int h = 0; h < kHc; ++h)
+                if (h == et) l = have_o ? __uint_as_float(h < 32 ? la[h] : lb[h - 32]) : 0.f;
+            const float lse = l > 0.f ? (mm + log2f(l)) * 0.69314718055994531f : -INFINITY;
             const int64_t row = (int64_t)r * p.H + hg * kHc + et;
             if (p.nsplit == 1)
                 p.lse[row] = lse;
@@ -538,7 +566,7 @@ nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const
         p.o_part = (float *)workspace;
         p.lse_part = p.o_part + (size_t)p.nsplit * R * H * kDl;
     }
-    const size_t smem = 1024 + kQBytes + kKvBytes + sizeof(MlaShared);
+    const size_t smem = 1024 + kQBytes + kKvBytes + 1024 + sizeof(MlaShared);
     dim3 grid((unsigned)((H + kHc - 1) / kHc), (unsigned)p.nsplit, (unsigned)R);
     if (kv_dtype == NSA_DT_E4M3) {
         auto kern = sparse_mla_tc_kernel<true>;
