@@ -24,6 +24,8 @@
 // At the end warps 4..7 normalise O^T by the head sums and write the output
 // (one split) or fp32 partials plus their log-sum-exp (several splits, merged
 // by sparse_mla_combine_kernel in a fixed order).
+#include <cstddef>
+
 #include "sparse_mla_tc.cuh"
 #include "sm100.cuh"
 
@@ -69,15 +71,17 @@ struct MlaParams {
     int32_t *status;
 };
 
-struct MlaShared {
+struct __align__(16) MlaShared {
+    alignas(16) float m_run[kHc];  // running max per head, log2 units (read as float4)
+    alignas(16) float alpha[kHc];
+    alignas(16) float red[4][kHc];
+    alignas(16) int idx[kTok];
     uint64_t q_full, kv_full, s_full, p_full, kv_empty, done;
     uint32_t tmem_base;
     volatile int abort;
-    int idx[kTok];
-    float red[4][kHc];
-    float alpha[kHc];
-    float m_run[kHc];  // running max per head, log2 units
 };
+static_assert(offsetof(MlaShared, m_run) % 16 == 0, "m_run is read with 16-byte loads");
+static_assert(offsetof(MlaShared, q_full) % 8 == 0, "mbarriers need 8-byte alignment");
 
 __device__ __forceinline__ void fail(MlaShared *sm, int32_t *status)
 {
