@@ -287,6 +287,35 @@ nsa_status nsa_sparse_mla(nsa_dtype q_dtype, nsa_dtype kv_dtype, const void *q_n
 size_t nsa_sparse_mla_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int H,
                                       int d_latent, int d_rope, int topk);
 
+/*
+ * nsa_sparse_mla without a caller workspace, for callers that cannot allocate
+ * device memory when they call in -- for example a plug-in inside a host
+ * framework that owns all device memory and gives the plug-in no allocator,
+ * or a serving loop that allows no allocation after start-up so that its
+ * memory footprint stays fixed.  The pages have no counterpart: they always
+ * run with framework-allocated buffers.
+ *
+ * Same arguments, semantics and results as nsa_sparse_mla, minus the
+ * workspace.  The split-KV scratch is one fixed 32 MiB device array inside
+ * this library (every GPU that loads the library holds it until the process
+ * exits); this call allocates nothing.  The first call on a device looks up
+ * that array's device address (cudaGetSymbolAddress) and caches it, so make
+ * the first call on each device before any stream capture.  All calls share
+ * the array: calls that may overlap on the GPU (other streams, other host
+ * threads) race on it and must be serialised by the caller.  Nothing in the
+ * array needs to start at zero.
+ * Returns NSA_ERR_UNSUPPORTED when nsa_sparse_mla_workspace_bytes() for the
+ * problem exceeds 32 MiB (use nsa_sparse_mla with a workspace instead);
+ * otherwise the same status codes as nsa_sparse_mla.
+ */
+nsa_status nsa_sparse_mla_noalloc(nsa_dtype q_dtype, nsa_dtype kv_dtype, const void *q_nope_dev,
+                                  int64_t nope_ld_r, int64_t nope_ld_h, const void *q_rope_dev,
+                                  int64_t rope_ld_r, int64_t rope_ld_h, const void *kv_dev,
+                                  int64_t num_slots, const int32_t *indices_dev, int64_t indices_ld,
+                                  int R, int H, int d_latent, int d_rope, int topk, float sm_scale,
+                                  void *out_dev, float *lse_dev, int32_t *status_dev,
+                                  nsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
