@@ -76,12 +76,15 @@ struct __align__(16) MlaShared {
     alignas(16) float alpha[kHc];
     alignas(16) float red[4][kHc];
     alignas(16) int idx[kTok];
-    uint64_t q_full, kv_full, s_full, p_full, kv_empty, done;
+    const uint8_t *rowbase[kTok];  // KV row of each token of the tile (slot 0 for masked ones)
+    uint64_t kvb_full[5];          // block pair m of the tile landed (m = 4: rope block)
+    uint64_t o_done[5];            // O^T block m of the tile done (m = 4: every MMA of the tile)
+    uint64_t q_full, s_full, p_full, done;
     uint32_t tmem_base;
     volatile int abort;
 };
 static_assert(offsetof(MlaShared, m_run) % 16 == 0, "m_run is read with 16-byte loads");
-static_assert(offsetof(MlaShared, q_full) % 8 == 0, "mbarriers need 8-byte alignment");
+static_assert(offsetof(MlaShared, kvb_full) % 8 == 0, "mbarriers need 8-byte alignment");
 
 __device__ __forceinline__ void fail(MlaShared *sm, int32_t *status)
 {
@@ -134,10 +137,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 
     if (threadIdx.x == 0) {
         mbar_init(&sm->q_full, kLoaders);
-        mbar_init(&sm->kv_full, kLoaders);
+        for (int m = 0; m < 5; ++m) {
+            mbar_init(&sm->kvb_full[m], kLoaders);
+            mbar_init(&sm->o_done[m], 1);
+        }
         mbar_init(&sm->s_full, 1);
         mbar_init(&sm->p_full, 128);
-        mbar_init(&sm->kv_empty, 1);
         mbar_init(&sm->done, 1);
         sm->abort = 0;
         fence_mbar_init();
@@ -184,13 +189,55 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                 v[u] = (j < kTok && tile < t0 + nt && pos < p.topk) ? __ldg(irow + pos) : -1;
             }
         };
+        // Block pair m of the tile: latent blocks 2m, 2m+1 (m < 4) or the rope block (m = 4).
+        auto issue_pair = [&](int m) {
+            if (m == 4) {
+                for (int q = lid; q < kTok * 8; q += kLoaders) {
+                    const int row = q >> 3, c = q & 7;
+                    cp_async16(kv_s + 8 * kKvBlk + sw128_offset(row, c),
+                               sm->rowbase[row] + (FP8 ? kDl + 16 : 2 * kDl) + c * 16);
+                }
+            } else if (!FP8) {
+                for (int q = lid; q < kTok * 16; q += kLoaders) {
+                    const int row = q >> 4, c = 16 * m + (q & 15);
+                    cp_async16(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7), sm->rowbase[row] + c * 16);
+                }
+            } else {
+                // 16 groups of 8 e4m3 codes per row (dims 128m .. 128m+127, one scale)
+#pragma unroll 1
+                for (int q0 = lid; q0 < kTok * 16; q0 += 4 * kLoaders) {
+                    uint2 w[4];
+                    float sc[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int q = q0 + u * kLoaders;
+                        w[u] = make_uint2(0u, 0u);
+                        sc[u] = 0.f;
+                        if (q < kTok * 16) {
+                            const uint8_t *rowp = sm->rowbase[q >> 4];
+                            w[u] = __ldg(reinterpret_cast<const uint2 *>(rowp + (16 * m + (q & 15)) * 8));
+                            sc[u] = __ldg(reinterpret_cast<const float *>(rowp + kDl) + m);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int q = q0 + u * kLoaders;
+                        if (q < kTok * 16) {
+                            const int row = q >> 4, c = 16 * m + (q & 15);
+                            uint32_t d4[4];
+                            dequant8(w[u], sc[u], d4);
+                            *reinterpret_cast<uint4 *>(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7)) =
+                                make_uint4(d4[0], d4[1], d4[2], d4[3]);
+                        }
+                    }
+                }
+            }
+        };
         int cur[2], nxt[2];
         fetch_idx(t0, cur);
         for (int i = 0; i < nt; ++i) {
-            if (i > 0) {
-                const bool ok = mbar_wait(&sm->kv_empty, (i - 1) & 1, kWaitBudget);
-                if (!ok) fail(sm, p.status);
-            }
+            // block pair 0 (and the token table) is free once the previous tile's O^T block 0 is done
+            if (i > 0 && !mbar_wait(&sm->o_done[0], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
             if (bar_red_or(2, kLoaders, sm->abort != 0)) break;  // uniform over the loaders
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -202,56 +249,23 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                         v = -1;
                     }
                     sm->idx[j] = v;
+                    sm->rowbase[j] = p.kv + (int64_t)(v < 0 ? 0 : v) * row_bytes;  // masked rows read slot 0
                 }
             }
             fetch_idx(t0 + i + 1, nxt);
             loader_sync();
-            if (!FP8) {
-                for (int q = lid; q < kTok * 72; q += kLoaders) {
-                    const int row = q / 72, c = q - row * 72;
-                    const int s = sm->idx[row];
-                    const uint8_t *src = p.kv + (int64_t)(s < 0 ? 0 : s) * row_bytes + c * 16;
-                    cp_async16(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7), src);
-                }
-                cp_async_commit();
-            } else {
-                // rope: 8 chunks of bf16 per row, copied as is
-                for (int q = lid; q < kTok * 8; q += kLoaders) {
-                    const int row = q >> 3, c = q & 7;
-                    const int s = sm->idx[row];
-                    const uint8_t *src = p.kv + (int64_t)(s < 0 ? 0 : s) * row_bytes + kDl + 16 + c * 16;
-                    cp_async16(kv_s + 8 * kKvBlk + sw128_offset(row, c), src);
-                }
-                cp_async_commit();
-                // latent: 64 groups of 8 codes per row -> 64 bf16 chunks
 #pragma unroll 1
-                for (int q0 = lid; q0 < kTok * 64; q0 += 4 * kLoaders) {
-                    uint2 w[4];
-                    float sc[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int q = q0 + u * kLoaders;
-                        w[u] = make_uint2(0u, 0u);
-                        sc[u] = 0.f;
-                        if (q < kTok * 64) {
-                            const int row = q >> 6, c = q & 63;
-                            const int s = sm->idx[row];
-                            const uint8_t *rowp = p.kv + (int64_t)(s < 0 ? 0 : s) * row_bytes;
-                            w[u] = __ldg(reinterpret_cast<const uint2 *>(rowp + c * 8));
-                            sc[u] = __ldg(reinterpret_cast<const float *>(rowp + kDl) + (c >> 4));
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int q = q0 + u * kLoaders;
-                        if (q < kTok * 64) {
-                            const int row = q >> 6, c = q & 63;  // bf16 chunk c of the latent
-                            uint32_t d4[4];
-                            dequant8(w[u], sc[u], d4);
-                            *reinterpret_cast<uint4 *>(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7)) =
-                                make_uint4(d4[0], d4[1], d4[2], d4[3]);
-                        }
-                    }
+            for (int m = 0; m < 5; ++m) {
+                if (m > 0 && i > 0 && !mbar_wait(&sm->o_done[m], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
+                issue_pair(m);
+                cp_async_commit();
+                if (FP8 && m < 4) {  // dequantised pairs are written with plain stores
+                    fence_proxy_async_smem();
+                    mbar_arrive(&sm->kvb_full[m]);
+                } else if (!FP8 && m > 0) {
+                    cp_async_wait_group<1>();
+                    fence_proxy_async_smem();
+                    mbar_arrive(&sm->kvb_full[m - 1]);
                 }
             }
             // bring the next tile's rows into L2 while this one is consumed
@@ -261,9 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                     prefetch_l2_bulk(p.kv + (int64_t)nxt[u] * row_bytes, (uint32_t)row_bytes);
             cur[0] = nxt[0];
             cur[1] = nxt[1];
-            cp_async_wait_all();
+            cp_async_wait_group<0>();
             fence_proxy_async_smem();
-            mbar_arrive(&sm->kv_full);
+            mbar_arrive(&sm->kvb_full[4]);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
@@ -271,25 +285,31 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             const uint32_t idesc_s = instr_desc(1, 1, 0, 0, kTok, kHc);  // bf16, K-major A and B
             const uint32_t idesc_o = instr_desc(1, 1, 1, 1, 128, kHc);   // bf16, MN-major A and B
             const uint32_t q_addr = smem_u32(q_s), kv_addr = smem_u32(kv_s), p_addr = smem_u32(p_s);
+            const uint64_t ones_d = smem_desc(smem_u32(ones_s), 0, 0, kSwizzle128B);
             bool ok = mbar_wait(&sm->q_full, 0, kWaitBudget);
             if (!ok) fail(sm, p.status);
             for (int i = 0; i < nt && ok && !sm->abort; ++i) {
-                if (!mbar_wait(&sm->kv_full, i & 1, kWaitBudget)) { fail(sm, p.status); break; }
-                tc_fence_after();
-                // S^T = KV (128 x 576) . Q^T (576 x 64)
+                // S^T = KV (128 x 576) . Q^T (576 x 64), block pair by block pair as they land
 #pragma unroll 1
-                for (int c = 0; c < kBlocks; ++c) {
+                for (int m = 0; m < 5 && ok; ++m) {
+                    if (!mbar_wait(&sm->kvb_full[m], i & 1, kWaitBudget)) { fail(sm, p.status); ok = false; break; }
+                    tc_fence_after();
+                    const int c0 = m < 4 ? 2 * m : 8, nc = m < 4 ? 2 : 1;
+                    for (int c = c0; c < c0 + nc; ++c) {
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t ad = smem_desc(kv_addr + c * kKvBlk + ks * 32, 16, 1024, kSwizzle128B);
-                        const uint64_t bd = smem_desc(q_addr + c * kQBlk + ks * 32, 16, 1024, kSwizzle128B);
-                        mma_f16(tmem + kColS, ad, bd, idesc_s, (c | ks) != 0);
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t ad = smem_desc(kv_addr + c * kKvBlk + ks * 32, 16, 1024, kSwizzle128B);
+                            const uint64_t bd = smem_desc(q_addr + c * kQBlk + ks * 32, 16, 1024, kSwizzle128B);
+                            mma_f16(tmem + kColS, ad, bd, idesc_s, (c | ks) != 0);
+                        }
                     }
                 }
+                if (!ok) break;
                 mma_commit(&sm->s_full);
                 if (!mbar_wait(&sm->p_full, i & 1, kWaitBudget)) { fail(sm, p.status); break; }
                 tc_fence_after();
-                // O^T[d, h] += sum_t V[t, d] P[t, h]: A = V^T (MN-major), B = P^T (MN-major)
+                // O^T[d, h] += sum_t V[t, d] P[t, h]: A = V^T (MN-major), B = P^T (MN-major);
+                // each finished block pair goes back to the loaders at once
 #pragma unroll 1
                 for (int m = 0; m < 4; ++m) {
 #pragma unroll
@@ -299,15 +319,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                         const uint64_t bd = smem_desc(p_addr + k * 2048, kKvBlk, 1024, kSwizzle128B);
                         mma_f16(tmem + m * kHc, ad, bd, idesc_o, (i > 0 || k > 0) ? 1u : 0u);
                     }
+                    mma_commit(&sm->o_done[m]);
                 }
                 // head sums l[h] = sum_t P[t, h] in every lane: A = all-ones (one atom, zero strides)
-                const uint64_t ones_d = smem_desc(smem_u32(ones_s), 0, 0, kSwizzle128B);
 #pragma unroll
                 for (int k = 0; k < kTok / 16; ++k) {
                     const uint64_t bd = smem_desc(p_addr + k * 2048, kKvBlk, 1024, kSwizzle128B);
                     mma_f16(tmem + kColL, ones_d, bd, idesc_o, (i > 0 || k > 0) ? 1u : 0u);
                 }
-                mma_commit(&sm->kv_empty);
+                mma_commit(&sm->o_done[4]);
             }
             mma_commit(&sm->done);
             mbar_wait(&sm->done, 0, kWaitBudget);
@@ -323,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         const float4 *m_run4 = reinterpret_cast<const float4 *>(sm->m_run);
         int done_tiles = 0;
         for (int i = 0; i < nt; ++i) {
-            const bool ok = mbar_wait(&sm->kv_full, i & 1, kWaitBudget) && mbar_wait(&sm->s_full, i & 1, kWaitBudget);
+            const bool ok = mbar_wait(&sm->kvb_full[0], i & 1, kWaitBudget) && mbar_wait(&sm->s_full, i & 1, kWaitBudget);
             if (bar_red_or(1, 128, !ok || sm->abort)) {
                 if (!ok) fail(sm, p.status);
                 break;
@@ -369,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                 bar_sync(1, 128);  // alpha[] and m_run[] complete; red[] free for the next refresh
                 if (i > 0) {
                     // the previous tile's O^T and head sums must be complete before they are rescaled
-                    if (!mbar_wait(&sm->kv_empty, (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
+                    if (!mbar_wait(&sm->o_done[4], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
                     tc_fence_after();
 #pragma unroll 1
                     for (int m = 0; m < 5; ++m) {  // 4 O^T blocks + the head-sum block
@@ -412,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         // ------------------------------------------------------------ epilogue
         const int hv = min(kHc, p.H - hg * kHc);  // real heads of this CTA
         const bool have_o = done_tiles > 0 && !sm->abort &&
-                            mbar_wait(&sm->kv_empty, (done_tiles - 1) & 1, kWaitBudget);
+                            mbar_wait(&sm->o_done[4], (done_tiles - 1) & 1, kWaitBudget);
         tc_fence_after();
         uint32_t la[32], lb[32];  // head sums (identical in every lane)
         if (have_o) {
