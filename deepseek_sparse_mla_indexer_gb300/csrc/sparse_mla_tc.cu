@@ -44,7 +44,7 @@ constexpr uint32_t kKvBlk = kTok * 128;
 constexpr uint32_t kQBytes = kBlocks * kQBlk;
 constexpr uint32_t kKvBytes = kBlocks * kKvBlk;
 constexpr int kThreads = 256;
-constexpr int kLoaders = 96;          // warps 0, 2, 3
+constexpr int kWorkers = 224;         // warps 0, 2..7 load; warps 4..7 also run the softmax
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColL = 256;   // ones . P^T: every lane holds the running head sums
 constexpr uint32_t kColS = 320;   // S^T accumulator
@@ -114,8 +114,8 @@ __device__ __forceinline__ void dequant8(uint2 w, float sc, uint32_t *dst4)
     }
 }
 
-// Loader-group barrier (warps 0, 2, 3).
-__device__ __forceinline__ void loader_sync() { bar_sync(2, kLoaders); }
+// Worker-group barrier (warps 0, 2..7).
+__device__ __forceinline__ void worker_sync() { bar_sync(2, kWorkers); }
 
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
@@ -136,9 +136,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
     const int64_t row_bytes = FP8 ? kFp8RowBytes : kBf16RowBytes;
 
     if (threadIdx.x == 0) {
-        mbar_init(&sm->q_full, kLoaders);
+        mbar_init(&sm->q_full, kWorkers);
         for (int m = 0; m < 5; ++m) {
-            mbar_init(&sm->kvb_full[m], kLoaders);
+            mbar_init(&sm->kvb_full[m], kWorkers);
             mbar_init(&sm->o_done[m], 1);
         }
         mbar_init(&sm->s_full, 1);
@@ -158,128 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
     tc_fence_after();
     const uint32_t tmem = sm->tmem_base;
 
-    if (warp == 0 || warp == 2 || warp == 3) {
-        // ---------------------------------------------------------------- loaders
-        const int lid = (warp == 0 ? 0 : warp - 1) * 32 + lane;  // 0 .. 95
-        // Q of this head group: 64 heads x (64 latent + 8 rope) 16-byte chunks
-        for (int q = lid; q < kHc * 72; q += kLoaders) {
-            const int h = q / 72, c = q - h * 72;
-            uint8_t *dst = q_s + (c >> 3) * kQBlk + sw128_offset(h, c & 7);
-            const int hh = hg * kHc + h;
-            if (hh < p.H) {
-                const uint16_t *src = c < 64 ? p.q_nope + r * p.nope_ld_r + hh * p.nope_ld_h + c * 8
-                                             : p.q_rope + r * p.rope_ld_r + hh * p.rope_ld_h + (c - 64) * 8;
-                cp_async16(dst, src);
-            } else {
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);  // padded head
-            }
-        }
-        cp_async_commit();
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        mbar_arrive(&sm->q_full);
-
-        const int32_t *irow = p.indices + (int64_t)r * p.indices_ld;
-        // the indices of a tile are read one tile ahead (lanes own j = lid, lid + 96)
-        auto fetch_idx = [&](int tile, int (&v)[2]) {
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int j = lid + u * kLoaders;
-                const int pos = tile * kTok + j;
-                v[u] = (j < kTok && tile < t0 + nt && pos < p.topk) ? __ldg(irow + pos) : -1;
-            }
-        };
-        // Block pair m of the tile: latent blocks 2m, 2m+1 (m < 4) or the rope block (m = 4).
-        auto issue_pair = [&](int m) {
-            if (m == 4) {
-                for (int q = lid; q < kTok * 8; q += kLoaders) {
-                    const int row = q >> 3, c = q & 7;
-                    cp_async16(kv_s + 8 * kKvBlk + sw128_offset(row, c),
-                               sm->rowbase[row] + (FP8 ? kDl + 16 : 2 * kDl) + c * 16);
-                }
-            } else if (!FP8) {
-                for (int q = lid; q < kTok * 16; q += kLoaders) {
-                    const int row = q >> 4, c = 16 * m + (q & 15);
-                    cp_async16(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7), sm->rowbase[row] + c * 16);
-                }
-            } else {
-                // 16 groups of 8 e4m3 codes per row (dims 128m .. 128m+127, one scale)
-#pragma unroll 1
-                for (int q0 = lid; q0 < kTok * 16; q0 += 4 * kLoaders) {
-                    uint2 w[4];
-                    float sc[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int q = q0 + u * kLoaders;
-                        w[u] = make_uint2(0u, 0u);
-                        sc[u] = 0.f;
-                        if (q < kTok * 16) {
-                            const uint8_t *rowp = sm->rowbase[q >> 4];
-                            w[u] = __ldg(reinterpret_cast<const uint2 *>(rowp + (16 * m + (q & 15)) * 8));
-                            sc[u] = __ldg(reinterpret_cast<const float *>(rowp + kDl) + m);
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int q = q0 + u * kLoaders;
-                        if (q < kTok * 16) {
-                            const int row = q >> 4, c = 16 * m + (q & 15);
-                            uint32_t d4[4];
-                            dequant8(w[u], sc[u], d4);
-                            *reinterpret_cast<uint4 *>(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7)) =
-                                make_uint4(d4[0], d4[1], d4[2], d4[3]);
-                        }
-                    }
-                }
-            }
-        };
-        int cur[2], nxt[2];
-        fetch_idx(t0, cur);
-        for (int i = 0; i < nt; ++i) {
-            // block pair 0 (and the token table) is free once the previous tile's O^T block 0 is done
-            if (i > 0 && !mbar_wait(&sm->o_done[0], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
-            if (bar_red_or(2, kLoaders, sm->abort != 0)) break;  // uniform over the loaders
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int j = lid + u * kLoaders;
-                if (j < kTok) {
-                    int v = cur[u];
-                    if (v < -1 || v >= p.num_slots) {
-                        set_status(p.status, NSA_ERR_BOUNDS);
-                        v = -1;
-                    }
-                    sm->idx[j] = v;
-                    sm->rowbase[j] = p.kv + (int64_t)(v < 0 ? 0 : v) * row_bytes;  // masked rows read slot 0
-                }
-            }
-            fetch_idx(t0 + i + 1, nxt);
-            loader_sync();
-#pragma unroll 1
-            for (int m = 0; m < 5; ++m) {
-                if (m > 0 && i > 0 && !mbar_wait(&sm->o_done[m], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
-                issue_pair(m);
-                cp_async_commit();
-                if (FP8 && m < 4) {  // dequantised pairs are written with plain stores
-                    fence_proxy_async_smem();
-                    mbar_arrive(&sm->kvb_full[m]);
-                } else if (!FP8 && m > 0) {
-                    cp_async_wait_group<1>();
-                    fence_proxy_async_smem();
-                    mbar_arrive(&sm->kvb_full[m - 1]);
-                }
-            }
-            // bring the next tile's rows into L2 while this one is consumed
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-                if (nxt[u] >= 0 && nxt[u] < p.num_slots)
-                    prefetch_l2_bulk(p.kv + (int64_t)nxt[u] * row_bytes, (uint32_t)row_bytes);
-            cur[0] = nxt[0];
-            cur[1] = nxt[1];
-            cp_async_wait_group<0>();
-            fence_proxy_async_smem();
-            mbar_arrive(&sm->kvb_full[4]);
-        }
-    } else if (warp == 1) {
+    if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc_s = instr_desc(1, 1, 0, 0, kTok, kHc);  // bf16, K-major A and B
@@ -333,150 +212,274 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             mbar_wait(&sm->done, 0, kWaitBudget);
         }
     } else {
-        // ---------------------------------------------------------------- softmax / epilogue
+        // ---------------------------------------------------------------- workers
+        // Warps 0, 2, 3 and the softmax warps 4..7 all load the KV tiles; warps
+        // 4..7 also run the softmax and the epilogue.
+        const int lid = (warp == 0 ? 0 : warp - 1) * 32 + lane;  // 0 .. 223
+        const bool softmax_warp = warp >= 4;
+        // Q of this head group: 64 heads x (64 latent + 8 rope) 16-byte chunks
+        for (int q = lid; q < kHc * 72; q += kWorkers) {
+            const int h = q / 72, c = q - h * 72;
+            uint8_t *dst = q_s + (c >> 3) * kQBlk + sw128_offset(h, c & 7);
+            const int hh = hg * kHc + h;
+            if (hh < p.H) {
+                const uint16_t *src = c < 64 ? p.q_nope + r * p.nope_ld_r + hh * p.nope_ld_h + c * 8
+                                             : p.q_rope + r * p.rope_ld_r + hh * p.rope_ld_h + (c - 64) * 8;
+                cp_async16(dst, src);
+            } else {
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);  // padded head
+            }
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        mbar_arrive(&sm->q_full);
+
+        const int32_t *irow = p.indices + (int64_t)r * p.indices_ld;
+        // the indices of a tile are read one tile ahead (lanes own j = lid, lid + 96)
+        auto fetch_idx = [&](int tile, int (&v)[2]) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int j = lid + u * kWorkers;
+                const int pos = tile * kTok + j;
+                v[u] = (j < kTok && tile < t0 + nt && pos < p.topk) ? __ldg(irow + pos) : -1;
+            }
+        };
+        // Block pair m of the tile: latent blocks 2m, 2m+1 (m < 4) or the rope block (m = 4).
+        auto issue_pair = [&](int m) {
+            if (m == 4) {
+                for (int q = lid; q < kTok * 8; q += kWorkers) {
+                    const int row = q >> 3, c = q & 7;
+                    cp_async16(kv_s + 8 * kKvBlk + sw128_offset(row, c),
+                               sm->rowbase[row] + (FP8 ? kDl + 16 : 2 * kDl) + c * 16);
+                }
+            } else if (!FP8) {
+                for (int q = lid; q < kTok * 16; q += kWorkers) {
+                    const int row = q >> 4, c = 16 * m + (q & 15);
+                    cp_async16(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7), sm->rowbase[row] + c * 16);
+                }
+            } else {
+                // 16 groups of 8 e4m3 codes per row (dims 128m .. 128m+127, one scale)
+#pragma unroll 1
+                for (int q0 = lid; q0 < kTok * 16; q0 += 4 * kWorkers) {
+                    uint2 w[4];
+                    float sc[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int q = q0 + u * kWorkers;
+                        w[u] = make_uint2(0u, 0u);
+                        sc[u] = 0.f;
+                        if (q < kTok * 16) {
+                            const uint8_t *rowp = sm->rowbase[q >> 4];
+                            w[u] = __ldg(reinterpret_cast<const uint2 *>(rowp + (16 * m + (q & 15)) * 8));
+                            sc[u] = __ldg(reinterpret_cast<const float *>(rowp + kDl) + m);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int q = q0 + u * kWorkers;
+                        if (q < kTok * 16) {
+                            const int row = q >> 4, c = 16 * m + (q & 15);
+                            uint32_t d4[4];
+                            dequant8(w[u], sc[u], d4);
+                            *reinterpret_cast<uint4 *>(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7)) =
+                                make_uint4(d4[0], d4[1], d4[2], d4[3]);
+                        }
+                    }
+                }
+            }
+        };
+        // softmax state (warps 4..7)
+        const float4 *m_run4 = reinterpret_cast<const float4 *>(sm->m_run);
         const int quad = warp & 3;
         const int t = quad * 32 + lane;  // token row of S^T; d row of each O^T block
         const int et = threadIdx.x - 128;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        if (et < kHc) sm->m_run[et] = -INFINITY;
-        bar_sync(1, 128);
-        const float4 *m_run4 = reinterpret_cast<const float4 *>(sm->m_run);
+        if (softmax_warp) {
+            if (et < kHc) sm->m_run[et] = -INFINITY;
+            bar_sync(1, 128);
+        }
         int done_tiles = 0;
+        int cur[2], nxt[2];
+        fetch_idx(t0, cur);
         for (int i = 0; i < nt; ++i) {
-            const bool ok = mbar_wait(&sm->kvb_full[0], i & 1, kWaitBudget) && mbar_wait(&sm->s_full, i & 1, kWaitBudget);
-            if (bar_red_or(1, 128, !ok || sm->abort)) {
+            // block pair 0 (and the token table) is free once the previous tile's O^T block 0 is done
+            if (i > 0 && !mbar_wait(&sm->o_done[0], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
+            if (bar_red_or(2, kWorkers, sm->abort != 0)) break;  // uniform over the workers
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int j = lid + u * kWorkers;
+                if (j < kTok) {
+                    int v = cur[u];
+                    if (v < -1 || v >= p.num_slots) {
+                        set_status(p.status, NSA_ERR_BOUNDS);
+                        v = -1;
+                    }
+                    sm->idx[j] = v;
+                    sm->rowbase[j] = p.kv + (int64_t)(v < 0 ? 0 : v) * row_bytes;  // masked rows read slot 0
+                }
+            }
+            fetch_idx(t0 + i + 1, nxt);
+            worker_sync();
+#pragma unroll 1
+            for (int m = 0; m < 5; ++m) {
+                if (m > 0 && i > 0 && !mbar_wait(&sm->o_done[m], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
+                issue_pair(m);
+                cp_async_commit();
+                if (FP8 && m < 4) {  // dequantised pairs are written with plain stores
+                    fence_proxy_async_smem();
+                    mbar_arrive(&sm->kvb_full[m]);
+                } else if (!FP8 && m > 0) {
+                    cp_async_wait_group<1>();
+                    fence_proxy_async_smem();
+                    mbar_arrive(&sm->kvb_full[m - 1]);
+                }
+            }
+            // bring the next tile's rows into L2 while this one is consumed
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (nxt[u] >= 0 && nxt[u] < p.num_slots)
+                    prefetch_l2_bulk(p.kv + (int64_t)nxt[u] * row_bytes, (uint32_t)row_bytes);
+            cur[0] = nxt[0];
+            cur[1] = nxt[1];
+            cp_async_wait_group<0>();
+            fence_proxy_async_smem();
+            mbar_arrive(&sm->kvb_full[4]);
+            if (softmax_warp) {
+                const bool ok = mbar_wait(&sm->kvb_full[0], i & 1, kWaitBudget) && mbar_wait(&sm->s_full, i & 1, kWaitBudget);
                 if (!ok) fail(sm, p.status);
-                break;
+                if (bar_red_or(1, 128, !ok || sm->abort)) continue;  // the worker-wide check ends the loop
+                tc_fence_after();
+                uint32_t sa[32], sb[32];
+                tmem_ld32(lane_base + kColS, sa);
+                tmem_ld32(lane_base + kColS + 32, sb);
+                tmem_ld_wait();
+                const bool valid = sm->idx[t] >= 0;
+                float s[kHc];
+                bool exceed = false;
+#pragma unroll
+                for (int c = 0; c < kHc / 4; ++c) {
+                    const float4 mr = m_run4[c];
+                    const float mv[4] = {mr.x, mr.y, mr.z, mr.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int h = 4 * c + j;
+                        const uint32_t raw = h < 32 ? sa[h] : sb[h - 32];
+                        s[h] = valid ? __uint_as_float(raw) * p.scale_log2 : -INFINITY;
+                        exceed |= s[h] > mv[j] + kRescale;
+                    }
+                }
+                if (bar_red_or(1, 128, exceed)) {
+                    // refresh the running max of every head from this tile's column maxima
+#pragma unroll
+                    for (int h = 0; h < kHc; ++h) {
+                        float v = s[h];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+                        if (lane == 0) sm->red[quad][h] = v;
+                    }
+                    bar_sync(1, 128);
+                    if (et < kHc) {
+                        const int h = et;
+                        const float cm = fmaxf(fmaxf(sm->red[0][h], sm->red[1][h]), fmaxf(sm->red[2][h], sm->red[3][h]));
+                        const float mo = sm->m_run[h];
+                        const float mn = fmaxf(mo, cm);
+                        sm->alpha[h] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
+                        sm->m_run[h] = mn;
+                    }
+                    bar_sync(1, 128);  // alpha[] and m_run[] complete; red[] free for the next refresh
+                    if (i > 0) {
+                        // the previous tile's O^T and head sums must be complete before they are rescaled
+                        if (!mbar_wait(&sm->o_done[4], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int m = 0; m < 5; ++m) {  // 4 O^T blocks + the head-sum block
+#pragma unroll 1
+                            for (int half = 0; half < 2; ++half) {
+                                uint32_t v[32];
+                                const uint32_t a = lane_base + m * kHc + half * 32;
+                                tmem_ld32(a, v);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    v[j] = __float_as_uint(__uint_as_float(v[j]) * sm->alpha[half * 32 + j]);
+                                tmem_st32(a, v);
+                            }
+                        }
+                        tmem_st_wait();
+                    }
+                }
+                // probabilities relative to the running max, written as P^T row t (bf16)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {  // heads 8c .. 8c+7 -> one 16-byte chunk of row t
+                    const float4 ma = m_run4[2 * c], mb = m_run4[2 * c + 1];
+                    const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int h = 8 * c + 2 * j;
+                        const float p0 = s[h] == -INFINITY ? 0.f : exp2f(s[h] - mv[2 * j]);
+                        const float p1 = s[h + 1] == -INFINITY ? 0.f : exp2f(s[h + 1] - mv[2 * j + 1]);
+                        pk[j] = pack_bf16x2(p0, p1);
+                    }
+                    *reinterpret_cast<uint4 *>(p_s + sw128_offset(t, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&sm->p_full);
+                done_tiles = i + 1;
             }
+        }
+        if (softmax_warp) {
+            // ------------------------------------------------------------ epilogue
+            const int hv = min(kHc, p.H - hg * kHc);  // real heads of this CTA
+            const bool have_o = done_tiles > 0 && !sm->abort &&
+                                mbar_wait(&sm->o_done[4], (done_tiles - 1) & 1, kWaitBudget);
             tc_fence_after();
-            uint32_t sa[32], sb[32];
-            tmem_ld32(lane_base + kColS, sa);
-            tmem_ld32(lane_base + kColS + 32, sb);
-            tmem_ld_wait();
-            const bool valid = sm->idx[t] >= 0;
-            float s[kHc];
-            bool exceed = false;
-#pragma unroll
-            for (int c = 0; c < kHc / 4; ++c) {
-                const float4 mr = m_run4[c];
-                const float mv[4] = {mr.x, mr.y, mr.z, mr.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int h = 4 * c + j;
-                    const uint32_t raw = h < 32 ? sa[h] : sb[h - 32];
-                    s[h] = valid ? __uint_as_float(raw) * p.scale_log2 : -INFINITY;
-                    exceed |= s[h] > mv[j] + kRescale;
-                }
+            uint32_t la[32], lb[32];  // head sums (identical in every lane)
+            if (have_o) {
+                tmem_ld32(lane_base + kColL, la);
+                tmem_ld32(lane_base + kColL + 32, lb);
+                tmem_ld_wait();
             }
-            if (bar_red_or(1, 128, exceed)) {
-                // refresh the running max of every head from this tile's column maxima
-#pragma unroll
-                for (int h = 0; h < kHc; ++h) {
-                    float v = s[h];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-                    if (lane == 0) sm->red[quad][h] = v;
-                }
-                bar_sync(1, 128);
-                if (et < kHc) {
-                    const int h = et;
-                    const float cm = fmaxf(fmaxf(sm->red[0][h], sm->red[1][h]), fmaxf(sm->red[2][h], sm->red[3][h]));
-                    const float mo = sm->m_run[h];
-                    const float mn = fmaxf(mo, cm);
-                    sm->alpha[h] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
-                    sm->m_run[h] = mn;
-                }
-                bar_sync(1, 128);  // alpha[] and m_run[] complete; red[] free for the next refresh
-                if (i > 0) {
-                    // the previous tile's O^T and head sums must be complete before they are rescaled
-                    if (!mbar_wait(&sm->o_done[4], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
-                    tc_fence_after();
 #pragma unroll 1
-                    for (int m = 0; m < 5; ++m) {  // 4 O^T blocks + the head-sum block
-#pragma unroll 1
-                        for (int half = 0; half < 2; ++half) {
-                            uint32_t v[32];
-                            const uint32_t a = lane_base + m * kHc + half * 32;
-                            tmem_ld32(a, v);
-                            tmem_ld_wait();
+            for (int m = 0; m < 4; ++m) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                v[j] = __float_as_uint(__uint_as_float(v[j]) * sm->alpha[half * 32 + j]);
-                            tmem_st32(a, v);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[32];
+                    if (have_o) {
+                        tmem_ld32(lane_base + m * kHc + half * 32, v);
+                        tmem_ld_wait();
+                    }
+                    const int d = m * 128 + t;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int h = half * 32 + j;
+                        if (h < hv) {
+                            const float l = have_o ? __uint_as_float(half ? lb[j] : la[j]) : 0.f;
+                            const float o = l > 0.f ? __uint_as_float(v[j]) / l : 0.f;
+                            const int64_t row = (int64_t)r * p.H + hg * kHc + h;
+                            if (p.nsplit == 1)
+                                p.out[row * kDl + d] = __float2bfloat16_rn(o);
+                            else
+                                p.o_part[((int64_t)sp * p.R * p.H + row) * kDl + d] = o;
                         }
                     }
-                    tmem_st_wait();
                 }
             }
-            // probabilities relative to the running max, written as P^T row t (bf16)
+            if (et < hv) {
+                const float mm = sm->m_run[et];
+                float l = 0.f;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {  // heads 8c .. 8c+7 -> one 16-byte chunk of row t
-                const float4 ma = m_run4[2 * c], mb = m_run4[2 * c + 1];
-                const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-                uint32_t pk[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int h = 8 * c + 2 * j;
-                    const float p0 = s[h] == -INFINITY ? 0.f : exp2f(s[h] - mv[2 * j]);
-                    const float p1 = s[h + 1] == -INFINITY ? 0.f : exp2f(s[h + 1] - mv[2 * j + 1]);
-                    pk[j] = pack_bf16x2(p0, p1);
-                }
-                *reinterpret_cast<uint4 *>(p_s + sw128_offset(t, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                for (int h = 0; h < kHc; ++h)
+                    if (h == et) l = have_o ? __uint_as_float(h < 32 ? la[h] : lb[h - 32]) : 0.f;
+                const float lse = l > 0.f ? (mm + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                const int64_t row = (int64_t)r * p.H + hg * kHc + et;
+                if (p.nsplit == 1)
+                    p.lse[row] = lse;
+                else
+                    p.lse_part[(int64_t)sp * p.R * p.H + row] = lse;
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&sm->p_full);
-            done_tiles = i + 1;
-        }
-
-        // ------------------------------------------------------------ epilogue
-        const int hv = min(kHc, p.H - hg * kHc);  // real heads of this CTA
-        const bool have_o = done_tiles > 0 && !sm->abort &&
-                            mbar_wait(&sm->o_done[4], (done_tiles - 1) & 1, kWaitBudget);
-        tc_fence_after();
-        uint32_t la[32], lb[32];  // head sums (identical in every lane)
-        if (have_o) {
-            tmem_ld32(lane_base + kColL, la);
-            tmem_ld32(lane_base + kColL + 32, lb);
-            tmem_ld_wait();
-        }
-#pragma unroll 1
-        for (int m = 0; m < 4; ++m) {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t v[32];
-                if (have_o) {
-                    tmem_ld32(lane_base + m * kHc + half * 32, v);
-                    tmem_ld_wait();
-                }
-                const int d = m * 128 + t;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int h = half * 32 + j;
-                    if (h < hv) {
-                        const float l = have_o ? __uint_as_float(half ? lb[j] : la[j]) : 0.f;
-                        const float o = l > 0.f ? __uint_as_float(v[j]) / l : 0.f;
-                        const int64_t row = (int64_t)r * p.H + hg * kHc + h;
-                        if (p.nsplit == 1)
-                            p.out[row * kDl + d] = __float2bfloat16_rn(o);
-                        else
-                            p.o_part[((int64_t)sp * p.R * p.H + row) * kDl + d] = o;
-                    }
-                }
-            }
-        }
-        if (et < hv) {
-            const float mm = sm->m_run[et];
-            float l = 0.f;
-#pragma unroll
-            for (int h = 0; h < kHc; ++h)
-                if (h == et) l = have_o ? __uint_as_float(h < 32 ? la[h] : lb[h - 32]) : 0.f;
-            const float lse = l > 0.f ? (mm + log2f(l)) * 0.69314718055994531f : -INFINITY;
-            const int64_t row = (int64_t)r * p.H + hg * kHc + et;
-            if (p.nsplit == 1)
-                p.lse[row] = lse;
-            else
-                p.lse_part[(int64_t)sp * p.R * p.H + row] = lse;
         }
     }
 
