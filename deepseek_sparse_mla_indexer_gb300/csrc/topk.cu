@@ -4,7 +4,8 @@
 // transformed page table directly"), [DSA] transform_index_page_table_* with
 // page size 1 and _pad_topk_indices (-1 padding).
 //
-// One block of 1024 threads per row.  Scores become order-preserving 32-bit
+// Short rows: one block of 1024 threads per row; long rows: a cluster of up
+// to 8 blocks per row (below).  Scores become order-preserving 32-bit
 // keys (-0 folded onto +0, NaN below every number).  The k-th largest key is
 // located by a most-significant-digit radix select with 11/11/10-bit digits:
 // each pass histograms the keys that still match the chosen prefix (eight
@@ -15,6 +16,8 @@
 // (k - #above) keys equal to it, in position order, so ties go to the lower
 // position and the output comes out sorted without a sort.  Rows up to
 // kCacheCap scores are read from HBM once and kept in shared memory.
+#include <algorithm>
+
 #include "nsa_internal.cuh"
 
 namespace nsa {
@@ -184,6 +187,200 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
     }
 }
 
+
+// ---------------------------------------------------------------- cluster variant
+// Long rows: a thread-block cluster of C CTAs per row, each owning a slice of
+// the row.  Histograms and selection counts are combined through distributed
+// shared memory between hardware cluster barriers (no spin-waits); every CTA
+// reaches the same decisions from the same merged data, so control flow stays
+// uniform across the cluster.
+constexpr int kCThreads = 512;
+constexpr int kCCopies = 4;
+constexpr int kCMaxCluster = 8;
+constexpr int kCSliceCap = 16 * 1024;  // keys of one slice cached in shared memory
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 32-bit load from the same shared-memory variable of CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t ld_cluster(const uint32_t *local, uint32_t rank)
+{
+    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local)), ra, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+    return v;
+}
+
+__global__ void __launch_bounds__(kCThreads)
+topk_cluster_kernel(const float *logits, int64_t logits_ld, const int32_t *row_len, const int32_t *row_to_req,
+                    const int32_t *pt, int64_t pt_ld, int topk, int max_row_len, int32_t *indices,
+                    int64_t indices_ld, int32_t *status)
+{
+    extern __shared__ uint32_t cache[];           // [kCSliceCap] keys of this slice
+    __shared__ uint32_t hist[kCCopies * kBins];  // replicated local histogram
+    __shared__ uint32_t merged[kBins];            // this CTA's combined copy (read by the peers)
+    __shared__ uint32_t warp_buf[32];
+    __shared__ uint32_t total;
+    __shared__ uint32_t sel_digit, sel_need, sel_exact;
+    __shared__ uint32_t counts[2];               // (#above, #equal) in this slice
+
+    const uint32_t rank = cluster_rank();
+    uint32_t csize;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
+    const int r = blockIdx.x / (int)csize;
+    const int tid = threadIdx.x;
+    int L = row_len[r];
+    const int b = row_to_req[r];
+    int32_t *out = indices + (int64_t)r * indices_ld;
+    const int32_t *ptr = pt + (int64_t)b * pt_ld;
+    const float *lg = logits + (int64_t)r * logits_ld;
+
+    if (L < 0 || L > max_row_len) {  // same decision in every CTA of the cluster
+        if (rank == 0) {
+            if (tid == 0) set_status(status, NSA_ERR_BOUNDS);
+            for (int i = tid; i < topk; i += kCThreads) out[i] = -1;
+        }
+        return;
+    }
+    if (L <= topk) {
+        if (rank == 0)
+            for (int i = tid; i < topk; i += kCThreads) out[i] = i < L ? ptr[i] : -1;
+        return;
+    }
+
+    // this CTA's slice of the row (a multiple of 4 positions)
+    const int seg = ((L + (int)csize - 1) / (int)csize + 3) & ~3;
+    const int s0 = min(L, (int)rank * seg), s1 = min(L, s0 + seg);
+    const int n = s1 - s0;
+    const bool cached = n <= kCSliceCap;
+    if (cached)
+        for (int i = tid; i < n; i += kCThreads) cache[i] = order_key(lg[s0 + i]);
+    auto key_at = [&](int i) -> uint32_t { return cached ? cache[i] : order_key(lg[s0 + i]); };
+
+    uint32_t prefix = 0u, need = (uint32_t)topk;
+    int S = 32;
+    uint32_t *myhist = hist + (size_t)((tid >> 5) % kCCopies) * kBins;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int width = pass < 2 ? 11 : 10;
+        const int shift = S - width;
+        const uint32_t dmask = (1u << width) - 1u;
+        for (int i = tid; i < kCCopies * kBins; i += kCThreads) hist[i] = 0u;
+        __syncthreads();
+        for (int i = tid; i < n; i += kCThreads) {
+            const uint32_t k = key_at(i);
+            if (S == 32 || (k >> S) == prefix) atomicAdd(&myhist[(k >> shift) & dmask], 1u);
+        }
+        __syncthreads();
+        for (int d = tid; d < kBins; d += kCThreads) {
+            uint32_t v = 0u;
+#pragma unroll
+            for (int c = 0; c < kCCopies; ++c) v += hist[c * kBins + d];
+            merged[d] = v;
+        }
+        if (tid == 0) {  // a decision every CTA agrees on even if no bin were chosen
+            sel_digit = 0u;
+            sel_need = need;
+            sel_exact = 1u;
+        }
+        cluster_sync();  // every slice histogram is complete
+        // thread t owns digits 2047-4t .. 2044-4t (largest first); sum them over the cluster
+        uint32_t c4[4], sum = 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int d = kBins - 1 - 4 * tid - j;
+            uint32_t v = 0u;
+            if (d <= (int)dmask)
+                for (uint32_t q = 0; q < csize; ++q) v += ld_cluster(&merged[d], q);
+            c4[j] = v;
+            sum += v;
+        }
+        const uint32_t incl = block_incl_scan(sum, warp_buf, &total);
+        uint32_t excl = incl - sum;
+        if (excl < need && need <= incl) {
+            uint32_t cum = excl;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (cum + c4[j] >= need) {
+                    sel_digit = (uint32_t)(kBins - 1 - 4 * tid - j);
+                    sel_need = need - cum;
+                    sel_exact = (c4[j] == need - cum);
+                    break;
+                }
+                cum += c4[j];
+            }
+        }
+        cluster_sync();  // peers are done reading `merged`; sel_* written
+        prefix = (S == 32 ? 0u : (prefix << width)) | sel_digit;
+        need = sel_need;
+        S = shift;
+        const bool exact = sel_exact != 0u;
+        __syncthreads();
+        if (exact) break;
+    }
+
+    // counts of this slice, then the offsets of the lower-ranked slices
+    uint32_t n_gt = 0u, n_eq = 0u;
+    for (int i = tid; i < n; i += kCThreads) {
+        const uint32_t v = key_at(i) >> S;
+        n_gt += v > prefix;
+        n_eq += v == prefix;
+    }
+    if (tid == 0) {
+        counts[0] = 0u;
+        counts[1] = 0u;
+    }
+    __syncthreads();
+    atomicAdd(&counts[0], n_gt);
+    atomicAdd(&counts[1], n_eq);
+    cluster_sync();
+    uint32_t gt_run = 0u, eq_run = 0u;
+    for (uint32_t q = 0; q < rank; ++q) {
+        gt_run += ld_cluster(&counts[0], q);
+        eq_run += ld_cluster(&counts[1], q);
+    }
+
+    for (int base = 0; base < n; base += kCThreads * kItems) {
+        const int i0 = base + tid * kItems;
+        uint32_t cls[kItems];
+        uint32_t a_gt = 0u, a_eq = 0u;
+#pragma unroll
+        for (int j = 0; j < kItems; ++j) {
+            cls[j] = 0u;
+            if (i0 + j < n) {
+                const uint32_t v = key_at(i0 + j) >> S;
+                cls[j] = v > prefix ? 2u : (v == prefix ? 1u : 0u);
+            }
+            a_gt += cls[j] == 2u;
+            a_eq += cls[j] == 1u;
+        }
+        const uint32_t packed = a_gt | (a_eq << 16);
+        const uint32_t incl = block_incl_scan(packed, warp_buf, &total);
+        uint32_t gt_before = gt_run + ((incl - packed) & 0xFFFFu);
+        uint32_t eq_before = eq_run + ((incl - packed) >> 16);
+#pragma unroll
+        for (int j = 0; j < kItems; ++j) {
+            if (cls[j] == 2u) {
+                out[gt_before + (eq_before < need ? eq_before : need)] = ptr[s0 + i0 + j];
+                ++gt_before;
+            } else if (cls[j] == 1u) {
+                if (eq_before < need) out[gt_before + eq_before] = ptr[s0 + i0 + j];
+                ++eq_before;
+            }
+        }
+        gt_run += total & 0xFFFFu;
+        eq_run += total >> 16;
+    }
+    cluster_sync();  // no CTA leaves while a peer may still read its shared memory
+}
+
 }  // namespace
 }  // namespace nsa
 
@@ -199,6 +396,28 @@ extern "C" nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits
     if (R == 0) return NSA_OK;
     if (!logits_dev || !row_len_dev || !row_to_req_dev || !page_table_1_dev || !indices_dev)
         return NSA_ERR_INVALID_ARG;
+    // long rows: one cluster of up to 8 CTAs per row
+    const int csize = max_row_len > topk ? (int)std::min<int64_t>(kCMaxCluster, ceil_div(max_row_len, 4096)) : 1;
+    if (csize > 1 && (int64_t)R * csize <= 2147483647LL) {
+        NSA_CUDA_TRY(cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)(kCSliceCap * sizeof(uint32_t))));
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(R * csize));
+        cfg.blockDim = dim3(kCThreads);
+        cfg.dynamicSmemBytes = kCSliceCap * sizeof(uint32_t);
+        cfg.stream = (cudaStream_t)stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)csize;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, topk_cluster_kernel, logits_dev, logits_ld, row_len_dev,
+                                        row_to_req_dev, page_table_1_dev, pt_ld, topk, max_row_len, indices_dev,
+                                        indices_ld, status_dev));
+        return NSA_OK;
+    }
     const int cap = max_row_len > topk ? (max_row_len < kCacheCap ? max_row_len : kCacheCap) : 0;
     const size_t smem = (size_t)(kCopies * kBins + cap) * sizeof(uint32_t);
     NSA_CUDA_TRY(cudaFuncSetAttribute(topk_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -135,3 +135,25 @@ def test_host_rejects_bad_arguments_without_launch():
         nsa.nsa_sparse_mla(nsa.DT_F32, nsa.DT_BF16, step.q_nope, step.q_rope, step.kv, step.indices,
                            1.0, step.out, step.lse)
     assert e.value.code == nsa.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("width", [2049, 4097, 9000, 20000, 33000, 131076])
+def test_topk_bit_exact_across_row_lengths(width):
+    """Rows of many lengths (short rows, one block per row; long rows, a cluster
+    of blocks per row), distinct and tied scores, against the oracle."""
+    import deepseek_sparse_mla_indexer_gb300 as nsa
+    import oracle
+    rng = np.random.default_rng(width)
+    R, k = 7, 2048
+    lg = rng.standard_normal((R, width)).astype(np.float32)
+    lg[1] = np.round(lg[1] * 2) / 2  # coarse values: many ties across slices
+    lg[2, : width // 3] = 5.0        # a plateau of equal maxima
+    L = np.array([width, width - 1, width, k + 1, k, 1, max(1, width // 2)], np.int32)
+    pt = rng.integers(0, 2 ** 31 - 1, size=(R, width)).astype(np.int32)
+    r2q = np.arange(R, dtype=np.int32)
+    exp = oracle.topk_transform(lg, L, r2q, pt, k)
+    d = "cuda"
+    idx = torch.empty((R, k), dtype=torch.int32, device=d)
+    nsa.nsa_topk_transform(torch.from_numpy(lg).to(d), torch.from_numpy(L).to(d), torch.from_numpy(r2q).to(d),
+                           torch.from_numpy(pt).to(d), k, width, idx)
+    assert np.array_equal(idx.cpu().numpy(), exp)
