@@ -50,7 +50,7 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *warp_b
     if (lane == 31) warp_buf[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        uint32_t w = warp_buf[lane];
+        uint32_t w = lane < (int)(blockDim.x >> 5) ? warp_buf[lane] : 0u;  // only the block's real warps
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
