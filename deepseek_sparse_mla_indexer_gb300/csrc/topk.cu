@@ -65,6 +65,34 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *warp_b
     return incl;
 }
 
+// Keys of lg[s0 .. s0 + n) into cache[0 .. n): 16-byte loads, all in flight at once.
+template <int NT, int MAXV>
+__device__ __forceinline__ void fill_keys(const float *lg, int s0, int n, uint32_t *cache)
+{
+    const float *src = lg + s0;
+    if ((((uintptr_t)src) & 15) == 0) {
+        const int nv = n >> 2;
+        for (int base = 0; base < nv; base += NT * MAXV) {
+            float4 v[MAXV];
+#pragma unroll
+            for (int u = 0; u < MAXV; ++u) {
+                const int j = base + u * NT + (int)threadIdx.x;
+                if (j < nv) v[u] = __ldg(reinterpret_cast<const float4 *>(src) + j);
+            }
+#pragma unroll
+            for (int u = 0; u < MAXV; ++u) {
+                const int j = base + u * NT + (int)threadIdx.x;
+                if (j < nv)
+                    reinterpret_cast<uint4 *>(cache)[j] =
+                        make_uint4(order_key(v[u].x), order_key(v[u].y), order_key(v[u].z), order_key(v[u].w));
+            }
+        }
+        for (int i = (nv << 2) + (int)threadIdx.x; i < n; i += NT) cache[i] = order_key(src[i]);
+    } else {
+        for (int i = threadIdx.x; i < n; i += NT) cache[i] = order_key(src[i]);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads)
 topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row_len,
                       const int32_t *row_to_req, const int32_t *pt, int64_t pt_ld, int topk,
@@ -97,8 +125,7 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
     }
 
     const bool cached = L <= cache_cap;
-    if (cached)
-        for (int i = tid; i < L; i += kThreads) cache[i] = order_key(lg[i]);
+    if (cached) fill_keys<kThreads, 8>(lg, 0, L, cache);
     auto key_at = [&](int i) -> uint32_t { return cached ? cache[i] : order_key(lg[i]); };
 
     // radix select: find the resolution shift S, value V and count `need`
@@ -218,6 +245,19 @@ __device__ __forceinline__ uint32_t ld_cluster(const uint32_t *local, uint32_t r
     return v;
 }
 
+// 16-byte load from CTA `rank` of the cluster (address 16-byte aligned).
+__device__ __forceinline__ uint4 ld_cluster4(const uint32_t *local, uint32_t rank)
+{
+    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local)), ra;
+    uint4 v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(ra)
+                 : "memory");
+    return v;
+}
+
 __global__ void __launch_bounds__(kCThreads)
 topk_cluster_kernel(const float *logits, int64_t logits_ld, const int32_t *row_len, const int32_t *row_to_req,
                     const int32_t *pt, int64_t pt_ld, int topk, int max_row_len, int32_t *indices,
@@ -225,7 +265,7 @@ topk_cluster_kernel(const float *logits, int64_t logits_ld, const int32_t *row_l
 {
     extern __shared__ uint32_t cache[];           // [kCSliceCap] keys of this slice
     __shared__ uint32_t hist[kCCopies * kBins];  // replicated local histogram
-    __shared__ uint32_t merged[kBins];            // this CTA's combined copy (read by the peers)
+    __shared__ __align__(16) uint32_t merged[kBins];  // this CTA's combined copy (read by the peers)
     __shared__ uint32_t warp_buf[32];
     __shared__ uint32_t total;
     __shared__ uint32_t sel_digit, sel_need, sel_exact;
@@ -260,8 +300,7 @@ topk_cluster_kernel(const float *logits, int64_t logits_ld, const int32_t *row_l
     const int s0 = min(L, (int)rank * seg), s1 = min(L, s0 + seg);
     const int n = s1 - s0;
     const bool cached = n <= kCSliceCap;
-    if (cached)
-        for (int i = tid; i < n; i += kCThreads) cache[i] = order_key(lg[s0 + i]);
+    if (cached) fill_keys<kCThreads, 8>(lg, s0, n, cache);
     auto key_at = [&](int i) -> uint32_t { return cached ? cache[i] : order_key(lg[s0 + i]); };
 
     uint32_t prefix = 0u, need = (uint32_t)topk;
@@ -292,16 +331,16 @@ topk_cluster_kernel(const float *logits, int64_t logits_ld, const int32_t *row_l
         }
         cluster_sync();  // every slice histogram is complete
         // thread t owns digits 2047-4t .. 2044-4t (largest first); sum them over the cluster
-        uint32_t c4[4], sum = 0u;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int d = kBins - 1 - 4 * tid - j;
-            uint32_t v = 0u;
-            if (d <= (int)dmask)
-                for (uint32_t q = 0; q < csize; ++q) v += ld_cluster(&merged[d], q);
-            c4[j] = v;
-            sum += v;
+        const int dlo = kBins - 4 - 4 * tid;  // digits dlo .. dlo+3, one 16-byte vector
+        uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+        if (dlo <= (int)dmask) {
+            for (uint32_t q = 0; q < csize; ++q) {
+                const uint4 v = ld_cluster4(&merged[dlo], q);
+                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            }
         }
+        const uint32_t c4[4] = {acc.w, acc.z, acc.y, acc.x};  // digit dlo+3 first
+        const uint32_t sum = acc.x + acc.y + acc.z + acc.w;
         const uint32_t incl = block_incl_scan(sum, warp_buf, &total);
         uint32_t excl = incl - sum;
         if (excl < need && need <= incl) {
@@ -333,13 +372,10 @@ topk_cluster_kernel(const float *logits, int64_t logits_ld, const int32_t *row_l
         n_gt += v > prefix;
         n_eq += v == prefix;
     }
-    if (tid == 0) {
-        counts[0] = 0u;
-        counts[1] = 0u;
-    }
-    __syncthreads();
-    atomicAdd(&counts[0], n_gt);
-    atomicAdd(&counts[1], n_eq);
+    block_incl_scan(n_gt, warp_buf, &total);
+    if (tid == 0) counts[0] = total;
+    block_incl_scan(n_eq, warp_buf, &total);
+    if (tid == 0) counts[1] = total;
     cluster_sync();
     uint32_t gt_run = 0u, eq_run = 0u;
     for (uint32_t q = 0; q < rank; ++q) {
