@@ -35,7 +35,8 @@ constexpr int kHi = 64;
 constexpr int kStages = 4;
 constexpr int kThreadsTc = 192;
 constexpr int kMaxG = 4;
-constexpr int kTilesPerCta = 16;
+constexpr int kTilesPerCta = 16;  // 2 half-tiles per tile: one per lane of the producer warp
+static_assert(kTilesPerCta * 2 == 32, "the producer warp owns one half-tile per lane");
 constexpr uint32_t kTileBytes = kTileTok * kDi;    // 16 KB of e4m3
 constexpr uint32_t kHalfBytes = kHalf * kDi;       // 8 KB
 constexpr uint32_t kQRowBytes = kHi * kDi;         // 8 KB per query row
@@ -147,50 +148,59 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            uint32_t it = 0, qi = 0;
-            uint32_t issued_mask = 0, last_parity = 0;
-            int r = g_begin;
-            SubGroup sg;
-            while (!bars->abort && next_subgroup(p, g_end, r, sg)) {
-                const int nt = (int)ceil_div(sg.lmax, kTileTok);
-                const int te = min(t_end, nt);
-                if (t_begin >= te) continue;
-                if (!mbar_wait(&bars->q_empty, (qi & 1) ^ 1, kWaitBudget)) { fail(bars, p.status); break; }
-                mbar_arrive_expect_tx(&bars->q_full, sg.c * kQRowBytes);
-                for (int i = 0; i < sg.c; ++i)
-                    tma_load_2d(q_smem + i * kQRowBytes, &qmap, 0, (sg.r0 + i) * kHi, &bars->q_full);
-                ++qi;
-                for (int t = t_begin; t < te; ++t, ++it) {
-                    const int st = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1;
-                    if (!mbar_wait(&bars->empty[st], ph ^ 1, kWaitBudget)) { fail(bars, p.status); break; }
-                    int64_t row0[2];
-                    uint32_t bytes = 0;
-                    for (int h = 0; h < 2; ++h) {
-                        const int s = t * kTileTok + h * kHalf;
-                        row0[h] = -1;
-                        if (s < sg.lmax) {
-                            const int64_t page = p.rpt[(int64_t)sg.b * p.rpt_ld + s / p.ps];
-                            if (page >= 0 && page < p.num_pages) {
-                                row0[h] = page * p.ps + s % p.ps;
-                                bytes += kHalfBytes;
-                            }
-                        }
-                    }
-                    mbar_arrive_expect_tx(&bars->full[st], bytes);
-                    for (int h = 0; h < 2; ++h)
-                        if (row0[h] >= 0)
-                            tma_load_2d(a_ring + st * kTileBytes + h * kHalfBytes, &kmap, 0, (int)row0[h],
-                                        &bars->full[st]);
-                    issued_mask |= 1u << st;
-                    last_parity = (last_parity & ~(1u << st)) | (ph << st);
+        // The whole warp walks the tiles; lane l owns half-tile l of the CTA
+        // (kTilesPerCta * 2 == 32), so all page ids arrive in one round trip.
+        uint32_t it = 0, qi = 0;
+        uint32_t issued_mask = 0, last_parity = 0;
+        int r = g_begin;
+        SubGroup sg;
+        while (!bars->abort && next_subgroup(p, g_end, r, sg)) {
+            const int nt = (int)ceil_div(sg.lmax, kTileTok);
+            const int te = min(t_end, nt);
+            if (t_begin >= te) continue;
+            int my_row = -1;  // first KV slot of my half-tile, -1 if none
+            {
+                const int s = (t_begin + (lane >> 1)) * kTileTok + (lane & 1) * kHalf;
+                if (s < sg.lmax) {
+                    const int64_t page = p.rpt[(int64_t)sg.b * p.rpt_ld + s / p.ps];
+                    if (page >= 0 && page < p.num_pages) my_row = (int)(page * p.ps + s % p.ps);
                 }
             }
-            // drain: never leave with copies in flight
+            bool ok = true;
+            if (lane == 0) {
+                ok = mbar_wait(&bars->q_empty, (qi & 1) ^ 1, kWaitBudget);
+                if (ok) {
+                    mbar_arrive_expect_tx(&bars->q_full, sg.c * kQRowBytes);
+                    for (int i = 0; i < sg.c; ++i)
+                        tma_load_2d(q_smem + i * kQRowBytes, &qmap, 0, (sg.r0 + i) * kHi, &bars->q_full);
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) { if (lane == 0) fail(bars, p.status); break; }
+            ++qi;
+            for (int t = t_begin; t < te; ++t, ++it) {
+                const int st = it % kStages;
+                const uint32_t ph = (it / kStages) & 1;
+                const int row0 = __shfl_sync(0xffffffffu, my_row, 2 * (t - t_begin));
+                const int row1 = __shfl_sync(0xffffffffu, my_row, 2 * (t - t_begin) + 1);
+                if (lane == 0) {
+                    ok = mbar_wait(&bars->empty[st], ph ^ 1, kWaitBudget);
+                    if (ok) {
+                        const uint32_t bytes = (row0 >= 0 ? kHalfBytes : 0u) + (row1 >= 0 ? kHalfBytes : 0u);
+                        mbar_arrive_expect_tx(&bars->full[st], bytes);
+                        if (row0 >= 0) tma_load_2d(a_ring + st * kTileBytes, &kmap, 0, row0, &bars->full[st]);
+                        if (row1 >= 0)
+                            tma_load_2d(a_ring + st * kTileBytes + kHalfBytes, &kmap, 0, row1, &bars->full[st]);
+                        issued_mask |= 1u << st;
+                        last_parity = (last_parity & ~(1u << st)) | (ph << st);
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) { if (lane == 0) fail(bars, p.status); break; }
+            }
+        }
+        // drain: never leave with copies in flight
+        if (lane == 0)
             for (int st = 0; st < kStages; ++st)
                 if (issued_mask & (1u << st)) mbar_wait(&bars->full[st], (last_parity >> st) & 1, kWaitBudget);
-        }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -249,20 +259,30 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             int Lrow[kMaxG];
 #pragma unroll
             for (int i = 0; i < kMaxG; ++i) Lrow[i] = i < sg.c ? clamp_len(p, sg.r0 + i) : 0;
+            // the key scale of my token, one tile ahead of the accumulator
+            auto fetch_scale = [&](int t, float &scale, bool &valid) {
+                const int s = t * kTileTok + tok;
+                scale = 0.f;
+                valid = false;
+                if (t < te && s < sg.lmax) {
+                    const int64_t page = p.rpt[(int64_t)sg.b * p.rpt_ld + s / p.ps];
+                    valid = page >= 0 && page < p.num_pages;
+                    if (valid) scale = __ldg(p.k_scale + page * p.ps + s % p.ps);
+                }
+            };
+            float scale_next;
+            bool valid_next;
+            fetch_scale(t_begin, scale_next, valid_next);
             for (int t = t_begin; t < te; ++t, ++ai) {
                 const int ab = ai & 1;
                 const uint32_t aph = (ai >> 1) & 1;
+                const int s = t * kTileTok + tok;
+                const float scale = scale_next;
+                const bool valid_page = valid_next;
+                fetch_scale(t + 1, scale_next, valid_next);
+                if (s < sg.lmax && !valid_page) set_status(p.status, NSA_ERR_BOUNDS);
                 if (!mbar_wait(&bars->acc_full[ab], aph, kWaitBudget)) { fail(bars, p.status); break; }
                 tc_fence_after();
-                const int s = t * kTileTok + tok;
-                float scale = 0.f;
-                bool valid_page = false;
-                if (s < sg.lmax) {
-                    const int64_t page = p.rpt[(int64_t)sg.b * p.rpt_ld + s / p.ps];
-                    valid_page = page >= 0 && page < p.num_pages;
-                    if (valid_page) scale = p.k_scale[page * p.ps + s % p.ps];
-                    else set_status(p.status, NSA_ERR_BOUNDS);
-                }
                 const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + ab * p.acc_stride;
                 for (int i = 0; i < sg.c; ++i) {
                     uint32_t v0[32], v1[32];

@@ -21,14 +21,19 @@ struct MetaParams {
     int32_t *status;
 };
 
-// out[0] = 0, out[i + 1] = f(0) + ... + f(i) for i < n, with the whole block.
+// out[0] = 0, out[i + 1] = f(0) + ... + f(i) for i < n, with the whole block;
+// the same values also go to `copy` (shared memory) when it is given.
 template <class F>
-__device__ void block_cumsum_pad(int n, F f, int32_t *out)
+__device__ void block_cumsum_pad(int n, F f, int32_t *out, int32_t *copy = nullptr)
 {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    if (threadIdx.x == 0) { carry = 0; out[0] = 0; }
+    if (threadIdx.x == 0) {
+        carry = 0;
+        out[0] = 0;
+        if (copy) copy[0] = 0;
+    }
     __syncthreads();
     for (int base = 0; base < n; base += blockDim.x) {
         int i = base + threadIdx.x;
@@ -51,11 +56,78 @@ __device__ void block_cumsum_pad(int n, F f, int32_t *out)
         }
         __syncthreads();
         int incl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x;
-        if (i < n) out[i + 1] = incl;
+        if (i < n) {
+            out[i + 1] = incl;
+            if (copy) copy[i + 1] = incl;
+        }
         __syncthreads();
         if (threadIdx.x == blockDim.x - 1) carry = incl;
         __syncthreads();
     }
+}
+
+constexpr int kSmemB = 2048;  // requests staged in shared memory by the fast path
+
+// Per-request lengths staged once in shared memory; every per-row value is
+// computed from there, so the block never reads back what it wrote to global.
+__device__ void build_rows_smem(const MetaParams &p)
+{
+    __shared__ int32_t s_seq[kSmemB], s_ext[kSmemB], s_cuq[kSmemB + 1], s_cuk[kSmemB + 1];
+    const nsa_metadata_out &o = p.out;
+    const int draft = p.mode == NSA_MODE_TARGET_VERIFY ? p.n_draft : 0;
+    const bool extend = p.mode == NSA_MODE_EXTEND;
+    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+        const int c = p.seq_lens[b] + draft;
+        s_seq[b] = c;
+        if (extend) s_ext[b] = p.extend_lens[b];
+        if (c < 0 || c > p.W) set_status(p.status, NSA_ERR_BOUNDS);
+        o.cache_seqlens[b] = c;
+    }
+    __syncthreads();
+    block_cumsum_pad(p.B, [&](int b) { return s_seq[b]; }, o.cu_seqlens_k, s_cuk);
+    if (extend) {
+        block_cumsum_pad(p.B, [&](int b) { return s_ext[b]; }, o.cu_seqlens_q, s_cuq);
+    } else {
+        const int n = p.mode == NSA_MODE_DECODE ? p.B : p.R;
+        for (int i = threadIdx.x; i <= n; i += blockDim.x) o.cu_seqlens_q[i] = i;
+    }
+    __syncthreads();
+    // (request, position in the request, rows of the request) of row r
+    auto row_info = [&](int r, int &b, int &q, int &i) {
+        if (p.mode == NSA_MODE_DECODE) {
+            b = r; q = 1; i = 0;
+        } else if (p.mode == NSA_MODE_TARGET_VERIFY) {
+            b = r / p.n_draft; q = p.n_draft; i = r - b * p.n_draft;
+        } else {
+            int lo = 0, hi = p.B - 1;  // largest b with cu_seqlens_q[b] <= r
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_cuq[mid] <= r) lo = mid; else hi = mid - 1;
+            }
+            b = lo; q = s_ext[b]; i = r - s_cuq[b];
+        }
+    };
+    for (int r = threadIdx.x; r < p.R; r += blockDim.x) {
+        int b, q, i;
+        row_info(r, b, q, i);
+        if (i >= q) set_status(p.status, NSA_ERR_BOUNDS);  // R exceeds sum(extend_lens)
+        const int L = s_seq[b] - q + 1 + i;  // arange(kv - q + 1, kv + 1)[i]
+        o.seqlens_expanded[r] = L;
+        o.nsa_cache_seqlens[r] = L < p.topk ? L : p.topk;
+        o.row_to_req[r] = b;
+        if (extend && o.indexer_ks) {
+            const int ks = s_cuk[b];
+            o.indexer_ks[r] = ks;
+            o.indexer_ke[r] = ks + L;
+        }
+    }
+    block_cumsum_pad(p.R, [&](int r) {
+        int b, q, i;
+        row_info(r, b, q, i);
+        const int L = s_seq[b] - q + 1 + i;
+        return L < p.topk ? L : p.topk;
+    }, o.nsa_cu_seqlens_k);
+    for (int i = threadIdx.x; i <= p.R; i += blockDim.x) o.nsa_cu_seqlens_q[i] = i;
 }
 
 __device__ void build_rows(const MetaParams &p)
@@ -176,7 +248,8 @@ __device__ void copy_tables(const MetaParams &p, int first_seg, int seg_stride)
 __global__ void __launch_bounds__(kRowThreads) metadata_kernel(MetaParams p)
 {
     if (blockIdx.x == 0) {
-        build_rows(p);
+        if (p.B <= kSmemB) build_rows_smem(p);
+        else build_rows(p);
     } else {
         copy_tables(p, (int)blockIdx.x - 1, (int)gridDim.x - 1);
     }
