@@ -126,6 +126,25 @@ class ClockSampler:
                     reasons=sorted(reasons), samples=len(sm))
 
 
+# ---------------------------------------------------------------- timestamps inside a graph
+
+_cudart = None
+
+
+def record_external(event, stream):
+    """Record `event` on `stream` as a timestamp node when the stream is being
+    captured (cudaEventRecordWithFlags, cudaEventRecordExternal)."""
+    global _cudart
+    import ctypes
+    if _cudart is None:
+        _cudart = ctypes.CDLL("libcudart.so.13")
+        _cudart.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        _cudart.cudaEventRecordWithFlags.restype = ctypes.c_int
+    rc = _cudart.cudaEventRecordWithFlags(ctypes.c_void_p(event.cuda_event), ctypes.c_void_p(stream.cuda_stream), 1)
+    if rc != 0:
+        raise RuntimeError(f"cudaEventRecordWithFlags failed ({rc})")
+
+
 # ---------------------------------------------------------------- replicas
 
 def replica_seed(rank: int) -> int:
@@ -182,27 +201,49 @@ def run_ours(args, rank, world, local_rank):
     if step.status_code() != 0:
         raise RuntimeError(f"device status {step.status_code()} after warm-up")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    # The step as one CUDA graph (how a serving loop replays a decode step), with
+    # timestamp nodes between the stages so that host launch gaps cannot enter
+    # the stage times.
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+    for e in ev:
+        e.record(stream)  # creates the events before capture
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.graph(graph, stream=cap):
+        for i, fn in enumerate(calls):
+            record_external(ev[i], cap)
+            fn(cap)
+        record_external(ev[len(calls)], cap)
+    stream.wait_stream(cap)
+    for _ in range(args.warmup):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize(dev)
+
     sampler = ClockSampler(local_rank)
     sampler.start()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    for k in range(args.steps):
-        flush.zero_()  # L2 flush between steps, outside the timed events
-        one_step(ev[k])
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop()
-
+    t_wall = time.perf_counter()
     per_stage = {s: [] for s in stages}
     totals = []
     for k in range(args.steps):
+        flush.zero_()  # L2 flush between steps, outside the timed events
+        graph.replay()
+        torch.cuda.synchronize(dev)
         for i, s in enumerate(stages):
-            per_stage[s].append(ev[k][i].elapsed_time(ev[k][i + 1]))
-        totals.append(ev[k][0].elapsed_time(ev[k][len(calls)]))
+            per_stage[s].append(ev[i].elapsed_time(ev[i + 1]))
+        totals.append(ev[0].elapsed_time(ev[len(calls)]))
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
     ms_step = float(np.mean(totals))
+    if step.status_code() != 0:
+        raise RuntimeError(f"device status {step.status_code()} after the timed steps")
 
     # end to end through the public API with host buffers: per step the
     # per-request inputs go host->device from pinned memory, the outputs come back.
@@ -242,6 +283,7 @@ def run_ours(args, rank, world, local_rank):
 
     ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], world)
 
+    launches_per_step = len(calls) + (1 if step.workspace is not None else 0)  # + split-KV combine
     md_len = step.md["seqlens_expanded"].cpu().numpy()
     work = algorithmic_work(wl, md_len)
     peaks = load_peaks()
@@ -267,13 +309,14 @@ def run_ours(args, rank, world, local_rank):
                 data="synthetic (seeded; random pages; see workloads/)",
                 config=dict(workload=WORKLOAD_DESC, global_batch=rows_total,
                             seq_len=int(np.mean(wl.seq_lens)), parallelism=f"replicas x{world}",
-                            l2="flushed between steps (512 MB write outside the timed events)"),
+                            l2="flushed between steps (512 MB write outside the timed events)",
+                            timing="step replayed as one CUDA graph; device timestamps between stages"),
                 stages=stage_info, roofline=roof,
                 e2e=dict(value=round(rows_total / (e2e_ms * 1e-3), 1), unit="tokens/s",
                          h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
                          note="per-request inputs host->device and out+lse device->host each step; "
                               "KV / indexer-K caches and the req_to_token pool stay resident"),
-                gpu_launches=len(calls) * args.steps,
+                gpu_launches=launches_per_step * args.steps,
                 clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"]))
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows)
