@@ -43,8 +43,9 @@ constexpr uint32_t kQBlk = kHc * 128;
 constexpr uint32_t kKvBlk = kTok * 128;
 constexpr uint32_t kQBytes = kBlocks * kQBlk;
 constexpr uint32_t kKvBytes = kBlocks * kKvBlk;
-constexpr int kThreads = 256;
-constexpr int kWorkers = 224;         // warps 0, 2..7 load; warps 4..7 also run the softmax
+constexpr int kThreads = 384;
+constexpr int kWorkers = 352;         // warps 0, 2..11 load; warps 4..11 also run the softmax
+constexpr int kHg = 32;               // heads per softmax group (warps 4..7: heads 0..31, 8..11: 32..63)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColL = 256;   // ones . P^T: every lane holds the running head sums
 constexpr uint32_t kColS = 320;   // S^T accumulator
@@ -142,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             mbar_init(&sm->o_done[m], 1);
         }
         mbar_init(&sm->s_full, 1);
-        mbar_init(&sm->p_full, 128);
+        mbar_init(&sm->p_full, 256);
         mbar_init(&sm->done, 1);
         sm->abort = 0;
         fence_mbar_init();
@@ -213,9 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         }
     } else {
         // ---------------------------------------------------------------- workers
-        // Warps 0, 2, 3 and the softmax warps 4..7 all load the KV tiles; warps
-        // 4..7 also run the softmax and the epilogue.
-        const int lid = (warp == 0 ? 0 : warp - 1) * 32 + lane;  // 0 .. 223
+        // Warps 0, 2, 3 and the softmax warps 4..11 all load the KV tiles; warps
+        // 4..11 also run the softmax and the epilogue, in two groups of four
+        // warps that own 32 heads each.
+        const int lid = (warp == 0 ? 0 : warp - 1) * 32 + lane;  // 0 .. 351
         const bool softmax_warp = warp >= 4;
         // Q of this head group: 64 heads x (64 latent + 8 rope) 16-byte chunks
         for (int q = lid; q < kHc * 72; q += kWorkers) {
@@ -289,15 +291,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                 }
             }
         };
-        // softmax state (warps 4..7)
-        const float4 *m_run4 = reinterpret_cast<const float4 *>(sm->m_run);
+        // softmax state: group g (warps 4+4g .. 7+4g) owns heads hb .. hb+31
+        const int grp = softmax_warp ? (warp - 4) >> 2 : 0;
+        const int hb = grp * kHg;
+        const int gbar = grp == 0 ? 1 : 3;                 // named barrier of the group
+        const float4 *m_run4 = reinterpret_cast<const float4 *>(sm->m_run + hb);
         const int quad = warp & 3;
         const int t = quad * 32 + lane;  // token row of S^T; d row of each O^T block
-        const int et = threadIdx.x - 128;
+        const int et = (threadIdx.x - 128) & 127;           // thread index inside the group
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         if (softmax_warp) {
-            if (et < kHc) sm->m_run[et] = -INFINITY;
-            bar_sync(1, 128);
+            if (et < kHg) sm->m_run[hb + et] = -INFINITY;
+            bar_sync(gbar, 128);
         }
         int done_tiles = 0;
         int cur[2], nxt[2];
@@ -348,70 +353,65 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             if (softmax_warp) {
                 const bool ok = mbar_wait(&sm->kvb_full[0], i & 1, kWaitBudget) && mbar_wait(&sm->s_full, i & 1, kWaitBudget);
                 if (!ok) fail(sm, p.status);
-                if (bar_red_or(1, 128, !ok || sm->abort)) continue;  // the worker-wide check ends the loop
+                if (bar_red_or(gbar, 128, !ok || sm->abort)) continue;  // the worker-wide check ends the loop
                 tc_fence_after();
-                uint32_t sa[32], sb[32];
-                tmem_ld32(lane_base + kColS, sa);
-                tmem_ld32(lane_base + kColS + 32, sb);
+                uint32_t sa[32];
+                tmem_ld32(lane_base + kColS + hb, sa);
                 tmem_ld_wait();
                 const bool valid = sm->idx[t] >= 0;
-                float s[kHc];
+                float s[kHg];
                 bool exceed = false;
 #pragma unroll
-                for (int c = 0; c < kHc / 4; ++c) {
+                for (int c = 0; c < kHg / 4; ++c) {
                     const float4 mr = m_run4[c];
                     const float mv[4] = {mr.x, mr.y, mr.z, mr.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int h = 4 * c + j;
-                        const uint32_t raw = h < 32 ? sa[h] : sb[h - 32];
-                        s[h] = valid ? __uint_as_float(raw) * p.scale_log2 : -INFINITY;
+                        s[h] = valid ? __uint_as_float(sa[h]) * p.scale_log2 : -INFINITY;
                         exceed |= s[h] > mv[j] + kRescale;
                     }
                 }
-                if (bar_red_or(1, 128, exceed)) {
-                    // refresh the running max of every head from this tile's column maxima
+                if (bar_red_or(gbar, 128, exceed)) {
+                    // refresh the running max of the group's heads from this tile's column maxima
 #pragma unroll
-                    for (int h = 0; h < kHc; ++h) {
+                    for (int h = 0; h < kHg; ++h) {
                         float v = s[h];
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-                        if (lane == 0) sm->red[quad][h] = v;
+                        if (lane == 0) sm->red[quad][hb + h] = v;
                     }
-                    bar_sync(1, 128);
-                    if (et < kHc) {
-                        const int h = et;
+                    bar_sync(gbar, 128);
+                    if (et < kHg) {
+                        const int h = hb + et;
                         const float cm = fmaxf(fmaxf(sm->red[0][h], sm->red[1][h]), fmaxf(sm->red[2][h], sm->red[3][h]));
                         const float mo = sm->m_run[h];
                         const float mn = fmaxf(mo, cm);
                         sm->alpha[h] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
                         sm->m_run[h] = mn;
                     }
-                    bar_sync(1, 128);  // alpha[] and m_run[] complete; red[] free for the next refresh
+                    bar_sync(gbar, 128);  // alpha[] and m_run[] complete; red[] free for the next refresh
                     if (i > 0) {
                         // the previous tile's O^T and head sums must be complete before they are rescaled
                         if (!mbar_wait(&sm->o_done[4], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
                         tc_fence_after();
 #pragma unroll 1
-                        for (int m = 0; m < 5; ++m) {  // 4 O^T blocks + the head-sum block
-#pragma unroll 1
-                            for (int half = 0; half < 2; ++half) {
-                                uint32_t v[32];
-                                const uint32_t a = lane_base + m * kHc + half * 32;
-                                tmem_ld32(a, v);
-                                tmem_ld_wait();
+                        for (int m = 0; m < 5; ++m) {  // 4 O^T blocks + the head-sum block, this group's columns
+                            uint32_t v[32];
+                            const uint32_t a = lane_base + m * kHc + hb;
+                            tmem_ld32(a, v);
+                            tmem_ld_wait();
 #pragma unroll
-                                for (int j = 0; j < 32; ++j)
-                                    v[j] = __float_as_uint(__uint_as_float(v[j]) * sm->alpha[half * 32 + j]);
-                                tmem_st32(a, v);
-                            }
+                            for (int j = 0; j < 32; ++j)
+                                v[j] = __float_as_uint(__uint_as_float(v[j]) * sm->alpha[hb + j]);
+                            tmem_st32(a, v);
                         }
                         tmem_st_wait();
                     }
                 }
-                // probabilities relative to the running max, written as P^T row t (bf16)
+                // probabilities relative to the running max, written into P^T row t (bf16)
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {  // heads 8c .. 8c+7 -> one 16-byte chunk of row t
+                for (int c = 0; c < kHg / 8; ++c) {  // heads hb+8c .. hb+8c+7 -> one 16-byte chunk of row t
                     const float4 ma = m_run4[2 * c], mb = m_run4[2 * c + 1];
                     const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
                     uint32_t pk[4];
@@ -422,7 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                         const float p1 = s[h + 1] == -INFINITY ? 0.f : exp2f(s[h + 1] - mv[2 * j + 1]);
                         pk[j] = pack_bf16x2(p0, p1);
                     }
-                    *reinterpret_cast<uint4 *>(p_s + sw128_offset(t, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4 *>(p_s + sw128_offset(t, hb / 8 + c)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -436,45 +437,41 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             const bool have_o = done_tiles > 0 && !sm->abort &&
                                 mbar_wait(&sm->o_done[4], (done_tiles - 1) & 1, kWaitBudget);
             tc_fence_after();
-            uint32_t la[32], lb[32];  // head sums (identical in every lane)
+            uint32_t la[32];  // head sums of the group's heads (identical in every lane)
             if (have_o) {
-                tmem_ld32(lane_base + kColL, la);
-                tmem_ld32(lane_base + kColL + 32, lb);
+                tmem_ld32(lane_base + kColL + hb, la);
                 tmem_ld_wait();
             }
 #pragma unroll 1
             for (int m = 0; m < 4; ++m) {
+                uint32_t v[32];
+                if (have_o) {
+                    tmem_ld32(lane_base + m * kHc + hb, v);
+                    tmem_ld_wait();
+                }
+                const int d = m * 128 + t;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t v[32];
-                    if (have_o) {
-                        tmem_ld32(lane_base + m * kHc + half * 32, v);
-                        tmem_ld_wait();
-                    }
-                    const int d = m * 128 + t;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int h = half * 32 + j;
-                        if (h < hv) {
-                            const float l = have_o ? __uint_as_float(half ? lb[j] : la[j]) : 0.f;
-                            const float o = l > 0.f ? __uint_as_float(v[j]) / l : 0.f;
-                            const int64_t row = (int64_t)r * p.H + hg * kHc + h;
-                            if (p.nsplit == 1)
-                                p.out[row * kDl + d] = __float2bfloat16_rn(o);
-                            else
-                                p.o_part[((int64_t)sp * p.R * p.H + row) * kDl + d] = o;
-                        }
+                for (int j = 0; j < 32; ++j) {
+                    const int h = hb + j;
+                    if (h < hv) {
+                        const float l = have_o ? __uint_as_float(la[j]) : 0.f;
+                        const float o = l > 0.f ? __uint_as_float(v[j]) / l : 0.f;
+                        const int64_t row = (int64_t)r * p.H + hg * kHc + h;
+                        if (p.nsplit == 1)
+                            p.out[row * kDl + d] = __float2bfloat16_rn(o);
+                        else
+                            p.o_part[((int64_t)sp * p.R * p.H + row) * kDl + d] = o;
                     }
                 }
             }
-            if (et < hv) {
-                const float mm = sm->m_run[et];
+            if (et < kHg && hb + et < hv) {
+                const float mm = sm->m_run[hb + et];
                 float l = 0.f;
 #pragma unroll
-                for (int h = 0; h < kHc; ++h)
-                    if (h == et) l = have_o ? __uint_as_float(h < 32 ? la[h] : lb[h - 32]) : 0.f;
+                for (int j = 0; j < 32; ++j)
+                    if (j == et) l = have_o ? __uint_as_float(la[j]) : 0.f;
                 const float lse = l > 0.f ? (mm + log2f(l)) * 0.69314718055994531f : -INFINITY;
-                const int64_t row = (int64_t)r * p.H + hg * kHc + et;
+                const int64_t row = (int64_t)r * p.H + hg * kHc + hb + et;
                 if (p.nsplit == 1)
                     p.lse[row] = lse;
                 else
