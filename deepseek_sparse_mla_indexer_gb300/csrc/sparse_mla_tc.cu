@@ -442,26 +442,35 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                 tmem_ld32(lane_base + kColL + hb, la);
                 tmem_ld_wait();
             }
+            float inv_l[32];  // one reciprocal per head instead of a division per element
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float l = have_o ? __uint_as_float(la[j]) : 0.f;
+                inv_l[j] = l > 0.f ? 1.f / l : 0.f;
+            }
+            const int nh = max(0, min(kHg, hv - hb));  // real heads of this group
+            const int64_t row0 = (int64_t)r * p.H + hg * kHc + hb;
 #pragma unroll 1
             for (int m = 0; m < 4; ++m) {
                 uint32_t v[32];
                 if (have_o) {
                     tmem_ld32(lane_base + m * kHc + hb, v);
                     tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = 0u;
                 }
                 const int d = m * 128 + t;
+                if (p.nsplit == 1) {
+                    __nv_bfloat16 *dst = p.out + row0 * kDl + d;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int h = hb + j;
-                    if (h < hv) {
-                        const float l = have_o ? __uint_as_float(la[j]) : 0.f;
-                        const float o = l > 0.f ? __uint_as_float(v[j]) / l : 0.f;
-                        const int64_t row = (int64_t)r * p.H + hg * kHc + h;
-                        if (p.nsplit == 1)
-                            p.out[row * kDl + d] = __float2bfloat16_rn(o);
-                        else
-                            p.o_part[((int64_t)sp * p.R * p.H + row) * kDl + d] = o;
-                    }
+                    for (int j = 0; j < 32; ++j)
+                        if (j < nh) dst[j * kDl] = __float2bfloat16_rn(__uint_as_float(v[j]) * inv_l[j]);
+                } else {
+                    float *dst = p.o_part + ((int64_t)sp * p.R * p.H + row0) * kDl + d;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < nh) dst[j * kDl] = __uint_as_float(v[j]) * inv_l[j];
                 }
             }
             if (et < kHg && hb + et < hv) {
