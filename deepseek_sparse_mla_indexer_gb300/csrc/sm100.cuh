@@ -283,6 +283,42 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t a_fmt, uint32_t b_fmt
            ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA of the cluster arrives; writes before it are visible after it.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The address of `local` (a shared-memory location of this CTA) in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank)
+{
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+    return ra;
+}
+__device__ __forceinline__ float dsmem_ld_f32(const float *local, uint32_t rank)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(dsmem_addr(local, rank)) : "memory");
+    return v;
+}
+// 16-byte load (the address must be 16-byte aligned).
+__device__ __forceinline__ float4 dsmem_ld_f32x4(const float *local, uint32_t rank)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(dsmem_addr(local, rank))
+                 : "memory");
+    return v;
+}
+
 // Byte offset of element chunk `c16` (16-byte unit within a 128-byte row) of
 // row `row` in a 128-byte-swizzled tile whose rows are 128 bytes apart.
 __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t c16)

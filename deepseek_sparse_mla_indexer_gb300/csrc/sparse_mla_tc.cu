@@ -21,9 +21,14 @@
 //   4. warp 1 issues O^T[512 d, 64 heads] += V^T . P^T, reading the latent
 //      tile a second time as an MN-major operand (4 blocks of 128 d rows,
 //      256 TMEM columns).
-// At the end warps 4..7 normalise O^T by the head sums and write the output
-// (one split) or fp32 partials plus their log-sum-exp (several splits, merged
-// by sparse_mla_combine_kernel in a fixed order).
+// At the end the softmax warps normalise O^T by the head sums and write the
+// output (one split).  With several splits of the top-k list (2 .. 8) the
+// splits of one (row, head group) form a thread-block cluster: each CTA leaves
+// its normalised fp32 partial and per-head log-sum-exp in its own shared
+// memory, and after a cluster barrier every CTA merges one slice of the
+// latent dimension from all partials through distributed shared memory.  More
+// splits than a cluster holds go through global fp32 partials merged by
+// sparse_mla_combine_kernel.
 #include <cstddef>
 
 #include "sparse_mla_tc.cuh"
@@ -54,6 +59,9 @@ constexpr long long kWaitBudget = 2000000000LL;
 constexpr int kNumSms = 152;
 constexpr int kBf16RowBytes = (kDl + kDr) * 2;        // 1152
 constexpr int kFp8RowBytes = kDl + 4 * (kDl / 128) + 2 * kDr;  // 656
+constexpr int kMaxClusterSplit = 8;   // portable cluster size
+constexpr int kMergeItems = (kHc * (kDl / 8) + kThreads - 1) / kThreads;  // 16-byte outputs per thread at 2 splits
+static_assert(kHc * kDl * 4 <= 8 * (int)kKvBlk, "the fp32 partial fits in the latent part of the KV tile");
 
 struct MlaParams {
     const uint8_t *kv;
@@ -69,6 +77,7 @@ struct MlaParams {
     float *lse;
     float *o_part;
     float *lse_part;
+    int cluster_merge;  // splits merged inside the cluster (blockIdx.y = rank)
     int32_t *status;
 };
 
@@ -466,6 +475,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         if (j < nh) dst[j * kDl] = __float2bfloat16_rn(__uint_as_float(v[j]) * inv_l[j]);
+                } else if (p.cluster_merge) {
+                    // the KV tile is dead (every MMA of the split is complete)
+                    float *dst = reinterpret_cast<float *>(kv_s) + (hb * kDl + d);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < nh) dst[j * kDl] = __uint_as_float(v[j]) * inv_l[j];
                 } else {
                     float *dst = p.o_part + ((int64_t)sp * p.R * p.H + row0) * kDl + d;
 #pragma unroll
@@ -483,6 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                 const int64_t row = (int64_t)r * p.H + hg * kHc + hb + et;
                 if (p.nsplit == 1)
                     p.lse[row] = lse;
+                else if (p.cluster_merge)
+                    sm->alpha[hb + et] = lse;  // the rescale factors are dead
                 else
                     p.lse_part[(int64_t)sp * p.R * p.H + row] = lse;
             }
@@ -494,6 +511,79 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+
+    if (p.cluster_merge) {
+        // ---------------------------------------------------------------- split merge
+        // out = sum_q w_q O_q with w_q = exp(lse_q - lse), lse = ln sum_q exp(lse_q)
+        cluster_sync_all();  // every partial and log-sum-exp of the cluster is written
+        const int ns = p.nsplit;
+        const uint32_t me = cluster_ctarank();
+        const int hv = min(kHc, p.H - hg * kHc);
+        const float *part = reinterpret_cast<const float *>(kv_s);
+        float *wts = reinterpret_cast<float *>(kv_s + 8 * kKvBlk);  // [split][head]
+        if (threadIdx.x < kHc) {
+            const int h = threadIdx.x;
+            float l[kMaxClusterSplit];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < kMaxClusterSplit; ++q) {
+                l[q] = q < ns ? dsmem_ld_f32(&sm->alpha[h], (uint32_t)q) : -INFINITY;
+                mx = fmaxf(mx, l[q]);
+            }
+            float wsum = 0.f;
+#pragma unroll
+            for (int q = 0; q < kMaxClusterSplit; ++q)
+                if (q < ns && mx != -INFINITY) wsum += __expf(l[q] - mx);
+#pragma unroll
+            for (int q = 0; q < kMaxClusterSplit; ++q)
+                if (q < ns) wts[q * kHc + h] = (wsum > 0.f && l[q] != -INFINITY) ? __expf(l[q] - mx) / wsum : 0.f;
+            if (me == 0 && h < hv) p.lse[(int64_t)r * p.H + hg * kHc + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+        }
+        __syncthreads();
+        // this CTA's slice of the latent dimension, in 16-byte chunks, for every real head
+        const int c0 = (int)me * (kDl / 4) / ns, c1 = ((int)me + 1) * (kDl / 4) / ns, nc = c1 - c0;
+        const int items = hv * nc;
+        float4 acc[kMergeItems];
+#pragma unroll
+        for (int k = 0; k < kMergeItems; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int base = 0; base < items; base += kMergeItems * kThreads) {
+#pragma unroll 1
+            for (int q = 0; q < ns; ++q) {
+                float4 v[kMergeItems];
+#pragma unroll
+                for (int k = 0; k < kMergeItems; ++k) {  // every load of this split in flight at once
+                    const int e = base + k * kThreads + (int)threadIdx.x;
+                    if (e < items) {
+                        const int h = e / nc, c = c0 + (e - h * nc);
+                        const float *src = part + h * kDl + 4 * c;
+                        v[k] = (uint32_t)q == me ? *reinterpret_cast<const float4 *>(src) : dsmem_ld_f32x4(src, (uint32_t)q);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kMergeItems; ++k) {
+                    const int e = base + k * kThreads + (int)threadIdx.x;
+                    if (e < items) {
+                        const float w = wts[q * kHc + e / nc];
+                        acc[k].x += w * v[k].x; acc[k].y += w * v[k].y;
+                        acc[k].z += w * v[k].z; acc[k].w += w * v[k].w;
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kMergeItems; ++k) {
+                const int e = base + k * kThreads + (int)threadIdx.x;
+                if (e < items) {
+                    const int h = e / nc, c = c0 + (e - h * nc);
+                    uint2 o;
+                    o.x = pack_bf16x2(acc[k].x, acc[k].y);
+                    o.y = pack_bf16x2(acc[k].z, acc[k].w);
+                    *reinterpret_cast<uint2 *>(p.out + ((int64_t)r * p.H + hg * kHc + h) * kDl + 4 * c) = o;
+                    acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+        }
+        cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
     }
 }
 
@@ -560,6 +650,42 @@ bool tc_applicable(nsa_dtype q_dtype, nsa_dtype kv_dtype, int H, int d_latent, i
            d_rope == kDr && (H % kHc == 0 || H < kHc) && H % 16 == 0;
 }
 
+size_t tc_smem_bytes() { return 1024 + kQBytes + kKvBytes + 1024 + sizeof(MlaShared); }
+
+// Whether `ns` splits (2 .. 8) of one (row, head group) can run as one
+// thread-block cluster of this kernel on the current device (queried once per
+// device, split count and KV type).
+bool cluster_merge_ok(int ns, bool fp8)
+{
+    if (ns < 2 || ns > kMaxClusterSplit) return false;
+    constexpr int kMaxDev = 64;
+    static int cache[kMaxDev][kMaxClusterSplit + 1][2];  // 0 unknown, 1 yes, 2 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+    int &c = cache[dev][ns][fp8 ? 1 : 0];
+    if (c == 0) {
+        const void *kern = fp8 ? (const void *)sparse_mla_tc_kernel<true> : (const void *)sparse_mla_tc_kernel<false>;
+        int n = 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, (unsigned)ns, 1);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = tc_smem_bytes();
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = (unsigned)ns;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes()) ==
+                            cudaSuccess &&
+                        cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1;
+        if (!ok) (void)cudaGetLastError();  // a failed query is not the caller's error
+        c = ok ? 1 : 2;
+    }
+    return c == 1;
+}
+
 }  // namespace
 
 size_t sparse_mla_tc_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int H, int d_latent, int d_rope,
@@ -568,7 +694,7 @@ size_t sparse_mla_tc_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int 
     if (!tc_applicable(q_dtype, kv_dtype, H, d_latent, d_rope) || R <= 0 || topk <= 0) return 0;
     int ns, tps;
     choose_split(R, H, topk, ns, tps);
-    if (ns <= 1) return 0;
+    if (ns <= 1 || cluster_merge_ok(ns, kv_dtype == NSA_DT_E4M3)) return 0;
     return (size_t)ns * R * H * (kDl + 1) * sizeof(float);
 }
 
@@ -594,24 +720,30 @@ nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const
     choose_split(R, H, topk, p.nsplit, p.tiles_per_split);
     p.out = (__nv_bfloat16 *)out; p.lse = lse; p.status = status;
     p.o_part = nullptr; p.lse_part = nullptr;
-    if (p.nsplit > 1) {
+    const bool fp8 = kv_dtype == NSA_DT_E4M3;
+    p.cluster_merge = cluster_merge_ok(p.nsplit, fp8) ? 1 : 0;
+    if (p.nsplit > 1 && !p.cluster_merge) {
         if (!workspace) return NSA_ERR_INVALID_ARG;
         p.o_part = (float *)workspace;
         p.lse_part = p.o_part + (size_t)p.nsplit * R * H * kDl;
     }
-    const size_t smem = 1024 + kQBytes + kKvBytes + 1024 + sizeof(MlaShared);
-    dim3 grid((unsigned)((H + kHc - 1) / kHc), (unsigned)p.nsplit, (unsigned)R);
-    if (kv_dtype == NSA_DT_E4M3) {
-        auto kern = sparse_mla_tc_kernel<true>;
-        NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        kern<<<grid, kThreads, smem, stream>>>(p);
-    } else {
-        auto kern = sparse_mla_tc_kernel<false>;
-        NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        kern<<<grid, kThreads, smem, stream>>>(p);
-    }
-    NSA_CUDA_TRY(cudaGetLastError());
-    if (p.nsplit > 1) {
+    const size_t smem = tc_smem_bytes();
+    auto kern = fp8 ? sparse_mla_tc_kernel<true> : sparse_mla_tc_kernel<false>;
+    NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((H + kHc - 1) / kHc), (unsigned)p.nsplit, (unsigned)R);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = p.cluster_merge ? (unsigned)p.nsplit : 1u;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, p));
+    if (p.nsplit > 1 && !p.cluster_merge) {
         const int64_t rows = (int64_t)R * H;
         sparse_mla_combine_kernel<<<(unsigned)rows, 128, 0, stream>>>(p.o_part, p.lse_part, p.nsplit, rows,
                                                                      (__nv_bfloat16 *)out, lse);
