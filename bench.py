@@ -201,26 +201,36 @@ def run_ours(args, rank, world, local_rank):
     if step.status_code() != 0:
         raise RuntimeError(f"device status {step.status_code()} after warm-up")
 
-    # The step as one CUDA graph (how a serving loop replays a decode step), with
-    # timestamp nodes between the stages so that host launch gaps cannot enter
-    # the stage times.
+    # The step as one CUDA graph (how a serving loop replays a decode step).  A
+    # second graph of the same step carries timestamp nodes between the stages
+    # for the per-stage split; the step time comes from the graph without them.
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
     for e in ev:
         e.record(stream)  # creates the events before capture
     torch.cuda.synchronize(dev)
-    graph = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    with torch.cuda.graph(graph, stream=cap):
-        for i, fn in enumerate(calls):
-            record_external(ev[i], cap)
-            fn(cap)
-        record_external(ev[len(calls)], cap)
-    stream.wait_stream(cap)
+
+    def capture(staged):
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            for i, fn in enumerate(calls):
+                if staged:
+                    record_external(ev[i], cap)
+                fn(cap)
+            if staged:
+                record_external(ev[len(calls)], cap)
+        stream.wait_stream(cap)
+        return g
+
+    graph, graph_staged = capture(False), capture(True)
     for _ in range(args.warmup):
         flush.zero_()
         graph.replay()
+        flush.zero_()
+        graph_staged.replay()
     torch.cuda.synchronize(dev)
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
 
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -229,15 +239,20 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter()
     per_stage = {s: [] for s in stages}
-    totals = []
     for k in range(args.steps):
         flush.zero_()  # L2 flush between steps, outside the timed events
+        step_ev[k][0].record(stream)
         graph.replay()
+        step_ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    totals = [a.elapsed_time(b) for a, b in step_ev]
+    t_wall = time.perf_counter() - t_wall
+    for k in range(args.steps):
+        flush.zero_()
+        graph_staged.replay()
         torch.cuda.synchronize(dev)
         for i, s in enumerate(stages):
             per_stage[s].append(ev[i].elapsed_time(ev[i + 1]))
-        totals.append(ev[0].elapsed_time(ev[len(calls)]))
-    t_wall = time.perf_counter() - t_wall
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
@@ -310,7 +325,8 @@ def run_ours(args, rank, world, local_rank):
                 config=dict(workload=WORKLOAD_DESC, global_batch=rows_total,
                             seq_len=int(np.mean(wl.seq_lens)), parallelism=f"replicas x{world}",
                             l2="flushed between steps (512 MB write outside the timed events)",
-                            timing="step replayed as one CUDA graph; device timestamps between stages"),
+                            timing="step replayed as one CUDA graph timed by events around the replay; stage "
+                                   "split from a second graph with timestamp nodes between the stages"),
                 stages=stage_info, roofline=roof,
                 e2e=dict(value=round(rows_total / (e2e_ms * 1e-3), 1), unit="tokens/s",
                          h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),

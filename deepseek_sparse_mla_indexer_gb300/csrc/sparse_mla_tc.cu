@@ -77,7 +77,8 @@ struct MlaParams {
     float *lse;
     float *o_part;
     float *lse_part;
-    int cluster_merge;  // splits merged inside the cluster (blockIdx.y = rank)
+    int pair;           // the two head groups of a row share each KV tile (cluster x = 2)
+    int cluster_merge;  // splits merged inside the cluster (cluster y = nsplit)
     int32_t *status;
 };
 
@@ -87,8 +88,10 @@ struct __align__(16) MlaShared {
     alignas(16) float red[4][kHc];
     alignas(16) int idx[kTok];
     const uint8_t *rowbase[kTok];  // KV row of each token of the tile (slot 0 for masked ones)
-    uint64_t kvb_full[5];          // block pair m of the tile landed (m = 4: rope block)
-    uint64_t o_done[5];            // O^T block m of the tile done (m = 4: every MMA of the tile)
+    uint64_t kvb_full[5];          // block pair m of the tile landed (m = 4: rope block); pair mode: this CTA's rows
+    uint64_t o_done[5];            // O^T block m of the tile done (m = 4: every MMA of the tile); pair mode: in both CTAs
+    uint64_t kvb_peer[5];          // pair mode: the partner's rows of block pair m arrived
+    uint64_t rope_read;            // pair mode: the partner holds this CTA's rope rows (the block may take P^T)
     uint64_t q_full, s_full, p_full, done;
     uint32_t tmem_base;
     volatile int abort;
@@ -144,13 +147,27 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
     const int t0 = sp * p.tiles_per_split;
     const int nt = max(0, min(t0 + p.tiles_per_split, ntiles_all) - t0);
     const int64_t row_bytes = FP8 ? kFp8RowBytes : kBf16RowBytes;
+    // Pair mode: the CTAs of head groups 2k and 2k+1 (ranks r and r^1 of the
+    // cluster) each load half of the rows of every tile and copy that half into
+    // the partner's shared memory, so each selected row enters one SM only.
+    const bool pair = p.pair != 0;
+    const bool clustered = pair || p.cluster_merge;
+    const uint32_t crank = clustered ? cluster_ctarank() : 0u;
+    const uint32_t partner = crank ^ 1u;
+    const uint16_t pair_mask = (uint16_t)(3u << (crank & ~1u));
+    const int half = hg & 1;
+    const int nrow = pair ? kTok / 2 : kTok;           // rows of a tile this CTA loads
+    const int row0 = pair ? half * (kTok / 2) : 0;
+    constexpr uint32_t kHalfBlk = kKvBlk / 2;            // 64 rows of one 128-byte column block
 
     if (threadIdx.x == 0) {
         mbar_init(&sm->q_full, kWorkers);
         for (int m = 0; m < 5; ++m) {
             mbar_init(&sm->kvb_full[m], kWorkers);
-            mbar_init(&sm->o_done[m], 1);
+            mbar_init(&sm->o_done[m], pair ? 2 : 1);
+            mbar_init(&sm->kvb_peer[m], 1);
         }
+        mbar_init(&sm->rope_read, 1);
         mbar_init(&sm->s_full, 1);
         mbar_init(&sm->p_full, 256);
         mbar_init(&sm->done, 1);
@@ -165,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
     }
     tc_fence_before();
     __syncthreads();
+    if (clustered) cluster_sync_all();  // every barrier of the cluster is initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem = sm->tmem_base;
 
@@ -182,8 +200,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 #pragma unroll 1
                 for (int m = 0; m < 5 && ok; ++m) {
                     if (!mbar_wait(&sm->kvb_full[m], i & 1, kWaitBudget)) { fail(sm, p.status); ok = false; break; }
-                    tc_fence_after();
                     const int c0 = m < 4 ? 2 * m : 8, nc = m < 4 ? 2 : 1;
+                    if (pair) {
+                        // this CTA's rows of the pair go to the partner; then wait for the partner's rows
+                        for (int c = c0; c < c0 + nc; ++c)
+                            bulk_copy_to_peer(kv_s + c * kKvBlk + half * kHalfBlk, kHalfBlk, &sm->kvb_peer[m], partner);
+                        mbar_arrive_expect_tx(&sm->kvb_peer[m], nc * kHalfBlk);
+                        if (!mbar_wait(&sm->kvb_peer[m], i & 1, kWaitBudget)) { fail(sm, p.status); ok = false; break; }
+                        if (m == 4) mbar_arrive_remote(&sm->rope_read, partner);  // its rope rows are all here
+                    }
+                    tc_fence_after();
                     for (int c = c0; c < c0 + nc; ++c) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
@@ -208,7 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                         const uint64_t bd = smem_desc(p_addr + k * 2048, kKvBlk, 1024, kSwizzle128B);
                         mma_f16(tmem + m * kHc, ad, bd, idesc_o, (i > 0 || k > 0) ? 1u : 0u);
                     }
-                    mma_commit(&sm->o_done[m]);
+                    if (pair)
+                        mma_commit_multicast(&sm->o_done[m], pair_mask);
+                    else
+                        mma_commit(&sm->o_done[m]);
                 }
                 // head sums l[h] = sum_t P[t, h] in every lane: A = all-ones (one atom, zero strides)
 #pragma unroll
@@ -216,7 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                     const uint64_t bd = smem_desc(p_addr + k * 2048, kKvBlk, 1024, kSwizzle128B);
                     mma_f16(tmem + kColL, ones_d, bd, idesc_o, (i > 0 || k > 0) ? 1u : 0u);
                 }
-                mma_commit(&sm->o_done[4]);
+                if (pair)
+                    mma_commit_multicast(&sm->o_done[4], pair_mask);
+                else
+                    mma_commit(&sm->o_done[4]);
             }
             mma_commit(&sm->done);
             mbar_wait(&sm->done, 0, kWaitBudget);
@@ -259,20 +291,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         // Block pair m of the tile: latent blocks 2m, 2m+1 (m < 4) or the rope block (m = 4).
         auto issue_pair = [&](int m) {
             if (m == 4) {
-                for (int q = lid; q < kTok * 8; q += kWorkers) {
-                    const int row = q >> 3, c = q & 7;
+                for (int q = lid; q < nrow * 8; q += kWorkers) {
+                    const int row = row0 + (q >> 3), c = q & 7;
                     cp_async16(kv_s + 8 * kKvBlk + sw128_offset(row, c),
                                sm->rowbase[row] + (FP8 ? kDl + 16 : 2 * kDl) + c * 16);
                 }
             } else if (!FP8) {
-                for (int q = lid; q < kTok * 16; q += kWorkers) {
-                    const int row = q >> 4, c = 16 * m + (q & 15);
+                for (int q = lid; q < nrow * 16; q += kWorkers) {
+                    const int row = row0 + (q >> 4), c = 16 * m + (q & 15);
                     cp_async16(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7), sm->rowbase[row] + c * 16);
                 }
             } else {
                 // 16 groups of 8 e4m3 codes per row (dims 128m .. 128m+127, one scale)
 #pragma unroll 1
-                for (int q0 = lid; q0 < kTok * 16; q0 += 4 * kWorkers) {
+                for (int q0 = lid; q0 < nrow * 16; q0 += 4 * kWorkers) {
                     uint2 w[4];
                     float sc[4];
 #pragma unroll
@@ -280,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                         const int q = q0 + u * kWorkers;
                         w[u] = make_uint2(0u, 0u);
                         sc[u] = 0.f;
-                        if (q < kTok * 16) {
-                            const uint8_t *rowp = sm->rowbase[q >> 4];
+                        if (q < nrow * 16) {
+                            const uint8_t *rowp = sm->rowbase[row0 + (q >> 4)];
                             w[u] = __ldg(reinterpret_cast<const uint2 *>(rowp + (16 * m + (q & 15)) * 8));
                             sc[u] = __ldg(reinterpret_cast<const float *>(rowp + kDl) + m);
                         }
@@ -289,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int q = q0 + u * kWorkers;
-                        if (q < kTok * 16) {
-                            const int row = q >> 4, c = 16 * m + (q & 15);
+                        if (q < nrow * 16) {
+                            const int row = row0 + (q >> 4), c = 16 * m + (q & 15);
                             uint32_t d4[4];
                             dequant8(w[u], sc[u], d4);
                             *reinterpret_cast<uint4 *>(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7)) =
@@ -352,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             // bring the next tile's rows into L2 while this one is consumed
 #pragma unroll
             for (int u = 0; u < 2; ++u)
-                if (nxt[u] >= 0 && nxt[u] < p.num_slots)
+                if (nxt[u] >= 0 && nxt[u] < p.num_slots && lid + u * kWorkers >= row0 && lid + u * kWorkers < row0 + nrow)
                     prefetch_l2_bulk(p.kv + (int64_t)nxt[u] * row_bytes, (uint32_t)row_bytes);
             cur[0] = nxt[0];
             cur[1] = nxt[1];
@@ -418,6 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                         tmem_st_wait();
                     }
                 }
+                // the rope block takes P^T once the partner holds this CTA's rope rows
+                if (pair && !mbar_wait(&sm->rope_read, i & 1, kWaitBudget)) fail(sm, p.status);
                 // probabilities relative to the running max, written into P^T row t (bf16)
 #pragma unroll
                 for (int c = 0; c < kHg / 8; ++c) {  // heads hb+8c .. hb+8c+7 -> one 16-byte chunk of row t
@@ -445,6 +479,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             const int hv = min(kHc, p.H - hg * kHc);  // real heads of this CTA
             const bool have_o = done_tiles > 0 && !sm->abort &&
                                 mbar_wait(&sm->o_done[4], (done_tiles - 1) & 1, kWaitBudget);
+            if (pair && done_tiles > 0) {
+                // the partner's last arrivals on this CTA's barriers have landed
+                for (int m = 0; m < 4; ++m)
+                    if (!mbar_wait(&sm->o_done[m], (done_tiles - 1) & 1, kWaitBudget)) fail(sm, p.status);
+            }
             tc_fence_after();
             uint32_t la[32];  // head sums of the group's heads (identical in every lane)
             if (have_o) {
@@ -518,7 +557,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         // out = sum_q w_q O_q with w_q = exp(lse_q - lse), lse = ln sum_q exp(lse_q)
         cluster_sync_all();  // every partial and log-sum-exp of the cluster is written
         const int ns = p.nsplit;
-        const uint32_t me = cluster_ctarank();
+        const uint32_t cx = pair ? 2u : 1u;       // cluster rank = head group in the pair + cx * split
+        const uint32_t hx = crank % cx;
+        const uint32_t me = crank / cx;          // this CTA's split
         const int hv = min(kHc, p.H - hg * kHc);
         const float *part = reinterpret_cast<const float *>(kv_s);
         float *wts = reinterpret_cast<float *>(kv_s + 8 * kKvBlk);  // [split][head]
@@ -528,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             float mx = -INFINITY;
 #pragma unroll
             for (int q = 0; q < kMaxClusterSplit; ++q) {
-                l[q] = q < ns ? dsmem_ld_f32(&sm->alpha[h], (uint32_t)q) : -INFINITY;
+                l[q] = q < ns ? dsmem_ld_f32(&sm->alpha[h], hx + cx * (uint32_t)q) : -INFINITY;
                 mx = fmaxf(mx, l[q]);
             }
             float wsum = 0.f;
@@ -557,7 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                     if (e < items) {
                         const int h = e / nc, c = c0 + (e - h * nc);
                         const float *src = part + h * kDl + 4 * c;
-                        v[k] = (uint32_t)q == me ? *reinterpret_cast<const float4 *>(src) : dsmem_ld_f32x4(src, (uint32_t)q);
+                        v[k] = (uint32_t)q == me ? *reinterpret_cast<const float4 *>(src)
+                                                 : dsmem_ld_f32x4(src, hx + cx * (uint32_t)q);
                     }
                 }
 #pragma unroll
@@ -584,6 +626,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             }
         }
         cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
+    } else if (pair) {
+        cluster_sync_all();  // nor while the partner may still copy from or signal into it
     }
 }
 
@@ -652,28 +696,27 @@ bool tc_applicable(nsa_dtype q_dtype, nsa_dtype kv_dtype, int H, int d_latent, i
 
 size_t tc_smem_bytes() { return 1024 + kQBytes + kKvBytes + 1024 + sizeof(MlaShared); }
 
-// Whether `ns` splits (2 .. 8) of one (row, head group) can run as one
-// thread-block cluster of this kernel on the current device (queried once per
-// device, split count and KV type).
-bool cluster_merge_ok(int ns, bool fp8)
+// Whether a cluster of cx x cy CTAs of this kernel can be resident on the
+// current device (queried once per device, shape and KV type).
+bool cluster_fits(int cx, int cy, bool fp8)
 {
-    if (ns < 2 || ns > kMaxClusterSplit) return false;
+    if (cx < 1 || cx > 2 || cy < 1 || cx * cy > kMaxClusterSplit) return false;
     constexpr int kMaxDev = 64;
-    static int cache[kMaxDev][kMaxClusterSplit + 1][2];  // 0 unknown, 1 yes, 2 no
+    static int cache[kMaxDev][3][kMaxClusterSplit + 1][2];  // 0 unknown, 1 yes, 2 no
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
-    int &c = cache[dev][ns][fp8 ? 1 : 0];
+    int &c = cache[dev][cx][cy][fp8 ? 1 : 0];
     if (c == 0) {
         const void *kern = fp8 ? (const void *)sparse_mla_tc_kernel<true> : (const void *)sparse_mla_tc_kernel<false>;
         int n = 0;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(1, (unsigned)ns, 1);
+        cfg.gridDim = dim3((unsigned)cx, (unsigned)cy, 1);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = tc_smem_bytes();
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 1;
-        attr[0].val.clusterDim.y = (unsigned)ns;
+        attr[0].val.clusterDim.x = (unsigned)cx;
+        attr[0].val.clusterDim.y = (unsigned)cy;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
@@ -686,6 +729,15 @@ bool cluster_merge_ok(int ns, bool fp8)
     return c == 1;
 }
 
+// Pair mode when the head groups come in pairs; the splits of a (row, head
+// group [pair]) merge inside the cluster when the cluster stays within 8 CTAs.
+void plan_clusters(int H, int ns, bool fp8, int &pair, int &merge)
+{
+    pair = (H % (2 * kHc) == 0 && cluster_fits(2, 1, fp8)) ? 1 : 0;
+    const int cx = pair ? 2 : 1;
+    merge = (ns >= 2 && cx * ns <= kMaxClusterSplit && cluster_fits(cx, ns, fp8)) ? 1 : 0;
+}
+
 }  // namespace
 
 size_t sparse_mla_tc_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int H, int d_latent, int d_rope,
@@ -694,7 +746,9 @@ size_t sparse_mla_tc_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int 
     if (!tc_applicable(q_dtype, kv_dtype, H, d_latent, d_rope) || R <= 0 || topk <= 0) return 0;
     int ns, tps;
     choose_split(R, H, topk, ns, tps);
-    if (ns <= 1 || cluster_merge_ok(ns, kv_dtype == NSA_DT_E4M3)) return 0;
+    int pair = 0, merge = 0;
+    if (ns > 1) plan_clusters(H, ns, kv_dtype == NSA_DT_E4M3, pair, merge);
+    if (ns <= 1 || merge) return 0;
     return (size_t)ns * R * H * (kDl + 1) * sizeof(float);
 }
 
@@ -721,7 +775,7 @@ nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const
     p.out = (__nv_bfloat16 *)out; p.lse = lse; p.status = status;
     p.o_part = nullptr; p.lse_part = nullptr;
     const bool fp8 = kv_dtype == NSA_DT_E4M3;
-    p.cluster_merge = cluster_merge_ok(p.nsplit, fp8) ? 1 : 0;
+    plan_clusters(H, p.nsplit, fp8, p.pair, p.cluster_merge);
     if (p.nsplit > 1 && !p.cluster_merge) {
         if (!workspace) return NSA_ERR_INVALID_ARG;
         p.o_part = (float *)workspace;
@@ -737,7 +791,7 @@ nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.x = p.pair ? 2u : 1u;
     attr[0].val.clusterDim.y = p.cluster_merge ? (unsigned)p.nsplit : 1u;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
