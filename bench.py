@@ -298,7 +298,9 @@ def run_ours(args, rank, world, local_rank):
 
     ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], world)
 
-    launches_per_step = len(calls) + (1 if step.workspace is not None else 0)  # + split-KV combine
+    _, mla_launches = nsa.nsa_sparse_mla_plan(wl.q_dtype, wl.kv_dtype, wl.R, wl.H, wl.d_latent, wl.d_rope,
+                                              wl.topk)
+    launches_per_step = len(calls) - 1 + mla_launches  # one launch per other stage
     md_len = step.md["seqlens_expanded"].cpu().numpy()
     work = algorithmic_work(wl, md_len)
     peaks = load_peaks()

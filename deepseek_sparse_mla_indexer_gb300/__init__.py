@@ -21,7 +21,7 @@ __all__ = [
     "NsaError", "load", "MODE_DECODE", "MODE_EXTEND", "MODE_TARGET_VERIFY", "DT_F32", "DT_BF16",
     "DT_E4M3", "nsa_metadata", "alloc_metadata", "nsa_local_virtual_batches", "nsa_effective_chunk_size",
     "nsa_indexer_logits", "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes",
-    "nsa_status_read", "nsa_status_string", "nsa_abi_version", "EXPORTED_SYMBOLS",
+    "nsa_sparse_mla_plan", "nsa_status_read", "nsa_status_string", "nsa_abi_version", "EXPORTED_SYMBOLS",
 ]
 
 MODE_DECODE, MODE_EXTEND, MODE_TARGET_VERIFY = 0, 1, 2
@@ -31,7 +31,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_BOUNDS, ERR_TIMEOUT = range(
 EXPORTED_SYMBOLS = [
     "nsa_status_string", "nsa_abi_version", "nsa_status_read", "nsa_metadata",
     "nsa_effective_chunk_size", "nsa_local_virtual_batches", "nsa_indexer_logits",
-    "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes",
+    "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes", "nsa_sparse_mla_plan",
 ]
 
 _lib = None
@@ -66,6 +66,7 @@ def load(build_if_missing: bool = True):
         "nsa_topk_transform": ([P, L, P, P, P, L, I, I, I, P, L, P, P], I),
         "nsa_sparse_mla": ([I, I, P, L, L, P, L, L, P, L, P, L, I, I, I, I, I, F, P, P, P, S, P, P], I),
         "nsa_sparse_mla_workspace_bytes": ([I, I, I, I, I, I, I], S),
+        "nsa_sparse_mla_plan": ([I, I, I, I, I, I, I, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -210,6 +211,15 @@ def nsa_topk_transform(logits: torch.Tensor, row_len: torch.Tensor, row_to_req: 
 def nsa_sparse_mla_workspace_bytes(q_dtype: int, kv_dtype: int, R: int, H: int, d_latent: int, d_rope: int,
                                    topk: int) -> int:
     return int(load().nsa_sparse_mla_workspace_bytes(q_dtype, kv_dtype, R, H, d_latent, d_rope, topk))
+
+
+def nsa_sparse_mla_plan(q_dtype: int, kv_dtype: int, R: int, H: int, d_latent: int, d_rope: int,
+                        topk: int):
+    """(splits per top-k list, kernel launches per call) of nsa_sparse_mla for this shape."""
+    ns, nl = C.c_int(0), C.c_int(0)
+    _check("nsa_sparse_mla_plan", load().nsa_sparse_mla_plan(q_dtype, kv_dtype, R, H, d_latent, d_rope, topk,
+                                                             C.byref(ns), C.byref(nl)))
+    return int(ns.value), int(nl.value)
 
 
 def nsa_sparse_mla(q_dtype: int, kv_dtype: int, q_nope: torch.Tensor, q_rope: torch.Tensor, kv: torch.Tensor,

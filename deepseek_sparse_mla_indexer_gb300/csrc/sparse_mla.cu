@@ -197,6 +197,20 @@ extern "C" size_t nsa_sparse_mla_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv
     return nsa::sparse_mla_tc_workspace_bytes(q_dtype, kv_dtype, R, H, d_latent, d_rope, topk);
 }
 
+extern "C" nsa_status nsa_sparse_mla_plan(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int H, int d_latent,
+                                          int d_rope, int topk, int *nsplit, int *launches)
+{
+    if (!nsplit || !launches) return NSA_ERR_INVALID_ARG;
+    if (R < 0 || H < 1 || d_latent < 1 || d_rope < 0 || topk < 1) return NSA_ERR_INVALID_ARG;
+    const bool combo_ok = (q_dtype == NSA_DT_F32 && kv_dtype == NSA_DT_F32) ||
+                          (q_dtype == NSA_DT_BF16 && (kv_dtype == NSA_DT_BF16 || kv_dtype == NSA_DT_E4M3));
+    if (!combo_ok || (kv_dtype == NSA_DT_E4M3 && d_latent % 128 != 0)) return NSA_ERR_UNSUPPORTED;
+    *nsplit = 1;
+    *launches = R == 0 ? 0 : 1;
+    if (R > 0) nsa::sparse_mla_tc_plan(q_dtype, kv_dtype, R, H, d_latent, d_rope, topk, nsplit, launches);
+    return NSA_OK;
+}
+
 extern "C" nsa_status nsa_sparse_mla(nsa_dtype q_dtype, nsa_dtype kv_dtype, const void *q_nope_dev,
                                      int64_t nope_ld_r, int64_t nope_ld_h, const void *q_rope_dev,
                                      int64_t rope_ld_r, int64_t rope_ld_h, const void *kv_dev,

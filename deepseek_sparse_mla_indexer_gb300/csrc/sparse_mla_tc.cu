@@ -8,27 +8,28 @@
 //
 // One CTA = one query row x 64 heads x one split of the top-k list.  Per tile
 // of 128 selected KV rows:
-//   1. loader warps (0, 2, 3) copy the 128 rows into shared memory with 16-byte
-//      cp.async (fp8 rows: loaded, dequantised to bf16 and stored), laid out as
-//      9 column blocks of 64 bf16, 128-byte swizzled, K-major -- and prefetch
-//      the next tile's rows into L2 so HBM keeps streaming during compute;
+//   1. the loader threads (warps 0, 2..11) copy the 128 rows into shared
+//      memory with 16-byte cp.async (fp8 rows: loaded into registers,
+//      dequantised to bf16 and stored), laid out as 9 column blocks of 64 bf16,
+//      128-byte swizzled, K-major; the five block pairs of a tile are all in
+//      flight at once (one commit group each) and each is released to the MMA
+//      warp as it lands; the next tile's rows are prefetched into L2;
 //   2. warp 1 issues S^T[128 tok, 64 heads] = KV_tile . Q^T on tcgen05 (TMEM);
-//   3. warps 4..7 (one thread per token) run the online softmax over the
-//      token axis: a lazily refreshed running max per head (refreshed only
-//      when a score exceeds it by 2^8; the TMEM accumulator is rescaled then),
-//      per-thread partial sums of the probabilities, and P^T written as bf16
-//      into the rope block (free once S^T is done) in the MN-major layout;
+//   3. warps 4..11 (two groups of 4 warps, 32 heads each; one thread per
+//      token) run the online softmax over the token axis: a lazily refreshed
+//      running max per head (refreshed only when a score exceeds it by 2^8; the
+//      TMEM accumulators are rescaled then), and P^T written as bf16 into the
+//      rope block (free once S^T is done) in the MN-major layout;
 //   4. warp 1 issues O^T[512 d, 64 heads] += V^T . P^T, reading the latent
 //      tile a second time as an MN-major operand (4 blocks of 128 d rows,
-//      256 TMEM columns).
-// At the end the softmax warps normalise O^T by the head sums and write the
-// output (one split).  With several splits of the top-k list (2 .. 8) the
-// splits of one (row, head group) form a thread-block cluster: each CTA leaves
-// its normalised fp32 partial and per-head log-sum-exp in its own shared
-// memory, and after a cluster barrier every CTA merges one slice of the
-// latent dimension from all partials through distributed shared memory.  More
-// splits than a cluster holds go through global fp32 partials merged by
-// sparse_mla_combine_kernel.
+//      256 TMEM columns), and the head sums l = ones . P^T.
+// At the end the softmax warps normalise O^T by the head sums, stage it in the
+// dead KV tile and write it out with 16-byte stores: the bf16 output (one
+// split) or fp32 partials plus their log-sum-exp (several splits).  Up to 8
+// splits of a (row, head group) form a thread-block cluster; after a cluster
+// barrier each CTA merges one slice of the latent dimension from all partials
+// (its own from shared memory, the others from L2).  More splits are merged by
+// sparse_mla_combine_kernel.  Both merges sum the splits in a fixed order.
 #include <cstddef>
 
 #include "sparse_mla_tc.cuh"
@@ -77,8 +78,7 @@ struct MlaParams {
     float *lse;
     float *o_part;
     float *lse_part;
-    int pair;           // the two head groups of a row share each KV tile (cluster x = 2)
-    int cluster_merge;  // splits merged inside the cluster (cluster y = nsplit)
+    int cluster_merge;  // splits merged inside the cluster (cluster y = nsplit, rank = split)
     int32_t *status;
 };
 
@@ -88,10 +88,8 @@ struct __align__(16) MlaShared {
     alignas(16) float red[4][kHc];
     alignas(16) int idx[kTok];
     const uint8_t *rowbase[kTok];  // KV row of each token of the tile (slot 0 for masked ones)
-    uint64_t kvb_full[5];          // block pair m of the tile landed (m = 4: rope block); pair mode: this CTA's rows
-    uint64_t o_done[5];            // O^T block m of the tile done (m = 4: every MMA of the tile); pair mode: in both CTAs
-    uint64_t kvb_peer[5];          // pair mode: the partner's rows of block pair m arrived
-    uint64_t rope_read;            // pair mode: the partner holds this CTA's rope rows (the block may take P^T)
+    uint64_t kvb_full[5];          // block pair m of the tile landed (m = 4: rope block)
+    uint64_t o_done[5];            // O^T block m of the tile done (m = 4: every MMA of the tile)
     uint64_t q_full, s_full, p_full, done;
     uint32_t tmem_base;
     volatile int abort;
@@ -127,7 +125,7 @@ __device__ __forceinline__ void dequant8(uint2 w, float sc, uint32_t *dst4)
     }
 }
 
-// Worker-group barrier (warps 0, 2..7).
+// Worker-group barrier (warps 0, 2..11).
 __device__ __forceinline__ void worker_sync() { bar_sync(2, kWorkers); }
 
 template <bool FP8>
@@ -147,27 +145,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
     const int t0 = sp * p.tiles_per_split;
     const int nt = max(0, min(t0 + p.tiles_per_split, ntiles_all) - t0);
     const int64_t row_bytes = FP8 ? kFp8RowBytes : kBf16RowBytes;
-    // Pair mode: the CTAs of head groups 2k and 2k+1 (ranks r and r^1 of the
-    // cluster) each load half of the rows of every tile and copy that half into
-    // the partner's shared memory, so each selected row enters one SM only.
-    const bool pair = p.pair != 0;
-    const bool clustered = pair || p.cluster_merge;
-    const uint32_t crank = clustered ? cluster_ctarank() : 0u;
-    const uint32_t partner = crank ^ 1u;
-    const uint16_t pair_mask = (uint16_t)(3u << (crank & ~1u));
-    const int half = hg & 1;
-    const int nrow = pair ? kTok / 2 : kTok;           // rows of a tile this CTA loads
-    const int row0 = pair ? half * (kTok / 2) : 0;
-    constexpr uint32_t kHalfBlk = kKvBlk / 2;            // 64 rows of one 128-byte column block
 
     if (threadIdx.x == 0) {
         mbar_init(&sm->q_full, kWorkers);
         for (int m = 0; m < 5; ++m) {
             mbar_init(&sm->kvb_full[m], kWorkers);
-            mbar_init(&sm->o_done[m], pair ? 2 : 1);
-            mbar_init(&sm->kvb_peer[m], 1);
+            mbar_init(&sm->o_done[m], 1);
         }
-        mbar_init(&sm->rope_read, 1);
         mbar_init(&sm->s_full, 1);
         mbar_init(&sm->p_full, 256);
         mbar_init(&sm->done, 1);
@@ -182,7 +166,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
     }
     tc_fence_before();
     __syncthreads();
-    if (clustered) cluster_sync_all();  // every barrier of the cluster is initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem = sm->tmem_base;
 
@@ -200,16 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 #pragma unroll 1
                 for (int m = 0; m < 5 && ok; ++m) {
                     if (!mbar_wait(&sm->kvb_full[m], i & 1, kWaitBudget)) { fail(sm, p.status); ok = false; break; }
-                    const int c0 = m < 4 ? 2 * m : 8, nc = m < 4 ? 2 : 1;
-                    if (pair) {
-                        // this CTA's rows of the pair go to the partner; then wait for the partner's rows
-                        for (int c = c0; c < c0 + nc; ++c)
-                            bulk_copy_to_peer(kv_s + c * kKvBlk + half * kHalfBlk, kHalfBlk, &sm->kvb_peer[m], partner);
-                        mbar_arrive_expect_tx(&sm->kvb_peer[m], nc * kHalfBlk);
-                        if (!mbar_wait(&sm->kvb_peer[m], i & 1, kWaitBudget)) { fail(sm, p.status); ok = false; break; }
-                        if (m == 4) mbar_arrive_remote(&sm->rope_read, partner);  // its rope rows are all here
-                    }
                     tc_fence_after();
+                    const int c0 = m < 4 ? 2 * m : 8, nc = m < 4 ? 2 : 1;
                     for (int c = c0; c < c0 + nc; ++c) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
@@ -234,10 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                         const uint64_t bd = smem_desc(p_addr + k * 2048, kKvBlk, 1024, kSwizzle128B);
                         mma_f16(tmem + m * kHc, ad, bd, idesc_o, (i > 0 || k > 0) ? 1u : 0u);
                     }
-                    if (pair)
-                        mma_commit_multicast(&sm->o_done[m], pair_mask);
-                    else
-                        mma_commit(&sm->o_done[m]);
+                    mma_commit(&sm->o_done[m]);
                 }
                 // head sums l[h] = sum_t P[t, h] in every lane: A = all-ones (one atom, zero strides)
 #pragma unroll
@@ -245,10 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                     const uint64_t bd = smem_desc(p_addr + k * 2048, kKvBlk, 1024, kSwizzle128B);
                     mma_f16(tmem + kColL, ones_d, bd, idesc_o, (i > 0 || k > 0) ? 1u : 0u);
                 }
-                if (pair)
-                    mma_commit_multicast(&sm->o_done[4], pair_mask);
-                else
-                    mma_commit(&sm->o_done[4]);
+                mma_commit(&sm->o_done[4]);
             }
             mma_commit(&sm->done);
             mbar_wait(&sm->done, 0, kWaitBudget);
@@ -260,7 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         // warps that own 32 heads each.
         const int lid = (warp == 0 ? 0 : warp - 1) * 32 + lane;  // 0 .. 351
         const bool softmax_warp = warp >= 4;
-        // Q of this head group: 64 heads x (64 latent + 8 rope) 16-byte chunks
+        // Q of this head group: 64 heads x (64 latent + 8 rope) 16-byte chunks; its
+        // commit group is the oldest, so it completes under the first tile's loads
         for (int q = lid; q < kHc * 72; q += kWorkers) {
             const int h = q / 72, c = q - h * 72;
             uint8_t *dst = q_s + (c >> 3) * kQBlk + sw128_offset(h, c & 7);
@@ -274,64 +244,42 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             }
         }
         cp_async_commit();
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        mbar_arrive(&sm->q_full);
+        auto release_q = [&]() {
+            fence_proxy_async_smem();
+            mbar_arrive(&sm->q_full);
+        };
+        if (nt == 0) {
+            cp_async_wait_all();
+            release_q();
+        }
 
         const int32_t *irow = p.indices + (int64_t)r * p.indices_ld;
-        // the indices of a tile are read one tile ahead (lanes own j = lid, lid + 96)
-        auto fetch_idx = [&](int tile, int (&v)[2]) {
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int j = lid + u * kWorkers;
-                const int pos = tile * kTok + j;
-                v[u] = (j < kTok && tile < t0 + nt && pos < p.topk) ? __ldg(irow + pos) : -1;
-            }
+        // the index of token j of a tile is read one tile ahead by worker j
+        auto fetch_idx = [&](int tile) -> int {
+            const int pos = tile * kTok + lid;
+            return (lid < kTok && tile < t0 + nt && pos < p.topk) ? __ldg(irow + pos) : -1;
         };
-        // Block pair m of the tile: latent blocks 2m, 2m+1 (m < 4) or the rope block (m = 4).
+        // Block pair m of the tile (latent blocks 2m, 2m+1 for m < 4; the rope block for m = 4) by cp.async
         auto issue_pair = [&](int m) {
             if (m == 4) {
-                for (int q = lid; q < nrow * 8; q += kWorkers) {
-                    const int row = row0 + (q >> 3), c = q & 7;
+                for (int q = lid; q < kTok * 8; q += kWorkers) {
+                    const int row = q >> 3, c = q & 7;
                     cp_async16(kv_s + 8 * kKvBlk + sw128_offset(row, c),
                                sm->rowbase[row] + (FP8 ? kDl + 16 : 2 * kDl) + c * 16);
                 }
-            } else if (!FP8) {
-                for (int q = lid; q < nrow * 16; q += kWorkers) {
-                    const int row = row0 + (q >> 4), c = 16 * m + (q & 15);
-                    cp_async16(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7), sm->rowbase[row] + c * 16);
-                }
             } else {
-                // 16 groups of 8 e4m3 codes per row (dims 128m .. 128m+127, one scale)
-#pragma unroll 1
-                for (int q0 = lid; q0 < nrow * 16; q0 += 4 * kWorkers) {
-                    uint2 w[4];
-                    float sc[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int q = q0 + u * kWorkers;
-                        w[u] = make_uint2(0u, 0u);
-                        sc[u] = 0.f;
-                        if (q < nrow * 16) {
-                            const uint8_t *rowp = sm->rowbase[row0 + (q >> 4)];
-                            w[u] = __ldg(reinterpret_cast<const uint2 *>(rowp + (16 * m + (q & 15)) * 8));
-                            sc[u] = __ldg(reinterpret_cast<const float *>(rowp + kDl) + m);
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int q = q0 + u * kWorkers;
-                        if (q < nrow * 16) {
-                            const int row = row0 + (q >> 4), c = 16 * m + (q & 15);
-                            uint32_t d4[4];
-                            dequant8(w[u], sc[u], d4);
-                            *reinterpret_cast<uint4 *>(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7)) =
-                                make_uint4(d4[0], d4[1], d4[2], d4[3]);
-                        }
-                    }
+                for (int q = lid; q < kTok * 16; q += kWorkers) {
+                    const int row = q >> 4, c = 16 * m + (q & 15);
+                    cp_async16(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7), sm->rowbase[row] + c * 16);
                 }
             }
         };
+        auto release_pair = [&](int m) {
+            fence_proxy_async_smem();
+            mbar_arrive(&sm->kvb_full[m]);
+        };
+        // fp8 rows: each worker dequantises up to kF8Items groups of 8 e4m3 codes per latent block pair
+        constexpr int kF8Items = (kTok * 16 + kWorkers - 1) / kWorkers;
         // softmax state: group g (warps 4+4g .. 7+4g) owns heads hb .. hb+31
         const int grp = softmax_warp ? (warp - 4) >> 2 : 0;
         const int hb = grp * kHg;
@@ -346,51 +294,92 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             bar_sync(gbar, 128);
         }
         int done_tiles = 0;
-        int cur[2], nxt[2];
-        fetch_idx(t0, cur);
+        int cur = fetch_idx(t0);
         for (int i = 0; i < nt; ++i) {
             // block pair 0 (and the token table) is free once the previous tile's O^T block 0 is done
             if (i > 0 && !mbar_wait(&sm->o_done[0], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
             if (bar_red_or(2, kWorkers, sm->abort != 0)) break;  // uniform over the workers
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int j = lid + u * kWorkers;
-                if (j < kTok) {
-                    int v = cur[u];
-                    if (v < -1 || v >= p.num_slots) {
-                        set_status(p.status, NSA_ERR_BOUNDS);
-                        v = -1;
-                    }
-                    sm->idx[j] = v;
-                    sm->rowbase[j] = p.kv + (int64_t)(v < 0 ? 0 : v) * row_bytes;  // masked rows read slot 0
+            if (lid < kTok) {
+                int v = cur;
+                if (v < -1 || v >= p.num_slots) {
+                    set_status(p.status, NSA_ERR_BOUNDS);
+                    v = -1;
                 }
+                sm->idx[lid] = v;
+                sm->rowbase[lid] = p.kv + (int64_t)(v < 0 ? 0 : v) * row_bytes;  // masked rows read slot 0
             }
-            fetch_idx(t0 + i + 1, nxt);
+            const int nxt = fetch_idx(t0 + i + 1);
             worker_sync();
+            if (!FP8) {
+                // every block pair in flight at once, one commit group each, released in order
 #pragma unroll 1
-            for (int m = 0; m < 5; ++m) {
-                if (m > 0 && i > 0 && !mbar_wait(&sm->o_done[m], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
-                issue_pair(m);
-                cp_async_commit();
-                if (FP8 && m < 4) {  // dequantised pairs are written with plain stores
-                    fence_proxy_async_smem();
-                    mbar_arrive(&sm->kvb_full[m]);
-                } else if (!FP8 && m > 0) {
-                    cp_async_wait_group<1>();
-                    fence_proxy_async_smem();
-                    mbar_arrive(&sm->kvb_full[m - 1]);
+                for (int m = 0; m < 5; ++m) {
+                    if (m > 0 && i > 0 && !mbar_wait(&sm->o_done[m], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
+                    issue_pair(m);
+                    cp_async_commit();
                 }
-            }
-            // bring the next tile's rows into L2 while this one is consumed
+                if (nxt >= 0 && nxt < p.num_slots) prefetch_l2_bulk(p.kv + (int64_t)nxt * row_bytes, (uint32_t)row_bytes);
+                if (i == 0) {
+                    cp_async_wait_group<5>();
+                    release_q();
+                }
+                cp_async_wait_group<4>();
+                release_pair(0);
+                cp_async_wait_group<3>();
+                release_pair(1);
+                cp_async_wait_group<2>();
+                release_pair(2);
+                cp_async_wait_group<1>();
+                release_pair(3);
+                cp_async_wait_group<0>();
+                release_pair(4);
+            } else {
+                // latent codes and scales of all four pairs go into registers first; the rope
+                // rows (bf16) go by cp.async
+                uint2 w[4][kF8Items];
+                float sc[4][kF8Items];
 #pragma unroll
-            for (int u = 0; u < 2; ++u)
-                if (nxt[u] >= 0 && nxt[u] < p.num_slots && lid + u * kWorkers >= row0 && lid + u * kWorkers < row0 + nrow)
-                    prefetch_l2_bulk(p.kv + (int64_t)nxt[u] * row_bytes, (uint32_t)row_bytes);
-            cur[0] = nxt[0];
-            cur[1] = nxt[1];
-            cp_async_wait_group<0>();
-            fence_proxy_async_smem();
-            mbar_arrive(&sm->kvb_full[4]);
+                for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                    for (int u = 0; u < kF8Items; ++u) {
+                        const int q = lid + u * kWorkers;
+                        w[m][u] = make_uint2(0u, 0u);
+                        sc[m][u] = 0.f;
+                        if (q < kTok * 16) {
+                            const uint8_t *rowp = sm->rowbase[q >> 4];
+                            w[m][u] = __ldg(reinterpret_cast<const uint2 *>(rowp + (16 * m + (q & 15)) * 8));
+                            sc[m][u] = __ldg(reinterpret_cast<const float *>(rowp + kDl) + m);
+                        }
+                    }
+                }
+                if (i > 0 && !mbar_wait(&sm->o_done[4], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
+                issue_pair(4);
+                cp_async_commit();
+                if (nxt >= 0 && nxt < p.num_slots) prefetch_l2_bulk(p.kv + (int64_t)nxt * row_bytes, (uint32_t)row_bytes);
+                if (i == 0) {
+                    cp_async_wait_group<1>();
+                    release_q();
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    if (m > 0 && i > 0 && !mbar_wait(&sm->o_done[m], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
+#pragma unroll
+                    for (int u = 0; u < kF8Items; ++u) {
+                        const int q = lid + u * kWorkers;
+                        if (q < kTok * 16) {
+                            const int row = q >> 4, c = 16 * m + (q & 15);
+                            uint32_t d4[4];
+                            dequant8(w[m][u], sc[m][u], d4);
+                            *reinterpret_cast<uint4 *>(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7)) =
+                                make_uint4(d4[0], d4[1], d4[2], d4[3]);
+                        }
+                    }
+                    release_pair(m);
+                }
+                cp_async_wait_group<0>();
+                release_pair(4);
+            }
+            cur = nxt;
             if (softmax_warp) {
                 const bool ok = mbar_wait(&sm->kvb_full[0], i & 1, kWaitBudget) && mbar_wait(&sm->s_full, i & 1, kWaitBudget);
                 if (!ok) fail(sm, p.status);
@@ -450,8 +439,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                         tmem_st_wait();
                     }
                 }
-                // the rope block takes P^T once the partner holds this CTA's rope rows
-                if (pair && !mbar_wait(&sm->rope_read, i & 1, kWaitBudget)) fail(sm, p.status);
                 // probabilities relative to the running max, written into P^T row t (bf16)
 #pragma unroll
                 for (int c = 0; c < kHg / 8; ++c) {  // heads hb+8c .. hb+8c+7 -> one 16-byte chunk of row t
@@ -479,11 +466,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             const int hv = min(kHc, p.H - hg * kHc);  // real heads of this CTA
             const bool have_o = done_tiles > 0 && !sm->abort &&
                                 mbar_wait(&sm->o_done[4], (done_tiles - 1) & 1, kWaitBudget);
-            if (pair && done_tiles > 0) {
-                // the partner's last arrivals on this CTA's barriers have landed
-                for (int m = 0; m < 4; ++m)
-                    if (!mbar_wait(&sm->o_done[m], (done_tiles - 1) & 1, kWaitBudget)) fail(sm, p.status);
-            }
             tc_fence_after();
             uint32_t la[32];  // head sums of the group's heads (identical in every lane)
             if (have_o) {
@@ -498,6 +480,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             }
             const int nh = max(0, min(kHg, hv - hb));  // real heads of this group
             const int64_t row0 = (int64_t)r * p.H + hg * kHc + hb;
+            const bool split = p.nsplit > 1;
+            // normalised O staged in the dead KV tile, heads x 512: fp32 partial (split) or bf16
+            float *stage_f = reinterpret_cast<float *>(kv_s);
+            __nv_bfloat16 *stage_h = reinterpret_cast<__nv_bfloat16 *>(kv_s);
 #pragma unroll 1
             for (int m = 0; m < 4; ++m) {
                 uint32_t v[32];
@@ -509,22 +495,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                     for (int j = 0; j < 32; ++j) v[j] = 0u;
                 }
                 const int d = m * 128 + t;
-                if (p.nsplit == 1) {
-                    __nv_bfloat16 *dst = p.out + row0 * kDl + d;
+                if (split) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j < nh) dst[j * kDl] = __float2bfloat16_rn(__uint_as_float(v[j]) * inv_l[j]);
-                } else if (p.cluster_merge) {
-                    // the KV tile is dead (every MMA of the split is complete)
-                    float *dst = reinterpret_cast<float *>(kv_s) + (hb * kDl + d);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j < nh) dst[j * kDl] = __uint_as_float(v[j]) * inv_l[j];
+                    for (int j = 0; j < 32; ++j) stage_f[(hb + j) * kDl + d] = __uint_as_float(v[j]) * inv_l[j];
                 } else {
-                    float *dst = p.o_part + ((int64_t)sp * p.R * p.H + row0) * kDl + d;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j < nh) dst[j * kDl] = __uint_as_float(v[j]) * inv_l[j];
+                    for (int j = 0; j < 32; ++j) stage_h[(hb + j) * kDl + d] = __float2bfloat16_rn(__uint_as_float(v[j]) * inv_l[j]);
                 }
             }
             if (et < kHg && hb + et < hv) {
@@ -534,13 +510,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                 for (int j = 0; j < 32; ++j)
                     if (j == et) l = have_o ? __uint_as_float(la[j]) : 0.f;
                 const float lse = l > 0.f ? (mm + log2f(l)) * 0.69314718055994531f : -INFINITY;
-                const int64_t row = (int64_t)r * p.H + hg * kHc + hb + et;
-                if (p.nsplit == 1)
-                    p.lse[row] = lse;
-                else if (p.cluster_merge)
-                    sm->alpha[hb + et] = lse;  // the rescale factors are dead
+                if (split)
+                    p.lse_part[(int64_t)sp * p.R * p.H + row0 + et] = lse;
                 else
-                    p.lse_part[(int64_t)sp * p.R * p.H + row] = lse;
+                    p.lse[row0 + et] = lse;
+            }
+            bar_sync(gbar, 128);  // the group's staged rows are complete
+            // the group's heads are contiguous in global memory: 16-byte copies
+            if (split) {
+                // in a cluster merge only the slices that the other splits merge leave the CTA
+                const int ns = p.nsplit;
+                const int s0 = p.cluster_merge ? sp * (kDl / 4) / ns : 0;
+                const int s1 = p.cluster_merge ? (sp + 1) * (kDl / 4) / ns : 0;
+                const float4 *src = reinterpret_cast<const float4 *>(stage_f + hb * kDl);
+                float4 *dst = reinterpret_cast<float4 *>(p.o_part + ((int64_t)sp * p.R * p.H + row0) * kDl);
+                for (int k = et; k < nh * (kDl / 4); k += 128) {
+                    const int c = k & (kDl / 4 - 1);
+                    if (c < s0 || c >= s1) dst[k] = src[k];
+                }
+            } else {
+                const uint4 *src = reinterpret_cast<const uint4 *>(stage_h + hb * kDl);
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out + row0 * kDl);
+                for (int k = et; k < nh * (kDl / 8); k += 128) dst[k] = src[k];
             }
         }
     }
@@ -554,14 +545,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 
     if (p.cluster_merge) {
         // ---------------------------------------------------------------- split merge
-        // out = sum_q w_q O_q with w_q = exp(lse_q - lse), lse = ln sum_q exp(lse_q)
-        cluster_sync_all();  // every partial and log-sum-exp of the cluster is written
+        // out = sum_q w_q O_q with w_q = exp(lse_q - lse), lse = ln sum_q exp(lse_q).
+        // The splits of this (row, head group) are the CTAs of the cluster (rank = split).
+        cluster_sync_all();  // every split's partial slices and log-sum-exp are in global memory
         const int ns = p.nsplit;
-        const uint32_t cx = pair ? 2u : 1u;       // cluster rank = head group in the pair + cx * split
-        const uint32_t hx = crank % cx;
-        const uint32_t me = crank / cx;          // this CTA's split
         const int hv = min(kHc, p.H - hg * kHc);
-        const float *part = reinterpret_cast<const float *>(kv_s);
+        const int64_t hrow0 = (int64_t)r * p.H + hg * kHc;
+        const int64_t split_stride = (int64_t)p.R * p.H;
+        const float *stage_f = reinterpret_cast<const float *>(kv_s);
         float *wts = reinterpret_cast<float *>(kv_s + 8 * kKvBlk);  // [split][head]
         if (threadIdx.x < kHc) {
             const int h = threadIdx.x;
@@ -569,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             float mx = -INFINITY;
 #pragma unroll
             for (int q = 0; q < kMaxClusterSplit; ++q) {
-                l[q] = q < ns ? dsmem_ld_f32(&sm->alpha[h], hx + cx * (uint32_t)q) : -INFINITY;
+                l[q] = (q < ns && h < hv) ? __ldcg(p.lse_part + q * split_stride + hrow0 + h) : -INFINITY;
                 mx = fmaxf(mx, l[q]);
             }
             float wsum = 0.f;
@@ -579,16 +570,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 #pragma unroll
             for (int q = 0; q < kMaxClusterSplit; ++q)
                 if (q < ns) wts[q * kHc + h] = (wsum > 0.f && l[q] != -INFINITY) ? __expf(l[q] - mx) / wsum : 0.f;
-            if (me == 0 && h < hv) p.lse[(int64_t)r * p.H + hg * kHc + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+            if (sp == 0 && h < hv) p.lse[hrow0 + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
         }
         __syncthreads();
         // this CTA's slice of the latent dimension, in 16-byte chunks, for every real head
-        const int c0 = (int)me * (kDl / 4) / ns, c1 = ((int)me + 1) * (kDl / 4) / ns, nc = c1 - c0;
+        const int c0 = sp * (kDl / 4) / ns, c1 = (sp + 1) * (kDl / 4) / ns, nc = c1 - c0;
         const int items = hv * nc;
-        float4 acc[kMergeItems];
-#pragma unroll
-        for (int k = 0; k < kMergeItems; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int base = 0; base < items; base += kMergeItems * kThreads) {
+            float4 acc[kMergeItems];
+#pragma unroll
+            for (int k = 0; k < kMergeItems; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
             for (int q = 0; q < ns; ++q) {
                 float4 v[kMergeItems];
@@ -597,9 +588,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                     const int e = base + k * kThreads + (int)threadIdx.x;
                     if (e < items) {
                         const int h = e / nc, c = c0 + (e - h * nc);
-                        const float *src = part + h * kDl + 4 * c;
-                        v[k] = (uint32_t)q == me ? *reinterpret_cast<const float4 *>(src)
-                                                 : dsmem_ld_f32x4(src, hx + cx * (uint32_t)q);
+                        v[k] = q == sp ? *reinterpret_cast<const float4 *>(stage_f + h * kDl + 4 * c)
+                                       : __ldcg(reinterpret_cast<const float4 *>(
+                                             p.o_part + (q * split_stride + hrow0 + h) * kDl + 4 * c));
                     }
                 }
 #pragma unroll
@@ -620,14 +611,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                     uint2 o;
                     o.x = pack_bf16x2(acc[k].x, acc[k].y);
                     o.y = pack_bf16x2(acc[k].z, acc[k].w);
-                    *reinterpret_cast<uint2 *>(p.out + ((int64_t)r * p.H + hg * kHc + h) * kDl + 4 * c) = o;
-                    acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    *reinterpret_cast<uint2 *>(p.out + (hrow0 + h) * kDl + 4 * c) = o;
                 }
             }
         }
-        cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
-    } else if (pair) {
-        cluster_sync_all();  // nor while the partner may still copy from or signal into it
     }
 }
 
@@ -696,27 +683,28 @@ bool tc_applicable(nsa_dtype q_dtype, nsa_dtype kv_dtype, int H, int d_latent, i
 
 size_t tc_smem_bytes() { return 1024 + kQBytes + kKvBytes + 1024 + sizeof(MlaShared); }
 
-// Whether a cluster of cx x cy CTAs of this kernel can be resident on the
-// current device (queried once per device, shape and KV type).
-bool cluster_fits(int cx, int cy, bool fp8)
+// Whether the `ns` splits of a (row, head group) can run as one thread-block
+// cluster of this kernel on the current device (queried once per device,
+// split count and KV type).
+bool cluster_merge_ok(int ns, bool fp8)
 {
-    if (cx < 1 || cx > 2 || cy < 1 || cx * cy > kMaxClusterSplit) return false;
+    if (ns < 2 || ns > kMaxClusterSplit) return false;
     constexpr int kMaxDev = 64;
-    static int cache[kMaxDev][3][kMaxClusterSplit + 1][2];  // 0 unknown, 1 yes, 2 no
+    static int cache[kMaxDev][kMaxClusterSplit + 1][2];  // 0 unknown, 1 yes, 2 no
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
-    int &c = cache[dev][cx][cy][fp8 ? 1 : 0];
+    int &c = cache[dev][ns][fp8 ? 1 : 0];
     if (c == 0) {
         const void *kern = fp8 ? (const void *)sparse_mla_tc_kernel<true> : (const void *)sparse_mla_tc_kernel<false>;
         int n = 0;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)cx, (unsigned)cy, 1);
+        cfg.gridDim = dim3(1, (unsigned)ns, 1);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = tc_smem_bytes();
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)cx;
-        attr[0].val.clusterDim.y = (unsigned)cy;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = (unsigned)ns;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
@@ -729,16 +717,18 @@ bool cluster_fits(int cx, int cy, bool fp8)
     return c == 1;
 }
 
-// Pair mode when the head groups come in pairs; the splits of a (row, head
-// group [pair]) merge inside the cluster when the cluster stays within 8 CTAs.
-void plan_clusters(int H, int ns, bool fp8, int &pair, int &merge)
-{
-    pair = (H % (2 * kHc) == 0 && cluster_fits(2, 1, fp8)) ? 1 : 0;
-    const int cx = pair ? 2 : 1;
-    merge = (ns >= 2 && cx * ns <= kMaxClusterSplit && cluster_fits(cx, ns, fp8)) ? 1 : 0;
-}
-
 }  // namespace
+
+bool sparse_mla_tc_plan(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int H, int d_latent, int d_rope, int topk,
+                        int *nsplit, int *launches)
+{
+    if (!tc_applicable(q_dtype, kv_dtype, H, d_latent, d_rope) || R <= 0 || R > 65535 || topk <= 0) return false;
+    int ns, tps;
+    choose_split(R, H, topk, ns, tps);
+    *nsplit = ns;
+    *launches = (ns > 1 && !cluster_merge_ok(ns, kv_dtype == NSA_DT_E4M3)) ? 2 : 1;
+    return true;
+}
 
 size_t sparse_mla_tc_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int H, int d_latent, int d_rope,
                                      int topk)
@@ -746,9 +736,7 @@ size_t sparse_mla_tc_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int 
     if (!tc_applicable(q_dtype, kv_dtype, H, d_latent, d_rope) || R <= 0 || topk <= 0) return 0;
     int ns, tps;
     choose_split(R, H, topk, ns, tps);
-    int pair = 0, merge = 0;
-    if (ns > 1) plan_clusters(H, ns, kv_dtype == NSA_DT_E4M3, pair, merge);
-    if (ns <= 1 || merge) return 0;
+    if (ns <= 1) return 0;
     return (size_t)ns * R * H * (kDl + 1) * sizeof(float);
 }
 
@@ -775,8 +763,8 @@ nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const
     p.out = (__nv_bfloat16 *)out; p.lse = lse; p.status = status;
     p.o_part = nullptr; p.lse_part = nullptr;
     const bool fp8 = kv_dtype == NSA_DT_E4M3;
-    plan_clusters(H, p.nsplit, fp8, p.pair, p.cluster_merge);
-    if (p.nsplit > 1 && !p.cluster_merge) {
+    p.cluster_merge = cluster_merge_ok(p.nsplit, fp8) ? 1 : 0;
+    if (p.nsplit > 1) {
         if (!workspace) return NSA_ERR_INVALID_ARG;
         p.o_part = (float *)workspace;
         p.lse_part = p.o_part + (size_t)p.nsplit * R * H * kDl;
@@ -791,7 +779,7 @@ nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = p.pair ? 2u : 1u;
+    attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = p.cluster_merge ? (unsigned)p.nsplit : 1u;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;

@@ -5,6 +5,9 @@
 namespace nsa {
 size_t sparse_mla_tc_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int H, int d_latent,
                                      int d_rope, int topk);
+// Split count and kernel launches of the tensor-core path; false when it does not apply.
+bool sparse_mla_tc_plan(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int H, int d_latent, int d_rope, int topk,
+                        int *nsplit, int *launches);
 // Launches the tensor-core kernel when the problem fits its shape; returns
 // NSA_ERR_UNSUPPORTED (without launching) when it does not.
 nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const void *q_nope,

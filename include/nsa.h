@@ -288,6 +288,19 @@ size_t nsa_sparse_mla_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int
                                       int d_latent, int d_rope, int topk);
 
 /*
+ * How nsa_sparse_mla runs a problem of this shape (a runtime aid; the pages
+ * have no counterpart): *nsplit receives the number of parts each top-k list
+ * is split into (1 = none), *launches the number of kernel launches one call
+ * makes (0 when R = 0).  Assumes the tensor-core path's alignment (q and KV
+ * 16-byte aligned, q strides multiples of 8 elements); calls without it run
+ * one CUDA-core launch.  Returns NSA_ERR_INVALID_ARG for NULL outputs or a
+ * shape nsa_sparse_mla rejects with that code, NSA_ERR_UNSUPPORTED for a
+ * dtype combination it does not support.
+ */
+nsa_status nsa_sparse_mla_plan(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int H, int d_latent,
+                               int d_rope, int topk, int *nsplit, int *launches);
+
+/*
  * nsa_sparse_mla without a caller workspace, for callers that cannot allocate
  * device memory when they call in -- for example a plug-in inside a host
  * framework that owns all device memory and gives the plug-in no allocator,
