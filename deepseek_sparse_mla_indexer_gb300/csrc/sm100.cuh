@@ -305,7 +305,7 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank)
 __device__ __forceinline__ float dsmem_ld_f32(const float *local, uint32_t rank)
 {
     float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(dsmem_addr(local, rank)) : "memory");
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(dsmem_addr(local, rank)));
     return v;
 }
 // 16-byte load (the address must be 16-byte aligned).
@@ -314,35 +314,8 @@ __device__ __forceinline__ float4 dsmem_ld_f32x4(const float *local, uint32_t ra
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(dsmem_addr(local, rank))
-                 : "memory");
+                 : "r"(dsmem_addr(local, rank)));
     return v;
-}
-
-// Arrive (release, cluster scope) on the mbarrier at the same offset as `local` in CTA `rank`.
-__device__ __forceinline__ void mbar_arrive_remote(uint64_t *local, uint32_t rank)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(dsmem_addr(local, rank))
-                 : "memory");
-}
-// Copy `bytes` (a multiple of 16, both addresses 16-byte aligned) from this CTA's
-// shared memory to the same offset in CTA `rank`; the transfer counts as
-// complete_tx bytes on the mbarrier at the same offset as `bar` in that CTA.
-__device__ __forceinline__ void bulk_copy_to_peer(const void *src, uint32_t bytes, uint64_t *bar, uint32_t rank)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dsmem_addr(src, rank)), "r"(smem_u32(src)), "r"(bytes), "r"(dsmem_addr(bar, rank))
-        : "memory");
-}
-// Arrive once on the mbarrier at the offset of `bar` in every CTA of `cta_mask`
-// when every tcgen05 operation this thread issued so far is done.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-        ::"r"(smem_u32(bar)), "h"(cta_mask)
-        : "memory");
 }
 
 // Byte offset of element chunk `c16` (16-byte unit within a 128-byte row) of

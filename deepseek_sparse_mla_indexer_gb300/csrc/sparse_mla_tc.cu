@@ -86,6 +86,9 @@ struct __align__(16) MlaShared {
     alignas(16) float m_run[kHc];  // running max per head, log2 units (read as float4)
     alignas(16) float alpha[kHc];
     alignas(16) float red[4][kHc];
+    alignas(16) float l_head[kHc];    // final head sums of this split
+    alignas(16) float lse_head[kHc];  // natural-log LSE of this split per head
+    alignas(16) float wts[kMaxClusterSplit][kHc];  // merge weights exp(lse_q - lse) / l_q
     alignas(16) int idx[kTok];
     const uint8_t *rowbase[kTok];  // KV row of each token of the tile (slot 0 for masked ones)
     uint64_t kvb_full[5];          // block pair m of the tile landed (m = 4: rope block)
@@ -96,6 +99,7 @@ struct __align__(16) MlaShared {
 };
 static_assert(offsetof(MlaShared, m_run) % 16 == 0, "m_run is read with 16-byte loads");
 static_assert(offsetof(MlaShared, kvb_full) % 8 == 0, "mbarriers need 8-byte alignment");
+static_assert(1024 + kQBytes + kKvBytes + 1024 + sizeof(MlaShared) <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ void fail(MlaShared *sm, int32_t *status)
 {
@@ -311,26 +315,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             const int nxt = fetch_idx(t0 + i + 1);
             worker_sync();
             if (!FP8) {
-                // every block pair in flight at once, one commit group each, released in order
+                // two block pairs in flight per thread: pair m is issued, then pair m-1 (tile 0:
+                // first the Q rows) is awaited and released to the MMA warp
 #pragma unroll 1
                 for (int m = 0; m < 5; ++m) {
                     if (m > 0 && i > 0 && !mbar_wait(&sm->o_done[m], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
                     issue_pair(m);
                     cp_async_commit();
+                    if (m == 0 && i == 0) {
+                        cp_async_wait_group<1>();
+                        release_q();
+                    } else if (m > 0) {
+                        cp_async_wait_group<1>();
+                        release_pair(m - 1);
+                    }
                 }
                 if (nxt >= 0 && nxt < p.num_slots) prefetch_l2_bulk(p.kv + (int64_t)nxt * row_bytes, (uint32_t)row_bytes);
-                if (i == 0) {
-                    cp_async_wait_group<5>();
-                    release_q();
-                }
-                cp_async_wait_group<4>();
-                release_pair(0);
-                cp_async_wait_group<3>();
-                release_pair(1);
-                cp_async_wait_group<2>();
-                release_pair(2);
-                cp_async_wait_group<1>();
-                release_pair(3);
                 cp_async_wait_group<0>();
                 release_pair(4);
             } else {
@@ -463,29 +463,21 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         }
         if (softmax_warp) {
             // ------------------------------------------------------------ epilogue
+            // O^T blocks are staged raw (fp32, heads x 512, in the dead KV tile) as their
+            // MMAs complete; the head sums arrive last and scale the copy-out or the merge
             const int hv = min(kHc, p.H - hg * kHc);  // real heads of this CTA
-            const bool have_o = done_tiles > 0 && !sm->abort &&
-                                mbar_wait(&sm->o_done[4], (done_tiles - 1) & 1, kWaitBudget);
-            tc_fence_after();
-            uint32_t la[32];  // head sums of the group's heads (identical in every lane)
-            if (have_o) {
-                tmem_ld32(lane_base + kColL + hb, la);
-                tmem_ld_wait();
-            }
-            float inv_l[32];  // one reciprocal per head instead of a division per element
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float l = have_o ? __uint_as_float(la[j]) : 0.f;
-                inv_l[j] = l > 0.f ? 1.f / l : 0.f;
-            }
             const int nh = max(0, min(kHg, hv - hb));  // real heads of this group
             const int64_t row0 = (int64_t)r * p.H + hg * kHc + hb;
-            const bool split = p.nsplit > 1;
-            // normalised O staged in the dead KV tile, heads x 512: fp32 partial (split) or bf16
+            const uint32_t last = (uint32_t)(done_tiles - 1) & 1u;
+            bool have_o = done_tiles > 0 && !sm->abort;
             float *stage_f = reinterpret_cast<float *>(kv_s);
-            __nv_bfloat16 *stage_h = reinterpret_cast<__nv_bfloat16 *>(kv_s);
 #pragma unroll 1
             for (int m = 0; m < 4; ++m) {
+                if (have_o && !mbar_wait(&sm->o_done[m], last, kWaitBudget)) {
+                    fail(sm, p.status);
+                    have_o = false;
+                }
+                tc_fence_after();
                 uint32_t v[32];
                 if (have_o) {
                     tmem_ld32(lane_base + m * kHc + hb, v);
@@ -495,43 +487,55 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                     for (int j = 0; j < 32; ++j) v[j] = 0u;
                 }
                 const int d = m * 128 + t;
-                if (split) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) stage_f[(hb + j) * kDl + d] = __uint_as_float(v[j]) * inv_l[j];
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) stage_h[(hb + j) * kDl + d] = __float2bfloat16_rn(__uint_as_float(v[j]) * inv_l[j]);
-                }
+                for (int j = 0; j < 32; ++j) stage_f[(hb + j) * kDl + d] = __uint_as_float(v[j]);
             }
-            if (et < kHg && hb + et < hv) {
-                const float mm = sm->m_run[hb + et];
+            if (have_o && !mbar_wait(&sm->o_done[4], last, kWaitBudget)) {
+                fail(sm, p.status);
+                have_o = false;
+            }
+            tc_fence_after();
+            uint32_t la[32];  // head sums of the group's heads (identical in every lane)
+            if (have_o) {
+                tmem_ld32(lane_base + kColL + hb, la);
+                tmem_ld_wait();
+            }
+            if (et < kHg) {
                 float l = 0.f;
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     if (j == et) l = have_o ? __uint_as_float(la[j]) : 0.f;
-                const float lse = l > 0.f ? (mm + log2f(l)) * 0.69314718055994531f : -INFINITY;
-                if (split)
-                    p.lse_part[(int64_t)sp * p.R * p.H + row0 + et] = lse;
-                else
-                    p.lse[row0 + et] = lse;
-            }
-            bar_sync(gbar, 128);  // the group's staged rows are complete
-            // the group's heads are contiguous in global memory: 16-byte copies
-            if (split) {
-                // in a cluster merge only the slices that the other splits merge leave the CTA
-                const int ns = p.nsplit;
-                const int s0 = p.cluster_merge ? sp * (kDl / 4) / ns : 0;
-                const int s1 = p.cluster_merge ? (sp + 1) * (kDl / 4) / ns : 0;
-                const float4 *src = reinterpret_cast<const float4 *>(stage_f + hb * kDl);
-                float4 *dst = reinterpret_cast<float4 *>(p.o_part + ((int64_t)sp * p.R * p.H + row0) * kDl);
-                for (int k = et; k < nh * (kDl / 4); k += 128) {
-                    const int c = k & (kDl / 4 - 1);
-                    if (c < s0 || c >= s1) dst[k] = src[k];
+                const float lse = l > 0.f ? (sm->m_run[hb + et] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                sm->l_head[hb + et] = l;
+                sm->lse_head[hb + et] = lse;
+                if (hb + et < hv) {
+                    if (p.nsplit == 1)
+                        p.lse[row0 + et] = lse;
+                    else if (!p.cluster_merge)
+                        p.lse_part[(int64_t)sp * p.R * p.H + row0 + et] = lse;
                 }
-            } else {
-                const uint4 *src = reinterpret_cast<const uint4 *>(stage_h + hb * kDl);
-                uint4 *dst = reinterpret_cast<uint4 *>(p.out + row0 * kDl);
-                for (int k = et; k < nh * (kDl / 8); k += 128) dst[k] = src[k];
+            }
+            bar_sync(gbar, 128);  // the group's staged rows and head sums are complete
+            if (!p.cluster_merge) {
+                // the group's heads are contiguous in global memory: normalised 16-byte chunks out
+                const float4 *src = reinterpret_cast<const float4 *>(stage_f + hb * kDl);
+                if (p.nsplit == 1) {
+                    uint2 *dst = reinterpret_cast<uint2 *>(p.out + row0 * kDl);
+                    for (int k = et; k < nh * (kDl / 4); k += 128) {
+                        const float l = sm->l_head[hb + k / (kDl / 4)];
+                        const float il = l > 0.f ? 1.f / l : 0.f;
+                        const float4 v = src[k];
+                        dst[k] = make_uint2(pack_bf16x2(v.x * il, v.y * il), pack_bf16x2(v.z * il, v.w * il));
+                    }
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + ((int64_t)sp * p.R * p.H + row0) * kDl);
+                    for (int k = et; k < nh * (kDl / 4); k += 128) {
+                        const float l = sm->l_head[hb + k / (kDl / 4)];
+                        const float il = l > 0.f ? 1.f / l : 0.f;
+                        const float4 v = src[k];
+                        dst[k] = make_float4(v.x * il, v.y * il, v.z * il, v.w * il);
+                    }
+                }
             }
         }
     }
@@ -545,31 +549,34 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 
     if (p.cluster_merge) {
         // ---------------------------------------------------------------- split merge
-        // out = sum_q w_q O_q with w_q = exp(lse_q - lse), lse = ln sum_q exp(lse_q).
-        // The splits of this (row, head group) are the CTAs of the cluster (rank = split).
-        cluster_sync_all();  // every split's partial slices and log-sum-exp are in global memory
+        // out = sum_q exp(lse_q - lse) O_q / l_q, lse = ln sum_q exp(lse_q), with O_q the raw
+        // accumulator and l_q the head sums of split q.  The splits of this (row, head group)
+        // are the CTAs of the cluster (rank = split); each merges one slice of the latent
+        // dimension, reading the other splits' staged accumulators from their shared memory.
+        cluster_sync_all();  // every split's staged accumulator, head sums and LSE are complete
         const int ns = p.nsplit;
         const int hv = min(kHc, p.H - hg * kHc);
         const int64_t hrow0 = (int64_t)r * p.H + hg * kHc;
-        const int64_t split_stride = (int64_t)p.R * p.H;
         const float *stage_f = reinterpret_cast<const float *>(kv_s);
-        float *wts = reinterpret_cast<float *>(kv_s + 8 * kKvBlk);  // [split][head]
         if (threadIdx.x < kHc) {
             const int h = threadIdx.x;
-            float l[kMaxClusterSplit];
+            float l[kMaxClusterSplit], ls[kMaxClusterSplit];
             float mx = -INFINITY;
 #pragma unroll
             for (int q = 0; q < kMaxClusterSplit; ++q) {
-                l[q] = (q < ns && h < hv) ? __ldcg(p.lse_part + q * split_stride + hrow0 + h) : -INFINITY;
-                mx = fmaxf(mx, l[q]);
+                ls[q] = q < ns ? dsmem_ld_f32(&sm->lse_head[h], (uint32_t)q) : -INFINITY;
+                l[q] = q < ns ? dsmem_ld_f32(&sm->l_head[h], (uint32_t)q) : 0.f;
             }
+#pragma unroll
+            for (int q = 0; q < kMaxClusterSplit; ++q) mx = fmaxf(mx, ls[q]);
             float wsum = 0.f;
 #pragma unroll
             for (int q = 0; q < kMaxClusterSplit; ++q)
-                if (q < ns && mx != -INFINITY) wsum += __expf(l[q] - mx);
+                if (q < ns && mx != -INFINITY) wsum += __expf(ls[q] - mx);
 #pragma unroll
             for (int q = 0; q < kMaxClusterSplit; ++q)
-                if (q < ns) wts[q * kHc + h] = (wsum > 0.f && l[q] != -INFINITY) ? __expf(l[q] - mx) / wsum : 0.f;
+                sm->wts[q][h] = (q < ns && wsum > 0.f && ls[q] != -INFINITY && l[q] > 0.f)
+                                    ? __expf(ls[q] - mx) / (wsum * l[q]) : 0.f;
             if (sp == 0 && h < hv) p.lse[hrow0 + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
         }
         __syncthreads();
@@ -577,44 +584,38 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         const int c0 = sp * (kDl / 4) / ns, c1 = (sp + 1) * (kDl / 4) / ns, nc = c1 - c0;
         const int items = hv * nc;
         for (int base = 0; base < items; base += kMergeItems * kThreads) {
+            int off[kMergeItems], hh[kMergeItems];
             float4 acc[kMergeItems];
 #pragma unroll
-            for (int k = 0; k < kMergeItems; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = 0; k < kMergeItems; ++k) {
+                const int e = min(base + k * kThreads + (int)threadIdx.x, items - 1);  // clamped: always a valid address
+                hh[k] = e / nc;
+                off[k] = hh[k] * kDl + 4 * (c0 + e - hh[k] * nc);
+                const float w = sm->wts[sp][hh[k]];
+                const float4 v = *reinterpret_cast<const float4 *>(stage_f + off[k]);
+                acc[k] = make_float4(w * v.x, w * v.y, w * v.z, w * v.w);
+            }
 #pragma unroll 1
             for (int q = 0; q < ns; ++q) {
+                if (q == sp) continue;
                 float4 v[kMergeItems];
 #pragma unroll
-                for (int k = 0; k < kMergeItems; ++k) {  // every load of this split in flight at once
-                    const int e = base + k * kThreads + (int)threadIdx.x;
-                    if (e < items) {
-                        const int h = e / nc, c = c0 + (e - h * nc);
-                        v[k] = q == sp ? *reinterpret_cast<const float4 *>(stage_f + h * kDl + 4 * c)
-                                       : __ldcg(reinterpret_cast<const float4 *>(
-                                             p.o_part + (q * split_stride + hrow0 + h) * kDl + 4 * c));
-                    }
-                }
+                for (int k = 0; k < kMergeItems; ++k) v[k] = dsmem_ld_f32x4(stage_f + off[k], (uint32_t)q);  // all in flight
 #pragma unroll
                 for (int k = 0; k < kMergeItems; ++k) {
-                    const int e = base + k * kThreads + (int)threadIdx.x;
-                    if (e < items) {
-                        const float w = wts[q * kHc + e / nc];
-                        acc[k].x += w * v[k].x; acc[k].y += w * v[k].y;
-                        acc[k].z += w * v[k].z; acc[k].w += w * v[k].w;
-                    }
+                    const float w = sm->wts[q][hh[k]];
+                    acc[k].x += w * v[k].x; acc[k].y += w * v[k].y;
+                    acc[k].z += w * v[k].z; acc[k].w += w * v[k].w;
                 }
             }
 #pragma unroll
             for (int k = 0; k < kMergeItems; ++k) {
-                const int e = base + k * kThreads + (int)threadIdx.x;
-                if (e < items) {
-                    const int h = e / nc, c = c0 + (e - h * nc);
-                    uint2 o;
-                    o.x = pack_bf16x2(acc[k].x, acc[k].y);
-                    o.y = pack_bf16x2(acc[k].z, acc[k].w);
-                    *reinterpret_cast<uint2 *>(p.out + (hrow0 + h) * kDl + 4 * c) = o;
-                }
+                if (base + k * kThreads + (int)threadIdx.x < items)
+                    *reinterpret_cast<uint2 *>(p.out + (hrow0 + hh[k]) * kDl + (off[k] - hh[k] * kDl)) =
+                        make_uint2(pack_bf16x2(acc[k].x, acc[k].y), pack_bf16x2(acc[k].z, acc[k].w));
             }
         }
+        cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
     }
 }
 
@@ -736,7 +737,7 @@ size_t sparse_mla_tc_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int 
     if (!tc_applicable(q_dtype, kv_dtype, H, d_latent, d_rope) || R <= 0 || topk <= 0) return 0;
     int ns, tps;
     choose_split(R, H, topk, ns, tps);
-    if (ns <= 1) return 0;
+    if (ns <= 1 || cluster_merge_ok(ns, kv_dtype == NSA_DT_E4M3)) return 0;
     return (size_t)ns * R * H * (kDl + 1) * sizeof(float);
 }
 
@@ -764,7 +765,7 @@ nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const
     p.o_part = nullptr; p.lse_part = nullptr;
     const bool fp8 = kv_dtype == NSA_DT_E4M3;
     p.cluster_merge = cluster_merge_ok(p.nsplit, fp8) ? 1 : 0;
-    if (p.nsplit > 1) {
+    if (p.nsplit > 1 && !p.cluster_merge) {
         if (!workspace) return NSA_ERR_INVALID_ARG;
         p.o_part = (float *)workspace;
         p.lse_part = p.o_part + (size_t)p.nsplit * R * H * kDl;
