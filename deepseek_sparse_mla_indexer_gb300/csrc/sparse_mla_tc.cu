@@ -129,6 +129,11 @@ __device__ __forceinline__ void dequant8(uint2 w, float sc, uint32_t *dst4)
     }
 }
 
+// Float offset of 16-byte chunk c (d = 4c .. 4c+3) of head h in the staged
+// accumulator: O^T block m = d / 128 sits in the two latent blocks that block m's
+// MMAs read (dead once they complete), heads x 128 d within it.
+__device__ __forceinline__ int stage_off(int h, int c) { return (c >> 5) * (kHc * 128) + h * 128 + ((c & 31) << 2); }
+
 // Worker-group barrier (warps 0, 2..11).
 __device__ __forceinline__ void worker_sync() { bar_sync(2, kWorkers); }
 
@@ -463,8 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         }
         if (softmax_warp) {
             // ------------------------------------------------------------ epilogue
-            // O^T blocks are staged raw (fp32, heads x 512, in the dead KV tile) as their
-            // MMAs complete; the head sums arrive last and scale the copy-out or the merge
+            // each O^T block is staged raw (fp32) in the two latent blocks its MMAs read, as
+            // soon as they complete; the head sums arrive last and scale the copy-out or merge
             const int hv = min(kHc, p.H - hg * kHc);  // real heads of this CTA
             const int nh = max(0, min(kHg, hv - hb));  // real heads of this group
             const int64_t row0 = (int64_t)r * p.H + hg * kHc + hb;
@@ -486,9 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0u;
                 }
-                const int d = m * 128 + t;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) stage_f[(hb + j) * kDl + d] = __uint_as_float(v[j]);
+                for (int j = 0; j < 32; ++j) stage_f[m * (kHc * 128) + (hb + j) * 128 + t] = __uint_as_float(v[j]);
             }
             if (have_o && !mbar_wait(&sm->o_done[4], last, kWaitBudget)) {
                 fail(sm, p.status);
@@ -518,21 +522,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             bar_sync(gbar, 128);  // the group's staged rows and head sums are complete
             if (!p.cluster_merge) {
                 // the group's heads are contiguous in global memory: normalised 16-byte chunks out
-                const float4 *src = reinterpret_cast<const float4 *>(stage_f + hb * kDl);
                 if (p.nsplit == 1) {
                     uint2 *dst = reinterpret_cast<uint2 *>(p.out + row0 * kDl);
                     for (int k = et; k < nh * (kDl / 4); k += 128) {
-                        const float l = sm->l_head[hb + k / (kDl / 4)];
+                        const int h = hb + k / (kDl / 4);
+                        const float l = sm->l_head[h];
                         const float il = l > 0.f ? 1.f / l : 0.f;
-                        const float4 v = src[k];
+                        const float4 v = *reinterpret_cast<const float4 *>(stage_f + stage_off(h, k & (kDl / 4 - 1)));
                         dst[k] = make_uint2(pack_bf16x2(v.x * il, v.y * il), pack_bf16x2(v.z * il, v.w * il));
                     }
                 } else {
                     float4 *dst = reinterpret_cast<float4 *>(p.o_part + ((int64_t)sp * p.R * p.H + row0) * kDl);
                     for (int k = et; k < nh * (kDl / 4); k += 128) {
-                        const float l = sm->l_head[hb + k / (kDl / 4)];
+                        const int h = hb + k / (kDl / 4);
+                        const float l = sm->l_head[h];
                         const float il = l > 0.f ? 1.f / l : 0.f;
-                        const float4 v = src[k];
+                        const float4 v = *reinterpret_cast<const float4 *>(stage_f + stage_off(h, k & (kDl / 4 - 1)));
                         dst[k] = make_float4(v.x * il, v.y * il, v.z * il, v.w * il);
                     }
                 }
@@ -584,13 +589,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         const int c0 = sp * (kDl / 4) / ns, c1 = (sp + 1) * (kDl / 4) / ns, nc = c1 - c0;
         const int items = hv * nc;
         for (int base = 0; base < items; base += kMergeItems * kThreads) {
-            int off[kMergeItems], hh[kMergeItems];
+            int off[kMergeItems], hh[kMergeItems], cc[kMergeItems];
             float4 acc[kMergeItems];
 #pragma unroll
             for (int k = 0; k < kMergeItems; ++k) {
                 const int e = min(base + k * kThreads + (int)threadIdx.x, items - 1);  // clamped: always a valid address
                 hh[k] = e / nc;
-                off[k] = hh[k] * kDl + 4 * (c0 + e - hh[k] * nc);
+                cc[k] = c0 + e - hh[k] * nc;
+                off[k] = stage_off(hh[k], cc[k]);
                 const float w = sm->wts[sp][hh[k]];
                 const float4 v = *reinterpret_cast<const float4 *>(stage_f + off[k]);
                 acc[k] = make_float4(w * v.x, w * v.y, w * v.z, w * v.w);
@@ -611,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 #pragma unroll
             for (int k = 0; k < kMergeItems; ++k) {
                 if (base + k * kThreads + (int)threadIdx.x < items)
-                    *reinterpret_cast<uint2 *>(p.out + (hrow0 + hh[k]) * kDl + (off[k] - hh[k] * kDl)) =
+                    *reinterpret_cast<uint2 *>(p.out + (hrow0 + hh[k]) * kDl + 4 * cc[k]) =
                         make_uint2(pack_bf16x2(acc[k].x, acc[k].y), pack_bf16x2(acc[k].z, acc[k].w));
             }
         }
