@@ -61,6 +61,7 @@ constexpr int kNumSms = 152;
 constexpr int kBf16RowBytes = (kDl + kDr) * 2;        // 1152
 constexpr int kFp8RowBytes = kDl + 4 * (kDl / 128) + 2 * kDr;  // 656
 constexpr int kMaxClusterSplit = 8;   // portable cluster size
+constexpr int kPartRow = kDl + 4;     // floats per split partial row: raw O (512) | lse, l, 0, 0
 constexpr int kMergeItems = (kHc * (kDl / 8) + kThreads - 1) / kThreads;  // 16-byte outputs per thread at 2 splits
 static_assert(kHc * kDl * 4 <= 8 * (int)kKvBlk, "the fp32 partial fits in the latent part of the KV tile");
 
@@ -76,8 +77,7 @@ struct MlaParams {
     float scale_log2;
     __nv_bfloat16 *out;
     float *lse;
-    float *o_part;
-    float *lse_part;
+    float *o_part;      // [nsplit][R][H][kPartRow]
     int cluster_merge;  // splits merged inside the cluster (cluster y = nsplit, rank = split)
     int32_t *status;
 };
@@ -515,31 +515,33 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                 if (hb + et < hv) {
                     if (p.nsplit == 1)
                         p.lse[row0 + et] = lse;
-                    else if (!p.cluster_merge)
-                        p.lse_part[(int64_t)sp * p.R * p.H + row0 + et] = lse;
+                    else
+                        *reinterpret_cast<float4 *>(p.o_part + ((int64_t)sp * p.R * p.H + row0 + et) * kPartRow + kDl) =
+                            make_float4(lse, l, 0.f, 0.f);
                 }
             }
             bar_sync(gbar, 128);  // the group's staged rows and head sums are complete
-            if (!p.cluster_merge) {
-                // the group's heads are contiguous in global memory: normalised 16-byte chunks out
-                if (p.nsplit == 1) {
-                    uint2 *dst = reinterpret_cast<uint2 *>(p.out + row0 * kDl);
-                    for (int k = et; k < nh * (kDl / 4); k += 128) {
-                        const int h = hb + k / (kDl / 4);
-                        const float l = sm->l_head[h];
-                        const float il = l > 0.f ? 1.f / l : 0.f;
-                        const float4 v = *reinterpret_cast<const float4 *>(stage_f + stage_off(h, k & (kDl / 4 - 1)));
-                        dst[k] = make_uint2(pack_bf16x2(v.x * il, v.y * il), pack_bf16x2(v.z * il, v.w * il));
-                    }
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + ((int64_t)sp * p.R * p.H + row0) * kDl);
-                    for (int k = et; k < nh * (kDl / 4); k += 128) {
-                        const int h = hb + k / (kDl / 4);
-                        const float l = sm->l_head[h];
-                        const float il = l > 0.f ? 1.f / l : 0.f;
-                        const float4 v = *reinterpret_cast<const float4 *>(stage_f + stage_off(h, k & (kDl / 4 - 1)));
-                        dst[k] = make_float4(v.x * il, v.y * il, v.z * il, v.w * il);
-                    }
+            if (p.nsplit == 1) {
+                // the group's heads are contiguous in global memory: normalised 8-byte chunks out
+                uint2 *dst = reinterpret_cast<uint2 *>(p.out + row0 * kDl);
+                for (int k = et; k < nh * (kDl / 4); k += 128) {
+                    const int h = hb + k / (kDl / 4);
+                    const float l = sm->l_head[h];
+                    const float il = l > 0.f ? 1.f / l : 0.f;
+                    const float4 v = *reinterpret_cast<const float4 *>(stage_f + stage_off(h, k & (kDl / 4 - 1)));
+                    dst[k] = make_uint2(pack_bf16x2(v.x * il, v.y * il), pack_bf16x2(v.z * il, v.w * il));
+                }
+            } else {
+                // raw partial rows out; in a cluster merge only the slices the other splits merge
+                const int ns = p.nsplit;
+                const int s0 = p.cluster_merge ? sp * (kDl / 4) / ns : 0;
+                const int s1 = p.cluster_merge ? (sp + 1) * (kDl / 4) / ns : 0;
+                float *dst = p.o_part + ((int64_t)sp * p.R * p.H + row0) * kPartRow;
+                for (int k = et; k < nh * (kDl / 4); k += 128) {
+                    const int hl = k / (kDl / 4), c = k & (kDl / 4 - 1);
+                    if (c < s0 || c >= s1)
+                        *reinterpret_cast<float4 *>(dst + hl * kPartRow + 4 * c) =
+                            *reinterpret_cast<const float4 *>(stage_f + stage_off(hb + hl, c));
                 }
             }
         }
@@ -557,31 +559,42 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         // out = sum_q exp(lse_q - lse) O_q / l_q, lse = ln sum_q exp(lse_q), with O_q the raw
         // accumulator and l_q the head sums of split q.  The splits of this (row, head group)
         // are the CTAs of the cluster (rank = split); each merges one slice of the latent
-        // dimension, reading the other splits' staged accumulators from their shared memory.
-        cluster_sync_all();  // every split's staged accumulator, head sums and LSE are complete
+        // dimension: its own accumulator from shared memory, the other splits' partial rows
+        // from L2 (all loads of one split in flight at once), summed in split order.
+        cluster_sync_all();  // every split's partial rows are in global memory
         const int ns = p.nsplit;
         const int hv = min(kHc, p.H - hg * kHc);
         const int64_t hrow0 = (int64_t)r * p.H + hg * kHc;
         const float *stage_f = reinterpret_cast<const float *>(kv_s);
         if (threadIdx.x < kHc) {
             const int h = threadIdx.x;
-            float l[kMaxClusterSplit], ls[kMaxClusterSplit];
-            float mx = -INFINITY;
+            float ls[kMaxClusterSplit], l[kMaxClusterSplit];
 #pragma unroll
             for (int q = 0; q < kMaxClusterSplit; ++q) {
-                ls[q] = q < ns ? dsmem_ld_f32(&sm->lse_head[h], (uint32_t)q) : -INFINITY;
-                l[q] = q < ns ? dsmem_ld_f32(&sm->l_head[h], (uint32_t)q) : 0.f;
+                ls[q] = -INFINITY;
+                l[q] = 0.f;
+                if (q < ns && h < hv) {
+                    if (q == sp) {
+                        ls[q] = sm->lse_head[h];
+                        l[q] = sm->l_head[h];
+                    } else {
+                        const float2 hd = __ldcg(reinterpret_cast<const float2 *>(
+                            p.o_part + ((int64_t)q * p.R * p.H + hrow0 + h) * kPartRow + kDl));
+                        ls[q] = hd.x;
+                        l[q] = hd.y;
+                    }
+                }
             }
+            float mx = -INFINITY;
 #pragma unroll
             for (int q = 0; q < kMaxClusterSplit; ++q) mx = fmaxf(mx, ls[q]);
             float wsum = 0.f;
 #pragma unroll
             for (int q = 0; q < kMaxClusterSplit; ++q)
-                if (q < ns && mx != -INFINITY) wsum += __expf(ls[q] - mx);
+                if (mx != -INFINITY && ls[q] != -INFINITY) wsum += __expf(ls[q] - mx);
 #pragma unroll
             for (int q = 0; q < kMaxClusterSplit; ++q)
-                sm->wts[q][h] = (q < ns && wsum > 0.f && ls[q] != -INFINITY && l[q] > 0.f)
-                                    ? __expf(ls[q] - mx) / (wsum * l[q]) : 0.f;
+                sm->wts[q][h] = (wsum > 0.f && ls[q] != -INFINITY && l[q] > 0.f) ? __expf(ls[q] - mx) / (wsum * l[q]) : 0.f;
             if (sp == 0 && h < hv) p.lse[hrow0 + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
         }
         __syncthreads();
@@ -589,65 +602,72 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         const int c0 = sp * (kDl / 4) / ns, c1 = (sp + 1) * (kDl / 4) / ns, nc = c1 - c0;
         const int items = hv * nc;
         for (int base = 0; base < items; base += kMergeItems * kThreads) {
-            int off[kMergeItems], hh[kMergeItems], cc[kMergeItems];
+            const int kcount = min(kMergeItems, (items - base - (int)threadIdx.x + kThreads - 1) / kThreads);
+            int hh[kMergeItems], cc[kMergeItems];
             float4 acc[kMergeItems];
 #pragma unroll
             for (int k = 0; k < kMergeItems; ++k) {
-                const int e = min(base + k * kThreads + (int)threadIdx.x, items - 1);  // clamped: always a valid address
+                const int e = min(base + k * kThreads + (int)threadIdx.x, items - 1);  // clamped: a valid address
                 hh[k] = e / nc;
                 cc[k] = c0 + e - hh[k] * nc;
-                off[k] = stage_off(hh[k], cc[k]);
-                const float w = sm->wts[sp][hh[k]];
-                const float4 v = *reinterpret_cast<const float4 *>(stage_f + off[k]);
-                acc[k] = make_float4(w * v.x, w * v.y, w * v.z, w * v.w);
+                acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll 1
             for (int q = 0; q < ns; ++q) {
-                if (q == sp) continue;
                 float4 v[kMergeItems];
+                if (q == sp) {
 #pragma unroll
-                for (int k = 0; k < kMergeItems; ++k) v[k] = dsmem_ld_f32x4(stage_f + off[k], (uint32_t)q);  // all in flight
+                    for (int k = 0; k < kMergeItems; ++k)
+                        v[k] = *reinterpret_cast<const float4 *>(stage_f + stage_off(hh[k], cc[k]));
+                } else {
+                    const float *rowq = p.o_part + ((int64_t)q * p.R * p.H + hrow0) * kPartRow;
+#pragma unroll
+                    for (int k = 0; k < kMergeItems; ++k)
+                        if (k < kcount) v[k] = __ldcg(reinterpret_cast<const float4 *>(rowq + hh[k] * kPartRow + 4 * cc[k]));
+                }
 #pragma unroll
                 for (int k = 0; k < kMergeItems; ++k) {
-                    const float w = sm->wts[q][hh[k]];
-                    acc[k].x += w * v[k].x; acc[k].y += w * v[k].y;
-                    acc[k].z += w * v[k].z; acc[k].w += w * v[k].w;
+                    if (k < kcount) {
+                        const float w = sm->wts[q][hh[k]];
+                        acc[k].x += w * v[k].x; acc[k].y += w * v[k].y;
+                        acc[k].z += w * v[k].z; acc[k].w += w * v[k].w;
+                    }
                 }
             }
 #pragma unroll
-            for (int k = 0; k < kMergeItems; ++k) {
-                if (base + k * kThreads + (int)threadIdx.x < items)
+            for (int k = 0; k < kMergeItems; ++k)
+                if (k < kcount)
                     *reinterpret_cast<uint2 *>(p.out + (hrow0 + hh[k]) * kDl + 4 * cc[k]) =
                         make_uint2(pack_bf16x2(acc[k].x, acc[k].y), pack_bf16x2(acc[k].z, acc[k].w));
-            }
         }
-        cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
     }
 }
 
-// out[r, h, :] = sum_s exp(lse_s - lse) * o_s,  lse = ln sum_s exp(lse_s)
+// Several splits without a cluster: out[r, h, :] = sum_s exp(lse_s - lse) O_s / l_s,
+// lse = ln sum_s exp(lse_s), folded in split order (partial rows: raw O | lse, l).
 __global__ void __launch_bounds__(128)
-sparse_mla_combine_kernel(const float *o_part, const float *lse_part, int nsplit, int64_t rows,
-                          __nv_bfloat16 *out, float *lse)
+sparse_mla_combine_kernel(const float *o_part, int nsplit, int64_t rows, __nv_bfloat16 *out, float *lse)
 {
     const int64_t row = blockIdx.x;
-    float mx = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, lse_part[s * rows + row]);
-    float wsum = 0.f;
-    for (int s = 0; s < nsplit; ++s)
-        if (mx != -INFINITY) wsum += __expf(lse_part[s * rows + row] - mx);
     const int d = threadIdx.x * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float mrun = -INFINITY, wsum = 0.f;
     for (int s = 0; s < nsplit; ++s) {
-        const float ls = lse_part[s * rows + row];
-        const float ws = (wsum > 0.f && ls != -INFINITY) ? __expf(ls - mx) / wsum : 0.f;
-        const float4 v = *reinterpret_cast<const float4 *>(o_part + (s * rows + row) * kDl + d);
-        acc.x += ws * v.x; acc.y += ws * v.y; acc.z += ws * v.z; acc.w += ws * v.w;
+        const float *pr = o_part + (s * rows + row) * kPartRow;
+        const float2 hd = *reinterpret_cast<const float2 *>(pr + kDl);
+        if (hd.x == -INFINITY || !(hd.y > 0.f)) continue;
+        const float4 v = *reinterpret_cast<const float4 *>(pr + d);
+        const float mn = fmaxf(mrun, hd.x);
+        const float a = __expf(mrun - mn), b = __expf(hd.x - mn) / hd.y;
+        acc = make_float4(acc.x * a + v.x * b, acc.y * a + v.y * b, acc.z * a + v.z * b, acc.w * a + v.w * b);
+        wsum = wsum * a + __expf(hd.x - mn);
+        mrun = mn;
     }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+    const float iw = wsum > 0.f ? 1.f / wsum : 0.f;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * iw, acc.y * iw), hi = __floats2bfloat162_rn(acc.z * iw, acc.w * iw);
     *reinterpret_cast<__nv_bfloat162 *>(out + row * kDl + d) = lo;
     *reinterpret_cast<__nv_bfloat162 *>(out + row * kDl + d + 2) = hi;
-    if (threadIdx.x == 0) lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+    if (threadIdx.x == 0) lse[row] = wsum > 0.f ? mrun + logf(wsum) : -INFINITY;
 }
 
 int num_sms()
@@ -743,8 +763,8 @@ size_t sparse_mla_tc_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int 
     if (!tc_applicable(q_dtype, kv_dtype, H, d_latent, d_rope) || R <= 0 || topk <= 0) return 0;
     int ns, tps;
     choose_split(R, H, topk, ns, tps);
-    if (ns <= 1 || cluster_merge_ok(ns, kv_dtype == NSA_DT_E4M3)) return 0;
-    return (size_t)ns * R * H * (kDl + 1) * sizeof(float);
+    if (ns <= 1) return 0;
+    return (size_t)ns * R * H * kPartRow * sizeof(float);
 }
 
 nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const void *q_nope, int64_t nope_ld_r,
@@ -768,13 +788,12 @@ nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     choose_split(R, H, topk, p.nsplit, p.tiles_per_split);
     p.out = (__nv_bfloat16 *)out; p.lse = lse; p.status = status;
-    p.o_part = nullptr; p.lse_part = nullptr;
+    p.o_part = nullptr;
     const bool fp8 = kv_dtype == NSA_DT_E4M3;
     p.cluster_merge = cluster_merge_ok(p.nsplit, fp8) ? 1 : 0;
-    if (p.nsplit > 1 && !p.cluster_merge) {
+    if (p.nsplit > 1) {
         if (!workspace) return NSA_ERR_INVALID_ARG;
         p.o_part = (float *)workspace;
-        p.lse_part = p.o_part + (size_t)p.nsplit * R * H * kDl;
     }
     const size_t smem = tc_smem_bytes();
     auto kern = fp8 ? sparse_mla_tc_kernel<true> : sparse_mla_tc_kernel<false>;
@@ -794,7 +813,7 @@ nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const
     NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, p));
     if (p.nsplit > 1 && !p.cluster_merge) {
         const int64_t rows = (int64_t)R * H;
-        sparse_mla_combine_kernel<<<(unsigned)rows, 128, 0, stream>>>(p.o_part, p.lse_part, p.nsplit, rows,
+        sparse_mla_combine_kernel<<<(unsigned)rows, 128, 0, stream>>>(p.o_part, p.nsplit, rows,
                                                                      (__nv_bfloat16 *)out, lse);
         NSA_CUDA_TRY(cudaGetLastError());
     }
