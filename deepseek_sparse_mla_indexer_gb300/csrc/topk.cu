@@ -1,21 +1,23 @@
 // nsa_topk_transform: per-row top-k of the indexer scores, mapped to KV slots.
 //
-// [NSA] NSAIndexerMetadata.topk_transform (the fused variant that "returns a
-// transformed page table directly"), [DSA] transform_index_page_table_* with
-// page size 1 and _pad_topk_indices (-1 padding).
+// [NSA] NSAIndexerMetadata.topk_transform (the fused variant that emits KV
+// slots of the page table instead of positions), [DSA]
+// transform_index_page_table_* with page size 1 and _pad_topk_indices (-1
+// padding).
 //
-// Short rows: one block of 1024 threads per row; long rows: a cluster of up
-// to 8 blocks per row (below).  Scores become order-preserving 32-bit
-// keys (-0 folded onto +0, NaN below every number).  The k-th largest key is
+// Rows up to kCacheCap scores: one block of 1024 threads per row, the scores
+// read from HBM once and kept in shared memory; longer rows: a cluster of up
+// to 8 blocks per row (below).  Scores become order-preserving 32-bit keys
+// (-0 folded onto +0, NaN below every number).  The k-th largest key is
 // located by a most-significant-digit radix select with 11/11/10-bit digits:
-// each pass histograms the keys that still match the chosen prefix (eight
-// replicated shared-memory histograms to spread atomic traffic), and a block
-// scan over the bins, largest digit first, picks the digit holding the k-th
-// key.  A pass stops the search early when the whole bin is selected.  A
-// final ordered pass keeps every key above the threshold and the first
-// (k - #above) keys equal to it, in position order, so ties go to the lower
-// position and the output comes out sorted without a sort.  Rows up to
-// kCacheCap scores are read from HBM once and kept in shared memory.
+// each pass histograms the keys that still match the chosen prefix (lanes of a
+// warp with the same digit add once), and a block scan over the bins, largest
+// digit first, picks the digit holding the k-th key.  A pass stops the search
+// early when the whole bin is selected.  A final ordered pass keeps every key
+// above the threshold and the first (k - #above) keys equal to it, in
+// position order, so ties go to the lower position and the output comes out
+// sorted without a sort: each thread owns a run of consecutive positions and
+// one block scan of its (#above, #equal) counts places them.
 #include <algorithm>
 
 #include "nsa_internal.cuh"
@@ -25,9 +27,8 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kBins = 2048;
-constexpr int kCopies = 8;
-constexpr int kCacheCap = 36 * 1024;  // 144 KB of keys
-constexpr int kItems = 4;             // consecutive elements per thread in the ordered pass
+constexpr int kCacheCap = 48 * 1024;  // 192 KB of keys
+constexpr int kItems = 4;             // consecutive elements per thread in the cluster's ordered pass
 
 __device__ __forceinline__ uint32_t order_key(float x)
 {
@@ -93,6 +94,16 @@ __device__ __forceinline__ void fill_keys(const float *lg, int s0, int n, uint32
     }
 }
 
+// Warp-aggregated histogram increment: lanes with the same bin add once
+// (scores concentrate in few bins of the leading digits).  Every lane of the
+// warp must call it; `bin` = kNoBin for lanes with nothing to count.
+constexpr uint32_t kNoBin = 0xFFFFFFFFu;
+__device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t bin)
+{
+    const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+    if (bin != kNoBin && (threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+}
+
 __global__ void __launch_bounds__(kThreads)
 topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row_len,
                       const int32_t *row_to_req, const int32_t *pt, int64_t pt_ld, int topk,
@@ -100,8 +111,8 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
                       int32_t *status)
 {
     extern __shared__ uint32_t dyn[];
-    uint32_t *hist = dyn;                      // [kCopies][kBins]
-    uint32_t *cache = dyn + kCopies * kBins;   // [cache_cap]
+    uint32_t *hist = dyn;           // [kBins]
+    uint32_t *cache = dyn + kBins;  // [cache_cap]
     __shared__ uint32_t warp_buf[32];
     __shared__ uint32_t total;
     __shared__ uint32_t sel_digit, sel_need, sel_exact;
@@ -133,30 +144,27 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
     // keys with (key >> S) == V are selected (the lowest positions).
     uint32_t prefix = 0u, need = (uint32_t)topk;
     int S = 32;
-    uint32_t *myhist = hist + (size_t)((tid >> 5) % kCopies) * kBins;
+    const int Lr = (L + kThreads - 1) / kThreads * kThreads;  // whole warps in every round
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
         const int width = pass < 2 ? 11 : 10;
         const int shift = S - width;
         const uint32_t dmask = (1u << width) - 1u;
-        for (int i = tid; i < kCopies * kBins; i += kThreads) hist[i] = 0u;
+        for (int i = tid; i < kBins; i += kThreads) hist[i] = 0u;
         __syncthreads();
-        for (int i = tid; i < L; i += kThreads) {
-            const uint32_t k = key_at(i);
-            if (S == 32 || (k >> S) == prefix) atomicAdd(&myhist[(k >> shift) & dmask], 1u);
+        for (int i = tid; i < Lr; i += kThreads) {
+            uint32_t bin = kNoBin;
+            if (i < L) {
+                const uint32_t k = key_at(i);
+                if (S == 32 || (k >> S) == prefix) bin = (k >> shift) & dmask;
+            }
+            hist_add(hist, bin);
         }
         __syncthreads();
         // thread t owns digits (2047 - 2t) and (2046 - 2t): largest digits first
         const int d_hi = kBins - 1 - 2 * tid, d_lo = d_hi - 1;
-        uint32_t c_hi = 0u, c_lo = 0u;
-        if (d_hi <= (int)dmask) {
-#pragma unroll
-            for (int c = 0; c < kCopies; ++c) c_hi += hist[c * kBins + d_hi];
-        }
-        if (d_lo >= 0 && d_lo <= (int)dmask) {
-#pragma unroll
-            for (int c = 0; c < kCopies; ++c) c_lo += hist[c * kBins + d_lo];
-        }
+        const uint32_t c_hi = d_hi <= (int)dmask ? hist[d_hi] : 0u;
+        const uint32_t c_lo = (d_lo >= 0 && d_lo <= (int)dmask) ? hist[d_lo] : 0u;
         const uint32_t incl = block_incl_scan(c_hi + c_lo, warp_buf, &total);
         const uint32_t excl = incl - c_hi - c_lo;
         if (excl < need && need <= incl) {
@@ -179,38 +187,37 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
         if (exact) break;
     }
 
-    // ordered selection: kItems consecutive positions per thread per round
-    uint32_t gt_run = 0u, eq_run = 0u;
-    for (int base = 0; base < L; base += kThreads * kItems) {
-        const int i0 = base + tid * kItems;
-        uint32_t cls[kItems];  // 2 = above, 1 = equal, 0 = below / past the row
-        uint32_t n_gt = 0u, n_eq = 0u;
-#pragma unroll
-        for (int j = 0; j < kItems; ++j) {
-            cls[j] = 0u;
-            if (i0 + j < L) {
-                const uint32_t v = key_at(i0 + j) >> S;
-                cls[j] = v > prefix ? 2u : (v == prefix ? 1u : 0u);
-            }
-            n_gt += cls[j] == 2u;
-            n_eq += cls[j] == 1u;
-        }
+    // ordered selection: thread t owns the C consecutive positions from t*C (C odd, so
+    // the threads of a warp read different shared-memory banks); one block scan of
+    // (#above, #equal) places every selected position, in position order
+    const int C = ((L + kThreads - 1) / kThreads) | 1;
+    const int p0 = min(L, tid * C), p1 = min(L, p0 + C);
+    uint32_t n_gt = 0u, n_eq = 0u;
+    for (int i = p0; i < p1; ++i) {
+        const uint32_t v = key_at(i) >> S;
+        n_gt += v > prefix;
+        n_eq += v == prefix;
+    }
+    uint32_t gt_before, eq_before;
+    if (L < 65536) {  // both counts fit 16 bits
         const uint32_t packed = n_gt | (n_eq << 16);
-        const uint32_t incl = block_incl_scan(packed, warp_buf, &total);
-        uint32_t gt_before = gt_run + ((incl - packed) & 0xFFFFu);
-        uint32_t eq_before = eq_run + ((incl - packed) >> 16);
-#pragma unroll
-        for (int j = 0; j < kItems; ++j) {
-            if (cls[j] == 2u) {
-                out[gt_before + (eq_before < need ? eq_before : need)] = ptr[i0 + j];
-                ++gt_before;
-            } else if (cls[j] == 1u) {
-                if (eq_before < need) out[gt_before + eq_before] = ptr[i0 + j];
-                ++eq_before;
-            }
+        const uint32_t ex = block_incl_scan(packed, warp_buf, &total) - packed;
+        gt_before = ex & 0xFFFFu;
+        eq_before = ex >> 16;
+    } else {
+        gt_before = block_incl_scan(n_gt, warp_buf, &total) - n_gt;
+        eq_before = block_incl_scan(n_eq, warp_buf, &total) - n_eq;
+    }
+#pragma unroll 4
+    for (int i = p0; i < p1; ++i) {
+        const uint32_t v = key_at(i) >> S;
+        if (v > prefix) {
+            out[gt_before + (eq_before < need ? eq_before : need)] = ptr[i];
+            ++gt_before;
+        } else if (v == prefix) {
+            if (eq_before < need) out[gt_before + eq_before] = ptr[i];
+            ++eq_before;
         }
-        gt_run += total & 0xFFFFu;
-        eq_run += total >> 16;
     }
 }
 
@@ -432,8 +439,8 @@ extern "C" nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits
     if (R == 0) return NSA_OK;
     if (!logits_dev || !row_len_dev || !row_to_req_dev || !page_table_1_dev || !indices_dev)
         return NSA_ERR_INVALID_ARG;
-    // long rows: one cluster of up to 8 CTAs per row
-    const int csize = max_row_len > topk ? (int)std::min<int64_t>(kCMaxCluster, ceil_div(max_row_len, 4096)) : 1;
+    // rows beyond the single-block key cache: one cluster of up to 8 CTAs per row
+    const int csize = max_row_len > kCacheCap ? (int)std::min<int64_t>(kCMaxCluster, ceil_div(max_row_len, kCSliceCap)) : 1;
     if (csize > 1 && (int64_t)R * csize <= 2147483647LL) {
         NSA_CUDA_TRY(cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)(kCSliceCap * sizeof(uint32_t))));
@@ -455,7 +462,7 @@ extern "C" nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits
         return NSA_OK;
     }
     const int cap = max_row_len > topk ? (max_row_len < kCacheCap ? max_row_len : kCacheCap) : 0;
-    const size_t smem = (size_t)(kCopies * kBins + cap) * sizeof(uint32_t);
+    const size_t smem = (size_t)(kBins + cap) * sizeof(uint32_t);
     NSA_CUDA_TRY(cudaFuncSetAttribute(topk_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)smem));
     topk_transform_kernel<<<(unsigned)R, kThreads, smem, (cudaStream_t)stream>>>(

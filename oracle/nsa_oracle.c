@@ -329,7 +329,7 @@ static int orc_int_cmp(const void *pa, const void *pb)
 
 /*
  * One row of top-k + transform ([NSA] NSAIndexerMetadata.topk_transform, the
- * fused "returns a transformed page table directly" branch; [DSA]
+ * fused branch that emits page-table slots instead of positions; [DSA]
  * _pad_topk_indices for the -1 sentinel):
  *   the positions s in [0, L) of the topk largest logits (all of [0, L) when
  *   L <= topk), listed in ascending s, each mapped to page_table_1[b, s],

@@ -88,18 +88,19 @@ def test_empty_batch_is_a_no_op():
     assert int(md["cu_seqlens_k"][0]) == 0 and int(md["nsa_cu_seqlens_k"][0]) == 0
 
 
-def test_topk_ties_nan_and_signed_zero_bit_exact():
+@pytest.mark.parametrize("Wd", [40000, 70000])  # one block per row; a cluster per row
+def test_topk_ties_nan_and_signed_zero_bit_exact(Wd):
     import deepseek_sparse_mla_indexer_gb300 as nsa
     import oracle
     rng = np.random.default_rng(5)
-    R, Wd, k = 6, 70000, 2048
+    R, k = 6, 2048
     lg = rng.integers(-3, 4, size=(R, Wd)).astype(np.float32)  # massive ties
     lg[1] = rng.standard_normal(Wd).astype(np.float32)
     lg[1, ::7] = -0.0
     lg[1, 5::11] = 0.0
     lg[2, ::3] = np.nan
     lg[3] = 1.0  # all equal: the first k positions win
-    L = np.array([Wd, 60000, 50001, 2049, 2048, 4000], np.int32)
+    L = np.array([Wd, Wd * 6 // 7, Wd * 5 // 7 + 1, 2049, 2048, 4000], np.int32)
     pt = rng.integers(0, 2 ** 31 - 1, size=(R, Wd)).astype(np.int32)
     r2q = np.arange(R, dtype=np.int32)
     exp = oracle.topk_transform(lg, L, r2q, pt, k)

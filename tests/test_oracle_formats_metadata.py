@@ -98,8 +98,8 @@ def test_metadata_closed_forms(mode, ps):
         ks = np.repeat(np.concatenate([[0], np.cumsum(seq)[:-1]]), ext)
         assert np.array_equal(md["indexer_ks"], ks)
         assert np.array_equal(md["indexer_ke"], ks + exp)
-    # clipped lengths and their cumulative sum (the "clipped to topk" field and
-    # "cumsum of nsa_cache_seqlens_int32")
+    # lengths clipped to topk and their cumulative sum (the per-row sparse
+    # lengths and their offsets)
     clipped = np.minimum(md["seqlens_expanded"], topk)
     assert np.array_equal(md["nsa_cache_seqlens"], clipped)
     assert np.array_equal(md["nsa_cu_seqlens_k"], np.concatenate([[0], np.cumsum(clipped)]))
