@@ -10,14 +10,16 @@
 // to 8 blocks per row (below).  Scores become order-preserving 32-bit keys
 // (-0 folded onto +0, NaN below every number).  The k-th largest key is
 // located by a most-significant-digit radix select with 11/11/10-bit digits:
-// each pass histograms the keys that still match the chosen prefix (lanes of a
-// warp with the same digit add once), and a block scan over the bins, largest
+// each pass histograms the keys that still match the chosen prefix (eight
+// replicated shared-memory histograms spread the atomic traffic of the few
+// crowded bins), and a block scan over the bins, largest
 // digit first, picks the digit holding the k-th key.  A pass stops the search
 // early when the whole bin is selected.  A final ordered pass keeps every key
 // above the threshold and the first (k - #above) keys equal to it, in
 // position order, so ties go to the lower position and the output comes out
 // sorted without a sort: each thread owns a run of consecutive positions and
-// one block scan of its (#above, #equal) counts places them.
+// one block scan of its (#above, #equal) counts places them; the page-table
+// gathers of all output slots then go out together.
 #include <algorithm>
 
 #include "nsa_internal.cuh"
@@ -27,7 +29,8 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kBins = 2048;
-constexpr int kCacheCap = 48 * 1024;  // 192 KB of keys
+constexpr int kCopies = 8;             // replicated histograms (warp w adds into copy w % 8)
+constexpr int kCacheCap = 40 * 1024;  // 160 KB of keys (+ 64 KB of histograms)
 constexpr int kItems = 4;             // consecutive elements per thread in the cluster's ordered pass
 
 __device__ __forceinline__ uint32_t order_key(float x)
@@ -94,16 +97,6 @@ __device__ __forceinline__ void fill_keys(const float *lg, int s0, int n, uint32
     }
 }
 
-// Warp-aggregated histogram increment: lanes with the same bin add once
-// (scores concentrate in few bins of the leading digits).  Every lane of the
-// warp must call it; `bin` = kNoBin for lanes with nothing to count.
-constexpr uint32_t kNoBin = 0xFFFFFFFFu;
-__device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t bin)
-{
-    const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-    if (bin != kNoBin && (threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
-}
-
 __global__ void __launch_bounds__(kThreads)
 topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row_len,
                       const int32_t *row_to_req, const int32_t *pt, int64_t pt_ld, int topk,
@@ -111,8 +104,8 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
                       int32_t *status)
 {
     extern __shared__ uint32_t dyn[];
-    uint32_t *hist = dyn;           // [kBins]
-    uint32_t *cache = dyn + kBins;  // [cache_cap]
+    uint32_t *hist = dyn;                     // [kCopies][kBins]; then the selected positions
+    uint32_t *cache = dyn + kCopies * kBins;  // [cache_cap]
     __shared__ uint32_t warp_buf[32];
     __shared__ uint32_t total;
     __shared__ uint32_t sel_digit, sel_need, sel_exact;
@@ -144,27 +137,30 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
     // keys with (key >> S) == V are selected (the lowest positions).
     uint32_t prefix = 0u, need = (uint32_t)topk;
     int S = 32;
-    const int Lr = (L + kThreads - 1) / kThreads * kThreads;  // whole warps in every round
+    uint32_t *myhist = hist + (size_t)((tid >> 5) % kCopies) * kBins;
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
         const int width = pass < 2 ? 11 : 10;
         const int shift = S - width;
         const uint32_t dmask = (1u << width) - 1u;
-        for (int i = tid; i < kBins; i += kThreads) hist[i] = 0u;
+        for (int i = tid; i < kCopies * kBins; i += kThreads) hist[i] = 0u;
         __syncthreads();
-        for (int i = tid; i < Lr; i += kThreads) {
-            uint32_t bin = kNoBin;
-            if (i < L) {
-                const uint32_t k = key_at(i);
-                if (S == 32 || (k >> S) == prefix) bin = (k >> shift) & dmask;
-            }
-            hist_add(hist, bin);
+        for (int i = tid; i < L; i += kThreads) {
+            const uint32_t k = key_at(i);
+            if (S == 32 || (k >> S) == prefix) atomicAdd(&myhist[(k >> shift) & dmask], 1u);
         }
         __syncthreads();
         // thread t owns digits (2047 - 2t) and (2046 - 2t): largest digits first
         const int d_hi = kBins - 1 - 2 * tid, d_lo = d_hi - 1;
-        const uint32_t c_hi = d_hi <= (int)dmask ? hist[d_hi] : 0u;
-        const uint32_t c_lo = (d_lo >= 0 && d_lo <= (int)dmask) ? hist[d_lo] : 0u;
+        uint32_t c_hi = 0u, c_lo = 0u;
+        if (d_hi <= (int)dmask) {
+#pragma unroll
+            for (int c = 0; c < kCopies; ++c) c_hi += hist[c * kBins + d_hi];
+        }
+        if (d_lo >= 0 && d_lo <= (int)dmask) {
+#pragma unroll
+            for (int c = 0; c < kCopies; ++c) c_lo += hist[c * kBins + d_lo];
+        }
         const uint32_t incl = block_incl_scan(c_hi + c_lo, warp_buf, &total);
         const uint32_t excl = incl - c_hi - c_lo;
         if (excl < need && need <= incl) {
@@ -208,17 +204,21 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
         gt_before = block_incl_scan(n_gt, warp_buf, &total) - n_gt;
         eq_before = block_incl_scan(n_eq, warp_buf, &total) - n_eq;
     }
-#pragma unroll 4
+    // output slot -> position, in shared memory (the histograms are dead); then the
+    // page-table gathers of all slots go out together
+    uint32_t *sel = hist;
     for (int i = p0; i < p1; ++i) {
         const uint32_t v = key_at(i) >> S;
         if (v > prefix) {
-            out[gt_before + (eq_before < need ? eq_before : need)] = ptr[i];
+            sel[gt_before + (eq_before < need ? eq_before : need)] = (uint32_t)i;
             ++gt_before;
         } else if (v == prefix) {
-            if (eq_before < need) out[gt_before + eq_before] = ptr[i];
+            if (eq_before < need) sel[gt_before + eq_before] = (uint32_t)i;
             ++eq_before;
         }
     }
+    __syncthreads();
+    for (int j = tid; j < topk; j += kThreads) out[j] = ptr[sel[j]];
 }
 
 
