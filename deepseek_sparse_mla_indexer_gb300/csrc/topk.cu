@@ -31,6 +31,9 @@ constexpr int kThreads = 1024;
 constexpr int kBins = 2048;
 constexpr int kCopies = 8;             // replicated histograms (warp w adds into copy w % 8)
 constexpr int kCacheCap = 40 * 1024;  // 160 KB of keys (+ 64 KB of histograms)
+// Dynamic shared memory of topk_transform_kernel: the histograms, then `cap` cached keys.
+constexpr size_t row_kernel_smem_bytes(int cap) { return (size_t)(kCopies * kBins + cap) * sizeof(uint32_t); }
+static_assert(row_kernel_smem_bytes(kCacheCap) <= 232448, "shared memory per block");
 constexpr int kItems = 4;             // consecutive elements per thread in the cluster's ordered pass
 
 __device__ __forceinline__ uint32_t order_key(float x)
@@ -462,7 +465,7 @@ extern "C" nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits
         return NSA_OK;
     }
     const int cap = max_row_len > topk ? (max_row_len < kCacheCap ? max_row_len : kCacheCap) : 0;
-    const size_t smem = (size_t)(kBins + cap) * sizeof(uint32_t);
+    const size_t smem = row_kernel_smem_bytes(cap);
     NSA_CUDA_TRY(cudaFuncSetAttribute(topk_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)smem));
     topk_transform_kernel<<<(unsigned)R, kThreads, smem, (cudaStream_t)stream>>>(
