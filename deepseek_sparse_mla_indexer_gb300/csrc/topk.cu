@@ -148,9 +148,17 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
         const uint32_t dmask = (1u << width) - 1u;
         for (int i = tid; i < kCopies * kBins; i += kThreads) hist[i] = 0u;
         __syncthreads();
-        for (int i = tid; i < L; i += kThreads) {
-            const uint32_t k = key_at(i);
+        auto count_key = [&](uint32_t k) {
             if (S == 32 || (k >> S) == prefix) atomicAdd(&myhist[(k >> shift) & dmask], 1u);
+        };
+        if (cached) {  // 16-byte reads of four consecutive keys
+            for (int i4 = tid; i4 < (L >> 2); i4 += kThreads) {
+                const uint4 k = reinterpret_cast<const uint4 *>(cache)[i4];
+                count_key(k.x); count_key(k.y); count_key(k.z); count_key(k.w);
+            }
+            for (int i = (L & ~3) + tid; i < L; i += kThreads) count_key(cache[i]);
+        } else {
+            for (int i = tid; i < L; i += kThreads) count_key(key_at(i));
         }
         __syncthreads();
         // thread t owns digits (2047 - 2t) and (2046 - 2t): largest digits first
@@ -186,16 +194,36 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
         if (exact) break;
     }
 
-    // ordered selection: thread t owns the C consecutive positions from t*C (C odd, so
-    // the threads of a warp read different shared-memory banks); one block scan of
-    // (#above, #equal) places every selected position, in position order
-    const int C = ((L + kThreads - 1) / kThreads) | 1;
+    // ordered selection: thread t owns the C consecutive positions from t*C (C = 4 x an
+    // odd number: 16-byte reads, and the threads of a warp hit different bank groups);
+    // one block scan of (#above, #equal) places every selected position in order
+    const int C = 4 * (((L + 4 * kThreads - 1) / (4 * kThreads)) | 1);
     const int p0 = min(L, tid * C), p1 = min(L, p0 + C);
+    // class of the keys p0+4c .. p0+4c+3: 2 above, 1 equal, 0 below or past the run
+    auto classes4 = [&](int i, uint32_t (&cls)[4]) {
+        uint32_t k[4];
+        if (cached && i + 4 <= p1) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(cache + i);
+            k[0] = v.x; k[1] = v.y; k[2] = v.z; k[3] = v.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) k[j] = i + j < p1 ? key_at(i + j) : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t v = k[j] >> S;
+            cls[j] = i + j >= p1 ? 0u : (v > prefix ? 2u : (v == prefix ? 1u : 0u));
+        }
+    };
     uint32_t n_gt = 0u, n_eq = 0u;
-    for (int i = p0; i < p1; ++i) {
-        const uint32_t v = key_at(i) >> S;
-        n_gt += v > prefix;
-        n_eq += v == prefix;
+    for (int i = p0; i < p1; i += 4) {
+        uint32_t cls[4];
+        classes4(i, cls);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            n_gt += cls[j] == 2u;
+            n_eq += cls[j] == 1u;
+        }
     }
     uint32_t gt_before, eq_before;
     if (L < 65536) {  // both counts fit 16 bits
@@ -210,14 +238,18 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
     // output slot -> position, in shared memory (the histograms are dead); then the
     // page-table gathers of all slots go out together
     uint32_t *sel = hist;
-    for (int i = p0; i < p1; ++i) {
-        const uint32_t v = key_at(i) >> S;
-        if (v > prefix) {
-            sel[gt_before + (eq_before < need ? eq_before : need)] = (uint32_t)i;
-            ++gt_before;
-        } else if (v == prefix) {
-            if (eq_before < need) sel[gt_before + eq_before] = (uint32_t)i;
-            ++eq_before;
+    for (int i = p0; i < p1; i += 4) {
+        uint32_t cls[4];
+        classes4(i, cls);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (cls[j] == 2u) {
+                sel[gt_before + (eq_before < need ? eq_before : need)] = (uint32_t)(i + j);
+                ++gt_before;
+            } else if (cls[j] == 1u) {
+                if (eq_before < need) sel[gt_before + eq_before] = (uint32_t)(i + j);
+                ++eq_before;
+            }
         }
     }
     __syncthreads();
