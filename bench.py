@@ -35,6 +35,32 @@ WORKLOAD_DESC = ("DeepSeek-V3.2-shaped decode, bf16 KV: batch 32, seqlens U{4096
 L2_FLUSH_BYTES = 512 << 20
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
+# stage's kernel from one ncu capture of this workload (profiles/ names the
+# command), valid only while the kernel sources hash as they did at capture.
+NCU_TRAFFIC = {
+    "sparse_mla": dict(bytes=int((81.303040 + 2.526464) * 1e6), sources=["sparse_mla_tc.cu", "sm100.cuh"],
+                       sha="91f9b0e650bb4c55"),
+    "indexer": dict(bytes=int((79.623168 + 1.778176) * 1e6), sources=["indexer_tc.cu", "sm100.cuh"],
+                    sha="2f3a3773e5ced00f"),
+    "topk": dict(bytes=int(4.720128e6), sources=["topk.cu"], sha="4290385163b3c39d"),
+    "metadata": dict(bytes=int(3.928320e6), sources=["metadata.cu"], sha="cdb2d7ca8df94125"),
+}
+
+
+def ncu_traffic(stage: str):
+    """Measured bytes per launch, or None once the kernel has changed since the capture."""
+    import hashlib
+    e = NCU_TRAFFIC.get(stage)
+    if e is None:
+        return None
+    m = hashlib.sha256()
+    for f in e["sources"]:
+        with open(os.path.join(ROOT, "deepseek_sparse_mla_indexer_gb300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    return e["bytes"] if m.hexdigest()[:16] == e["sha"] else None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -316,7 +342,7 @@ def run_ours(args, rank, world, local_rank):
     dom_sec = stage_ms[dom] * 1e-3
     achieved = work[dom]["bytes"] / dom_sec / 1e9
     roof = dict(kernel=dom, bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
-                frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None,
+                frac=round(achieved / peaks["hbm_gbs"], 4), traffic=ncu_traffic(dom),
                 algorithmic_bytes=work[dom]["bytes"], peak_source=peaks["source"])
 
     rows_total = wl.R * world
