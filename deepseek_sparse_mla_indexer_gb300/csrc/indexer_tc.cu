@@ -115,9 +115,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     Bars *bars = (Bars *)(q_smem + p.G * kQRowBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g_begin = blockIdx.y * p.G;
+    // blockIdx.x = row group, blockIdx.y = chunk of kTilesPerCta tiles: the CTAs start in
+    // chunk order, so the empty chunks of short rows come last instead of holding SMs
+    const int g_begin = blockIdx.x * p.G;
     const int g_end = min(g_begin + p.G, p.R);
-    const int t_begin = blockIdx.x * kTilesPerCta;
+    const int t_begin = blockIdx.y * kTilesPerCta;
     const int t_end = t_begin + kTilesPerCta;
 
     if (threadIdx.x == 0) {
@@ -346,7 +348,7 @@ nsa_status indexer_tc_try_launch(nsa_dtype dtype, const void *q, const float *w,
     auto kern = indexer_tc_kernel;
     NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     const int tiles = (int)ceil_div(max_row_len, kTileTok);
-    dim3 grid((unsigned)ceil_div(tiles, kTilesPerCta), (unsigned)ceil_div(R, G));
+    dim3 grid((unsigned)ceil_div(R, G), (unsigned)ceil_div(tiles, kTilesPerCta));
     if (grid.y > 65535) return NSA_ERR_UNSUPPORTED;
     kern<<<grid, kThreadsTc, smem, stream>>>(kmap, qmap, p);
     return launch_status();
