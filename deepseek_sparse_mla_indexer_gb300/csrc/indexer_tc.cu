@@ -347,6 +347,8 @@ nsa_status indexer_tc_try_launch(nsa_dtype dtype, const void *q, const float *w,
     const size_t smem = 1024 + (size_t)kStages * kTileBytes + (size_t)G * kQRowBytes + sizeof(Bars);
     auto kern = indexer_tc_kernel;
     NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    // the whole shared memory for the carveout: three CTAs per SM at one row per group
+    NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100));
     const int tiles = (int)ceil_div(max_row_len, kTileTok);
     dim3 grid((unsigned)ceil_div(R, G), (unsigned)ceil_div(tiles, kTilesPerCta));
     if (grid.y > 65535) return NSA_ERR_UNSUPPORTED;

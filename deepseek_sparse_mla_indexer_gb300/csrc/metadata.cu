@@ -183,7 +183,7 @@ __device__ void build_rows(const MetaParams &p)
     for (int i = threadIdx.x; i <= p.R; i += blockDim.x) o.nsa_cu_seqlens_q[i] = i;
 }
 
-constexpr int kSeg = 8192;  // page-table entries per copy segment
+constexpr int kSeg = 4096;  // page-table entries per copy segment (one 16-byte load per thread)
 
 // page_table_1[b, 0:W] = req_to_token[rpi[b], 0:W], and every page start also
 // lands in real_page_table.  Segments of kSeg entries are spread over the copy
