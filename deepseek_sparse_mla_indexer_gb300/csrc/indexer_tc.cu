@@ -14,11 +14,17 @@
 // (one thread per token) applies ReLU, the per-head weights, the head sum and
 // the key's scale, and stores one fp32 logit per (row, token).
 //
+// Grid: up to three CTAs per SM, persistent: the tiles of all row groups,
+// flattened in (group, subgroup, tile) order, are cut into equal shares, one
+// per CTA (each CTA finds its start with one block-wide pass over the row
+// lengths), so no SM idles while another works through a long row.
 // Roles (192 threads): warp 0 issues TMA loads of K pages and q rows into
 // 128B-swizzled shared memory; warp 1 owns TMEM and issues the MMAs; warps
 // 2..5 are the epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
 // Stages are tracked with mbarriers; every wait is bounded and reports
 // NSA_ERR_TIMEOUT instead of hanging.
+#include <algorithm>
+
 #include "indexer_tc.cuh"
 #include "sm100.cuh"
 #include "tma_host.h"
@@ -35,8 +41,8 @@ constexpr int kHi = 64;
 constexpr int kStages = 4;
 constexpr int kThreadsTc = 192;
 constexpr int kMaxG = 4;
-constexpr int kTilesPerCta = 16;  // 2 half-tiles per tile: one per lane of the producer warp
-static_assert(kTilesPerCta * 2 == 32, "the producer warp owns one half-tile per lane");
+constexpr int kPieceTiles = 16;  // tiles whose page ids the producer warp fetches at once (one half-tile per lane)
+static_assert(kPieceTiles * 2 == 32, "the producer warp owns one half-tile per lane");
 constexpr uint32_t kTileBytes = kTileTok * kDi;    // 16 KB of e4m3
 constexpr uint32_t kHalfBytes = kHalf * kDi;       // 8 KB
 constexpr uint32_t kQRowBytes = kHi * kDi;         // 8 KB per query row
@@ -68,6 +74,9 @@ struct Bars {
     uint64_t done;
     uint32_t tmem_base;
     volatile int abort;
+    int g0, uo0;                       // first row group of this CTA's share, units into it
+    long long u_begin, u_end;          // this CTA's share of the flattened tiles
+    long long red[kThreadsTc / 32];
     float w[kMaxG * kHi];
 };
 
@@ -105,7 +114,45 @@ __device__ __forceinline__ void fail(Bars *bars, int32_t *status)
     set_status(status, NSA_ERR_TIMEOUT);
 }
 
-__global__ void __launch_bounds__(kThreadsTc)
+// Units of work of row group g: the tiles of each of its subgroups.
+__device__ __forceinline__ int group_units(const TcParams &p, int g)
+{
+    int r = g * p.G, units = 0;
+    const int g_end = min(r + p.G, p.R);
+    SubGroup sg;
+    while (next_subgroup(p, g_end, r, sg)) units += (int)ceil_div(sg.lmax, kTileTok);
+    return units;
+}
+
+// Walks the CTA's share of the work: calls seg(sg, tb, te) for each run of tiles
+// [tb, te) of one subgroup, in (row group, subgroup, tile) order.
+template <class F>
+__device__ __forceinline__ void for_each_segment(const TcParams &p, const Bars *bars, F seg)
+{
+    int g = bars->g0, uo = bars->uo0;
+    long long left = bars->u_end - bars->u_begin;
+    const int ngroups = (int)ceil_div(p.R, p.G);
+    while (left > 0 && g < ngroups && !bars->abort) {
+        int r = g * p.G;
+        const int g_end = min(r + p.G, p.R);
+        SubGroup sg;
+        while (left > 0 && next_subgroup(p, g_end, r, sg)) {
+            const int nt = (int)ceil_div(sg.lmax, kTileTok);
+            if (uo >= nt) {
+                uo -= nt;
+                continue;
+            }
+            const int tb = uo;
+            const int te = (int)min((long long)nt, (long long)tb + left);
+            uo = 0;
+            left -= te - tb;
+            if (!seg(sg, tb, te)) return;
+        }
+        ++g;
+    }
+}
+
+__global__ void __maxnreg__(112)  // 192 threads, three CTAs per SM
 indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -115,12 +162,56 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     Bars *bars = (Bars *)(q_smem + p.G * kQRowBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // blockIdx.x = row group, blockIdx.y = chunk of kTilesPerCta tiles: the CTAs start in
-    // chunk order, so the empty chunks of short rows come last instead of holding SMs
-    const int g_begin = blockIdx.x * p.G;
-    const int g_end = min(g_begin + p.G, p.R);
-    const int t_begin = blockIdx.y * kTilesPerCta;
-    const int t_end = t_begin + kTilesPerCta;
+
+    // ------------------------------------------------------------------ work split
+    // The tiles of all row groups, flattened in (group, subgroup, tile) order, are cut
+    // into gridDim.x equal shares: every CTA gets the same load and none is empty
+    // while another holds a long row.
+    const int ngroups = (int)ceil_div(p.R, p.G);
+    {
+        long long mine = 0;
+        for (int g = threadIdx.x; g < ngroups; g += kThreadsTc) mine += group_units(p, g);
+        for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+        if (lane == 0) bars->red[warp] = mine;
+        if (threadIdx.x == 0) {
+            bars->g0 = ngroups;
+            bars->uo0 = 0;
+        }
+        __syncthreads();
+        long long total = 0;
+        for (int w = 0; w < kThreadsTc / 32; ++w) total += bars->red[w];
+        const long long u_begin = total * blockIdx.x / gridDim.x;
+        const long long u_end = total * (blockIdx.x + 1) / gridDim.x;
+        if (threadIdx.x == 0) {
+            bars->u_begin = u_begin;
+            bars->u_end = u_end;
+        }
+        // the group holding unit u_begin: a block scan over the groups, chunk by chunk
+        long long carry = 0;
+        for (int base = 0; base < ngroups && u_end > u_begin; base += kThreadsTc) {
+            const int g = base + threadIdx.x;
+            const long long u = g < ngroups ? group_units(p, g) : 0;
+            long long incl = u;
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            __syncthreads();  // red[] free
+            if (lane == 31) bars->red[warp] = incl;
+            __syncthreads();
+            long long before = carry;
+            for (int w = 0; w < warp; ++w) before += bars->red[w];
+            long long chunk = 0;
+            for (int w = 0; w < kThreadsTc / 32; ++w) chunk += bars->red[w];
+            const long long excl = before + incl - u;
+            if (g < ngroups && u > 0 && excl <= u_begin && u_begin < excl + u) {
+                bars->g0 = g;
+                bars->uo0 = (int)(u_begin - excl);
+            }
+            carry += chunk;
+            if (carry > u_begin) break;  // uniform: every thread holds the same carry
+        }
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -150,24 +241,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
-        // The whole warp walks the tiles; lane l owns half-tile l of the CTA
-        // (kTilesPerCta * 2 == 32), so all page ids arrive in one round trip.
+        // The whole warp walks the tiles; lane l owns half-tile l of each piece of
+        // up to kPieceTiles tiles, so its page ids arrive in one round trip.
         uint32_t it = 0, qi = 0;
         uint32_t issued_mask = 0, last_parity = 0;
-        int r = g_begin;
-        SubGroup sg;
-        while (!bars->abort && next_subgroup(p, g_end, r, sg)) {
-            const int nt = (int)ceil_div(sg.lmax, kTileTok);
-            const int te = min(t_end, nt);
-            if (t_begin >= te) continue;
-            int my_row = -1;  // first KV slot of my half-tile, -1 if none
-            {
-                const int s = (t_begin + (lane >> 1)) * kTileTok + (lane & 1) * kHalf;
-                if (s < sg.lmax) {
-                    const int64_t page = p.rpt[(int64_t)sg.b * p.rpt_ld + s / p.ps];
-                    if (page >= 0 && page < p.num_pages) my_row = (int)(page * p.ps + s % p.ps);
-                }
-            }
+        for_each_segment(p, bars, [&](const SubGroup &sg, int tb, int te) -> bool {
             bool ok = true;
             if (lane == 0) {
                 ok = mbar_wait(&bars->q_empty, (qi & 1) ^ 1, kWaitBudget);
@@ -177,28 +255,40 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                         tma_load_2d(q_smem + i * kQRowBytes, &qmap, 0, (sg.r0 + i) * kHi, &bars->q_full);
                 }
             }
-            if (!__shfl_sync(0xffffffffu, ok, 0)) { if (lane == 0) fail(bars, p.status); break; }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) { if (lane == 0) fail(bars, p.status); return false; }
             ++qi;
-            for (int t = t_begin; t < te; ++t, ++it) {
-                const int st = it % kStages;
-                const uint32_t ph = (it / kStages) & 1;
-                const int row0 = __shfl_sync(0xffffffffu, my_row, 2 * (t - t_begin));
-                const int row1 = __shfl_sync(0xffffffffu, my_row, 2 * (t - t_begin) + 1);
-                if (lane == 0) {
-                    ok = mbar_wait(&bars->empty[st], ph ^ 1, kWaitBudget);
-                    if (ok) {
-                        const uint32_t bytes = (row0 >= 0 ? kHalfBytes : 0u) + (row1 >= 0 ? kHalfBytes : 0u);
-                        mbar_arrive_expect_tx(&bars->full[st], bytes);
-                        if (row0 >= 0) tma_load_2d(a_ring + st * kTileBytes, &kmap, 0, row0, &bars->full[st]);
-                        if (row1 >= 0)
-                            tma_load_2d(a_ring + st * kTileBytes + kHalfBytes, &kmap, 0, row1, &bars->full[st]);
-                        issued_mask |= 1u << st;
-                        last_parity = (last_parity & ~(1u << st)) | (ph << st);
+            for (int pb = tb; pb < te; pb += kPieceTiles) {
+                const int pe = min(te, pb + kPieceTiles);
+                int my_row = -1;  // first KV slot of my half-tile, -1 if none
+                {
+                    const int s = (pb + (lane >> 1)) * kTileTok + (lane & 1) * kHalf;
+                    if (pb + (lane >> 1) < pe && s < sg.lmax) {
+                        const int64_t page = p.rpt[(int64_t)sg.b * p.rpt_ld + s / p.ps];
+                        if (page >= 0 && page < p.num_pages) my_row = (int)(page * p.ps + s % p.ps);
                     }
                 }
-                if (!__shfl_sync(0xffffffffu, ok, 0)) { if (lane == 0) fail(bars, p.status); break; }
+                for (int t = pb; t < pe; ++t, ++it) {
+                    const int st = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
+                    const int row0 = __shfl_sync(0xffffffffu, my_row, 2 * (t - pb));
+                    const int row1 = __shfl_sync(0xffffffffu, my_row, 2 * (t - pb) + 1);
+                    if (lane == 0) {
+                        ok = mbar_wait(&bars->empty[st], ph ^ 1, kWaitBudget);
+                        if (ok) {
+                            const uint32_t bytes = (row0 >= 0 ? kHalfBytes : 0u) + (row1 >= 0 ? kHalfBytes : 0u);
+                            mbar_arrive_expect_tx(&bars->full[st], bytes);
+                            if (row0 >= 0) tma_load_2d(a_ring + st * kTileBytes, &kmap, 0, row0, &bars->full[st]);
+                            if (row1 >= 0)
+                                tma_load_2d(a_ring + st * kTileBytes + kHalfBytes, &kmap, 0, row1, &bars->full[st]);
+                            issued_mask |= 1u << st;
+                            last_parity = (last_parity & ~(1u << st)) | (ph << st);
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) { if (lane == 0) fail(bars, p.status); return false; }
+                }
             }
-        }
+            return true;
+        });
         // drain: never leave with copies in flight
         if (lane == 0)
             for (int st = 0; st < kStages; ++st)
@@ -207,23 +297,18 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             uint32_t it = 0, ai = 0, qi = 0;
-            int r = g_begin;
-            SubGroup sg;
-            while (!bars->abort && next_subgroup(p, g_end, r, sg)) {
-                const int nt = (int)ceil_div(sg.lmax, kTileTok);
-                const int te = min(t_end, nt);
-                if (t_begin >= te) continue;
+            for_each_segment(p, bars, [&](const SubGroup &sg, int tb, int te) -> bool {
                 const uint32_t N = kHi * sg.c;
                 const uint32_t idesc = instr_desc(0, 0, 0, 0, kTileTok, N);
-                if (!mbar_wait(&bars->q_full, qi & 1, kWaitBudget)) { fail(bars, p.status); break; }
+                if (!mbar_wait(&bars->q_full, qi & 1, kWaitBudget)) { fail(bars, p.status); return false; }
                 ++qi;
-                for (int t = t_begin; t < te; ++t, ++it, ++ai) {
+                for (int t = tb; t < te; ++t, ++it, ++ai) {
                     const int st = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
                     const int ab = ai & 1;
                     const uint32_t aph = (ai >> 1) & 1;
-                    if (!mbar_wait(&bars->full[st], ph, kWaitBudget)) { fail(bars, p.status); break; }
-                    if (!mbar_wait(&bars->acc_empty[ab], aph ^ 1, kWaitBudget)) { fail(bars, p.status); break; }
+                    if (!mbar_wait(&bars->full[st], ph, kWaitBudget)) { fail(bars, p.status); return false; }
+                    if (!mbar_wait(&bars->acc_empty[ab], aph ^ 1, kWaitBudget)) { fail(bars, p.status); return false; }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(a_ring + st * kTileBytes);
                     const uint32_t b_addr = smem_u32(q_smem);
@@ -238,7 +323,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     mma_commit(&bars->acc_full[ab]);
                 }
                 mma_commit(&bars->q_empty);
-            }
+                return true;
+            });
             // all MMAs retired before TMEM is released
             mma_commit(&bars->done);
             mbar_wait(&bars->done, 0, kWaitBudget);
@@ -249,12 +335,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
         const int tok = quad * 32 + lane;         // token within the tile
         uint32_t ai = 0;
-        int r = g_begin;
-        SubGroup sg;
-        while (!bars->abort && next_subgroup(p, g_end, r, sg)) {
-            const int nt = (int)ceil_div(sg.lmax, kTileTok);
-            const int te = min(t_end, nt);
-            if (t_begin >= te) continue;
+        for_each_segment(p, bars, [&](const SubGroup &sg, int tb, int te) -> bool {
             asm volatile("bar.sync 1, 128;" ::: "memory");
             for (int i = et; i < sg.c * kHi; i += 128) bars->w[i] = p.w[(int64_t)sg.r0 * kHi + i];
             asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -274,8 +355,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             };
             float scale_next;
             bool valid_next;
-            fetch_scale(t_begin, scale_next, valid_next);
-            for (int t = t_begin; t < te; ++t, ++ai) {
+            fetch_scale(tb, scale_next, valid_next);
+            for (int t = tb; t < te; ++t, ++ai) {
                 const int ab = ai & 1;
                 const uint32_t aph = (ai >> 1) & 1;
                 const int s = t * kTileTok + tok;
@@ -283,7 +364,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 const bool valid_page = valid_next;
                 fetch_scale(t + 1, scale_next, valid_next);
                 if (s < sg.lmax && !valid_page) set_status(p.status, NSA_ERR_BOUNDS);
-                if (!mbar_wait(&bars->acc_full[ab], aph, kWaitBudget)) { fail(bars, p.status); break; }
+                if (!mbar_wait(&bars->acc_full[ab], aph, kWaitBudget)) { fail(bars, p.status); return false; }
                 tc_fence_after();
                 const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + ab * p.acc_stride;
                 for (int i = 0; i < sg.c; ++i) {
@@ -303,7 +384,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 tc_fence_before();
                 mbar_arrive(&bars->acc_empty[ab]);
             }
-        }
+            return true;
+        });
     }
 
     tc_fence_before();
@@ -349,9 +431,13 @@ nsa_status indexer_tc_try_launch(nsa_dtype dtype, const void *q, const float *w,
     NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     // the whole shared memory for the carveout: three CTAs per SM at one row per group
     NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100));
-    const int tiles = (int)ceil_div(max_row_len, kTileTok);
-    dim3 grid((unsigned)ceil_div(R, G), (unsigned)ceil_div(tiles, kTilesPerCta));
-    if (grid.y > 65535) return NSA_ERR_UNSUPPORTED;
+    // a persistent grid of up to three CTAs per SM shares the flattened tiles evenly
+    const int64_t units_max = ceil_div(R, G) * ceil_div(max_row_len, kTileTok);
+    int dev = 0, sms = 0;
+    NSA_CUDA_TRY(cudaGetDevice(&dev));
+    NSA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(units_max, 3LL * sms));
+    dim3 grid((unsigned)ctas);
     kern<<<grid, kThreadsTc, smem, stream>>>(kmap, qmap, p);
     return launch_status();
 }
