@@ -14,7 +14,7 @@
 // (one thread per token) applies ReLU, the per-head weights, the head sum and
 // the key's scale, and stores one fp32 logit per (row, token).
 //
-// Grid: up to three CTAs per SM, persistent: the tiles of all row groups,
+// Grid: one CTA per SM, persistent, with a deep TMA ring: the tiles of all row groups,
 // flattened in (group, subgroup, tile) order, are cut into equal shares, one
 // per CTA (each CTA finds its start with one block-wide pass over the row
 // lengths), so no SM idles while another works through a long row.
@@ -38,7 +38,7 @@ constexpr int kTileTok = 128;
 constexpr int kHalf = 64;
 constexpr int kDi = 128;
 constexpr int kHi = 64;
-constexpr int kStages = 4;
+constexpr int kMaxStages = 12;      // TMA ring depth: as many 16 KB stages as fit one CTA per SM
 constexpr int kThreadsTc = 192;
 constexpr int kMaxG = 4;
 constexpr int kPieceTiles = 16;  // tiles whose page ids the producer warp fetches at once (one half-tile per lane)
@@ -62,11 +62,12 @@ struct TcParams {
     int32_t *status;
     uint32_t acc_stride;  // TMEM columns per accumulator buffer
     uint32_t tmem_cols;
+    int stages;           // TMA ring depth (<= kMaxStages)
 };
 
 struct Bars {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t q_full;
@@ -152,13 +153,13 @@ __device__ __forceinline__ void for_each_segment(const TcParams &p, const Bars *
     }
 }
 
-__global__ void __maxnreg__(112)  // 192 threads, three CTAs per SM
+__global__ void __launch_bounds__(kThreadsTc, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *a_ring = smem;                              // kStages x 16 KB
-    uint8_t *q_smem = a_ring + kStages * kTileBytes;     // G x 8 KB
+    uint8_t *a_ring = smem;                              // stages x 16 KB
+    uint8_t *q_smem = a_ring + p.stages * kTileBytes;    // G x 8 KB
     Bars *bars = (Bars *)(q_smem + p.G * kQRowBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -170,7 +171,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const int ngroups = (int)ceil_div(p.R, p.G);
     {
         long long mine = 0;
-        for (int g = threadIdx.x; g < ngroups; g += kThreadsTc) mine += group_units(p, g);
+        const int first_units = threadIdx.x < ngroups ? group_units(p, threadIdx.x) : 0;  // reused by the scan
+        mine = first_units;
+        for (int g = threadIdx.x + kThreadsTc; g < ngroups; g += kThreadsTc) mine += group_units(p, g);
         for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
         if (lane == 0) bars->red[warp] = mine;
         if (threadIdx.x == 0) {
@@ -190,7 +193,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         long long carry = 0;
         for (int base = 0; base < ngroups && u_end > u_begin; base += kThreadsTc) {
             const int g = base + threadIdx.x;
-            const long long u = g < ngroups ? group_units(p, g) : 0;
+            const long long u = g < ngroups ? (base == 0 ? first_units : group_units(p, g)) : 0;
             long long incl = u;
             for (int o = 1; o < 32; o <<= 1) {
                 const long long y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -214,7 +217,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     }
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < p.stages; ++i) {
             mbar_init(&bars->full[i], 1);
             mbar_init(&bars->empty[i], 1);
         }
@@ -268,8 +271,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     }
                 }
                 for (int t = pb; t < pe; ++t, ++it) {
-                    const int st = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1;
+                    const int st = it % p.stages;
+                    const uint32_t ph = (it / p.stages) & 1;
                     const int row0 = __shfl_sync(0xffffffffu, my_row, 2 * (t - pb));
                     const int row1 = __shfl_sync(0xffffffffu, my_row, 2 * (t - pb) + 1);
                     if (lane == 0) {
@@ -291,7 +294,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         });
         // drain: never leave with copies in flight
         if (lane == 0)
-            for (int st = 0; st < kStages; ++st)
+            for (int st = 0; st < p.stages; ++st)
                 if (issued_mask & (1u << st)) mbar_wait(&bars->full[st], (last_parity >> st) & 1, kWaitBudget);
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
@@ -303,8 +306,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 if (!mbar_wait(&bars->q_full, qi & 1, kWaitBudget)) { fail(bars, p.status); return false; }
                 ++qi;
                 for (int t = tb; t < te; ++t, ++it, ++ai) {
-                    const int st = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1;
+                    const int st = it % p.stages;
+                    const uint32_t ph = (it / p.stages) & 1;
                     const int ab = ai & 1;
                     const uint32_t aph = (ai >> 1) & 1;
                     if (!mbar_wait(&bars->full[st], ph, kWaitBudget)) { fail(bars, p.status); return false; }
@@ -426,17 +429,18 @@ nsa_status indexer_tc_try_launch(nsa_dtype dtype, const void *q, const float *w,
     while (cols < 2 * p.acc_stride) cols <<= 1;
     p.tmem_cols = cols;
 
-    const size_t smem = 1024 + (size_t)kStages * kTileBytes + (size_t)G * kQRowBytes + sizeof(Bars);
+    // one CTA per SM; the ring takes what the q rows and barriers leave of 227 KB
+    const size_t fixed = 1024 + (size_t)G * kQRowBytes + sizeof(Bars);
+    p.stages = (int)std::min<size_t>(kMaxStages, (232448 - fixed) / kTileBytes);
+    const size_t smem = fixed + (size_t)p.stages * kTileBytes;
     auto kern = indexer_tc_kernel;
     NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    // the whole shared memory for the carveout: three CTAs per SM at one row per group
-    NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100));
-    // a persistent grid of up to three CTAs per SM shares the flattened tiles evenly
+    // a persistent grid of one CTA per SM shares the flattened tiles evenly
     const int64_t units_max = ceil_div(R, G) * ceil_div(max_row_len, kTileTok);
     int dev = 0, sms = 0;
     NSA_CUDA_TRY(cudaGetDevice(&dev));
     NSA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(units_max, 3LL * sms));
+    const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(units_max, (int64_t)sms));
     dim3 grid((unsigned)ctas);
     kern<<<grid, kThreadsTc, smem, stream>>>(kmap, qmap, p);
     return launch_status();
