@@ -12,7 +12,8 @@
 //
 // accumulates in TMEM (fp32) via tcgen05.mma kind::f8f6f4.  The epilogue
 // (one thread per token) applies ReLU, the per-head weights, the head sum and
-// the key's scale, and stores one fp32 logit per (row, token).
+// the key's scale (bulk-copied into shared memory with the tile), and stores
+// one fp32 logit per (row, token).
 //
 // Grid: one CTA per SM, persistent, with a deep TMA ring: the tiles of all row groups,
 // flattened in (group, subgroup, tile) order, are cut into equal shares, one
@@ -79,6 +80,8 @@ struct Bars {
     long long u_begin, u_end;          // this CTA's share of the flattened tiles
     long long red[kThreadsTc / 32];
     float w[kMaxG * kHi];
+    float scale[kMaxStages][kTileTok];  // key scales of each stage's tile (bulk-copied with it)
+    int half_ok[kMaxStages][2];         // the stage's 64-token halves hold real keys
 };
 
 // Sub-group n of the CTA's row group: the n-th maximal run of rows sharing a request.
@@ -219,7 +222,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&bars->full[i], 1);
-            mbar_init(&bars->empty[i], 1);
+            mbar_init(&bars->empty[i], 1 + 128);  // the MMA and every epilogue thread release a stage
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->acc_full[i], 1);
@@ -267,7 +270,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     const int s = (pb + (lane >> 1)) * kTileTok + (lane & 1) * kHalf;
                     if (pb + (lane >> 1) < pe && s < sg.lmax) {
                         const int64_t page = p.rpt[(int64_t)sg.b * p.rpt_ld + s / p.ps];
-                        if (page >= 0 && page < p.num_pages) my_row = (int)(page * p.ps + s % p.ps);
+                        if (page >= 0 && page < p.num_pages)
+                            my_row = (int)(page * p.ps + s % p.ps);
+                        else
+                            set_status(p.status, NSA_ERR_BOUNDS);  // its keys score -inf
                     }
                 }
                 for (int t = pb; t < pe; ++t, ++it) {
@@ -278,11 +284,21 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     if (lane == 0) {
                         ok = mbar_wait(&bars->empty[st], ph ^ 1, kWaitBudget);
                         if (ok) {
-                            const uint32_t bytes = (row0 >= 0 ? kHalfBytes : 0u) + (row1 >= 0 ? kHalfBytes : 0u);
+                            // each real half: 8 KB of keys and their 64 scales (256 B)
+                            constexpr uint32_t kScaleBytes = kHalf * sizeof(float);
+                            bars->half_ok[st][0] = row0 >= 0;
+                            bars->half_ok[st][1] = row1 >= 0;
+                            const uint32_t bytes = (row0 >= 0 ? kHalfBytes + kScaleBytes : 0u) +
+                                                   (row1 >= 0 ? kHalfBytes + kScaleBytes : 0u);
                             mbar_arrive_expect_tx(&bars->full[st], bytes);
-                            if (row0 >= 0) tma_load_2d(a_ring + st * kTileBytes, &kmap, 0, row0, &bars->full[st]);
-                            if (row1 >= 0)
+                            if (row0 >= 0) {
+                                tma_load_2d(a_ring + st * kTileBytes, &kmap, 0, row0, &bars->full[st]);
+                                bulk_load(&bars->scale[st][0], p.k_scale + row0, kScaleBytes, &bars->full[st]);
+                            }
+                            if (row1 >= 0) {
                                 tma_load_2d(a_ring + st * kTileBytes + kHalfBytes, &kmap, 0, row1, &bars->full[st]);
+                                bulk_load(&bars->scale[st][kHalf], p.k_scale + row1, kScaleBytes, &bars->full[st]);
+                            }
                             issued_mask |= 1u << st;
                             last_parity = (last_parity & ~(1u << st)) | (ph << st);
                         }
@@ -337,7 +353,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const int et = threadIdx.x - 64;          // 0..127
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
         const int tok = quad * 32 + lane;         // token within the tile
-        uint32_t ai = 0;
+        uint32_t ai = 0, it = 0;
         for_each_segment(p, bars, [&](const SubGroup &sg, int tb, int te) -> bool {
             asm volatile("bar.sync 1, 128;" ::: "memory");
             for (int i = et; i < sg.c * kHi; i += 128) bars->w[i] = p.w[(int64_t)sg.r0 * kHi + i];
@@ -345,28 +361,16 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             int Lrow[kMaxG];
 #pragma unroll
             for (int i = 0; i < kMaxG; ++i) Lrow[i] = i < sg.c ? clamp_len(p, sg.r0 + i) : 0;
-            // the key scale of my token, one tile ahead of the accumulator
-            auto fetch_scale = [&](int t, float &scale, bool &valid) {
-                const int s = t * kTileTok + tok;
-                scale = 0.f;
-                valid = false;
-                if (t < te && s < sg.lmax) {
-                    const int64_t page = p.rpt[(int64_t)sg.b * p.rpt_ld + s / p.ps];
-                    valid = page >= 0 && page < p.num_pages;
-                    if (valid) scale = __ldg(p.k_scale + page * p.ps + s % p.ps);
-                }
-            };
-            float scale_next;
-            bool valid_next;
-            fetch_scale(tb, scale_next, valid_next);
-            for (int t = tb; t < te; ++t, ++ai) {
+            for (int t = tb; t < te; ++t, ++ai, ++it) {
                 const int ab = ai & 1;
                 const uint32_t aph = (ai >> 1) & 1;
                 const int s = t * kTileTok + tok;
-                const float scale = scale_next;
-                const bool valid_page = valid_next;
-                fetch_scale(t + 1, scale_next, valid_next);
-                if (s < sg.lmax && !valid_page) set_status(p.status, NSA_ERR_BOUNDS);
+                // my token's key scale arrived with the tile; then the stage is released
+                const int st = it % p.stages;
+                if (!mbar_wait(&bars->full[st], (it / p.stages) & 1, kWaitBudget)) { fail(bars, p.status); return false; }
+                const float scale = bars->scale[st][tok];
+                const bool valid_page = bars->half_ok[st][tok >> 6] != 0;
+                mbar_arrive(&bars->empty[st]);
                 if (!mbar_wait(&bars->acc_full[ab], aph, kWaitBudget)) { fail(bars, p.status); return false; }
                 tc_fence_after();
                 const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + ab * p.acc_stride;
@@ -408,7 +412,7 @@ nsa_status indexer_tc_try_launch(nsa_dtype dtype, const void *q, const float *w,
                                  int64_t logits_ld, int32_t *status, cudaStream_t stream, int rows_per_group)
 {
     if (dtype != NSA_DT_E4M3 || Hi != kHi || Di != kDi || page_size % kHalf != 0) return NSA_ERR_UNSUPPORTED;
-    if (((uintptr_t)q & 15) || ((uintptr_t)k_cache & 15)) return NSA_ERR_UNSUPPORTED;
+    if (((uintptr_t)q & 15) || ((uintptr_t)k_cache & 15) || ((uintptr_t)k_scale & 15)) return NSA_ERR_UNSUPPORTED;
     if (num_pages * page_size > 2147483647LL || (int64_t)R * kHi > 2147483647LL) return NSA_ERR_UNSUPPORTED;
     const int G = rows_per_group < 1 ? 1 : (rows_per_group > kMaxG ? kMaxG : rows_per_group);
 

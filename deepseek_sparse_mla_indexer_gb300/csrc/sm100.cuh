@@ -123,6 +123,15 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
+// Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to
+// shared memory; the transfer counts as complete_tx bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // Bring `bytes` (multiple of 16, 16-byte aligned) at `src` into L2.
 __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
 {
