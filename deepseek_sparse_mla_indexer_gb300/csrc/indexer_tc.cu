@@ -25,6 +25,7 @@
 // Stages are tracked with mbarriers; every wait is bounded and reports
 // NSA_ERR_TIMEOUT instead of hanging.
 #include <algorithm>
+#include <cstddef>
 
 #include "indexer_tc.cuh"
 #include "sm100.cuh"
@@ -80,9 +81,11 @@ struct Bars {
     long long u_begin, u_end;          // this CTA's share of the flattened tiles
     long long red[kThreadsTc / 32];
     float w[kMaxG * kHi];
-    float scale[kMaxStages][kTileTok];  // key scales of each stage's tile (bulk-copied with it)
-    int half_ok[kMaxStages][2];         // the stage's 64-token halves hold real keys
+    alignas(16) float scale[kMaxStages][kTileTok];  // key scales of each stage's tile (bulk-copied with it)
+    int half_ok[kMaxStages][2];                     // the stage's 64-token halves hold real keys
 };
+static_assert(offsetof(Bars, scale) % 16 == 0, "bulk-copy destinations are 16-byte aligned");
+static_assert(offsetof(Bars, full) % 8 == 0 && offsetof(Bars, u_begin) % 8 == 0, "mbarriers / 64-bit fields");
 
 // Sub-group n of the CTA's row group: the n-th maximal run of rows sharing a request.
 struct SubGroup {
