@@ -169,6 +169,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     Bars *bars = (Bars *)(q_smem + p.G * kQRowBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&qmap);
+    }
+    pdl_wait();  // row lengths and page tables come from the metadata kernel
 
     // ------------------------------------------------------------------ work split
     // The tiles of all row groups, flattened in (group, subgroup, tile) order, are cut
@@ -236,8 +242,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         mbar_init(&bars->done, 1);
         bars->abort = 0;
         fence_mbar_init();
-        prefetch_tensormap(&kmap);
-        prefetch_tensormap(&qmap);
     }
     if (warp == 1) {
         tmem_alloc(&bars->tmem_base, p.tmem_cols);
@@ -449,8 +453,16 @@ nsa_status indexer_tc_try_launch(nsa_dtype dtype, const void *q, const float *w,
     NSA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(units_max, (int64_t)sms));
     dim3 grid((unsigned)ctas);
-    kern<<<grid, kThreadsTc, smem, stream>>>(kmap, qmap, p);
-    return launch_status();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreadsTc);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, kmap, qmap, p));
+    return NSA_OK;
 }
 
 }  // namespace nsa

@@ -247,6 +247,8 @@ __device__ void copy_tables(const MetaParams &p, int first_seg, int seg_stride)
 
 __global__ void __launch_bounds__(kRowThreads) metadata_kernel(MetaParams p)
 {
+    pdl_trigger();
+    pdl_wait();  // the previous step's kernels may still read these tables
     if (blockIdx.x == 0) {
         if (p.B <= kSmemB) build_rows_smem(p);
         else build_rows(p);
@@ -297,6 +299,13 @@ extern "C" nsa_status nsa_metadata(nsa_mode mode, int B, int R, int W, int n_dra
     int64_t copy_blocks = segs;
     if (copy_blocks > 152 * 4) copy_blocks = 152 * 4;
     if (copy_blocks < 1) copy_blocks = 1;
-    metadata_kernel<<<(unsigned)(1 + copy_blocks), kRowThreads, 0, (cudaStream_t)stream>>>(p);
-    return launch_status();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(1 + copy_blocks));
+    cfg.blockDim = dim3(kRowThreads);
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, metadata_kernel, p));
+    return NSA_OK;
 }

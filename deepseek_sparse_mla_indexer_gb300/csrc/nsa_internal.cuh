@@ -43,6 +43,24 @@ __device__ __forceinline__ int32_t floor_div(int32_t a, int32_t b)
     return (r != 0 && ((r < 0) != (b < 0))) ? q - 1 : q;
 }
 
+// Programmatic dependent launch: the step's kernels are launched so that each
+// may start while its predecessor on the stream finishes.  A kernel lets its
+// dependents launch at entry (pdl_trigger) and, before it reads anything an
+// earlier kernel wrote or writes anything an earlier kernel reads, waits for its
+// predecessor to complete with its memory visible (pdl_wait).  Both are no-ops
+// for a launch without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// The launch attribute that allows the overlap.
+inline cudaLaunchAttribute pdl_attribute()
+{
+    cudaLaunchAttribute a = {};
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return a;
+}
+
 inline nsa_status launch_status()
 {
     return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;

@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hg = blockIdx.x, sp = blockIdx.y, r = blockIdx.z;
+    pdl_trigger();
     const int ntiles_all = (p.topk + kTok - 1) / kTok;
     const int t0 = sp * p.tiles_per_split;
     const int nt = max(0, min(t0 + p.tiles_per_split, ntiles_all) - t0);
@@ -180,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 
     if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
+        pdl_wait();  // every thread passes the wait before this grid writes global memory
         if (lane == 0) {
             const uint32_t idesc_s = instr_desc(1, 1, 0, 0, kTok, kHc);  // bf16, K-major A and B
             const uint32_t idesc_o = instr_desc(1, 1, 1, 1, 128, kHc);   // bf16, MN-major A and B
@@ -253,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             }
         }
         cp_async_commit();
+        pdl_wait();  // the indices come from the top-k kernel (q and the KV cache do not)
         auto release_q = [&]() {
             fence_proxy_async_smem();
             mbar_arrive(&sm->q_full);
@@ -803,13 +806,14 @@ nsa_status sparse_mla_tc_try_launch(nsa_dtype q_dtype, nsa_dtype kv_dtype, const
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = p.cluster_merge ? (unsigned)p.nsplit : 1u;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, p));
     if (p.nsplit > 1 && !p.cluster_merge) {
         const int64_t rows = (int64_t)R * H;

@@ -113,6 +113,8 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
     __shared__ uint32_t total;
     __shared__ uint32_t sel_digit, sel_need, sel_exact;
 
+    pdl_trigger();
+    pdl_wait();  // the scores come from the indexer
     const int r = blockIdx.x;
     const int L = row_len[r];
     const int b = row_to_req[r];
@@ -313,6 +315,8 @@ topk_cluster_kernel(const float *logits, int64_t logits_ld, const int32_t *row_l
     __shared__ uint32_t sel_digit, sel_need, sel_exact;
     __shared__ uint32_t counts[2];               // (#above, #equal) in this slice
 
+    pdl_trigger();
+    pdl_wait();  // the scores come from the indexer
     const uint32_t rank = cluster_rank();
     uint32_t csize;
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
@@ -484,13 +488,14 @@ extern "C" nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits
         cfg.blockDim = dim3(kCThreads);
         cfg.dynamicSmemBytes = kCSliceCap * sizeof(uint32_t);
         cfg.stream = (cudaStream_t)stream;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = (unsigned)csize;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1] = pdl_attribute();
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, topk_cluster_kernel, logits_dev, logits_ld, row_len_dev,
                                         row_to_req_dev, page_table_1_dev, pt_ld, topk, max_row_len, indices_dev,
                                         indices_ld, status_dev));
@@ -500,8 +505,16 @@ extern "C" nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits
     const size_t smem = row_kernel_smem_bytes(cap);
     NSA_CUDA_TRY(cudaFuncSetAttribute(topk_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)smem));
-    topk_transform_kernel<<<(unsigned)R, kThreads, smem, (cudaStream_t)stream>>>(
-        logits_dev, logits_ld, row_len_dev, row_to_req_dev, page_table_1_dev, pt_ld, topk, max_row_len,
-        cap, indices_dev, indices_ld, status_dev);
-    return launch_status();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)R);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, topk_transform_kernel, logits_dev, logits_ld, row_len_dev, row_to_req_dev,
+                                    page_table_1_dev, pt_ld, topk, max_row_len, cap, indices_dev, indices_ld,
+                                    status_dev));
+    return NSA_OK;
 }
