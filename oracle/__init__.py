@@ -60,6 +60,11 @@ def _load():
             lib.orc_fp8_row_bytes.argtypes, lib.orc_fp8_row_bytes.restype = [I, I], L
             lib.orc_sparse_mla_row.argtypes = [I, I, I, I, I, I, P, L, P, L, P, L, P, D, P, P]
             lib.orc_sparse_mla_row.restype = I
+            lib.orc_e4m3_encode.argtypes, lib.orc_e4m3_encode.restype = [C.c_float], C.c_uint8
+            lib.orc_f32_to_bf16.argtypes, lib.orc_f32_to_bf16.restype = [C.c_float], C.c_uint16
+            lib.orc_quantize_mla_row.argtypes, lib.orc_quantize_mla_row.restype = [P, P, I, I, P], None
+            lib.orc_dequantize_mla_row.argtypes, lib.orc_dequantize_mla_row.restype = [P, I, I, P], None
+            lib.orc_quantize_index_row.argtypes, lib.orc_quantize_index_row.restype = [P, I, P], C.c_float
             _lib = lib
     return _lib
 
@@ -255,3 +260,52 @@ def sparse_mla(q_dtype: int, kv_dtype: int, q_nope, q_rope, kv, indices, sm_scal
         if rc != 0:
             raise ValueError(f"oracle sparse MLA: index out of range in row {r}")
     return out, lse
+
+
+# ---------------------------------------------------------------- KV-cache write side
+
+def e4m3_encode(x) -> np.ndarray:
+    """fp32 values -> e4m3 codes (nearest, ties to even, saturating at 448)."""
+    lib = _load()
+    a = np.asarray(x, dtype=np.float32)
+    return np.array([lib.orc_e4m3_encode(float(v)) for v in a.reshape(-1)], dtype=np.uint8).reshape(a.shape)
+
+
+def f32_to_bf16(x) -> np.ndarray:
+    lib = _load()
+    a = np.asarray(x, dtype=np.float32)
+    return np.array([lib.orc_f32_to_bf16(float(v)) for v in a.reshape(-1)], dtype=np.uint16).reshape(a.shape)
+
+
+def quantize_mla_rows(latent, rope) -> np.ndarray:
+    """bf16 bits [N, d_latent] and [N, d_rope] -> fp8 rows uint8 [N, row_bytes]."""
+    lib = _load()
+    lat = _c(latent, np.uint16)
+    rp = _c(rope, np.uint16)
+    n, dl = lat.shape
+    dr = rp.shape[1]
+    out = np.zeros((n, fp8_row_bytes(dl, dr)), dtype=np.uint8)
+    for i in range(n):
+        lib.orc_quantize_mla_row(_p(lat[i]), _p(rp[i]), dl, dr, _p(out[i]))
+    return out
+
+
+def dequantize_mla_rows(rows, d_latent: int, d_rope: int) -> np.ndarray:
+    """fp8 rows uint8 [N, row_bytes] -> bf16 bits [N, d_latent + d_rope]."""
+    lib = _load()
+    r = _c(rows, np.uint8)
+    out = np.zeros((r.shape[0], d_latent + d_rope), dtype=np.uint16)
+    for i in range(r.shape[0]):
+        lib.orc_dequantize_mla_row(_p(r[i]), d_latent, d_rope, _p(out[i]))
+    return out
+
+
+def quantize_index_rows(k):
+    """bf16 bits [N, D] -> (e4m3 codes [N, D], fp32 scales [N])."""
+    lib = _load()
+    a = _c(k, np.uint16)
+    codes = np.zeros(a.shape, dtype=np.uint8)
+    scales = np.zeros((a.shape[0],), dtype=np.float32)
+    for i in range(a.shape[0]):
+        scales[i] = lib.orc_quantize_index_row(_p(a[i]), a.shape[1], _p(codes[i]))
+    return codes, scales

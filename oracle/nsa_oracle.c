@@ -445,3 +445,101 @@ int orc_sparse_mla_row(int q_dtype, int kv_dtype, int H, int d_latent, int d_rop
     free(s);
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* KV-cache write side: the rows the attention reads, written from bf16.    */
+/* ------------------------------------------------------------------------ */
+
+/* The pages name the conversions only ([NSA] set_mla_kv_buffer(layer, loc, k,
+ * k_rope) and quantize_k_cache(kv_cache), which turns a bf16 cache into the
+ * fp8 layout; [DSA] the same plus dequantize_k_cache_paged(kv_cache,
+ * page_table_1_flattened)).  The rule written out here: a block of values gets
+ * one fp32 scale, its largest magnitude divided by 448 (1 for an all-zero
+ * block); each value divided by the scale (fp32) is rounded to the nearest
+ * e4m3 value, ties to even mantissa, magnitudes beyond 448 saturating. */
+
+/* x -> e4m3 code (round to nearest, ties to even; saturating; NaN -> 0x7F). */
+uint8_t orc_e4m3_encode(float x)
+{
+    double a = fabs((double)x);
+    uint8_t sign = (uint8_t)(signbit(x) ? 0x80 : 0x00);
+    if (x != x) return 0x7F;
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E); /* largest finite */
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range: multiples of 2^-9; a mantissa of 8 is the smallest normal */
+        double m = nearbyint(a * 512.0); /* exact scaling; ties to even */
+        return (uint8_t)(sign | (uint8_t)m);
+    }
+    {
+        int e;
+        double fr = frexp(a, &e);           /* a = fr * 2^e, fr in [0.5, 1) */
+        double m = nearbyint((fr * 2.0 - 1.0) * 8.0); /* 3 mantissa bits, ties to even */
+        int ef = (e - 1) + 7;               /* biased exponent of 2^(e-1) */
+        if (m >= 8.0) {
+            m = 0.0;
+            ef += 1;
+        }
+        if (ef > 15 || (ef == 15 && m > 6.0)) return (uint8_t)(sign | 0x7E);
+        return (uint8_t)(sign | (uint8_t)(ef << 3) | (uint8_t)m);
+    }
+}
+
+/* fp32 -> bf16 bits, round to nearest even (NaN stays a quiet NaN). */
+uint16_t orc_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x0040u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+static float bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* One block of n bf16 values -> n codes and the block's scale. */
+static float quantize_block(const uint16_t *x, int n, uint8_t *codes)
+{
+    float amax = 0.0f, scale;
+    for (int i = 0; i < n; ++i) {
+        float v = fabsf(bf16_to_f32(x[i]));
+        if (v > amax) amax = v;
+    }
+    scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int i = 0; i < n; ++i) codes[i] = orc_e4m3_encode(bf16_to_f32(x[i]) / scale);
+    return scale;
+}
+
+/* One MLA KV row in the fp8 layout: latent codes (d_latent) | one fp32 scale per
+ * 128 latent values | rope bf16 (d_rope), from bf16 latent and rope. */
+void orc_quantize_mla_row(const uint16_t *latent, const uint16_t *rope, int d_latent, int d_rope, uint8_t *row)
+{
+    for (int b = 0; b < d_latent / 128; ++b) {
+        float sc = quantize_block(latent + 128 * b, 128, row + 128 * b);
+        memcpy(row + d_latent + 4 * b, &sc, 4);
+    }
+    memcpy(row + d_latent + 4 * (d_latent / 128), rope, 2 * (size_t)d_rope);
+}
+
+/* One fp8 MLA row back to bf16: code * scale rounded once to fp32 (the exact
+ * product of two fp32 values fits a double), then to bf16. */
+void orc_dequantize_mla_row(const uint8_t *row, int d_latent, int d_rope, uint16_t *out)
+{
+    for (int d = 0; d < d_latent; ++d) {
+        float sc;
+        memcpy(&sc, row + d_latent + 4 * (d / 128), 4);
+        out[d] = orc_f32_to_bf16((float)(orc_e4m3_to_f64(row[d]) * (double)sc));
+    }
+    memcpy(out + d_latent, row + d_latent + 4 * (d_latent / 128), 2 * (size_t)d_rope);
+}
+
+/* One indexer key row: D codes and one fp32 scale. */
+float orc_quantize_index_row(const uint16_t *k, int D, uint8_t *codes)
+{
+    return quantize_block(k, D, codes);
+}
