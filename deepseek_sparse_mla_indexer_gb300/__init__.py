@@ -21,7 +21,8 @@ __all__ = [
     "NsaError", "load", "MODE_DECODE", "MODE_EXTEND", "MODE_TARGET_VERIFY", "DT_F32", "DT_BF16",
     "DT_E4M3", "nsa_metadata", "alloc_metadata", "nsa_local_virtual_batches", "nsa_effective_chunk_size",
     "nsa_indexer_logits", "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes",
-    "nsa_sparse_mla_plan", "nsa_status_read", "nsa_status_string", "nsa_abi_version", "EXPORTED_SYMBOLS",
+    "nsa_sparse_mla_plan", "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged",
+    "nsa_set_index_k", "nsa_status_read", "nsa_status_string", "nsa_abi_version", "EXPORTED_SYMBOLS",
 ]
 
 MODE_DECODE, MODE_EXTEND, MODE_TARGET_VERIFY = 0, 1, 2
@@ -32,6 +33,7 @@ EXPORTED_SYMBOLS = [
     "nsa_status_string", "nsa_abi_version", "nsa_status_read", "nsa_metadata",
     "nsa_effective_chunk_size", "nsa_local_virtual_batches", "nsa_indexer_logits",
     "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes", "nsa_sparse_mla_plan",
+    "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged", "nsa_set_index_k",
 ]
 
 _lib = None
@@ -67,6 +69,10 @@ def load(build_if_missing: bool = True):
         "nsa_sparse_mla": ([I, I, P, L, L, P, L, L, P, L, P, L, I, I, I, I, I, F, P, P, P, S, P, P], I),
         "nsa_sparse_mla_workspace_bytes": ([I, I, I, I, I, I, I], S),
         "nsa_sparse_mla_plan": ([I, I, I, I, I, I, I, P, P], I),
+        "nsa_set_mla_kv": ([I, P, L, P, L, P, I, I, I, P, L, P, P], I),
+        "nsa_quantize_kv_cache": ([P, L, I, I, P, P], I),
+        "nsa_dequantize_kv_paged": ([P, L, I, I, P, L, P, P, P], I),
+        "nsa_set_index_k": ([P, L, P, I, I, P, P, L, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -239,3 +245,40 @@ def nsa_sparse_mla(q_dtype: int, kv_dtype: int, q_nope: torch.Tensor, q_rope: to
                                indices.stride(0), R, H, d_latent, d_rope, topk, float(sm_scale), _ptr(out),
                                _ptr(lse), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
     _check("nsa_sparse_mla", rc)
+
+
+# ---------------------------------------------------------------- KV-cache write side
+
+def nsa_set_mla_kv(kv_dtype: int, k_nope: torch.Tensor, k_rope: torch.Tensor, loc: torch.Tensor,
+                   kv: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """New tokens' latent [n, 512] and rope [n, 64] (bf16) into the KV cache at slots `loc` (int32)."""
+    n = loc.shape[0]
+    num_slots = kv.shape[0]
+    rc = load().nsa_set_mla_kv(kv_dtype, _ptr(k_nope), k_nope.stride(0), _ptr(k_rope), k_rope.stride(0), _ptr(loc),
+                               n, k_nope.shape[1], k_rope.shape[1], _ptr(kv), num_slots, _ptr(status),
+                               _stream(stream))
+    _check("nsa_set_mla_kv", rc)
+
+
+def nsa_quantize_kv_cache(kv_bf16: torch.Tensor, kv_fp8: torch.Tensor, d_latent: int = 512, d_rope: int = 64,
+                          stream=None) -> None:
+    rc = load().nsa_quantize_kv_cache(_ptr(kv_bf16), kv_bf16.shape[0], d_latent, d_rope, _ptr(kv_fp8),
+                                      _stream(stream))
+    _check("nsa_quantize_kv_cache", rc)
+
+
+def nsa_dequantize_kv_paged(kv_fp8: torch.Tensor, slots: torch.Tensor, out_bf16: torch.Tensor,
+                            d_latent: int = 512, d_rope: int = 64, status: Optional[torch.Tensor] = None,
+                            stream=None) -> None:
+    rc = load().nsa_dequantize_kv_paged(_ptr(kv_fp8), kv_fp8.shape[0], d_latent, d_rope, _ptr(slots),
+                                        slots.shape[0], _ptr(out_bf16), _ptr(status), _stream(stream))
+    _check("nsa_dequantize_kv_paged", rc)
+
+
+def nsa_set_index_k(k: torch.Tensor, loc: torch.Tensor, k_cache: torch.Tensor, k_scale: torch.Tensor,
+                    status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Indexer keys [n, 128] (bf16) -> e4m3 codes and fp32 scales at slots `loc` of the paged key cache."""
+    num_slots = k_scale.numel()
+    rc = load().nsa_set_index_k(_ptr(k), k.stride(0), _ptr(loc), loc.shape[0], k.shape[1], _ptr(k_cache),
+                                _ptr(k_scale), num_slots, _ptr(status), _stream(stream))
+    _check("nsa_set_index_k", rc)

@@ -300,6 +300,57 @@ size_t nsa_sparse_mla_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int
 nsa_status nsa_sparse_mla_plan(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int H, int d_latent,
                                int d_rope, int topk, int *nsplit, int *launches);
 
+/* ------------------------------------------------------------------------
+ * KV-cache write side: the rows the attention and the indexer read.
+ *
+ * [NSA] / [DSA] set_mla_kv_buffer(layer, loc, k, k_rope) stores the new tokens'
+ * latent (k, 512 values) and rope (k_rope, 64 values) parts at their KV slots;
+ * quantize_k_cache turns a bf16 cache into the fp8 row layout; [DSA]
+ * dequantize_k_cache_paged gathers fp8 rows back to bf16 through the flattened
+ * page table.  The pages only name these conversions; the rule used for a
+ * block of values: scale = (largest magnitude) / 448 in fp32 (1 for an
+ * all-zero block), code = e4m3(value / scale) rounded to nearest, ties to even,
+ * saturating at +-448.  fp8 row (656 bytes): 512 e4m3 latent codes | 4 fp32
+ * scales (one per 128 latent values) | 64 bf16 rope values.  bf16 row: 576
+ * bf16 values (1152 bytes).  Dequantised value: code x scale rounded to fp32,
+ * then to bf16 (nearest even).
+ *
+ * All calls are asynchronous on `stream`, allocate nothing, and return
+ * NSA_ERR_UNSUPPORTED for other dims (d_latent 512, d_rope 64, Di 128 only)
+ * and NSA_ERR_INVALID_ARG for NULL or misaligned buffers (16-byte aligned KV
+ * caches and rope rows, 8-byte aligned bf16 rows) before any launch.
+ * A slot outside [0, num_slots) sets NSA_ERR_BOUNDS in the optional status word
+ * and its row is skipped (written as zeros by the dequantiser; a negative slot
+ * there is padding and gives a zero row without error).
+ * ------------------------------------------------------------------------ */
+
+/* New tokens into the MLA KV cache: row i (k_nope_dev + i * nope_ld, k_rope_dev +
+ * i * rope_ld, both bf16) goes to slot loc_dev[i] of kv_dev, a [num_slots] array
+ * of fp8 rows (kv_dtype NSA_DT_E4M3) or bf16 rows (NSA_DT_BF16).  Slots of one
+ * call must be distinct. */
+nsa_status nsa_set_mla_kv(nsa_dtype kv_dtype, const void *k_nope_dev, int64_t nope_ld,
+                          const void *k_rope_dev, int64_t rope_ld, const int32_t *loc_dev, int n,
+                          int d_latent, int d_rope, void *kv_dev, int64_t num_slots,
+                          int32_t *status_dev, nsa_stream_t stream);
+
+/* The whole bf16 cache [num_slots][576] to fp8 rows [num_slots][656]. */
+nsa_status nsa_quantize_kv_cache(const void *kv_bf16_dev, int64_t num_slots, int d_latent, int d_rope,
+                                 void *kv_fp8_dev, nsa_stream_t stream);
+
+/* out_bf16_dev[i] = dequantised fp8 row slots_dev[i] of kv_fp8_dev, i < m
+ * (bf16 rows of 576). */
+nsa_status nsa_dequantize_kv_paged(const void *kv_fp8_dev, int64_t num_slots, int d_latent, int d_rope,
+                                   const int32_t *slots_dev, int64_t m, void *out_bf16_dev,
+                                   int32_t *status_dev, nsa_stream_t stream);
+
+/* Indexer keys of new tokens: row i of k_dev (bf16, Di = 128 values, row stride
+ * k_ld) -> e4m3 codes at k_cache_dev[loc_dev[i] * 128 ..] and one fp32 scale at
+ * k_scale_dev[loc_dev[i]] (the [pages][page_size] arrays nsa_indexer_logits reads,
+ * indexed by slot = page * page_size + offset). */
+nsa_status nsa_set_index_k(const void *k_dev, int64_t k_ld, const int32_t *loc_dev, int n, int Di,
+                           void *k_cache_dev, float *k_scale_dev, int64_t num_slots, int32_t *status_dev,
+                           nsa_stream_t stream);
+
 /*
  * nsa_sparse_mla without a caller workspace, for callers that cannot allocate
  * device memory when they call in -- for example a plug-in inside a host
