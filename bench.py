@@ -4,6 +4,7 @@ decode workload: 32 requests, seqlens U{4096..32768}, page 64, indexer
 64 heads x 128 e4m3, topk 2048, MLA 128 heads d_qk 576 / d_v 512.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --kv-write      # the KV-cache write-side kernels instead
 
 Prints ONE JSON line (rank 0).  Under torchrun every rank runs an independent
 replica of the workload on its own GPU (replicas only: the path has no
@@ -423,6 +424,67 @@ def run_reference(args, rank, world):
                 e2e=dict(value=v, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
 
 
+# ---------------------------------------------------------------- KV-cache write side
+
+def run_kv_write(args):
+    """The write-side kernels on this workload's shapes: the step's new tokens
+    into the fp8 KV cache and the indexer key cache, the whole bf16 cache to fp8
+    (the pages' quantize_k_cache), and the gather of the step's selected rows back
+    to bf16 (dequantize_k_cache_paged).  One JSON line, HBM roofline per kernel."""
+    import torch
+    import deepseek_sparse_mla_indexer_gb300 as nsa
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    nsa.load()
+    wl = W.config(WORKLOAD, seed=replica_seed(0))
+    rng = np.random.default_rng(7)
+    n_slots = wl.kv.shape[0]
+    kv_bf16 = torch.from_numpy(wl.kv.view(np.int16)).to(dev)
+    kv_fp8 = torch.empty((n_slots, 656), dtype=torch.uint8, device=dev)
+    k_cache = torch.empty((n_slots, 128), dtype=torch.uint8, device=dev)
+    k_scale = torch.empty((n_slots,), dtype=torch.float32, device=dev)
+    new = wl.B  # one new token per request in a decode step
+    loc = torch.from_numpy(rng.choice(n_slots, size=new, replace=False).astype(np.int32)).to(dev)
+    k_nope = torch.randn((new, 512), device=dev).to(torch.bfloat16).view(torch.int16)
+    k_rope = torch.randn((new, 64), device=dev).to(torch.bfloat16).view(torch.int16)
+    k_idx = torch.randn((new, 128), device=dev).to(torch.bfloat16).view(torch.int16)
+    sel = torch.from_numpy(rng.integers(0, n_slots, size=wl.R * wl.topk).astype(np.int32)).to(dev)
+    gathered = torch.empty((sel.numel(), 576), dtype=torch.int16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kernels = {
+        "quantize_kv_cache": (lambda: nsa.nsa_quantize_kv_cache(kv_bf16, kv_fp8), n_slots * (1152 + 656)),
+        "dequantize_kv_paged": (lambda: nsa.nsa_dequantize_kv_paged(kv_fp8, sel, gathered),
+                                sel.numel() * (656 + 1152 + 4)),
+        "set_mla_kv_fp8": (lambda: nsa.nsa_set_mla_kv(nsa.DT_E4M3, k_nope, k_rope, loc, kv_fp8), new * (1152 + 656 + 4)),
+        "set_index_k": (lambda: nsa.nsa_set_index_k(k_idx, loc, k_cache, k_scale), new * (256 + 128 + 4 + 4)),
+    }
+    peaks = load_peaks()
+    res = {}
+    for name, (fn, nbytes) in kernels.items():
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        us = float(np.median([a.elapsed_time(b) for a, b in ev])) * 1e3
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[name] = dict(us=round(us, 2), algorithmic_bytes=int(nbytes), gbs=round(gbs, 1),
+                         hbm_frac=round(gbs / peaks["hbm_gbs"], 4))
+    q = res["quantize_kv_cache"]
+    return dict(metric="KV-cache write side: GB/s of the whole-cache fp8 quantisation (HBM roofline)",
+                value=q["gbs"], unit="GB/s", n_gpus=1, steps=args.steps, warmup=args.warmup,
+                higher_is_better=True, dtype="bf16 -> e4m3 + f32 scales", data="synthetic (seeded)",
+                config=dict(workload=WORKLOAD_DESC, kv_slots=int(n_slots), new_tokens=int(new),
+                            gathered_rows=int(sel.numel()), l2="flushed before each launch"),
+                kernels=res, peak_gbs=peaks["hbm_gbs"], peak_source=peaks["source"])
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -431,12 +493,18 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-write", action="store_true",
+                    help="measure the KV-cache write-side kernels instead of the attention step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.kv_write:
+        if rank == 0:
+            print(json.dumps(run_kv_write(args)), flush=True)
+        return
     if args.impl == "reference":
         line = run_reference(args, rank, world)
         if line is not None:
