@@ -22,7 +22,7 @@ __all__ = [
     "DT_E4M3", "nsa_metadata", "alloc_metadata", "nsa_local_virtual_batches", "nsa_effective_chunk_size",
     "nsa_indexer_logits", "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes",
     "nsa_sparse_mla_plan", "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged",
-    "nsa_set_index_k", "nsa_status_read", "nsa_status_string", "nsa_abi_version", "EXPORTED_SYMBOLS",
+    "nsa_set_index_k", "nsa_topk_transform_ragged", "nsa_flatten_page_table", "nsa_status_read", "nsa_status_string", "nsa_abi_version", "EXPORTED_SYMBOLS",
 ]
 
 MODE_DECODE, MODE_EXTEND, MODE_TARGET_VERIFY = 0, 1, 2
@@ -34,6 +34,7 @@ EXPORTED_SYMBOLS = [
     "nsa_effective_chunk_size", "nsa_local_virtual_batches", "nsa_indexer_logits",
     "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes", "nsa_sparse_mla_plan",
     "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged", "nsa_set_index_k",
+    "nsa_topk_transform_ragged", "nsa_flatten_page_table",
 ]
 
 _lib = None
@@ -73,6 +74,8 @@ def load(build_if_missing: bool = True):
         "nsa_quantize_kv_cache": ([P, L, I, I, P, P], I),
         "nsa_dequantize_kv_paged": ([P, L, I, I, P, L, P, P, P], I),
         "nsa_set_index_k": ([P, L, P, I, I, P, P, L, P, P], I),
+        "nsa_topk_transform_ragged": ([P, L, P, P, P, I, I, I, P, L, P, P], I),
+        "nsa_flatten_page_table": ([I, P, L, P, P, P, L, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -282,3 +285,23 @@ def nsa_set_index_k(k: torch.Tensor, loc: torch.Tensor, k_cache: torch.Tensor, k
     rc = load().nsa_set_index_k(_ptr(k), k.stride(0), _ptr(loc), loc.shape[0], k.shape[1], _ptr(k_cache),
                                 _ptr(k_scale), num_slots, _ptr(status), _stream(stream))
     _check("nsa_set_index_k", rc)
+
+
+# ---------------------------------------------------------------- RAGGED extend
+
+def nsa_topk_transform_ragged(logits: torch.Tensor, row_len: torch.Tensor, row_to_req: torch.Tensor,
+                              req_offset: torch.Tensor, topk: int, max_row_len: int, indices: torch.Tensor,
+                              status: Optional[torch.Tensor] = None, stream=None) -> None:
+    R = row_len.shape[0]
+    rc = load().nsa_topk_transform_ragged(_ptr(logits), logits.stride(0), _ptr(row_len), _ptr(row_to_req),
+                                          _ptr(req_offset), R, topk, max_row_len, _ptr(indices), indices.stride(0),
+                                          _ptr(status), _stream(stream))
+    _check("nsa_topk_transform_ragged", rc)
+
+
+def nsa_flatten_page_table(page_table_1: torch.Tensor, kv_len: torch.Tensor, kv_start: torch.Tensor,
+                           out: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    B = kv_len.shape[0]
+    rc = load().nsa_flatten_page_table(B, _ptr(page_table_1), page_table_1.stride(0), _ptr(kv_len), _ptr(kv_start),
+                                       _ptr(out), out.numel(), _ptr(status), _stream(stream))
+    _check("nsa_flatten_page_table", rc)

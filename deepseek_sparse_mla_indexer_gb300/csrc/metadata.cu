@@ -309,3 +309,47 @@ extern "C" nsa_status nsa_metadata(nsa_mode mode, int B, int R, int W, int n_dra
     NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, metadata_kernel, p));
     return NSA_OK;
 }
+
+namespace nsa {
+namespace {
+
+// out[kv_start[b] + t] = page_table_1[b, t] for t < kv_len[b]: 4096-entry segments
+// of each request spread over the blocks.
+__global__ void __launch_bounds__(256)
+flatten_page_table_kernel(int B, const int32_t *pt, int64_t pt_ld, const int32_t *kv_len, const int32_t *kv_start,
+                          int32_t *out, int64_t out_len, int segs_per_row, int32_t *status)
+{
+    const int64_t total = (int64_t)B * segs_per_row;
+    for (int64_t g = blockIdx.x; g < total; g += gridDim.x) {
+        const int b = (int)(g / segs_per_row);
+        const int t0 = (int)(g - (int64_t)b * segs_per_row) * kSeg;
+        const int L = kv_len[b];
+        const int64_t start = kv_start[b];
+        if (L < 0 || L > pt_ld || start < 0 || start + L > out_len) {
+            if (threadIdx.x == 0 && t0 == 0) set_status(status, NSA_ERR_BOUNDS);
+            continue;
+        }
+        const int t1 = min(L, t0 + kSeg);
+        for (int t = t0 + (int)threadIdx.x; t < t1; t += blockDim.x) out[start + t] = pt[(int64_t)b * pt_ld + t];
+    }
+}
+
+}  // namespace
+}  // namespace nsa
+
+extern "C" nsa_status nsa_flatten_page_table(int B, const int32_t *page_table_1_dev, int64_t pt_ld,
+                                             const int32_t *kv_len_dev, const int32_t *kv_start_dev,
+                                             int32_t *out_dev, int64_t out_len, int32_t *status_dev,
+                                             nsa_stream_t stream)
+{
+    using namespace nsa;
+    if (B < 0 || pt_ld < 0 || out_len < 0) return NSA_ERR_INVALID_ARG;
+    if (B == 0 || pt_ld == 0) return NSA_OK;
+    if (!page_table_1_dev || !kv_len_dev || !kv_start_dev || (!out_dev && out_len > 0)) return NSA_ERR_INVALID_ARG;
+    const int segs = (int)ceil_div(pt_ld, kSeg);
+    int64_t blocks = (int64_t)B * segs;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    flatten_page_table_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
+        B, page_table_1_dev, pt_ld, kv_len_dev, kv_start_dev, out_dev, out_len, segs, status_dev);
+    return launch_status();
+}

@@ -102,8 +102,8 @@ __device__ __forceinline__ void fill_keys(const float *lg, int s0, int n, uint32
 
 __global__ void __launch_bounds__(kThreads)
 topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row_len,
-                      const int32_t *row_to_req, const int32_t *pt, int64_t pt_ld, int topk,
-                      int max_row_len, int cache_cap, int32_t *indices, int64_t indices_ld,
+                      const int32_t *row_to_req, const int32_t *pt, int64_t pt_ld, const int32_t *req_offset,
+                      int topk, int max_row_len, int cache_cap, int32_t *indices, int64_t indices_ld,
                       int32_t *status)
 {
     extern __shared__ uint32_t dyn[];
@@ -119,7 +119,10 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
     const int L = row_len[r];
     const int b = row_to_req[r];
     int32_t *out = indices + (int64_t)r * indices_ld;
-    const int32_t *ptr = pt + (int64_t)b * pt_ld;
+    // paged: the KV slot page_table_1[b, s]; ragged: s + the request's offset
+    const int32_t *ptr = pt ? pt + (int64_t)b * pt_ld : nullptr;
+    const int32_t off = req_offset ? req_offset[b] : 0;
+    auto slot_of = [&](int s) -> int32_t { return ptr ? ptr[s] : off + s; };
     const float *lg = logits + (int64_t)r * logits_ld;
     const int tid = threadIdx.x;
 
@@ -129,7 +132,7 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
         return;
     }
     if (L <= topk) {
-        for (int i = tid; i < topk; i += kThreads) out[i] = i < L ? ptr[i] : -1;
+        for (int i = tid; i < topk; i += kThreads) out[i] = i < L ? slot_of(i) : -1;
         return;
     }
 
@@ -255,7 +258,7 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
         }
     }
     __syncthreads();
-    for (int j = tid; j < topk; j += kThreads) out[j] = ptr[sel[j]];
+    for (int j = tid; j < topk; j += kThreads) out[j] = slot_of((int)sel[j]);
 }
 
 
@@ -304,8 +307,8 @@ __device__ __forceinline__ uint4 ld_cluster4(const uint32_t *local, uint32_t ran
 
 __global__ void __launch_bounds__(kCThreads)
 topk_cluster_kernel(const float *logits, int64_t logits_ld, const int32_t *row_len, const int32_t *row_to_req,
-                    const int32_t *pt, int64_t pt_ld, int topk, int max_row_len, int32_t *indices,
-                    int64_t indices_ld, int32_t *status)
+                    const int32_t *pt, int64_t pt_ld, const int32_t *req_offset, int topk, int max_row_len,
+                    int32_t *indices, int64_t indices_ld, int32_t *status)
 {
     extern __shared__ uint32_t cache[];           // [kCSliceCap] keys of this slice
     __shared__ uint32_t hist[kCCopies * kBins];  // replicated local histogram
@@ -325,7 +328,10 @@ topk_cluster_kernel(const float *logits, int64_t logits_ld, const int32_t *row_l
     int L = row_len[r];
     const int b = row_to_req[r];
     int32_t *out = indices + (int64_t)r * indices_ld;
-    const int32_t *ptr = pt + (int64_t)b * pt_ld;
+    // paged: the KV slot page_table_1[b, s]; ragged: s + the request's offset
+    const int32_t *ptr = pt ? pt + (int64_t)b * pt_ld : nullptr;
+    const int32_t off = req_offset ? req_offset[b] : 0;
+    auto slot_of = [&](int s) -> int32_t { return ptr ? ptr[s] : off + s; };
     const float *lg = logits + (int64_t)r * logits_ld;
 
     if (L < 0 || L > max_row_len) {  // same decision in every CTA of the cluster
@@ -337,7 +343,7 @@ topk_cluster_kernel(const float *logits, int64_t logits_ld, const int32_t *row_l
     }
     if (L <= topk) {
         if (rank == 0)
-            for (int i = tid; i < topk; i += kCThreads) out[i] = i < L ? ptr[i] : -1;
+            for (int i = tid; i < topk; i += kCThreads) out[i] = i < L ? slot_of(i) : -1;
         return;
     }
 
@@ -450,10 +456,10 @@ topk_cluster_kernel(const float *logits, int64_t logits_ld, const int32_t *row_l
 #pragma unroll
         for (int j = 0; j < kItems; ++j) {
             if (cls[j] == 2u) {
-                out[gt_before + (eq_before < need ? eq_before : need)] = ptr[s0 + i0 + j];
+                out[gt_before + (eq_before < need ? eq_before : need)] = slot_of(s0 + i0 + j);
                 ++gt_before;
             } else if (cls[j] == 1u) {
-                if (eq_before < need) out[gt_before + eq_before] = ptr[s0 + i0 + j];
+                if (eq_before < need) out[gt_before + eq_before] = slot_of(s0 + i0 + j);
                 ++eq_before;
             }
         }
@@ -466,17 +472,20 @@ topk_cluster_kernel(const float *logits, int64_t logits_ld, const int32_t *row_l
 }  // namespace
 }  // namespace nsa
 
-extern "C" nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits_ld,
-                                         const int32_t *row_len_dev, const int32_t *row_to_req_dev,
-                                         const int32_t *page_table_1_dev, int64_t pt_ld, int R,
-                                         int topk, int max_row_len, int32_t *indices_dev,
-                                         int64_t indices_ld, int32_t *status_dev, nsa_stream_t stream)
+namespace nsa {
+namespace {
+
+nsa_status topk_launch(const float *logits_dev, int64_t logits_ld, const int32_t *row_len_dev,
+                       const int32_t *row_to_req_dev, const int32_t *page_table_1_dev, int64_t pt_ld,
+                       const int32_t *req_offset_dev, int R, int topk, int max_row_len, int32_t *indices_dev,
+                       int64_t indices_ld, int32_t *status_dev, nsa_stream_t stream)
 {
     using namespace nsa;
     if (R < 0 || topk < 1 || topk > 4096 || max_row_len < 0) return NSA_ERR_INVALID_ARG;
-    if (indices_ld < topk || logits_ld < max_row_len || pt_ld < max_row_len) return NSA_ERR_INVALID_ARG;
+    if (indices_ld < topk || logits_ld < max_row_len || (page_table_1_dev && pt_ld < max_row_len))
+        return NSA_ERR_INVALID_ARG;
     if (R == 0) return NSA_OK;
-    if (!logits_dev || !row_len_dev || !row_to_req_dev || !page_table_1_dev || !indices_dev)
+    if (!logits_dev || !row_len_dev || !row_to_req_dev || !indices_dev || (!page_table_1_dev && !req_offset_dev))
         return NSA_ERR_INVALID_ARG;
     // rows beyond the single-block key cache: one cluster of up to 8 CTAs per row
     const int csize = max_row_len > kCacheCap ? (int)std::min<int64_t>(kCMaxCluster, ceil_div(max_row_len, kCSliceCap)) : 1;
@@ -497,8 +506,8 @@ extern "C" nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits
         cfg.attrs = attr;
         cfg.numAttrs = 2;
         NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, topk_cluster_kernel, logits_dev, logits_ld, row_len_dev,
-                                        row_to_req_dev, page_table_1_dev, pt_ld, topk, max_row_len, indices_dev,
-                                        indices_ld, status_dev));
+                                        row_to_req_dev, page_table_1_dev, pt_ld, req_offset_dev, topk, max_row_len,
+                                        indices_dev, indices_ld, status_dev));
         return NSA_OK;
     }
     const int cap = max_row_len > topk ? (max_row_len < kCacheCap ? max_row_len : kCacheCap) : 0;
@@ -514,7 +523,32 @@ extern "C" nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, topk_transform_kernel, logits_dev, logits_ld, row_len_dev, row_to_req_dev,
-                                    page_table_1_dev, pt_ld, topk, max_row_len, cap, indices_dev, indices_ld,
-                                    status_dev));
+                                    page_table_1_dev, pt_ld, req_offset_dev, topk, max_row_len, cap, indices_dev,
+                                    indices_ld, status_dev));
     return NSA_OK;
+}
+
+}  // namespace
+}  // namespace nsa
+
+extern "C" nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits_ld,
+                                         const int32_t *row_len_dev, const int32_t *row_to_req_dev,
+                                         const int32_t *page_table_1_dev, int64_t pt_ld, int R,
+                                         int topk, int max_row_len, int32_t *indices_dev,
+                                         int64_t indices_ld, int32_t *status_dev, nsa_stream_t stream)
+{
+    if (!page_table_1_dev && R > 0) return NSA_ERR_INVALID_ARG;
+    return nsa::topk_launch(logits_dev, logits_ld, row_len_dev, row_to_req_dev, page_table_1_dev, pt_ld, nullptr, R,
+                            topk, max_row_len, indices_dev, indices_ld, status_dev, stream);
+}
+
+extern "C" nsa_status nsa_topk_transform_ragged(const float *logits_dev, int64_t logits_ld,
+                                                const int32_t *row_len_dev, const int32_t *row_to_req_dev,
+                                                const int32_t *req_offset_dev, int R, int topk, int max_row_len,
+                                                int32_t *indices_dev, int64_t indices_ld, int32_t *status_dev,
+                                                nsa_stream_t stream)
+{
+    if (!req_offset_dev && R > 0) return NSA_ERR_INVALID_ARG;
+    return nsa::topk_launch(logits_dev, logits_ld, row_len_dev, row_to_req_dev, nullptr, 0, req_offset_dev, R, topk,
+                            max_row_len, indices_dev, indices_ld, status_dev, stream);
 }

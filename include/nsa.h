@@ -301,6 +301,31 @@ nsa_status nsa_sparse_mla_plan(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int
                                int d_rope, int topk, int *nsplit, int *launches);
 
 /* ------------------------------------------------------------------------
+ * RAGGED extend ([DSA] TopkTransformMethod.RAGGED): the KV of each request is
+ * laid out contiguously (request b from offset cu_seqlens_k[b]), gathered by
+ * nsa_dequantize_kv_paged through page_table_1_flattened, and the top-k
+ * indices are token positions shifted by the row's request offset
+ * (topk_indices_offset = repeat_interleave(cu_seqlens_k[:-1], extend_lens)).
+ * ------------------------------------------------------------------------ */
+
+/* As nsa_topk_transform, but row r's selected positions s become
+ * s + req_offset_dev[row_to_req[r]] instead of page-table slots (-1 padding
+ * kept).  req_offset_dev is typically the metadata's cu_seqlens_k; the sums
+ * must fit int32. */
+nsa_status nsa_topk_transform_ragged(const float *logits_dev, int64_t logits_ld, const int32_t *row_len_dev,
+                                     const int32_t *row_to_req_dev, const int32_t *req_offset_dev, int R,
+                                     int topk, int max_row_len, int32_t *indices_dev, int64_t indices_ld,
+                                     int32_t *status_dev, nsa_stream_t stream);
+
+/* page_table_1_flattened: out_dev[kv_start_dev[b] + t] = page_table_1_dev[b *
+ * pt_ld + t] for t < kv_len_dev[b] (typically cache_seqlens and cu_seqlens_k of
+ * the metadata).  A request whose range leaves [0, out_len) or whose length
+ * exceeds pt_ld sets NSA_ERR_BOUNDS and is skipped. */
+nsa_status nsa_flatten_page_table(int B, const int32_t *page_table_1_dev, int64_t pt_ld,
+                                  const int32_t *kv_len_dev, const int32_t *kv_start_dev, int32_t *out_dev,
+                                  int64_t out_len, int32_t *status_dev, nsa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * KV-cache write side: the rows the attention and the indexer read.
  *
  * [NSA] / [DSA] set_mla_kv_buffer(layer, loc, k, k_rope) stores the new tokens'

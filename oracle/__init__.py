@@ -65,6 +65,8 @@ def _load():
             lib.orc_quantize_mla_row.argtypes, lib.orc_quantize_mla_row.restype = [P, P, I, I, P], None
             lib.orc_dequantize_mla_row.argtypes, lib.orc_dequantize_mla_row.restype = [P, I, I, P], None
             lib.orc_quantize_index_row.argtypes, lib.orc_quantize_index_row.restype = [P, I, P], C.c_float
+            lib.orc_topk_ragged_row.argtypes, lib.orc_topk_ragged_row.restype = [P, I, I, C.c_int32, P], I
+            lib.orc_flatten_page_table.argtypes, lib.orc_flatten_page_table.restype = [I, P, L, P, P], L
             _lib = lib
     return _lib
 
@@ -309,3 +311,32 @@ def quantize_index_rows(k):
     for i in range(a.shape[0]):
         scales[i] = lib.orc_quantize_index_row(_p(a[i]), a.shape[1], _p(codes[i]))
     return codes, scales
+
+
+# ---------------------------------------------------------------- RAGGED extend
+
+def topk_ragged(logits, row_len, row_to_req, req_offset, topk: int, rows: Optional[Sequence[int]] = None):
+    """indices int32 [len(rows), topk]: top-k positions of each row plus its
+    request's offset in the flattened KV (ascending, -1 padded)."""
+    lib = _load()
+    lg = _c(logits, np.float32)
+    rl = _c(row_len, np.int32)
+    r2q = _c(row_to_req, np.int32)
+    off = _c(req_offset, np.int32)
+    rows = list(range(len(rl))) if rows is None else list(rows)
+    out = np.zeros((len(rows), topk), dtype=np.int32)
+    for i, r in enumerate(rows):
+        L = int(rl[r])
+        lp = C.c_void_p(lg.ctypes.data + r * lg.shape[1] * 4)
+        op = C.c_void_p(out.ctypes.data + i * topk * 4)
+        lib.orc_topk_ragged_row(lp, L, topk, int(off[int(r2q[r])]), op)
+    return out
+
+
+def flatten_page_table(page_table_1, kv_len) -> np.ndarray:
+    lib = _load()
+    pt = _c(page_table_1, np.int32)
+    kl = _c(kv_len, np.int32)
+    out = np.zeros((max(1, int(kl.sum())),), dtype=np.int32)
+    n = lib.orc_flatten_page_table(len(kl), _p(pt), pt.shape[1], _p(kl), _p(out))
+    return out[:n]

@@ -543,3 +543,34 @@ float orc_quantize_index_row(const uint16_t *k, int D, uint8_t *codes)
 {
     return quantize_block(k, D, codes);
 }
+
+/* ------------------------------------------------------------------------ */
+/* RAGGED extend: the top-k as positions in a request-contiguous KV buffer.  */
+/* ------------------------------------------------------------------------ */
+
+/* [DSA] RAGGED topk transform: the selected positions s of the row (the same
+ * set and order as orc_topk_row), each shifted by the row's offset (the start
+ * of its request in the flattened KV, cu_seqlens_k[b]); -1 stays -1. */
+int orc_topk_ragged_row(const float *logits_row, int L, int topk, int32_t offset, int32_t *out_row)
+{
+    int32_t *ident = (int32_t *)malloc(sizeof(int32_t) * (size_t)(L > 0 ? L : 1));
+    int n;
+    for (int s = 0; s < L; ++s) ident[s] = s;
+    n = orc_topk_row(logits_row, L, topk, ident, out_row);
+    for (int i = 0; i < topk; ++i)
+        if (out_row[i] != -1) out_row[i] += offset;
+    free(ident);
+    return n;
+}
+
+/* [DSA] page_table_1_flattened: the first kv_len[b] entries of each request's
+ * page-table row, requests one after another (request b starts at
+ * sum_{b' < b} kv_len[b']). Returns the total length. */
+int64_t orc_flatten_page_table(int B, const int32_t *page_table_1, int64_t pt_ld, const int32_t *kv_len,
+                               int32_t *out)
+{
+    int64_t n = 0;
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < kv_len[b]; ++t) out[n++] = page_table_1[(int64_t)b * pt_ld + t];
+    return n;
+}

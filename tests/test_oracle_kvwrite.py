@@ -150,3 +150,32 @@ def test_sparse_mla_reads_the_quantised_rows_as_their_dequantised_values():
     ob, lb = oracle.sparse_mla(W.DT_BF16, W.DT_BF16, q_nope, q_rope, back, idx, 0.07)
     assert np.allclose(o8, ob, rtol=0, atol=2e-2 * (1 + np.abs(ob)).max())
     assert np.allclose(l8, lb, rtol=0, atol=1e-2)
+
+
+# ------------------------------------------------------------------ RAGGED extend
+
+def test_ragged_topk_is_the_paged_topk_through_an_offset_identity_table():
+    # RAGGED indices = positions + the request's offset; the paged transform through a
+    # page table that maps position s to offset + s gives the same row
+    rng = np.random.default_rng(21)
+    B, Wd, k = 3, 500, 64
+    lens = np.array([400, 30, 500], np.int32)
+    offsets = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.int32)
+    lg = rng.standard_normal((B, Wd)).astype(np.float32)
+    lg[0, ::5] = 1.0  # ties
+    r2q = np.arange(B, dtype=np.int32)
+    rag = oracle.topk_ragged(lg, lens, r2q, offsets, k)
+    table = offsets[:, None] + np.arange(Wd, dtype=np.int32)[None, :]
+    assert np.array_equal(rag, oracle.topk_transform(lg, lens, r2q, table, k))
+    # the pages' formula: where(idx != -1, idx + offset, idx) on the position top-k
+    pos = oracle.topk_transform(lg, lens, r2q, np.tile(np.arange(Wd, dtype=np.int32), (B, 1)), k)
+    assert np.array_equal(rag, np.where(pos != -1, pos + offsets[:, None], pos))
+    assert np.all(rag[1, 30:] == -1) and np.array_equal(rag[1, :30], offsets[1] + np.arange(30))
+
+
+def test_flatten_page_table_is_the_concatenation_of_live_prefixes():
+    rng = np.random.default_rng(22)
+    pt = rng.integers(0, 10 ** 6, size=(4, 50)).astype(np.int32)
+    kv = np.array([50, 0, 17, 33], np.int32)
+    flat = oracle.flatten_page_table(pt, kv)
+    assert np.array_equal(flat, np.concatenate([pt[b, :kv[b]] for b in range(4)]))
