@@ -96,14 +96,48 @@ set_mla_kv_kernel(bool fp8, const uint16_t *k_nope, int64_t nope_ld, const uint1
     }
 }
 
+// A bf16 row held in registers: lane l has latent values 4l .. 4l+3 of each block and
+// (lanes 0..7) 16 bytes of the rope.
+struct RowRegs {
+    uint2 lat[kDl / 128];
+    uint4 rope;
+};
+
+__device__ __forceinline__ void load_row(const uint16_t *row, int lane, RowRegs &r)
+{
+#pragma unroll
+    for (int b = 0; b < kDl / 128; ++b) r.lat[b] = __ldcs(reinterpret_cast<const uint2 *>(row + 128 * b + 4 * lane));
+    if (lane < 2 * kDr / 16) r.rope = __ldcs(reinterpret_cast<const uint4 *>(row + kDl + 8 * lane));
+}
+
+__device__ __forceinline__ void store_fp8_row(const RowRegs &r, uint8_t *row, int lane)
+{
+#pragma unroll
+    for (int b = 0; b < kDl / 128; ++b) {
+        float scale;
+        const uint32_t codes = quantize4(r.lat[b], scale);
+        *reinterpret_cast<uint32_t *>(row + 128 * b + 4 * lane) = codes;
+        if (lane == 0) *reinterpret_cast<float *>(row + kDl + 4 * b) = scale;
+    }
+    if (lane < 2 * kDr / 16) *reinterpret_cast<uint4 *>(row + kDl + 4 * (kDl / 128) + 16 * lane) = r.rope;
+}
+
+// The whole cache: each warp walks its rows with the next row's loads in flight
+// while the current one is quantised and stored.
 __global__ void __launch_bounds__(32 * kWarpsPerBlock)
 quantize_kv_cache_kernel(const uint16_t *src, int64_t num_slots, uint8_t *dst)
 {
     const int lane = threadIdx.x & 31;
-    for (int64_t s = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); s < num_slots;
-         s += (int64_t)gridDim.x * kWarpsPerBlock) {
-        const uint16_t *row = src + s * (kDl + kDr);
-        write_fp8_row(row, row + kDl, dst + s * kFp8Row, lane);
+    const int64_t stride = (int64_t)gridDim.x * kWarpsPerBlock;
+    int64_t s = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (s >= num_slots) return;
+    RowRegs cur, nxt;
+    load_row(src + s * (kDl + kDr), lane, cur);
+    for (; s < num_slots; s += stride) {
+        const bool more = s + stride < num_slots;
+        if (more) load_row(src + (s + stride) * (kDl + kDr), lane, nxt);
+        store_fp8_row(cur, dst + s * kFp8Row, lane);
+        if (more) cur = nxt;
     }
 }
 
