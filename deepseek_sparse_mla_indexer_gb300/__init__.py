@@ -22,7 +22,8 @@ __all__ = [
     "DT_E4M3", "nsa_metadata", "alloc_metadata", "nsa_local_virtual_batches", "nsa_effective_chunk_size",
     "nsa_indexer_logits", "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes",
     "nsa_sparse_mla_plan", "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged",
-    "nsa_set_index_k", "nsa_topk_transform_ragged", "nsa_flatten_page_table", "nsa_status_read", "nsa_status_string", "nsa_abi_version", "EXPORTED_SYMBOLS",
+    "nsa_set_index_k", "nsa_topk_transform_ragged", "nsa_flatten_page_table", "nsa_copy_buffers",
+    "nsa_status_read", "nsa_status_string", "nsa_abi_version", "EXPORTED_SYMBOLS",
 ]
 
 MODE_DECODE, MODE_EXTEND, MODE_TARGET_VERIFY = 0, 1, 2
@@ -34,7 +35,7 @@ EXPORTED_SYMBOLS = [
     "nsa_effective_chunk_size", "nsa_local_virtual_batches", "nsa_indexer_logits",
     "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes", "nsa_sparse_mla_plan",
     "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged", "nsa_set_index_k",
-    "nsa_topk_transform_ragged", "nsa_flatten_page_table",
+    "nsa_topk_transform_ragged", "nsa_flatten_page_table", "nsa_copy_buffers",
 ]
 
 _lib = None
@@ -76,6 +77,7 @@ def load(build_if_missing: bool = True):
         "nsa_set_index_k": ([P, L, P, I, I, P, P, L, P, P], I),
         "nsa_topk_transform_ragged": ([P, L, P, P, P, I, I, I, P, L, P, P], I),
         "nsa_flatten_page_table": ([I, P, L, P, P, P, L, P, P], I),
+        "nsa_copy_buffers": ([I, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -305,3 +307,16 @@ def nsa_flatten_page_table(page_table_1: torch.Tensor, kv_len: torch.Tensor, kv_
     rc = load().nsa_flatten_page_table(B, _ptr(page_table_1), page_table_1.stride(0), _ptr(kv_len), _ptr(kv_start),
                                        _ptr(out), out.numel(), _ptr(status), _stream(stream))
     _check("nsa_flatten_page_table", rc)
+
+
+# ---------------------------------------------------------------- copies
+
+def nsa_copy_buffers(pairs, stream=None) -> None:
+    """[(dst, src), ...] tensors of equal byte size (device or pinned host), copied in one launch."""
+    n = len(pairs)
+    src = (C.c_void_p * max(1, n))(*[p[1].data_ptr() for p in pairs])
+    dst = (C.c_void_p * max(1, n))(*[p[0].data_ptr() for p in pairs])
+    nb = (C.c_int64 * max(1, n))(*[p[1].numel() * p[1].element_size() for p in pairs])
+    for d, s in pairs:
+        assert d.numel() * d.element_size() == s.numel() * s.element_size()
+    _check("nsa_copy_buffers", load().nsa_copy_buffers(n, src, dst, nb, _stream(stream)))

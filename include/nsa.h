@@ -300,6 +300,19 @@ size_t nsa_sparse_mla_workspace_bytes(nsa_dtype q_dtype, nsa_dtype kv_dtype, int
 nsa_status nsa_sparse_mla_plan(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int H, int d_latent,
                                int d_rope, int topk, int *nsplit, int *launches);
 
+/*
+ * Up to 16 copies in one kernel launch (a runtime aid; the pages have no
+ * counterpart): bytes[i] bytes from src[i] to dst[i], asynchronously on
+ * `stream`.  The pointer arrays are read on the host during the call; the
+ * buffers may be device memory or pinned host memory that the device can
+ * address (cudaHostAlloc / a pinned torch tensor), so a step's host inputs and
+ * outputs can move without one memcpy per buffer.  Buffers must not overlap.
+ * Returns NSA_ERR_INVALID_ARG for n outside [0, 16] or a NULL pointer with a
+ * non-zero size.
+ */
+nsa_status nsa_copy_buffers(int n, const void *const *src, void *const *dst, const int64_t *bytes,
+                            nsa_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * RAGGED extend ([DSA] TopkTransformMethod.RAGGED): the KV of each request is
  * laid out contiguously (request b from offset cu_seqlens_k[b]), gathered by

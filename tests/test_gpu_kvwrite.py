@@ -159,3 +159,27 @@ def test_host_rejects_bad_arguments():
         nsa.nsa_set_mla_kv(nsa.DT_E4M3, lat, torch.zeros((4, 64), dtype=torch.int16, device="cuda"),
                            torch.zeros(4, dtype=torch.int32, device="cuda"),
                            torch.zeros((8, 656), dtype=torch.uint8, device="cuda"))
+
+
+def test_copy_buffers_between_pinned_host_and_device():
+    # several copies in one launch, host inputs in and device results out, bit-exact
+    import deepseek_sparse_mla_indexer_gb300 as nsa
+    rng = np.random.default_rng(9)
+    sizes = [16, 4096, 12345, 1 << 20, 0, 48]
+    hsrc = [torch.from_numpy(rng.integers(0, 255, n, dtype=np.uint8)).pin_memory() for n in sizes]
+    dev = [torch.empty(n, dtype=torch.uint8, device="cuda") for n in sizes]
+    nsa.nsa_copy_buffers(list(zip(dev, hsrc)))
+    back = [torch.empty(n, dtype=torch.uint8).pin_memory() for n in sizes]
+    nsa.nsa_copy_buffers(list(zip(back, dev)))
+    torch.cuda.synchronize()
+    for a, b in zip(hsrc, back):
+        assert torch.equal(a, b)
+    # 16-byte aligned sizes take the vector path
+    a16 = torch.from_numpy(rng.integers(0, 255, 1 << 16, dtype=np.uint8)).pin_memory()
+    d16 = torch.empty(1 << 16, dtype=torch.uint8, device="cuda")
+    nsa.nsa_copy_buffers([(d16, a16)])
+    torch.cuda.synchronize()
+    assert torch.equal(d16.cpu(), a16)
+    # pageable host memory is refused, not touched
+    with pytest.raises(nsa.NsaError):
+        nsa.nsa_copy_buffers([(d16, torch.zeros(1 << 16, dtype=torch.uint8))])
