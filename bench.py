@@ -40,12 +40,12 @@ L2_FLUSH_BYTES = 512 << 20
 # stage's kernel from one ncu capture of this workload (profiles/ names the
 # command), valid only while the kernel sources hash as they did at capture.
 NCU_TRAFFIC = {
-    "sparse_mla": dict(bytes=int((81.303040 + 2.526464) * 1e6), sources=["sparse_mla_tc.cu", "sm100.cuh"],
-                       sha="91f9b0e650bb4c55"),
-    "indexer": dict(bytes=int((79.623168 + 1.778176) * 1e6), sources=["indexer_tc.cu", "sm100.cuh"],
-                    sha="2f3a3773e5ced00f"),
-    "topk": dict(bytes=int(4.720128e6), sources=["topk.cu"], sha="4290385163b3c39d"),
-    "metadata": dict(bytes=int(3.928320e6), sources=["metadata.cu"], sha="cdb2d7ca8df94125"),
+    "sparse_mla": dict(bytes=int((81.310976 + 2.798592) * 1e6), sources=["sparse_mla_tc.cu", "sm100.cuh"],
+                       sha="d1889b4bf2303db5"),
+    "indexer": dict(bytes=int((79.634688 + 1.645824) * 1e6), sources=["indexer_tc.cu", "sm100.cuh"],
+                    sha="4b3b2f1c3334e74e"),
+    "topk": dict(bytes=int(4.724224e6), sources=["topk.cu"], sha="5f899ae023482290"),
+    "metadata": dict(bytes=int(3.929344e6), sources=["metadata.cu"], sha="3685cc120270cc92"),
 }
 
 
