@@ -63,6 +63,7 @@ constexpr int kFp8RowBytes = kDl + 4 * (kDl / 128) + 2 * kDr;  // 656
 constexpr int kMaxClusterSplit = 8;   // portable cluster size
 constexpr int kPartRow = kDl + 4;     // floats per split partial row: raw O (512) | lse, l, 0, 0
 constexpr int kMergeItems = (kHc * (kDl / 8) + kThreads - 1) / kThreads;  // 16-byte outputs per thread at 2 splits
+static_assert(kHc * (kDl / 4 / 2) <= kMergeItems * kThreads, "a merge slice (2 or more splits) fits one pass");
 static_assert(kHc * kDl * 4 <= 8 * (int)kKvBlk, "the fp32 partial fits in the latent part of the KV tile");
 
 struct MlaParams {
@@ -569,6 +570,27 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
         const int hv = min(kHc, p.H - hg * kHc);
         const int64_t hrow0 = (int64_t)r * p.H + hg * kHc;
         const float *stage_f = reinterpret_cast<const float *>(kv_s);
+        // this CTA's slice of the latent dimension, in 16-byte chunks, for every real head
+        // (at most 64 heads x 64 chunks: one pass of kMergeItems per thread)
+        const int c0 = sp * (kDl / 4) / ns, c1 = (sp + 1) * (kDl / 4) / ns, nc = c1 - c0;
+        const int items = hv * nc;
+        const int kcount = min(kMergeItems, (items - (int)threadIdx.x + kThreads - 1) / kThreads);
+        int hh[kMergeItems], cc[kMergeItems];
+#pragma unroll
+        for (int k = 0; k < kMergeItems; ++k) {
+            const int e = min(k * kThreads + (int)threadIdx.x, items - 1);  // clamped: a valid address
+            hh[k] = e / nc;
+            cc[k] = c0 + e - hh[k] * nc;
+        }
+        // the first other split's partial rows are in flight while the weights are formed
+        const int q0 = sp == 0 ? 1 : 0;
+        float4 v0[kMergeItems];
+        {
+            const float *rowq = p.o_part + ((int64_t)q0 * p.R * p.H + hrow0) * kPartRow;
+#pragma unroll
+            for (int k = 0; k < kMergeItems; ++k)
+                if (k < kcount) v0[k] = __ldcg(reinterpret_cast<const float4 *>(rowq + hh[k] * kPartRow + 4 * cc[k]));
+        }
         if (threadIdx.x < kHc) {
             const int h = threadIdx.x;
             float ls[kMaxClusterSplit], l[kMaxClusterSplit];
@@ -601,48 +623,40 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             if (sp == 0 && h < hv) p.lse[hrow0 + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
         }
         __syncthreads();
-        // this CTA's slice of the latent dimension, in 16-byte chunks, for every real head
-        const int c0 = sp * (kDl / 4) / ns, c1 = (sp + 1) * (kDl / 4) / ns, nc = c1 - c0;
-        const int items = hv * nc;
-        for (int base = 0; base < items; base += kMergeItems * kThreads) {
-            const int kcount = min(kMergeItems, (items - base - (int)threadIdx.x + kThreads - 1) / kThreads);
-            int hh[kMergeItems], cc[kMergeItems];
-            float4 acc[kMergeItems];
+        // split q0 (its rows already here) opens the sums, the others follow in index order
+        float4 acc[kMergeItems];
+#pragma unroll
+        for (int k = 0; k < kMergeItems; ++k) {
+            const float w = k < kcount ? sm->wts[q0][hh[k]] : 0.f;
+            acc[k] = make_float4(w * v0[k].x, w * v0[k].y, w * v0[k].z, w * v0[k].w);
+        }
+#pragma unroll 1
+        for (int q = 0; q < ns; ++q) {
+            if (q == q0) continue;
+            float4 v[kMergeItems];
+            if (q == sp) {
+#pragma unroll
+                for (int k = 0; k < kMergeItems; ++k) v[k] = *reinterpret_cast<const float4 *>(stage_f + stage_off(hh[k], cc[k]));
+            } else {
+                const float *rowq = p.o_part + ((int64_t)q * p.R * p.H + hrow0) * kPartRow;
+#pragma unroll
+                for (int k = 0; k < kMergeItems; ++k)
+                    if (k < kcount) v[k] = __ldcg(reinterpret_cast<const float4 *>(rowq + hh[k] * kPartRow + 4 * cc[k]));
+            }
 #pragma unroll
             for (int k = 0; k < kMergeItems; ++k) {
-                const int e = min(base + k * kThreads + (int)threadIdx.x, items - 1);  // clamped: a valid address
-                hh[k] = e / nc;
-                cc[k] = c0 + e - hh[k] * nc;
-                acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll 1
-            for (int q = 0; q < ns; ++q) {
-                float4 v[kMergeItems];
-                if (q == sp) {
-#pragma unroll
-                    for (int k = 0; k < kMergeItems; ++k)
-                        v[k] = *reinterpret_cast<const float4 *>(stage_f + stage_off(hh[k], cc[k]));
-                } else {
-                    const float *rowq = p.o_part + ((int64_t)q * p.R * p.H + hrow0) * kPartRow;
-#pragma unroll
-                    for (int k = 0; k < kMergeItems; ++k)
-                        if (k < kcount) v[k] = __ldcg(reinterpret_cast<const float4 *>(rowq + hh[k] * kPartRow + 4 * cc[k]));
-                }
-#pragma unroll
-                for (int k = 0; k < kMergeItems; ++k) {
-                    if (k < kcount) {
-                        const float w = sm->wts[q][hh[k]];
-                        acc[k].x += w * v[k].x; acc[k].y += w * v[k].y;
-                        acc[k].z += w * v[k].z; acc[k].w += w * v[k].w;
-                    }
+                if (k < kcount) {
+                    const float w = sm->wts[q][hh[k]];
+                    acc[k].x += w * v[k].x; acc[k].y += w * v[k].y;
+                    acc[k].z += w * v[k].z; acc[k].w += w * v[k].w;
                 }
             }
-#pragma unroll
-            for (int k = 0; k < kMergeItems; ++k)
-                if (k < kcount)
-                    *reinterpret_cast<uint2 *>(p.out + (hrow0 + hh[k]) * kDl + 4 * cc[k]) =
-                        make_uint2(pack_bf16x2(acc[k].x, acc[k].y), pack_bf16x2(acc[k].z, acc[k].w));
         }
+#pragma unroll
+        for (int k = 0; k < kMergeItems; ++k)
+            if (k < kcount)
+                *reinterpret_cast<uint2 *>(p.out + (hrow0 + hh[k]) * kDl + 4 * cc[k]) =
+                    make_uint2(pack_bf16x2(acc[k].x, acc[k].y), pack_bf16x2(acc[k].z, acc[k].w));
     }
 }
 
