@@ -204,57 +204,70 @@ topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row
     // one block scan of (#above, #equal) places every selected position in order
     const int C = 4 * (((L + 4 * kThreads - 1) / (4 * kThreads)) | 1);
     const int p0 = min(L, tid * C), p1 = min(L, p0 + C);
-    // class of the keys p0+4c .. p0+4c+3: 2 above, 1 equal, 0 below or past the run
-    auto classes4 = [&](int i, uint32_t (&cls)[4]) {
-        uint32_t k[4];
-        if (cached && i + 4 <= p1) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(cache + i);
-            k[0] = v.x; k[1] = v.y; k[2] = v.z; k[3] = v.w;
+    uint32_t *sel = hist;  // output slot -> position (the histograms are dead)
+    auto place = [&](uint32_t n_gt, uint32_t n_eq, uint32_t &gt_before, uint32_t &eq_before) {
+        if (L < 65536) {  // both counts fit 16 bits
+            const uint32_t packed = n_gt | (n_eq << 16);
+            const uint32_t ex = block_incl_scan(packed, warp_buf, &total) - packed;
+            gt_before = ex & 0xFFFFu;
+            eq_before = ex >> 16;
         } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) k[j] = i + j < p1 ? key_at(i + j) : 0u;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t v = k[j] >> S;
-            cls[j] = i + j >= p1 ? 0u : (v > prefix ? 2u : (v == prefix ? 1u : 0u));
+            gt_before = block_incl_scan(n_gt, warp_buf, &total) - n_gt;
+            eq_before = block_incl_scan(n_eq, warp_buf, &total) - n_eq;
         }
     };
-    uint32_t n_gt = 0u, n_eq = 0u;
-    for (int i = p0; i < p1; i += 4) {
-        uint32_t cls[4];
-        classes4(i, cls);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            n_gt += cls[j] == 2u;
-            n_eq += cls[j] == 1u;
+    auto record = [&](bool above, int pos, uint32_t &gt_before, uint32_t &eq_before) {
+        if (above) {
+            sel[gt_before + (eq_before < need ? eq_before : need)] = (uint32_t)pos;
+            ++gt_before;
+        } else {
+            if (eq_before < need) sel[gt_before + eq_before] = (uint32_t)pos;
+            ++eq_before;
         }
-    }
-    uint32_t gt_before, eq_before;
-    if (L < 65536) {  // both counts fit 16 bits
-        const uint32_t packed = n_gt | (n_eq << 16);
-        const uint32_t ex = block_incl_scan(packed, warp_buf, &total) - packed;
-        gt_before = ex & 0xFFFFu;
-        eq_before = ex >> 16;
-    } else {
-        gt_before = block_incl_scan(n_gt, warp_buf, &total) - n_gt;
-        eq_before = block_incl_scan(n_eq, warp_buf, &total) - n_eq;
-    }
-    // output slot -> position, in shared memory (the histograms are dead); then the
-    // page-table gathers of all slots go out together
-    uint32_t *sel = hist;
-    for (int i = p0; i < p1; i += 4) {
-        uint32_t cls[4];
-        classes4(i, cls);
+    };
+    if (cached && C <= 64) {
+        // one read of the run: its classes kept as two 64-bit masks (above, equal)
+        uint64_t mgt = 0ull, meq = 0ull;
+        for (int i = p0; i < p1; i += 4) {
+            uint32_t k[4];
+            if (i + 4 <= p1) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(cache + i);
+                k[0] = v.x; k[1] = v.y; k[2] = v.z; k[3] = v.w;
+            } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (cls[j] == 2u) {
-                sel[gt_before + (eq_before < need ? eq_before : need)] = (uint32_t)(i + j);
-                ++gt_before;
-            } else if (cls[j] == 1u) {
-                if (eq_before < need) sel[gt_before + eq_before] = (uint32_t)(i + j);
-                ++eq_before;
+                for (int j = 0; j < 4; ++j) k[j] = i + j < p1 ? cache[i + j] : 0u;
             }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (i + j >= p1) continue;
+                const uint32_t v = k[j] >> S;
+                const uint64_t bit = 1ull << (i + j - p0);
+                if (v > prefix) mgt |= bit;
+                else if (v == prefix) meq |= bit;
+            }
+        }
+        uint32_t gt_before, eq_before;
+        place((uint32_t)__popcll(mgt), (uint32_t)__popcll(meq), gt_before, eq_before);
+        for (uint64_t m = mgt | meq; m; m &= m - 1) {
+            const int bit = __ffsll((long long)m) - 1;
+            record(((mgt >> bit) & 1ull) != 0ull, p0 + bit, gt_before, eq_before);
+        }
+    } else {
+        auto cls_of = [&](int i) -> uint32_t {
+            const uint32_t v = key_at(i) >> S;
+            return v > prefix ? 2u : (v == prefix ? 1u : 0u);
+        };
+        uint32_t n_gt = 0u, n_eq = 0u;
+        for (int i = p0; i < p1; ++i) {
+            const uint32_t c = cls_of(i);
+            n_gt += c == 2u;
+            n_eq += c == 1u;
+        }
+        uint32_t gt_before, eq_before;
+        place(n_gt, n_eq, gt_before, eq_before);
+        for (int i = p0; i < p1; ++i) {
+            const uint32_t c = cls_of(i);
+            if (c != 0u) record(c == 2u, i, gt_before, eq_before);
         }
     }
     __syncthreads();
