@@ -23,7 +23,7 @@ __all__ = [
     "nsa_indexer_logits", "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes",
     "nsa_sparse_mla_plan", "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged",
     "nsa_set_index_k", "nsa_topk_transform_ragged", "nsa_flatten_page_table", "nsa_copy_buffers",
-    "nsa_status_read", "nsa_status_string", "nsa_abi_version", "EXPORTED_SYMBOLS",
+    "nsa_check_bounded_wait", "nsa_status_read", "nsa_status_string", "nsa_abi_version", "EXPORTED_SYMBOLS",
 ]
 
 MODE_DECODE, MODE_EXTEND, MODE_TARGET_VERIFY = 0, 1, 2
@@ -36,6 +36,7 @@ EXPORTED_SYMBOLS = [
     "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes", "nsa_sparse_mla_plan",
     "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged", "nsa_set_index_k",
     "nsa_topk_transform_ragged", "nsa_flatten_page_table", "nsa_copy_buffers",
+    "nsa_check_bounded_wait",
 ]
 
 _lib = None
@@ -78,6 +79,7 @@ def load(build_if_missing: bool = True):
         "nsa_topk_transform_ragged": ([P, L, P, P, P, I, I, I, P, L, P, P], I),
         "nsa_flatten_page_table": ([I, P, L, P, P, P, L, P, P], I),
         "nsa_copy_buffers": ([I, P, P, P, P], I),
+        "nsa_check_bounded_wait": ([P, C.c_longlong, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -320,3 +322,7 @@ def nsa_copy_buffers(pairs, stream=None) -> None:
     for d, s in pairs:
         assert d.numel() * d.element_size() == s.numel() * s.element_size()
     _check("nsa_copy_buffers", load().nsa_copy_buffers(n, src, dst, nb, _stream(stream)))
+
+
+def nsa_check_bounded_wait(status: torch.Tensor, budget_cycles: int, stream=None) -> None:
+    _check("nsa_check_bounded_wait", load().nsa_check_bounded_wait(_ptr(status), int(budget_cycles), _stream(stream)))

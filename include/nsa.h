@@ -301,6 +301,15 @@ nsa_status nsa_sparse_mla_plan(nsa_dtype q_dtype, nsa_dtype kv_dtype, int R, int
                                int d_rope, int topk, int *nsplit, int *launches);
 
 /*
+ * Self-test of the library's bounded device waits (a test aid; the pages have
+ * no counterpart): one block waits for `budget_cycles` SM clocks on an
+ * mbarrier that nothing arrives on, gives up and writes NSA_ERR_TIMEOUT into
+ * the caller-zeroed status word, the way every tensor-core kernel here reports
+ * a wait that ran out instead of hanging.  budget_cycles in [1, 4e9].
+ */
+nsa_status nsa_check_bounded_wait(int32_t *status_dev, long long budget_cycles, nsa_stream_t stream);
+
+/*
  * Up to 16 copies in one kernel launch (a runtime aid; the pages have no
  * counterpart): bytes[i] bytes from src[i] to dst[i], asynchronously on
  * `stream`.  The pointer arrays are read on the host during the call; the

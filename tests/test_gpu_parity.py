@@ -158,3 +158,15 @@ def test_topk_bit_exact_across_row_lengths(width):
     nsa.nsa_topk_transform(torch.from_numpy(lg).to(d), torch.from_numpy(L).to(d), torch.from_numpy(r2q).to(d),
                            torch.from_numpy(pt).to(d), k, width, idx)
     assert np.array_equal(idx.cpu().numpy(), exp)
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable():
+    # the wait helper of every tensor-core kernel, on a barrier nothing arrives on
+    import deepseek_sparse_mla_indexer_gb300 as nsa
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nsa.nsa_check_bounded_wait(status, 100000)  # ~50 us of SM clocks
+    torch.cuda.synchronize()
+    assert status.item() == nsa.ERR_TIMEOUT
+    # the context still runs work
+    wl = SMALL["decode_small_heads_ps16"]()
+    H.full_parity(_step(wl), wl)
