@@ -67,6 +67,8 @@ def _load():
             lib.orc_quantize_index_row.argtypes, lib.orc_quantize_index_row.restype = [P, I, P], C.c_float
             lib.orc_topk_ragged_row.argtypes, lib.orc_topk_ragged_row.restype = [P, I, I, C.c_int32, P], I
             lib.orc_flatten_page_table.argtypes, lib.orc_flatten_page_table.restype = [I, P, L, P, P], L
+            lib.orc_local_attention_row.argtypes = [I, I, I, I, I, I, L, P, L, P, P, P, P, P, D, P, P]
+            lib.orc_local_attention_row.restype = I
             _lib = lib
     return _lib
 
@@ -340,3 +342,32 @@ def flatten_page_table(page_table_1, kv_len) -> np.ndarray:
     out = np.zeros((max(1, int(kl.sum())),), dtype=np.int32)
     n = lib.orc_flatten_page_table(len(kl), _p(pt), pt.shape[1], _p(kl), _p(out))
     return out[:n]
+
+
+# ---------------------------------------------------------------- chunk-local attention
+
+def local_attention(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, sm_scale: float):
+    """q bf16 bits [total_q, Hq, D]; caches bf16 bits [pages, ps, Hkv, D]; block_table int32
+    [nvb, bt_ld]; cu_seqlens_q [nvb + 1]; seqused_k [nvb].  Returns (out [total_q, Hq, D],
+    lse [total_q, Hq]) in float64."""
+    lib = _load()
+    qq = _c(q, np.uint16)
+    kc = _c(k_cache, np.uint16)
+    vc = _c(v_cache, np.uint16)
+    bt = _c(block_table, np.int32)
+    cq = _c(cu_seqlens_q, np.int32)
+    sk = _c(seqused_k, np.int32)
+    total, Hq, D = qq.shape
+    num_pages, ps, Hkv, _ = kc.shape
+    out = np.zeros((total, Hq, D), dtype=np.float64)
+    lse = np.zeros((total, Hq), dtype=np.float64)
+    for b in range(len(sk)):
+        for i in range(int(cq[b + 1] - cq[b])):
+            t = int(cq[b]) + i
+            rc = lib.orc_local_attention_row(b, i, Hq, Hkv, D, ps, num_pages, _p(bt), bt.shape[1], _p(cq), _p(sk),
+                                             _p(qq[t]), _p(kc), _p(vc), float(sm_scale),
+                                             C.c_void_p(out.ctypes.data + t * Hq * D * 8),
+                                             C.c_void_p(lse.ctypes.data + t * Hq * 8))
+            if rc != 0:
+                raise ValueError("page id out of range")
+    return out, lse

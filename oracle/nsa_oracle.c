@@ -574,3 +574,56 @@ int64_t orc_flatten_page_table(int B, const int32_t *page_table_1, int64_t pt_ld
         for (int t = 0; t < kv_len[b]; ++t) out[n++] = page_table_1[(int64_t)b * pt_ld + t];
     return n;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Chunk-local dense attention over the local virtual batches.              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [FA3-diff] FlashAttentionBackend with local attention: for virtual batch
+ * b (from make_local_attention_virtual_batches) the queries
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 attend, causally with the queries
+ * aligned to the end of the keys, to the first seqused_k[b] keys of the
+ * chunk, key j stored in page block_table[b, j / ps] at offset j % ps; query
+ * head h reads key/value head h / (Hq / Hkv).  Query i of n_q sees keys
+ * j <= seqused_k[b] - n_q + i.  out = softmax(sm_scale q.k) v, lse = ln sum exp;
+ * a query that sees no key gets out 0, lse -inf.  One query token, all heads;
+ * q [Hq][D], caches [pages][ps][Hkv][D] (bf16 bits), out [Hq][D], lse [Hq].
+ */
+int orc_local_attention_row(int b, int i, int Hq, int Hkv, int D, int ps, int64_t num_pages,
+                            const int32_t *block_table, int64_t bt_ld, const int32_t *cu_seqlens_q,
+                            const int32_t *seqused_k, const uint16_t *q, const uint16_t *k_cache,
+                            const uint16_t *v_cache, double sm_scale, double *out, double *lse)
+{
+    int nq = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+    int nk = seqused_k[b];
+    int last = nk - nq + i; /* last key this query sees */
+    int G = Hq / Hkv;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
+    for (int h = 0; h < Hq; ++h) {
+        int hk = h / G;
+        double m = -INFINITY, sum = 0.0;
+        for (int d = 0; d < D; ++d) out[(int64_t)h * D + d] = 0.0;
+        for (int j = 0; j <= last && j < nk; ++j) {
+            int32_t page = block_table[(int64_t)b * bt_ld + j / ps];
+            const uint16_t *kr;
+            double dot = 0.0;
+            if (page < 0 || page >= num_pages) { free(s); return ORC_EBOUNDS; }
+            kr = k_cache + (((int64_t)page * ps + j % ps) * Hkv + hk) * D;
+            for (int d = 0; d < D; ++d) dot += orc_bf16_to_f64(q[(int64_t)h * D + d]) * orc_bf16_to_f64(kr[d]);
+            s[j] = sm_scale * dot;
+            if (s[j] > m) m = s[j];
+        }
+        if (last < 0 || nk <= 0) { lse[h] = -INFINITY; continue; }
+        for (int j = 0; j <= last && j < nk; ++j) sum += exp(s[j] - m);
+        lse[h] = m + log(sum);
+        for (int j = 0; j <= last && j < nk; ++j) {
+            int32_t page = block_table[(int64_t)b * bt_ld + j / ps];
+            const uint16_t *vr = v_cache + (((int64_t)page * ps + j % ps) * Hkv + hk) * D;
+            double p = exp(s[j] - lse[h]);
+            for (int d = 0; d < D; ++d) out[(int64_t)h * D + d] += p * orc_bf16_to_f64(vr[d]);
+        }
+    }
+    free(s);
+    return ORC_OK;
+}
