@@ -23,7 +23,8 @@ __all__ = [
     "nsa_indexer_logits", "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes",
     "nsa_sparse_mla_plan", "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged",
     "nsa_set_index_k", "nsa_topk_transform_ragged", "nsa_flatten_page_table", "nsa_copy_buffers",
-    "nsa_check_bounded_wait", "nsa_status_read", "nsa_status_string", "nsa_abi_version", "EXPORTED_SYMBOLS",
+    "nsa_check_bounded_wait", "nsa_local_attention", "nsa_status_read", "nsa_status_string", "nsa_abi_version",
+    "EXPORTED_SYMBOLS",
 ]
 
 MODE_DECODE, MODE_EXTEND, MODE_TARGET_VERIFY = 0, 1, 2
@@ -36,7 +37,7 @@ EXPORTED_SYMBOLS = [
     "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes", "nsa_sparse_mla_plan",
     "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged", "nsa_set_index_k",
     "nsa_topk_transform_ragged", "nsa_flatten_page_table", "nsa_copy_buffers",
-    "nsa_check_bounded_wait",
+    "nsa_check_bounded_wait", "nsa_local_attention",
 ]
 
 _lib = None
@@ -80,6 +81,7 @@ def load(build_if_missing: bool = True):
         "nsa_flatten_page_table": ([I, P, L, P, P, P, L, P, P], I),
         "nsa_copy_buffers": ([I, P, P, P, P], I),
         "nsa_check_bounded_wait": ([P, C.c_longlong, P], I),
+        "nsa_local_attention": ([P, L, P, P, L, I, P, L, P, P, I, I, I, I, I, F, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -326,3 +328,25 @@ def nsa_copy_buffers(pairs, stream=None) -> None:
 
 def nsa_check_bounded_wait(status: torch.Tensor, budget_cycles: int, stream=None) -> None:
     _check("nsa_check_bounded_wait", load().nsa_check_bounded_wait(_ptr(status), int(budget_cycles), _stream(stream)))
+
+
+# ---------------------------------------------------------------- chunk-local attention
+
+def nsa_local_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+                        cu_seqlens_q: torch.Tensor, seqused_k: torch.Tensor, sm_scale: float, out: torch.Tensor,
+                        lse: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q bf16 [total_q, Hq, D] (rows may be strided); k_cache / v_cache bf16 [pages, page_size, Hkv, D];
+    block_table int32 [nvb, bt_ld]; cu_seqlens_q int32 [nvb + 1]; seqused_k int32 [nvb];
+    out bf16 [total_q, Hq, D]; lse float32 [total_q, Hq]."""
+    total_q, Hq, D = q.shape
+    assert q.stride(2) == 1 and q.stride(1) == D
+    num_pages, ps, Hkv, Dk = k_cache.shape
+    assert Dk == D and tuple(v_cache.shape) == tuple(k_cache.shape)
+    assert k_cache.is_contiguous() and v_cache.is_contiguous() and block_table.stride(1) == 1
+    assert out.is_contiguous() and lse.is_contiguous()
+    nvb = seqused_k.shape[0]
+    rc = load().nsa_local_attention(_ptr(q), q.stride(0), _ptr(k_cache), _ptr(v_cache), num_pages, ps,
+                                    _ptr(block_table), block_table.stride(0), _ptr(cu_seqlens_q), _ptr(seqused_k),
+                                    nvb, total_q, Hq, Hkv, D, float(sm_scale), _ptr(out), _ptr(lse), _ptr(status),
+                                    _stream(stream))
+    _check("nsa_local_attention", rc)

@@ -427,6 +427,44 @@ nsa_status nsa_sparse_mla_noalloc(nsa_dtype q_dtype, nsa_dtype kv_dtype, const v
                                   void *out_dev, float *lse_dev, int32_t *status_dev,
                                   nsa_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * nsa_local_attention: dense attention inside attention chunks
+ * ------------------------------------------------------------------------ */
+
+/*
+ * Chunk-local attention over the virtual batches that
+ * nsa_local_virtual_batches builds.  [FA3-diff] FlashAttentionBackend, local
+ * attention: the attention call over local_query_start_loc, local_seqused_k
+ * and local_block_table, causal.  Virtual batch b holds the query rows
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and the first seqused_k[b] keys of
+ * its chunk; the queries are the last n_q positions of those keys, so query i
+ * (of n_q) sees keys 0 .. seqused_k[b] - n_q + i.  Query head h reads key/value
+ * head h / (Hq / Hkv).  For each query row t and head h:
+ *   out[t, h, :] = sum_j p_j v_j,  p = softmax_j(sm_scale * q[t, h] . k_j)
+ *   lse[t, h]    = ln sum_j exp(sm_scale * q[t, h] . k_j)   (natural log)
+ * over the visible keys j; a row that sees no key gets out 0 and lse -inf.
+ *
+ *   q_dev            [total_q, q_ld] bf16; head h of row t at t*q_ld + h*D
+ *                    (q_ld >= Hq*D, even; 4-byte aligned)
+ *   k_cache_dev, v_cache_dev  [num_pages, page_size, Hkv, D] bf16, 16-byte aligned
+ *   block_table_dev  [nvb, bt_ld] int32 page ids (the local block table)
+ *   cu_seqlens_q_dev [nvb + 1], seqused_k_dev [nvb]  int32
+ *   out_dev          [total_q, Hq, D] bf16 (written), lse_dev [total_q, Hq] float32
+ * D is 64 or 128 and Hq / Hkv at most 16 (else NSA_ERR_UNSUPPORTED).  Asynchronous
+ * on `stream`; allocates nothing.  Returns NSA_ERR_INVALID_ARG for NULL or
+ * misaligned buffers, Hq not a multiple of Hkv, num_pages < 1 or a bad size,
+ * before any launch.  Device errors: a page id outside [0, num_pages) sets
+ * NSA_ERR_BOUNDS in the optional status word (the result is then invalid);
+ * the inputs must satisfy cu_seqlens_q[nvb] == total_q and
+ * seqused_k[b] <= bt_ld * page_size, which the kernel does not check.
+ */
+nsa_status nsa_local_attention(const void *q_dev, int64_t q_ld, const void *k_cache_dev,
+                               const void *v_cache_dev, int64_t num_pages, int page_size,
+                               const int32_t *block_table_dev, int64_t bt_ld,
+                               const int32_t *cu_seqlens_q_dev, const int32_t *seqused_k_dev, int nvb,
+                               int total_q, int Hq, int Hkv, int D, float sm_scale, void *out_dev,
+                               float *lse_dev, int32_t *status_dev, nsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

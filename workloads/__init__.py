@@ -330,3 +330,87 @@ def config(name: str, seed: Optional[int] = None, *, scale: float = 1.0) -> Work
 
 CONFIG_NAMES = ["tiny_fp32_decode", "v32_decode_bf16", "fp8kv_decode_h16", "chunked_extend",
                 "verify_long_fp8kv"]
+
+
+# --------------------------------------------------------------------------
+# chunk-local dense attention (the second workload)
+# --------------------------------------------------------------------------
+
+@dataclass
+class LocalAttnWorkload:
+    name: str
+    chunk: int                 # attention chunk size (a multiple of page_size)
+    page_size: int
+    Hq: int
+    Hkv: int
+    D: int
+    seq_lens: np.ndarray       # int32 [B]: keys of each request, new queries included
+    q_lens: np.ndarray         # int32 [B]: new query rows (the last q_lens[b] positions)
+    cu_seqlens_q: np.ndarray   # int32 [B + 1]: query row start of each request
+    block_table: np.ndarray    # int32 [B, W]: page ids; W covers each request's last chunk
+    q: np.ndarray              # bf16 bits [total_q, Hq, D]
+    k_cache: np.ndarray        # bf16 bits [num_pages, page_size, Hkv, D]
+    v_cache: np.ndarray        # bf16 bits [num_pages, page_size, Hkv, D]
+    sm_scale: float
+
+    @property
+    def B(self) -> int:
+        return len(self.seq_lens)
+
+    @property
+    def total_q(self) -> int:
+        return int(self.cu_seqlens_q[-1])
+
+
+def make_local_attention(name: str, *, seq_lens, q_lens, chunk: int, Hq: int, Hkv: int, D: int,
+                         page_size: int, seed: int, slack: float = 0.02) -> LocalAttnWorkload:
+    """Requests own whole pages of a randomly permuted page pool; q, K and V are
+    standard normal values rounded to bfloat16.  Block-table columns past a
+    request's pages hold page 0 (never read: they lie past the request's keys)."""
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    q_lens = np.asarray(q_lens, dtype=np.int32)
+    assert chunk % page_size == 0 and np.all(q_lens >= 1) and np.all(q_lens <= seq_lens)
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 77]))
+    ps = page_size
+    pages_per = (seq_lens.astype(np.int64) + ps - 1) // ps
+    used = int(pages_per.sum())
+    num_pages = used + max(1, int(math.ceil(used * slack)))
+    perm = rng.permutation(num_pages).astype(np.int32)
+    W = int(max((int(L) + chunk - 1) // chunk * (chunk // ps) for L in seq_lens))
+    bt = np.zeros((len(seq_lens), W), dtype=np.int32)
+    off = 0
+    for b, n in enumerate(pages_per):
+        bt[b, :n] = perm[off: off + n]
+        off += int(n)
+    cu = np.zeros(len(q_lens) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(q_lens)
+    total_q = int(cu[-1])
+    q_ss, k_ss, v_ss = np.random.SeedSequence([seed, 78]).spawn(3)
+    shape = (num_pages, ps, Hkv, D)
+    n = num_pages * ps * Hkv * D
+    q = _to_bf16(_draw(q_ss, total_q * Hq * D, "normal")).reshape(total_q, Hq, D)
+    k = _to_bf16(_draw(k_ss, n, "normal")).reshape(shape)
+    v = _to_bf16(_draw(v_ss, n, "normal")).reshape(shape)
+    return LocalAttnWorkload(name, chunk, ps, Hq, Hkv, D, seq_lens, q_lens, cu, bt, q, k, v, D ** -0.5)
+
+
+def local_config(name: str, seed: Optional[int] = None, *, scale: float = 1.0) -> LocalAttnWorkload:
+    """Named chunk-local attention workloads.
+
+    local_decode_c8192: 32 decoding requests (one new query each) whose lengths
+    are uniform in [1, 16384], attention chunk 8192, 40 query heads over 8
+    key/value heads of 128 dims, pages of 64 tokens: each query attends to the
+    1..8192 keys of its current chunk.  `scale` < 1 shrinks the batch and the
+    lengths (chunk included) for quick tests."""
+    if name == "local_decode_c8192":
+        seed = 6 if seed is None else seed
+        rng = np.random.default_rng(np.random.SeedSequence([seed, 1234]))
+        B = max(1, int(round(32 * scale)))
+        chunk = max(64, int(8192 * scale) // 64 * 64)
+        L = rng.integers(1, 2 * chunk + 1, size=B)
+        return make_local_attention(name, seq_lens=L, q_lens=np.ones(B, np.int32), chunk=chunk, Hq=40,
+                                    Hkv=8, D=128, page_size=64, seed=seed)
+    raise KeyError(name)
+
+
+LOCAL_CONFIG_NAMES = ["local_decode_c8192"]
