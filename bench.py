@@ -5,6 +5,7 @@ decode workload: 32 requests, seqlens U{4096..32768}, page 64, indexer
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --kv-write      # the KV-cache write-side kernels instead
+    python bench.py --local-attn    # chunk-local dense attention (the second workload)
 
 Prints ONE JSON line (rank 0).  Under torchrun every rank runs an independent
 replica of the workload on its own GPU (replicas only: the path has no
@@ -34,6 +35,23 @@ WORKLOAD_DESC = ("DeepSeek-V3.2-shaped decode, bf16 KV: batch 32, seqlens U{4096
                  "order, indexer 64x128 e4m3 + fp32 row scale, weights N(0,1)/8, topk 2048, MLA 128 heads "
                  "d_qk 576 (512+64) d_v 512 bf16, sm_scale 192^-0.5")
 L2_FLUSH_BYTES = 512 << 20
+
+
+class L2Flush:
+    """Between timed launches: write a buffer larger than L2 (every input line is
+    evicted), then read a second buffer larger than L2, so that the write's dirty
+    lines go back to HBM here and not inside the next timed region."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 8, dtype=torch.float32, device=dev)
+        self.acc = torch.zeros((), dtype=torch.float32, device=dev)
+
+    def zero_(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.acc)
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
@@ -208,7 +226,7 @@ def run_ours(args, rank, world, local_rank):
     wl = W.config(WORKLOAD, seed=replica_seed(rank))  # an independent replica per rank
     step = SparseAttentionStep(wl, dev)
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
 
     stages = ["metadata", "indexer", "topk", "sparse_mla"]
     calls = [step.metadata, step.indexer, step.topk_transform, step.attention]
@@ -366,7 +384,7 @@ def run_ours(args, rank, world, local_rank):
                 data="synthetic (seeded; random pages; see workloads/)",
                 config=dict(workload=WORKLOAD_DESC, global_batch=rows_total,
                             seq_len=int(np.mean(wl.seq_lens)), parallelism=f"replicas x{world}",
-                            l2="flushed between steps (512 MB write outside the timed events)",
+                            l2="flushed between steps (512 MB write, then a 256 MB read that retires its dirty lines, outside the timed events)",
                             timing="step replayed as one CUDA graph timed by events around the replay; stage "
                                    "split from a second graph with timestamp nodes between the stages"),
                 stages=stage_info, roofline=roof,
@@ -464,7 +482,7 @@ def run_kv_write(args):
     k_idx = torch.randn((new, 128), device=dev).to(torch.bfloat16).view(torch.int16)
     sel = torch.from_numpy(rng.integers(0, n_slots, size=wl.R * wl.topk).astype(np.int32)).to(dev)
     gathered = torch.empty((sel.numel(), 576), dtype=torch.int16, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     kernels = {
         "quantize_kv_cache": (lambda: nsa.nsa_quantize_kv_cache(kv_bf16, kv_fp8), n_slots * (1152 + 656)),
@@ -495,8 +513,164 @@ def run_kv_write(args):
                 value=q["gbs"], unit="GB/s", n_gpus=1, steps=args.steps, warmup=args.warmup,
                 higher_is_better=True, dtype="bf16 -> e4m3 + f32 scales", data="synthetic (seeded)",
                 config=dict(workload=WORKLOAD_DESC, kv_slots=int(n_slots), new_tokens=int(new),
-                            gathered_rows=int(sel.numel()), l2="flushed before each launch"),
+                            gathered_rows=int(sel.numel()), l2="flushed before each launch (512 MB write, then a 256 MB read)"),
                 kernels=res, peak_gbs=peaks["hbm_gbs"], peak_source=peaks["source"])
+
+
+# ---------------------------------------------------------------- chunk-local dense attention
+
+LOCAL_WORKLOAD = "local_decode_c8192"
+LOCAL_DESC = ("chunk-local dense attention, decode: 32 requests of lengths U{1..16384}, attention chunk 8192, "
+              "40 query heads over 8 key/value heads of 128 dims, bf16 paged K/V (page 64, random page order)")
+
+
+def local_visible_keys(cu: np.ndarray, sk: np.ndarray) -> int:
+    """Keys all query rows see: query i of n_q in a virtual batch with k keys sees k - n_q + i + 1."""
+    tot = 0
+    for v in range(len(sk)):
+        n, k = int(cu[v + 1] - cu[v]), int(sk[v])
+        i = np.arange(n)
+        tot += int(np.clip(k - n + i + 1, 0, k).sum())
+    return tot
+
+
+def local_algorithmic_bytes(wl, cu, sk) -> int:
+    """K and V rows of every visible key (per key/value head), q in, out and lse out,
+    plus the virtual batches' tables and lengths."""
+    rows = local_visible_keys(cu, sk)
+    pages = int(((sk.astype(np.int64) + wl.page_size - 1) // wl.page_size).sum())
+    return (rows * wl.Hkv * wl.D * 2 * 2 + wl.total_q * wl.Hq * wl.D * 2 * 2 + wl.total_q * wl.Hq * 4
+            + pages * 4 + len(sk) * 8 + 4)
+
+
+def local_cpu_baseline(wl, max_keys: int = 300000):
+    """The oracle as it stands: its virtual batches for the whole batch, then its
+    attention on a bounded sample of them, scaled to the whole step by the visible
+    keys (its attention time is proportional to them)."""
+    import oracle
+    t0 = time.perf_counter()
+    _, cu, sk, _, bt = oracle.local_virtual_batches(wl.chunk, wl.page_size, wl.cu_seqlens_q, wl.seq_lens,
+                                                    wl.block_table)
+    t_vb = time.perf_counter() - t0
+    order = np.argsort(sk)
+    rows, keys = [], 0
+    for v in np.concatenate([order[len(order) // 2:], order[: len(order) // 2]]):  # from the median length up
+        rows.append(int(v))
+        keys += local_visible_keys(cu[[v, v + 1]] - cu[v], sk[[v]])
+        if keys >= max_keys:
+            break
+    sel_q = np.concatenate([np.arange(cu[v], cu[v + 1]) for v in rows])
+    cu_s = np.zeros(len(rows) + 1, np.int32)
+    cu_s[1:] = np.cumsum([cu[v + 1] - cu[v] for v in rows])
+    t0 = time.perf_counter()
+    oracle.local_attention(wl.q[sel_q], wl.k_cache, wl.v_cache, bt[rows], cu_s, sk[rows], wl.sm_scale)
+    dt = time.perf_counter() - t0
+    total = local_visible_keys(cu, sk)
+    full_s = t_vb + dt * total / max(1, keys)
+    return dict(value=round(wl.total_q / full_s, 3), unit="query tokens/s", cores=1, kind="oracle",
+                sample=f"virtual batches for the whole batch, attention for {len(rows)} of {len(sk)} of them "
+                       f"({keys} of {total} visible keys) scaled by visible keys; single-threaded C, fp64")
+
+
+def run_local_attention(args):
+    """nsa_local_attention on the chunk-local decode workload: query tokens/s of the
+    kernel with inputs resident (L2 flushed between launches), end to end from host
+    buffers (the host builds the virtual batches each step, as the pages do), the
+    HBM roofline and the oracle's CPU time."""
+    import torch
+    import deepseek_sparse_mla_indexer_gb300 as nsa
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    nsa.load()
+    wl = W.local_config(LOCAL_WORKLOAD)
+    _, cu, sk, _, bt = nsa.nsa_local_virtual_batches(wl.chunk, wl.page_size, wl.cu_seqlens_q, wl.seq_lens,
+                                                     wl.block_table)
+    q = torch.from_numpy(wl.q.view(np.int16)).to(dev).view(torch.bfloat16)
+    kc = torch.from_numpy(wl.k_cache.view(np.int16)).to(dev).view(torch.bfloat16)
+    vc = torch.from_numpy(wl.v_cache.view(np.int16)).to(dev).view(torch.bfloat16)
+    d_cu, d_sk, d_bt = [torch.from_numpy(np.ascontiguousarray(x)).to(dev) for x in (cu, sk, bt)]
+    out = torch.empty((wl.total_q, wl.Hq, wl.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((wl.total_q, wl.Hq), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        nsa.nsa_local_attention(q, kc, vc, d_bt, d_cu, d_sk, wl.sm_scale, out, lse, status=status, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(0)
+    sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item()} after the timed launches")
+
+    # end to end from host buffers: per step the host builds the virtual batches
+    # (library C++), q and the local tables go in, out and lse come back
+    h_q = torch.from_numpy(wl.q.view(np.int16)).pin_memory()
+    h_cu = torch.empty(len(cu), dtype=torch.int32).pin_memory()
+    h_sk = torch.empty(len(sk), dtype=torch.int32).pin_memory()
+    h_bt = torch.empty(bt.shape, dtype=torch.int32).pin_memory()
+    h_out = torch.empty(out.shape, dtype=torch.int16).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        _, c2, s2, _, b2 = nsa.nsa_local_virtual_batches(wl.chunk, wl.page_size, wl.cu_seqlens_q, wl.seq_lens,
+                                                         wl.block_table)
+        h_cu.numpy()[:] = c2
+        h_sk.numpy()[:] = s2
+        h_bt.numpy()[:] = b2
+        nsa.nsa_copy_buffers([(q.view(torch.int16), h_q), (d_cu, h_cu), (d_sk, h_sk), (d_bt, h_bt)], stream)
+        call()
+        nsa.nsa_copy_buffers([(h_out, out.view(torch.int16)), (h_lse, lse)], stream)
+        stream.synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    e2e_t = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        e2e_step()
+        e2e_t.append(time.perf_counter() - t0)
+    e2e_s = float(np.mean(e2e_t))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_cu, h_sk, h_bt))
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+    peaks = load_peaks()
+    nbytes = local_algorithmic_bytes(wl, cu, sk)
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    line = dict(metric="chunk-local attention decode query tokens/s (% of HBM roofline)",
+                value=round(wl.total_q / (ms * 1e-3), 1), unit="query tokens/s", n_gpus=1, steps=args.steps,
+                warmup=args.warmup, ms_per_step=round(ms, 5), higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype="bf16 (f32 accumulate)", data="synthetic (seeded; random pages; see workloads/)",
+                config=dict(workload=LOCAL_DESC, global_batch=int(wl.total_q), virtual_batches=int(len(sk)),
+                            seq_len=int(np.mean(wl.seq_lens)), visible_keys=local_visible_keys(cu, sk),
+                            parallelism="replicas x1", l2="flushed before each launch (512 MB write, then a 256 MB read that retires its dirty lines, outside the events)"),
+                roofline=dict(kernel="local_attention", bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"],
+                              unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4), traffic=ncu_traffic("local_attention"),
+                              algorithmic_bytes=int(nbytes), peak_source=peaks["source"]),
+                e2e=dict(value=round(wl.total_q / e2e_s, 1), unit="query tokens/s", h2d_bytes_per_step=int(h2d),
+                         d2h_bytes_per_step=int(d2h),
+                         note="per step: host builds the virtual batches, q and the local tables go host->device "
+                              "and out+lse come back (one copy kernel each way), wall clock to the stream's end"),
+                gpu_launches=args.steps,
+                clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"]))
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = local_cpu_baseline(wl)
+    return line
 
 
 def main():
@@ -509,6 +683,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv-write", action="store_true",
                     help="measure the KV-cache write-side kernels instead of the attention step")
+    ap.add_argument("--local-attn", action="store_true",
+                    help="measure chunk-local dense attention (the second workload) instead of the step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -518,6 +694,10 @@ def main():
     if args.kv_write:
         if rank == 0:
             print(json.dumps(run_kv_write(args)), flush=True)
+        return
+    if args.local_attn:
+        if rank == 0:
+            print(json.dumps(run_local_attention(args)), flush=True)
         return
     if args.impl == "reference":
         line = run_reference(args, rank, world)

@@ -66,7 +66,7 @@ struct LaParams {
     const int32_t *block_table;
     int64_t bt_ld;
     const int32_t *cu_seqlens_q, *seqused_k;
-    int nvb, nsplit;
+    int nvb, nsplit, total_q;
     float scale_log2;
     uint16_t *out;                 // [total_q][Hq][D] bf16
     float *lse;                    // [total_q][Hq]
@@ -135,7 +135,10 @@ __global__ void __launch_bounds__(kLaThreads, 2) local_attention_kernel(LaParams
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;  // MMA fragment row group and column pair
     const int rank = (int)cluster_ctarank();
-    const int t = blockIdx.x / p.nsplit, hk = blockIdx.y;
+    // CTA order: split fastest (the cluster), then query token, then key/value
+    // head (measured a little faster than keeping a token's heads together)
+    const int pair = (int)(blockIdx.x / (unsigned)p.nsplit);
+    const int hk = pair / p.total_q, t = pair - hk * p.total_q;
     const int b = block_batch_of(p.cu_seqlens_q, p.nvb, t);
     const int nq = p.cu_seqlens_q[b + 1] - p.cu_seqlens_q[b];
     const int nk = p.seqused_k[b];
@@ -415,12 +418,12 @@ nsa_status launch(LaParams p, int total_q, cudaStream_t stream)
     int ns = 1;
     while (ns < kLaMaxSplit && pairs * ns < want) ns *= 2;
     while (ns > 1 && !cluster_fits<D>(ns)) ns /= 2;
-    if ((int64_t)total_q * ns > 0x7fffffffLL) return NSA_ERR_UNSUPPORTED;
+    if (pairs * ns > 0x7fffffffLL) return NSA_ERR_UNSUPPORTED;
     p.nsplit = ns;
     NSA_CUDA_TRY(cudaFuncSetAttribute(local_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       LaCfg<D>::kSmemBytes));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(total_q * ns), (unsigned)p.Hkv, 1);
+    cfg.gridDim = dim3((unsigned)(pairs * ns), 1, 1);
     cfg.blockDim = dim3(kLaThreads);
     cfg.dynamicSmemBytes = LaCfg<D>::kSmemBytes;
     cfg.stream = stream;
@@ -450,13 +453,13 @@ extern "C" nsa_status nsa_local_attention(const void *q_dev, int64_t q_ld, const
         return NSA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0 || !(sm_scale > 0.f) || !(sm_scale < INFINITY)) return NSA_ERR_INVALID_ARG;
     const int G = Hq / Hkv;
-    if (G > kLaRows || (D != 64 && D != 128) || Hkv > 65535) return NSA_ERR_UNSUPPORTED;
+    if (G > kLaRows || (D != 64 && D != 128)) return NSA_ERR_UNSUPPORTED;
     if (q_ld < (int64_t)Hq * D || q_ld % 2 != 0) return NSA_ERR_INVALID_ARG;
     if (total_q == 0) return NSA_OK;
     if (nvb == 0 || num_pages < 1 || !q_dev || !k_cache_dev || !v_cache_dev || !block_table_dev ||
         !cu_seqlens_q_dev || !seqused_k_dev || !out_dev || !lse_dev)
         return NSA_ERR_INVALID_ARG;
-    // bulk copies move 16-byte aligned rows; Q is read as bf16 pairs
+    // rows move in aligned 16-byte pieces; Q is read as bf16 pairs
     if (((uintptr_t)k_cache_dev | (uintptr_t)v_cache_dev) % 16 != 0 || (uintptr_t)q_dev % 4 != 0 ||
         (uintptr_t)lse_dev % 4 != 0 || (uintptr_t)out_dev % 2 != 0)
         return NSA_ERR_INVALID_ARG;
@@ -476,6 +479,7 @@ extern "C" nsa_status nsa_local_attention(const void *q_dev, int64_t q_ld, const
     p.seqused_k = seqused_k_dev;
     p.nvb = nvb;
     p.nsplit = 1;
+    p.total_q = total_q;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.out = (uint16_t *)out_dev;
     p.lse = lse_dev;
