@@ -58,12 +58,14 @@ class L2Flush:
 # stage's kernel from one ncu capture of this workload (profiles/ names the
 # command), valid only while the kernel sources hash as they did at capture.
 NCU_TRAFFIC = {
-    "sparse_mla": dict(bytes=int((81.310976 + 2.798592) * 1e6), sources=["sparse_mla_tc.cu", "sm100.cuh"],
-                       sha="d1889b4bf2303db5"),
-    "indexer": dict(bytes=int((79.634688 + 1.645824) * 1e6), sources=["indexer_tc.cu", "sm100.cuh"],
+    "sparse_mla": dict(bytes=int((81.316864 + 2.461440) * 1e6), sources=["sparse_mla_tc.cu", "sm100.cuh"],
+                       sha="149ce04c4033598b"),
+    "indexer": dict(bytes=int((79.633664 + 1.633536) * 1e6), sources=["indexer_tc.cu", "sm100.cuh"],
                     sha="4b3b2f1c3334e74e"),
-    "topk": dict(bytes=int(4.724224e6), sources=["topk.cu"], sha="5f899ae023482290"),
+    "topk": dict(bytes=int(4.731648e6), sources=["topk.cu"], sha="2f5262ea063997bf"),
     "metadata": dict(bytes=int(3.929344e6), sources=["metadata.cu"], sha="3685cc120270cc92"),
+    "local_attention": dict(bytes=int((642.401536 + 3.537664) * 1e6), sources=["local_attention.cu", "sm100.cuh"],
+                            sha="288109ae3093d44c"),
 }
 
 
