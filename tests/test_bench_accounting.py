@@ -1,0 +1,46 @@
+"""The benchmark's work accounting (CPU only): the visible-key count behind the
+chunk-local attention roofline, checked against a brute-force count of the
+keys each query row attends to in the oracle's virtual batches, and the
+algorithmic bytes built from it."""
+import numpy as np
+import pytest
+
+import bench
+import oracle
+import workloads as W
+
+
+def _brute_visible(cu, sk):
+    total = 0
+    for v in range(len(sk)):
+        nq, nk = int(cu[v + 1] - cu[v]), int(sk[v])
+        for i in range(nq):
+            total += sum(1 for j in range(nk) if j <= nk - nq + i)
+    return total
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_visible_keys_match_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    B = 5
+    L = rng.integers(1, 300, size=B)
+    qn = np.array([int(rng.integers(1, l + 1)) for l in L], np.int32)
+    wl = W.make_local_attention("acct", seq_lens=L, q_lens=qn, chunk=64, Hq=4, Hkv=2, D=64, page_size=16,
+                                seed=seed)
+    _, cu, sk, _, _ = oracle.local_virtual_batches(wl.chunk, wl.page_size, wl.cu_seqlens_q, wl.seq_lens,
+                                                   wl.block_table)
+    assert bench.local_visible_keys(cu, sk) == _brute_visible(cu, sk)
+    # fewer keys than queries: leading rows see nothing
+    assert bench.local_visible_keys(np.array([0, 5], np.int32), np.array([3], np.int32)) == 0 + 0 + 1 + 2 + 3
+
+
+def test_local_bytes_decode_workload():
+    # decode: one row per virtual batch, each sees all its keys
+    wl = W.local_config("local_decode_c8192", scale=0.05)
+    _, cu, sk, _, _ = oracle.local_virtual_batches(wl.chunk, wl.page_size, wl.cu_seqlens_q, wl.seq_lens,
+                                                   wl.block_table)
+    keys = int(sk.sum())
+    assert bench.local_visible_keys(cu, sk) == keys
+    pages = int(((sk + wl.page_size - 1) // wl.page_size).sum())
+    expect = (keys * wl.Hkv * wl.D * 4 + wl.total_q * wl.Hq * (wl.D * 4 + 4) + pages * 4 + len(sk) * 8 + 4)
+    assert bench.local_algorithmic_bytes(wl, cu, sk) == expect
