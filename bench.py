@@ -315,20 +315,32 @@ def run_ours(args, rank, world, local_rank):
            "q_rope": torch.from_numpy(wl.q_rope.view(np.int16)).pin_memory()}
     h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     h_lse = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in list(h_in.values()) + list(h_q.values()))
+    h2d = sum(t.numel() * t.element_size() for t in list(h_in.values()) + list(h_q.values()))  # all of it, every step
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * 4
 
     # the step's host inputs in and results out with one copy kernel each way (the
     # device reads and writes the pinned host buffers directly)
     ins = [(step.seq_lens, h_in["seq_lens"]), (step.req_pool_indices, h_in["req_pool_indices"]),
-           (step.q_idx, h_in["q_idx"]), (step.weights, h_in["weights"]),
-           (step.q_nope.view(torch.int16), h_q["q_nope"]), (step.q_rope.view(torch.int16), h_q["q_rope"])]
+           (step.q_idx, h_in["q_idx"]), (step.weights, h_in["weights"])]
+    ins_q = [(step.q_nope.view(torch.int16), h_q["q_nope"]), (step.q_rope.view(torch.int16), h_q["q_rope"])]
     outs = [(h_out, step.out), (h_lse, step.lse)]
+    side = torch.cuda.Stream(dev)
+    q_ready = torch.cuda.Event()
 
     def e2e_step(st):
+        # the attention queries (most of the input bytes) travel on a side stream by the
+        # copy engines (no SMs taken) while metadata, indexer and top-k run; the
+        # attention call waits for them
+        side.wait_stream(st)
+        with torch.cuda.stream(side):
+            for d, h in ins_q:
+                d.copy_(h, non_blocking=True)
+        q_ready.record(side)
         nsa.nsa_copy_buffers(ins, st)
-        for fn in calls:
+        for fn in calls[:-1]:
             fn(st)
+        st.wait_event(q_ready)
+        calls[-1](st)
         nsa.nsa_copy_buffers(outs, st)
 
     # the whole host-to-host step (copies in, the four calls, copies out) replayed as
@@ -393,7 +405,9 @@ def run_ours(args, rank, world, local_rank):
                 e2e=dict(value=round(rows_total / (e2e_ms * 1e-3), 1), unit="tokens/s",
                          h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
                          note="per-request inputs host->device from pinned memory and out+lse device->host "
-                              "each step (one copy kernel each way), the step replayed as one CUDA graph; "
+                              "each step (the attention queries by the copy engines on a side stream, overlapping "
+                              "metadata, indexer and top-k; the rest by copy kernels), the step replayed as one "
+                              "CUDA graph; "
                               "KV / indexer-K caches and the req_to_token pool stay resident"),
                 gpu_launches=launches_per_step * args.steps,
                 clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"]))
