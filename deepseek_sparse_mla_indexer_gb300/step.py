@@ -86,9 +86,13 @@ class SparseAttentionStep:
                            self.md["row_to_req"], self.md["page_table_1"], self.topk, self.W, self.indices,
                            self.status, stream)
 
-    def attention(self, stream=None, indices: Optional[torch.Tensor] = None):
+    def attention(self, stream=None, indices: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                  lse: Optional[torch.Tensor] = None):
+        """out / lse default to the step's device buffers; pinned host tensors (mapped
+        into the device's address space) receive the result directly."""
         nsa_sparse_mla(self.q_dtype, self.kv_dtype, self.q_nope, self.q_rope, self.kv,
-                       self.indices if indices is None else indices, self.sm_scale, self.out, self.lse,
+                       self.indices if indices is None else indices, self.sm_scale,
+                       self.out if out is None else out, self.lse if lse is None else lse,
                        self.workspace, self.status, stream, num_slots=self.num_slots)
 
     def run(self, stream=None):

@@ -269,6 +269,9 @@ nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits_ld, const 
  *   indices_dev       [R, indices_ld] int32 slots or -1
  *   out_dev           [R, H, d_latent] contiguous, dtype = q_dtype
  *   lse_dev           [R, H] float32
+ *                     (out and lse are only written, once each: they may also be
+ *                     pinned host memory mapped into the device's address space,
+ *                     which then receives the result without a separate copy)
  *   workspace_dev     scratch of nsa_sparse_mla_workspace_bytes(...) bytes
  *                     (16-byte aligned; may be NULL if that size is 0)
  * q_dtype F32 requires kv_dtype F32; BF16 q takes BF16 or E4M3 KV.

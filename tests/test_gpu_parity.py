@@ -111,6 +111,24 @@ def test_topk_ties_nan_and_signed_zero_bit_exact(Wd):
     assert np.array_equal(idx.cpu().numpy(), exp)
 
 
+@pytest.mark.parametrize("case", ["decode_bf16_ragged", "decode_fp8kv_h16"])
+def test_attention_writes_into_pinned_host_memory(case):
+    # out / lse given as pinned host tensors (the end-to-end benchmark's zero-copy
+    # result) receive exactly what the device buffers receive, on the in-cluster
+    # merge and the combine-kernel split paths alike
+    wl = SMALL[case]()
+    step = _step(wl)
+    step.run()
+    torch.cuda.synchronize()
+    h_out = torch.full(tuple(step.out.shape), 7, dtype=step.out.dtype).pin_memory()
+    h_lse = torch.full(tuple(step.lse.shape), 7.0, dtype=torch.float32).pin_memory()
+    step.attention(out=h_out, lse=h_lse)
+    torch.cuda.synchronize()
+    assert step.status_code() == 0
+    assert torch.equal(h_out.view(torch.int16), step.out.cpu().view(torch.int16))
+    assert torch.equal(h_lse, step.lse.cpu())
+
+
 def test_out_of_range_index_sets_bounds_status():
     import deepseek_sparse_mla_indexer_gb300 as nsa
     wl = SMALL["decode_fp8kv_h16"]()
