@@ -245,7 +245,9 @@ __device__ void copy_tables(const MetaParams &p, int first_seg, int seg_stride)
     }
 }
 
-__global__ void __launch_bounds__(kRowThreads) metadata_kernel(MetaParams p)
+// Two 1024-thread blocks per SM (at most 32 registers a thread): the copy blocks of
+// a 32-request decode step then start in one wave instead of two.
+__global__ void __launch_bounds__(kRowThreads, 2) metadata_kernel(MetaParams p)
 {
     pdl_trigger();
     pdl_wait();  // the previous step's kernels may still read these tables
