@@ -63,7 +63,7 @@ NCU_TRAFFIC = {
     "indexer": dict(bytes=int((79.633664 + 1.633536) * 1e6), sources=["indexer_tc.cu", "sm100.cuh"],
                     sha="4b3b2f1c3334e74e"),
     "topk": dict(bytes=int(4.731648e6), sources=["topk.cu"], sha="2f5262ea063997bf"),
-    "metadata": dict(bytes=int(3.929344e6), sources=["metadata.cu"], sha="3685cc120270cc92"),
+    "metadata": dict(bytes=int(5.872640e6), sources=["metadata.cu"], sha="6d9df76679a4256d"),
     "local_attention": dict(bytes=int((642.401536 + 3.537664) * 1e6), sources=["local_attention.cu", "sm100.cuh"],
                             sha="288109ae3093d44c"),
 }
