@@ -83,3 +83,35 @@ def test_local_virtual_batches_rejects_chunk_not_multiple_of_page(nsa):
 def test_effective_chunk_size_matches_oracle(nsa):
     for c, m, ps in [(8192, 100000, 64), (8192, 1000, 64), (8192, 10, 64), (100, 1000, 64), (4, 17, 2)]:
         assert nsa.nsa_effective_chunk_size(c, m, ps) == oracle.effective_chunk_size(c, m, ps)
+
+
+def _la_call(lib, **kw):
+    """nsa_local_attention with fake (never dereferenced) device addresses: only the
+    host-side checks run, which return before anything touches CUDA."""
+    import ctypes as C
+    a = dict(q=0x10000, q_ld=8 * 128, k=0x20000, v=0x30000, num_pages=4, ps=16, bt=0x40000, bt_ld=2,
+             cu=0x50000, sk=0x60000, nvb=1, total_q=1, Hq=8, Hkv=2, D=128, scale=0.1, out=0x70000,
+             lse=0x80000)
+    a.update(kw)
+    P = lambda x: C.c_void_p(x) if x else None
+    return lib.nsa_local_attention(P(a["q"]), a["q_ld"], P(a["k"]), P(a["v"]), a["num_pages"], a["ps"], P(a["bt"]),
+                                   a["bt_ld"], P(a["cu"]), P(a["sk"]), a["nvb"], a["total_q"], a["Hq"], a["Hkv"],
+                                   a["D"], C.c_float(a["scale"]), P(a["out"]), P(a["lse"]), None, None)
+
+
+def test_local_attention_host_checks(nsa):
+    lib = nsa.load()
+    ok, inval, unsup = 0, nsa.ERR_INVALID_ARG, nsa.ERR_UNSUPPORTED
+    assert _la_call(lib, total_q=0) == ok                       # nothing to do: no launch
+    assert _la_call(lib, Hq=6, Hkv=4) == inval                  # Hq not a multiple of Hkv
+    assert _la_call(lib, D=96, q_ld=8 * 96) == unsup            # only D 64 and 128
+    assert _la_call(lib, Hq=32, Hkv=1, q_ld=32 * 128) == unsup  # more than 16 query heads per KV head
+    assert _la_call(lib, q_ld=8 * 128 - 2) == inval             # rows shorter than Hq * D
+    assert _la_call(lib, q_ld=8 * 128 + 1) == inval             # odd row stride (bf16 pairs)
+    assert _la_call(lib, num_pages=0) == inval                  # no page to read
+    assert _la_call(lib, k=0x20008) == inval                    # K cache not 16-byte aligned
+    assert _la_call(lib, q=0x10002) == inval                    # q not 4-byte aligned
+    assert _la_call(lib, scale=0.0) == inval                    # sm_scale must be positive and finite
+    assert _la_call(lib, scale=float("inf")) == inval
+    assert _la_call(lib, lse=0) == inval                        # NULL output
+    assert _la_call(lib, ps=0) == inval
