@@ -453,13 +453,17 @@ nsa_status nsa_sparse_mla_noalloc(nsa_dtype q_dtype, nsa_dtype kv_dtype, const v
  *   block_table_dev  [nvb, bt_ld] int32 page ids (the local block table)
  *   cu_seqlens_q_dev [nvb + 1], seqused_k_dev [nvb]  int32
  *   out_dev          [total_q, Hq, D] bf16 (written), lse_dev [total_q, Hq] float32
+ *                    (only written, once each: they may be pinned host memory mapped
+ *                    into the device's address space, which then receives the result
+ *                    without a separate copy)
  * D is 64 or 128 and Hq / Hkv at most 16 (else NSA_ERR_UNSUPPORTED).  Asynchronous
  * on `stream`; allocates nothing.  Returns NSA_ERR_INVALID_ARG for NULL or
  * misaligned buffers, Hq not a multiple of Hkv, num_pages < 1 or a bad size,
  * before any launch.  Device errors: a page id outside [0, num_pages) sets
  * NSA_ERR_BOUNDS in the optional status word (the result is then invalid);
- * the inputs must satisfy cu_seqlens_q[nvb] == total_q and
- * seqused_k[b] <= bt_ld * page_size, which the kernel does not check.
+ * the inputs must satisfy cu_seqlens_q[nvb] == total_q (non-decreasing) and
+ * 0 <= seqused_k[b] <= bt_ld * page_size, which the kernel does not check: a
+ * larger seqused_k reads past the block-table row.
  */
 nsa_status nsa_local_attention(const void *q_dev, int64_t q_ld, const void *k_cache_dev,
                                const void *v_cache_dev, int64_t num_pages, int page_size,

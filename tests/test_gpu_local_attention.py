@@ -198,3 +198,26 @@ def test_host_rejects_bad_arguments():
                             torch.zeros(1, dtype=torch.int32, device=d), sk[:0], 0.1,
                             torch.zeros((0, 6, 128), dtype=torch.bfloat16, device=d),
                             torch.zeros((0, 6), device=d))
+
+
+def test_outputs_into_pinned_host_memory():
+    # out / lse as pinned host tensors (the end-to-end benchmark's zero-copy result)
+    # receive exactly what device buffers receive
+    import deepseek_sparse_mla_indexer_gb300 as nsa
+    wl = W.local_config("local_decode_c8192", scale=0.1)
+    _, cu, sk, _, bt = nsa.nsa_local_virtual_batches(wl.chunk, wl.page_size, wl.cu_seqlens_q, wl.seq_lens,
+                                                     wl.block_table)
+    d = "cuda"
+    q = _dev(wl.q, torch.bfloat16)
+    kc, vc = _dev(wl.k_cache, torch.bfloat16), _dev(wl.v_cache, torch.bfloat16)
+    args = (q, kc, vc, _dev(bt), _dev(cu), _dev(sk), wl.sm_scale)
+    out = torch.empty((wl.total_q, wl.Hq, wl.D), dtype=torch.bfloat16, device=d)
+    lse = torch.empty((wl.total_q, wl.Hq), dtype=torch.float32, device=d)
+    nsa.nsa_local_attention(*args, out, lse)
+    h_out = torch.full((wl.total_q, wl.Hq, wl.D), 3.0, dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.full((wl.total_q, wl.Hq), 3.0, dtype=torch.float32).pin_memory()
+    nsa.nsa_local_attention(*args, h_out, h_lse)
+    torch.cuda.synchronize()
+    assert torch.equal(h_out.view(torch.int16), out.cpu().view(torch.int16))
+    assert torch.equal(h_lse, lse.cpu())
+
