@@ -345,8 +345,11 @@ def nsa_local_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
     assert k_cache.is_contiguous() and v_cache.is_contiguous() and block_table.stride(1) == 1
     assert out.is_contiguous() and lse.is_contiguous()
     nvb = seqused_k.shape[0]
+    # the row stride is also the row's capacity; a single row's stride is arbitrary
+    # (0 for a broadcast view), its length is what counts
+    bt_ld = block_table.stride(0) if block_table.shape[0] > 1 else block_table.shape[1]
     rc = load().nsa_local_attention(_ptr(q), q.stride(0), _ptr(k_cache), _ptr(v_cache), num_pages, ps,
-                                    _ptr(block_table), block_table.stride(0), _ptr(cu_seqlens_q), _ptr(seqused_k),
+                                    _ptr(block_table), bt_ld, _ptr(cu_seqlens_q), _ptr(seqused_k),
                                     nvb, total_q, Hq, Hkv, D, float(sm_scale), _ptr(out), _ptr(lse), _ptr(status),
                                     _stream(stream))
     _check("nsa_local_attention", rc)

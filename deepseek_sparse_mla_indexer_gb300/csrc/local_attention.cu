@@ -140,9 +140,17 @@ __global__ void __launch_bounds__(kLaThreads, 2) local_attention_kernel(LaParams
     const int pair = (int)(blockIdx.x / (unsigned)p.nsplit);
     const int hk = pair / p.total_q, t = pair - hk * p.total_q;
     const int b = block_batch_of(p.cu_seqlens_q, p.nvb, t);
-    const int nq = p.cu_seqlens_q[b + 1] - p.cu_seqlens_q[b];
-    const int nk = p.seqused_k[b];
-    const int visible = max(0, min(nk, nk - nq + (t - p.cu_seqlens_q[b]) + 1));  // keys 0 .. visible-1
+    const int q0 = p.cu_seqlens_q[b], q1 = p.cu_seqlens_q[b + 1];
+    int nk = p.seqused_k[b];
+    // A batch whose key count its block-table row cannot hold, or whose query rows do
+    // not contain t, is reported and treated as having no keys: every table read below
+    // then stays inside the row.
+    if (nk < 0 || (int64_t)nk > p.bt_ld * p.ps || t < q0 || t >= q1) {
+        if (threadIdx.x == 0) set_status(p.status, NSA_ERR_BOUNDS);
+        nk = 0;
+    }
+    const int nq = q1 - q0;
+    const int visible = max(0, min(nk, nk - nq + (t - q0) + 1));  // keys 0 .. visible-1
 
     // this CTA's tiles of the query's keys, then this warp's (round robin)
     const int T = (visible + kLaTile - 1) / kLaTile;

@@ -450,7 +450,9 @@ nsa_status nsa_sparse_mla_noalloc(nsa_dtype q_dtype, nsa_dtype kv_dtype, const v
  *   q_dev            [total_q, q_ld] bf16; head h of row t at t*q_ld + h*D
  *                    (q_ld >= Hq*D, even; 4-byte aligned)
  *   k_cache_dev, v_cache_dev  [num_pages, page_size, Hkv, D] bf16, 16-byte aligned
- *   block_table_dev  [nvb, bt_ld] int32 page ids (the local block table)
+ *   block_table_dev  [nvb, bt_ld] int32 page ids (the local block table); bt_ld is
+ *                    the row stride and also the row's capacity: a row holds
+ *                    page ids for bt_ld * page_size keys
  *   cu_seqlens_q_dev [nvb + 1], seqused_k_dev [nvb]  int32
  *   out_dev          [total_q, Hq, D] bf16 (written), lse_dev [total_q, Hq] float32
  *                    (only written, once each: they may be pinned host memory mapped
@@ -459,11 +461,12 @@ nsa_status nsa_sparse_mla_noalloc(nsa_dtype q_dtype, nsa_dtype kv_dtype, const v
  * D is 64 or 128 and Hq / Hkv at most 16 (else NSA_ERR_UNSUPPORTED).  Asynchronous
  * on `stream`; allocates nothing.  Returns NSA_ERR_INVALID_ARG for NULL or
  * misaligned buffers, Hq not a multiple of Hkv, num_pages < 1 or a bad size,
- * before any launch.  Device errors: a page id outside [0, num_pages) sets
- * NSA_ERR_BOUNDS in the optional status word (the result is then invalid);
- * the inputs must satisfy cu_seqlens_q[nvb] == total_q (non-decreasing) and
- * 0 <= seqused_k[b] <= bt_ld * page_size, which the kernel does not check: a
- * larger seqused_k reads past the block-table row.
+ * before any launch.  Device errors (NSA_ERR_BOUNDS in the optional status
+ * word; the result is then invalid): a page id outside [0, num_pages) (slot 0
+ * is read instead), and a virtual batch whose seqused_k is negative or above
+ * bt_ld * page_size or whose query range does not hold a row it is asked for
+ * (cu_seqlens_q must be non-decreasing with cu_seqlens_q[nvb] == total_q); such
+ * a batch is treated as having no keys.
  */
 nsa_status nsa_local_attention(const void *q_dev, int64_t q_ld, const void *k_cache_dev,
                                const void *v_cache_dev, int64_t num_pages, int page_size,

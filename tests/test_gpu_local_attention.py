@@ -221,3 +221,23 @@ def test_outputs_into_pinned_host_memory():
     assert torch.equal(h_out.view(torch.int16), out.cpu().view(torch.int16))
     assert torch.equal(h_lse, lse.cpu())
 
+
+
+def test_key_count_beyond_the_table_sets_bounds():
+    # a seqused_k the block-table row cannot hold is reported and that batch gets no
+    # keys (out 0, lse -inf); the other batch is unaffected
+    import deepseek_sparse_mla_indexer_gb300 as nsa
+    rng = np.random.default_rng(11)
+    Hq, Hkv, D, ps = 8, 2, 64, 16
+    kc = W._to_bf16(rng.standard_normal((6, ps, Hkv, D)).astype(np.float32))
+    vc = W._to_bf16(rng.standard_normal((6, ps, Hkv, D)).astype(np.float32))
+    q = W._to_bf16(rng.standard_normal((2, Hq, D)).astype(np.float32))
+    bt = np.array([[0, 1, 2], [3, 4, 5]], np.int32)
+    cu = np.array([0, 1, 2], np.int32)
+    sk = np.array([40, 3 * ps + 1], np.int32)  # batch 1: one key past its 3-page row
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out_g, lse_g = _gpu(q, kc, vc, bt, cu, sk, 0.1, status=status)
+    assert status.item() == nsa.ERR_BOUNDS
+    assert not out_g[1].any() and np.all(np.isneginf(lse_g[1]))
+    out_o, lse_o = oracle.local_attention(q[:1], kc, vc, bt[:1], cu[:2], sk[:1], 0.1)
+    H.check_attention(out_g[:1], lse_g[:1], out_o, lse_o, TOL)
