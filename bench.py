@@ -64,8 +64,8 @@ NCU_TRAFFIC = {
                     sha="4b3b2f1c3334e74e"),
     "topk": dict(bytes=int(4.731648e6), sources=["topk.cu"], sha="2f5262ea063997bf"),
     "metadata": dict(bytes=int(5.872640e6), sources=["metadata.cu"], sha="6d9df76679a4256d"),
-    "local_attention": dict(bytes=int((642.401536 + 3.537664) * 1e6), sources=["local_attention.cu", "sm100.cuh"],
-                            sha="288109ae3093d44c"),
+    "local_attention": dict(bytes=int((642.419968 + 3.919616) * 1e6), sources=["local_attention.cu", "sm100.cuh"],
+                            sha="bf69a294053f9ee8"),
 }
 
 
