@@ -105,6 +105,12 @@ def _ptr(t: Optional[torch.Tensor]):
     return C.c_void_p(t.data_ptr())
 
 
+def _ld(t: torch.Tensor) -> int:
+    """Leading dimension of a row-major 2D tensor: its row stride, or for a single
+    row (whose stride is arbitrary, 0 for a broadcast view) its row length."""
+    return t.stride(0) if t.shape[0] > 1 else t.shape[1]
+
+
 def _stream(stream) -> C.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -158,10 +164,10 @@ def nsa_metadata(mode: int, B: int, R: int, W: int, n_draft: int, topk: int, pag
     o = _MetadataOut(*(_ptr(out[k]) for k in ["cache_seqlens", "cu_seqlens_k", "cu_seqlens_q",
                                               "seqlens_expanded", "nsa_cache_seqlens", "nsa_cu_seqlens_k",
                                               "nsa_cu_seqlens_q", "row_to_req", "page_table_1"]),
-                     out["page_table_1"].stride(0), _ptr(out["real_page_table"]),
-                     out["real_page_table"].stride(0), _ptr(out.get("indexer_ks")), _ptr(out.get("indexer_ke")))
+                     _ld(out["page_table_1"]), _ptr(out["real_page_table"]),
+                     _ld(out["real_page_table"]), _ptr(out.get("indexer_ks")), _ptr(out.get("indexer_ke")))
     rc = load().nsa_metadata(mode, B, R, W, n_draft, topk, page_size, _ptr(seq_lens), _ptr(extend_lens),
-                             _ptr(req_to_token), req_to_token.stride(0), req_to_token.shape[0],
+                             _ptr(req_to_token), _ld(req_to_token), req_to_token.shape[0],
                              _ptr(req_pool_indices), C.byref(o), _ptr(status), _stream(stream))
     _check("nsa_metadata", rc)
 
@@ -207,9 +213,9 @@ def nsa_indexer_logits(dtype: int, q_idx: torch.Tensor, weights: torch.Tensor, k
     num_pages, ps = k_cache.shape[0], k_cache.shape[1]
     assert q_idx.is_contiguous() and k_cache.is_contiguous() and weights.is_contiguous() and k_scale.is_contiguous()
     rc = load().nsa_indexer_logits(dtype, _ptr(q_idx), _ptr(weights), _ptr(k_cache), _ptr(k_scale), num_pages,
-                                   ps, Hi, Di, _ptr(real_page_table), real_page_table.stride(0),
+                                   ps, Hi, Di, _ptr(real_page_table), _ld(real_page_table),
                                    _ptr(row_to_req), _ptr(row_len), R, rows_per_group, max_row_len, _ptr(logits),
-                                   logits.stride(0), _ptr(status), _stream(stream))
+                                   _ld(logits), _ptr(status), _stream(stream))
     _check("nsa_indexer_logits", rc)
 
 
@@ -217,9 +223,9 @@ def nsa_topk_transform(logits: torch.Tensor, row_len: torch.Tensor, row_to_req: 
                        page_table_1: torch.Tensor, topk: int, max_row_len: int, indices: torch.Tensor,
                        status: Optional[torch.Tensor] = None, stream=None) -> None:
     R = row_len.shape[0]
-    rc = load().nsa_topk_transform(_ptr(logits), logits.stride(0), _ptr(row_len), _ptr(row_to_req),
-                                   _ptr(page_table_1), page_table_1.stride(0), R, topk, max_row_len,
-                                   _ptr(indices), indices.stride(0), _ptr(status), _stream(stream))
+    rc = load().nsa_topk_transform(_ptr(logits), _ld(logits), _ptr(row_len), _ptr(row_to_req),
+                                   _ptr(page_table_1), _ld(page_table_1), R, topk, max_row_len,
+                                   _ptr(indices), _ld(indices), _ptr(status), _stream(stream))
     _check("nsa_topk_transform", rc)
 
 
@@ -251,7 +257,7 @@ def nsa_sparse_mla(q_dtype: int, kv_dtype: int, q_nope: torch.Tensor, q_rope: to
     rc = load().nsa_sparse_mla(q_dtype, kv_dtype, _ptr(q_nope), q_nope.stride(0), q_nope.stride(1), _ptr(q_rope),
                                q_rope.stride(0), q_rope.stride(1), _ptr(kv),
                                kv.shape[0] if num_slots is None else num_slots, _ptr(indices),
-                               indices.stride(0), R, H, d_latent, d_rope, topk, float(sm_scale), _ptr(out),
+                               _ld(indices), R, H, d_latent, d_rope, topk, float(sm_scale), _ptr(out),
                                _ptr(lse), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
     _check("nsa_sparse_mla", rc)
 
@@ -299,8 +305,8 @@ def nsa_topk_transform_ragged(logits: torch.Tensor, row_len: torch.Tensor, row_t
                               req_offset: torch.Tensor, topk: int, max_row_len: int, indices: torch.Tensor,
                               status: Optional[torch.Tensor] = None, stream=None) -> None:
     R = row_len.shape[0]
-    rc = load().nsa_topk_transform_ragged(_ptr(logits), logits.stride(0), _ptr(row_len), _ptr(row_to_req),
-                                          _ptr(req_offset), R, topk, max_row_len, _ptr(indices), indices.stride(0),
+    rc = load().nsa_topk_transform_ragged(_ptr(logits), _ld(logits), _ptr(row_len), _ptr(row_to_req),
+                                          _ptr(req_offset), R, topk, max_row_len, _ptr(indices), _ld(indices),
                                           _ptr(status), _stream(stream))
     _check("nsa_topk_transform_ragged", rc)
 
@@ -308,7 +314,7 @@ def nsa_topk_transform_ragged(logits: torch.Tensor, row_len: torch.Tensor, row_t
 def nsa_flatten_page_table(page_table_1: torch.Tensor, kv_len: torch.Tensor, kv_start: torch.Tensor,
                            out: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None) -> None:
     B = kv_len.shape[0]
-    rc = load().nsa_flatten_page_table(B, _ptr(page_table_1), page_table_1.stride(0), _ptr(kv_len), _ptr(kv_start),
+    rc = load().nsa_flatten_page_table(B, _ptr(page_table_1), _ld(page_table_1), _ptr(kv_len), _ptr(kv_start),
                                        _ptr(out), out.numel(), _ptr(status), _stream(stream))
     _check("nsa_flatten_page_table", rc)
 
@@ -345,9 +351,7 @@ def nsa_local_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
     assert k_cache.is_contiguous() and v_cache.is_contiguous() and block_table.stride(1) == 1
     assert out.is_contiguous() and lse.is_contiguous()
     nvb = seqused_k.shape[0]
-    # the row stride is also the row's capacity; a single row's stride is arbitrary
-    # (0 for a broadcast view), its length is what counts
-    bt_ld = block_table.stride(0) if block_table.shape[0] > 1 else block_table.shape[1]
+    bt_ld = _ld(block_table)  # the row stride, which is also the row's capacity
     rc = load().nsa_local_attention(_ptr(q), q.stride(0), _ptr(k_cache), _ptr(v_cache), num_pages, ps,
                                     _ptr(block_table), bt_ld, _ptr(cu_seqlens_q), _ptr(seqused_k),
                                     nvb, total_q, Hq, Hkv, D, float(sm_scale), _ptr(out), _ptr(lse), _ptr(status),
