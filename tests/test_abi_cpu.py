@@ -115,3 +115,13 @@ def test_local_attention_host_checks(nsa):
     assert _la_call(lib, scale=float("inf")) == inval
     assert _la_call(lib, lse=0) == inval                        # NULL output
     assert _la_call(lib, ps=0) == inval
+
+
+def test_leading_dimension_of_one_row_views(nsa):
+    import torch
+    from deepseek_sparse_mla_indexer_gb300 import _ld
+    assert _ld(torch.zeros(3, 5)) == 5
+    assert _ld(torch.zeros(3, 8)[:, :5]) == 8           # a column slice keeps the row stride
+    assert _ld(torch.zeros(5).expand(1, 5)) == 5        # broadcast row: stride 0, length 5
+    assert _ld(torch.arange(5)[None, :]) == 5
+    assert _ld(torch.zeros(1, 8)[:, :5]) == 5           # one row: only its length matters
