@@ -320,27 +320,30 @@ def run_ours(args, rank, world, local_rank):
 
     # the step's host inputs in and results out with one copy kernel each way (the
     # device reads and writes the pinned host buffers directly)
-    ins = [(step.seq_lens, h_in["seq_lens"]), (step.req_pool_indices, h_in["req_pool_indices"]),
-           (step.q_idx, h_in["q_idx"]), (step.weights, h_in["weights"])]
+    ins_idx = [(step.q_idx, h_in["q_idx"]), (step.weights, h_in["weights"])]
     ins_q = [(step.q_nope.view(torch.int16), h_q["q_nope"]), (step.q_rope.view(torch.int16), h_q["q_rope"])]
     side = torch.cuda.Stream(dev)
-    q_ready = torch.cuda.Event()
+    idx_ready, q_ready = torch.cuda.Event(), torch.cuda.Event()
 
     def e2e_step(st):
-        # the attention queries (most of the input bytes) travel on a side stream by the
-        # copy engines (no SMs taken) while metadata, indexer and top-k run; the
-        # attention call waits for them
+        # the indexer's and the attention's queries travel by the copy engines on a side
+        # stream (no SMs taken) while the metadata runs; the metadata kernel reads the
+        # per-request lengths and pool rows straight from pinned host memory; each
+        # consumer waits only for its own inputs; the attention writes out and lse straight
+        # into the pinned host buffers (the device-to-host transfer happens in its epilogue)
         side.wait_stream(st)
         with torch.cuda.stream(side):
+            for d, h in ins_idx:
+                d.copy_(h, non_blocking=True)
+            idx_ready.record(side)
             for d, h in ins_q:
                 d.copy_(h, non_blocking=True)
-        q_ready.record(side)
-        nsa.nsa_copy_buffers(ins, st)
-        for fn in calls[:-1]:
-            fn(st)
+            q_ready.record(side)
+        step.metadata(st, seq_lens=h_in["seq_lens"], req_pool_indices=h_in["req_pool_indices"])
+        st.wait_event(idx_ready)
+        step.indexer(st)
+        step.topk_transform(st)
         st.wait_event(q_ready)
-        # the attention writes out and lse straight into the pinned host buffers (the
-        # device-to-host transfer happens in its epilogue, over the chip-to-chip link)
         step.attention(st, out=h_out, lse=h_lse)
 
     # the whole host-to-host step (copies in, the four calls, copies out) replayed as
@@ -367,6 +370,11 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e2e_ev]))
     if step.status_code() != 0:
         raise RuntimeError(f"device status {step.status_code()} after the timed steps")
+    # the end-to-end step computes what the device-resident step computes, bit for bit
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    if not (torch.equal(h_out.view(torch.int16), step.out.cpu().view(torch.int16)) and torch.equal(h_lse, step.lse.cpu())):
+        raise RuntimeError("the end-to-end step's result differs from the device-resident step's")
 
     ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], world)
 
@@ -405,10 +413,10 @@ def run_ours(args, rank, world, local_rank):
                 e2e=dict(value=round(rows_total / (e2e_ms * 1e-3), 1), unit="tokens/s",
                          h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
                          note="per-request inputs host->device from pinned memory and out+lse device->host "
-                              "each step (the attention queries by the copy engines on a side stream, overlapping "
-                              "metadata, indexer and top-k; the other inputs by a copy kernel; out and lse written "
-                              "by the attention kernel straight into pinned host memory), the step replayed as one "
-                              "CUDA graph; "
+                              "each step (the indexer's and the attention's queries by the copy engines on a side "
+                              "stream, overlapping the earlier stages; lengths and pool rows read by the metadata "
+                              "kernel from pinned host memory; out and lse written by the attention kernel into "
+                              "pinned host memory), the step replayed as one CUDA graph; "
                               "KV / indexer-K caches and the req_to_token pool stay resident"),
                 gpu_launches=launches_per_step * args.steps,
                 clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"]))

@@ -72,9 +72,14 @@ class SparseAttentionStep:
         self.status = torch.zeros(1, dtype=torch.int32, device=d)
 
     # ---------------------------------------------------------- stages
-    def metadata(self, stream=None):
-        nsa_metadata(self.mode, self.B, self.R, self.W, self.n_draft, self.topk, self.ps, self.seq_lens,
-                     self.extend_lens, self.req_to_token, self.req_pool_indices, self.md, self.status, stream)
+    def metadata(self, stream=None, seq_lens: Optional[torch.Tensor] = None,
+                 req_pool_indices: Optional[torch.Tensor] = None):
+        """seq_lens / req_pool_indices default to the step's device copies; pinned host
+        tensors (mapped into the device's address space) are read directly."""
+        nsa_metadata(self.mode, self.B, self.R, self.W, self.n_draft, self.topk, self.ps,
+                     self.seq_lens if seq_lens is None else seq_lens, self.extend_lens, self.req_to_token,
+                     self.req_pool_indices if req_pool_indices is None else req_pool_indices, self.md,
+                     self.status, stream)
 
     def indexer(self, stream=None):
         nsa_indexer_logits(self.idx_dtype, self.q_idx, self.weights, self.k_cache, self.k_scale,
