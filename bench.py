@@ -318,8 +318,8 @@ def run_ours(args, rank, world, local_rank):
     h2d = sum(t.numel() * t.element_size() for t in list(h_in.values()) + list(h_q.values()))  # all of it, every step
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * 4
 
-    # the step's host inputs in and results out with one copy kernel each way (the
-    # device reads and writes the pinned host buffers directly)
+    # the queries go in by the copy engines; the rest of the traffic is done by the
+    # kernels themselves reading and writing the pinned host buffers
     ins_idx = [(step.q_idx, h_in["q_idx"]), (step.weights, h_in["weights"])]
     ins_q = [(step.q_nope.view(torch.int16), h_q["q_nope"]), (step.q_rope.view(torch.int16), h_q["q_rope"])]
     side = torch.cuda.Stream(dev)
@@ -346,7 +346,7 @@ def run_ours(args, rank, world, local_rank):
         st.wait_event(q_ready)
         step.attention(st, out=h_out, lse=h_lse)
 
-    # the whole host-to-host step (copies in, the four calls, copies out) replayed as
+    # the whole host-to-host step (inputs in, the four calls, results out) replayed as
     # one CUDA graph, as a serving loop runs it
     for _ in range(args.warmup):
         e2e_step(stream)
