@@ -202,7 +202,9 @@ nsa_status nsa_local_virtual_batches(int attn_chunk_size, int page_size, int B,
  * page_size % 64 == 0 runs on the tensor cores (tcgen05, fp8); every other
  * shape runs on the CUDA cores.
  * Device errors: a page id outside [0, num_pages) sets NSA_ERR_BOUNDS and the
- * affected logits are written as -inf.
+ * affected logits are written as -inf.  Not checked on the device (the metadata
+ * arrays from nsa_metadata always satisfy them): row_to_req[r] names a row of
+ * real_page_table, and rpt_ld >= ceil(max_row_len / page_size).
  */
 nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, const float *weights_dev,
                               const void *k_cache_dev, const float *k_scale_dev, int64_t num_pages,
@@ -235,7 +237,8 @@ nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, const float *w
  *   indices_dev      [R, indices_ld] int32, indices_ld >= topk
  * Supported: 1 <= topk <= 4096.
  * Device errors: row_len[r] > max_row_len sets NSA_ERR_BOUNDS and that row is
- * written as all -1.
+ * written as all -1.  Not checked on the device (nsa_metadata's arrays always
+ * satisfy it): row_to_req[r] names a row of page_table_1.
  */
 nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits_ld, const int32_t *row_len_dev,
                               const int32_t *row_to_req_dev, const int32_t *page_table_1_dev,
