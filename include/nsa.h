@@ -202,9 +202,10 @@ nsa_status nsa_local_virtual_batches(int attn_chunk_size, int page_size, int B,
  * page_size % 64 == 0 runs on the tensor cores (tcgen05, fp8); every other
  * shape runs on the CUDA cores.
  * Device errors: a page id outside [0, num_pages) sets NSA_ERR_BOUNDS and the
- * affected logits are written as -inf.  Not checked on the device (the metadata
- * arrays from nsa_metadata always satisfy them): row_to_req[r] names a row of
- * real_page_table, and rpt_ld >= ceil(max_row_len / page_size).
+ * affected logits are written as -inf.  rpt_ld < ceil(max_row_len / page_size)
+ * or logits_ld < max_row_len returns NSA_ERR_INVALID_ARG.  Not checked (the
+ * arrays from nsa_metadata always satisfy it): row_to_req[r] names a row of
+ * real_page_table.
  */
 nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, const float *weights_dev,
                               const void *k_cache_dev, const float *k_scale_dev, int64_t num_pages,
