@@ -1,11 +1,20 @@
-"""Benchmark of the sparse-attention decode step (metadata -> indexer logits ->
-top-k + slot transform -> sparse MLA) on the DeepSeek-V3.2-shaped bf16-KV
-decode workload: 32 requests, seqlens U{4096..32768}, page 64, indexer
-64 heads x 128 e4m3, topk 2048, MLA 128 heads d_qk 576 / d_v 512.
+"""Benchmark of the sparse-attention step (metadata -> indexer logits -> top-k +
+slot transform -> sparse MLA) on the method's five synthetic workloads; by
+default the DeepSeek-V3.2-shaped bf16-KV decode batch (32 requests, seqlens
+U{4096..32768}, page 64, indexer 64 heads x 128 e4m3, topk 2048, MLA 128 heads
+d_qk 576 / d_v 512).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config NAME] [--cpu-full]
     python bench.py --kv-write      # the KV-cache write-side kernels instead
     python bench.py --local-attn    # chunk-local dense attention (the second workload)
+
+--config picks one of the five workloads (`workloads.CONFIG_NAMES`).  Every
+stage is graded against its binding roofline: HBM bandwidth, or the tensor
+cores (fp8 for the indexer, bf16 for the attention) where the stage's flops
+take longer at peak than its bytes.  --cpu-full times the oracle on the full
+CPU sample of the workload (every row; the chunked extend on its 260 sampled
+rows) instead of a ~12 s bounded sample.
 
 Prints ONE JSON line (rank 0).  Under torchrun every rank runs an independent
 replica of the workload on its own GPU (replicas only: the path has no
@@ -30,10 +39,23 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "sparse-MLA decode tokens/s + indexer/top-k µs per step; % of HBM/TC roofline"
-WORKLOAD = "v32_decode_bf16"
-WORKLOAD_DESC = ("DeepSeek-V3.2-shaped decode, bf16 KV: batch 32, seqlens U{4096..32768}, page 64 in random "
-                 "order, indexer 64x128 e4m3 + fp32 row scale, weights N(0,1)/8, topk 2048, MLA 128 heads "
-                 "d_qk 576 (512+64) d_v 512 bf16, sm_scale 192^-0.5")
+WORKLOAD = "v32_decode_bf16"  # the workload the metric is quoted on
+WORKLOADS = {
+    "tiny_fp32_decode": "tiny fp32 decode: batch 2, seqlens {64,100}, page 16, indexer 4 heads x 32 fp32, topk 32, "
+                        "MLA 4 heads kv_lora 64 + rope 16 (d_v 64) fp32, sm_scale 80^-0.5",
+    "v32_decode_bf16": "DeepSeek-V3.2-shaped decode, bf16 KV: batch 32, seqlens U{4096..32768}, page 64 in random "
+                       "order, indexer 64x128 e4m3 + fp32 row scale, weights N(0,1)/8, topk 2048, MLA 128 heads "
+                       "d_qk 576 (512+64) d_v 512 bf16, sm_scale 192^-0.5",
+    "fp8kv_decode_h16": "fp8-KV decode, 16 MLA heads: batch 128, seqlen 8192, page 64, indexer 64x128 e4m3, topk 2048, "
+                        "latent e4m3 with per-128 fp32 scales + bf16 rope (656-byte rows), 1% latent outliers x20",
+    "chunked_extend": "chunked extend: 4 sequences x (8192 prefix + 2048 new tokens), causal rows see 8193..10240 "
+                      "tokens (clipped to topk 2048), page 64, indexer 64x128 e4m3, MLA 128 heads 576/512 bf16",
+    "verify_long_fp8kv": "speculative target-verify, long context: batch 64 x 4 draft tokens, seqlens log-uniform "
+                         "16384..131072, page 64, indexer 64x128 e4m3, topk 2048, MLA 128 heads 576/512 fp8 KV",
+}
+WORKLOAD_DESC = WORKLOADS[WORKLOAD]
+DEFAULT_SEED = {"tiny_fp32_decode": 0, "v32_decode_bf16": 2, "fp8kv_decode_h16": 3, "chunked_extend": 4,
+                "verify_long_fp8kv": 5}
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -55,31 +77,37 @@ class L2Flush:
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
-# stage's kernel from one ncu capture of this workload (profiles/ names the
-# command), valid only while the kernel sources hash as they did at capture.
+# stage's kernel from one ncu capture of a workload (profiles/ names the command),
+# keyed by (workload, stage); valid only while the kernel sources hash as they did
+# at capture.
 NCU_TRAFFIC = {
-    "sparse_mla": dict(bytes=int((81.316864 + 2.461440) * 1e6), sources=["sparse_mla_tc.cu", "sm100.cuh"],
-                       sha="149ce04c4033598b"),
-    "indexer": dict(bytes=int((79.633664 + 1.633536) * 1e6), sources=["indexer_tc.cu", "sm100.cuh"],
-                    sha="4b3b2f1c3334e74e"),
-    "topk": dict(bytes=int(4.731648e6), sources=["topk.cu"], sha="2f5262ea063997bf"),
-    "metadata": dict(bytes=int(5.872640e6), sources=["metadata.cu"], sha="6d9df76679a4256d"),
-    "local_attention": dict(bytes=int((642.419968 + 3.919616) * 1e6), sources=["local_attention.cu", "sm100.cuh"],
-                            sha="bf69a294053f9ee8"),
+    ("v32_decode_bf16", "sparse_mla"): dict(bytes=int((81.316864 + 2.461440) * 1e6),
+                                            sources=["sparse_mla_tc.cu", "sm100.cuh"], sha="149ce04c4033598b"),
+    ("v32_decode_bf16", "indexer"): dict(bytes=int((79.633664 + 1.633536) * 1e6), sources=["indexer_tc.cu", "sm100.cuh"],
+                                         sha="4b3b2f1c3334e74e"),
+    ("v32_decode_bf16", "topk"): dict(bytes=int(4.731648e6), sources=["topk.cu"], sha="2f5262ea063997bf"),
+    ("v32_decode_bf16", "metadata"): dict(bytes=int(5.872640e6), sources=["metadata.cu"], sha="6d9df76679a4256d"),
+    ("local_decode_c8192", "local_attention"): dict(bytes=int((642.419968 + 3.919616) * 1e6),
+                                                    sources=["local_attention.cu", "sm100.cuh"], sha="bf69a294053f9ee8"),
 }
 
 
-def ncu_traffic(stage: str):
-    """Measured bytes per launch, or None once the kernel has changed since the capture."""
+def sources_sha(files) -> str:
     import hashlib
-    e = NCU_TRAFFIC.get(stage)
-    if e is None:
-        return None
     m = hashlib.sha256()
-    for f in e["sources"]:
+    for f in files:
         with open(os.path.join(ROOT, "deepseek_sparse_mla_indexer_gb300", "csrc", f), "rb") as fh:
             m.update(fh.read())
-    return e["bytes"] if m.hexdigest()[:16] == e["sha"] else None
+    return m.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, stage: str):
+    """Measured bytes per launch, or None when there is no capture for this
+    workload or the kernel has changed since the capture."""
+    e = NCU_TRAFFIC.get((workload, stage))
+    if e is None:
+        return None
+    return e["bytes"] if sources_sha(e["sources"]) == e["sha"] else None
 
 
 def load_peaks():
@@ -114,6 +142,33 @@ def algorithmic_work(wl, seqlens_expanded: np.ndarray):
                            + wl.R * wl.H * 4 + wl.R * wl.topk * 4,
                            flops=2 * wl.H * int(nsel.sum()) * (dq + wl.d_latent))
     return w
+
+
+def stage_roofline(wl, stage: str, work: dict, sec: float, peaks: dict) -> dict:
+    """A stage's binding roofline: the larger of its bytes at the measured HBM copy
+    bandwidth and its flops at the tensor-core peak of the precision it runs in
+    (the indexer's e4m3 contraction at 2x the measured bf16 peak, the nominal fp8 to
+    bf16 ratio; the attention's bf16 products at the measured bf16 peak).  fp32
+    stages (the tiny workload) run on CUDA cores and are graded against HBM."""
+    nbytes, flops = work["bytes"], work["flops"]
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    tc_name, tc_peak = None, None
+    if stage == "indexer" and wl.idx_dtype == W.DT_E4M3:
+        tc_name, tc_peak = "fp8 dense (2x measured bf16)", 2.0 * peaks["bf16_tflops"]
+    elif stage == "sparse_mla" and wl.q_dtype == W.DT_BF16:
+        tc_name, tc_peak = "bf16 dense (measured)", peaks["bf16_tflops"]
+    t_tc = flops / (tc_peak * 1e12) if tc_peak else 0.0
+    gbs = nbytes / sec / 1e9
+    tfl = flops / sec / 1e12
+    d = dict(us=round(sec * 1e6, 2), bytes=int(nbytes), flops=int(flops), gbs=round(gbs, 1), tflops=round(tfl, 2),
+             hbm_frac=round(gbs / peaks["hbm_gbs"], 4))
+    if tc_peak:
+        d["tc_peak_tflops"] = round(tc_peak, 1)
+        d["tc_frac"] = round(tfl / tc_peak, 4)
+    d["bound"] = "tensor" if t_tc > t_hbm else "hbm"
+    d["roofline_us"] = round(max(t_hbm, t_tc) * 1e6, 2)
+    d["frac"] = round(max(t_hbm, t_tc) / sec, 4)
+    return d
 
 
 # ---------------------------------------------------------------- clocks
@@ -194,9 +249,10 @@ def record_external(event, stream):
 
 # ---------------------------------------------------------------- replicas
 
-def replica_seed(rank: int) -> int:
-    """Each rank draws an independent batch of the same workload."""
-    return 2 + 1000 * rank
+def replica_seed(rank: int, base: int = 2) -> int:
+    """Each rank draws an independent batch of the same workload (rank 0 the
+    workload's own seed)."""
+    return base + 1000 * rank
 
 
 def max_over_ranks(values, world: int):
@@ -222,10 +278,17 @@ def run_ours(args, rank, world, local_rank):
     import deepseek_sparse_mla_indexer_gb300 as nsa
     from deepseek_sparse_mla_indexer_gb300.step import SparseAttentionStep
 
+    name = args.config
+    wl = W.config(name, seed=replica_seed(rank, DEFAULT_SEED[name]))  # an independent replica per rank
+    # the oracle's CPU time is taken before the first GPU call (its worker threads
+    # never share a process with a started CUDA context mid-flight)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, full=args.cpu_full)
+
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     nsa.load()
-    wl = W.config(WORKLOAD, seed=replica_seed(rank))  # an independent replica per rank
     step = SparseAttentionStep(wl, dev)
     stream = torch.cuda.current_stream(dev)
     flush = L2Flush(dev)
@@ -233,13 +296,9 @@ def run_ours(args, rank, world, local_rank):
     stages = ["metadata", "indexer", "topk", "sparse_mla"]
     calls = [step.metadata, step.indexer, step.topk_transform, step.attention]
 
-    def one_step(evs=None):
-        for i, fn in enumerate(calls):
-            if evs is not None:
-                evs[i].record(stream)
+    def one_step():
+        for fn in calls:
             fn(stream)
-        if evs is not None:
-            evs[len(calls)].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -284,7 +343,6 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    t_wall = time.perf_counter()
     per_stage = {s: [] for s in stages}
     for k in range(args.steps):
         flush.zero_()  # L2 flush between steps, outside the timed events
@@ -293,7 +351,6 @@ def run_ours(args, rank, world, local_rank):
         step_ev[k][1].record(stream)
     torch.cuda.synchronize(dev)
     totals = [a.elapsed_time(b) for a, b in step_ev]
-    t_wall = time.perf_counter() - t_wall
     for k in range(args.steps):
         flush.zero_()
         graph_staged.replay()
@@ -309,19 +366,27 @@ def run_ours(args, rank, world, local_rank):
 
     # end to end through the public API with host buffers: per step the
     # per-request inputs go host->device from pinned memory, the outputs come back.
-    h_in = {k: torch.from_numpy(np.ascontiguousarray(getattr(wl, k))).pin_memory()
-            for k in ["seq_lens", "req_pool_indices", "q_idx", "weights"]}
-    h_q = {"q_nope": torch.from_numpy(wl.q_nope.view(np.int16)).pin_memory(),
-           "q_rope": torch.from_numpy(wl.q_rope.view(np.int16)).pin_memory()}
+    def pinned(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).reshape(-1)).pin_memory()
+
+    h_md = {k: torch.from_numpy(np.ascontiguousarray(getattr(wl, k))).pin_memory()
+            for k in ["seq_lens", "req_pool_indices"]}
+    if wl.extend_lens is not None:
+        h_md["extend_lens"] = torch.from_numpy(np.ascontiguousarray(wl.extend_lens)).pin_memory()
+    h_idx = {k: pinned(getattr(wl, k)) for k in ["q_idx", "weights"]}
+    h_q = {k: pinned(getattr(wl, k)) for k in ["q_nope", "q_rope"]}
     h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     h_lse = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in list(h_in.values()) + list(h_q.values()))  # all of it, every step
+    h2d = sum(t.numel() * t.element_size() for t in list(h_md.values()) + list(h_idx.values()) + list(h_q.values()))
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * 4
+
+    def dev_bytes(t):
+        return t.view(torch.uint8).reshape(-1)
 
     # the queries go in by the copy engines; the rest of the traffic is done by the
     # kernels themselves reading and writing the pinned host buffers
-    ins_idx = [(step.q_idx, h_in["q_idx"]), (step.weights, h_in["weights"])]
-    ins_q = [(step.q_nope.view(torch.int16), h_q["q_nope"]), (step.q_rope.view(torch.int16), h_q["q_rope"])]
+    ins_idx = [(dev_bytes(step.q_idx), h_idx["q_idx"]), (dev_bytes(step.weights), h_idx["weights"])]
+    ins_q = [(dev_bytes(step.q_nope), h_q["q_nope"]), (dev_bytes(step.q_rope), h_q["q_rope"])]
     side = torch.cuda.Stream(dev)
     idx_ready, q_ready = torch.cuda.Event(), torch.cuda.Event()
 
@@ -339,7 +404,7 @@ def run_ours(args, rank, world, local_rank):
             for d, h in ins_q:
                 d.copy_(h, non_blocking=True)
             q_ready.record(side)
-        step.metadata(st, seq_lens=h_in["seq_lens"], req_pool_indices=h_in["req_pool_indices"])
+        step.metadata(st, **h_md)
         st.wait_event(idx_ready)
         step.indexer(st)
         step.topk_transform(st)
@@ -373,7 +438,7 @@ def run_ours(args, rank, world, local_rank):
     # the end-to-end step computes what the device-resident step computes, bit for bit
     graph.replay()
     torch.cuda.synchronize(dev)
-    if not (torch.equal(h_out.view(torch.int16), step.out.cpu().view(torch.int16)) and torch.equal(h_lse, step.lse.cpu())):
+    if not (torch.equal(dev_bytes(h_out), dev_bytes(step.out.cpu())) and torch.equal(h_lse, step.lse.cpu())):
         raise RuntimeError("the end-to-end step's result differs from the device-resident step's")
 
     ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], world)
@@ -385,26 +450,29 @@ def run_ours(args, rank, world, local_rank):
     work = algorithmic_work(wl, md_len)
     peaks = load_peaks()
     stage_ms = {s: float(np.mean(v)) for s, v in per_stage.items()}
-    stage_info = {}
+    stage_info = {s: stage_roofline(wl, s, work[s], stage_ms[s] * 1e-3, peaks) for s in stages}
     for s in stages:
-        sec = stage_ms[s] * 1e-3
-        gbs = work[s]["bytes"] / sec / 1e9
-        tfl = work[s]["flops"] / sec / 1e12
-        stage_info[s] = dict(us=round(stage_ms[s] * 1e3, 2), gbs=round(gbs, 1), tflops=round(tfl, 2),
-                             hbm_frac=round(gbs / peaks["hbm_gbs"], 4))
+        stage_info[s]["traffic"] = ncu_traffic(name, s)
     dom = max(stages, key=lambda s: stage_ms[s])
-    dom_sec = stage_ms[dom] * 1e-3
-    achieved = work[dom]["bytes"] / dom_sec / 1e9
-    roof = dict(kernel=dom, bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
-                frac=round(achieved / peaks["hbm_gbs"], 4), traffic=ncu_traffic(dom),
-                algorithmic_bytes=work[dom]["bytes"], peak_source=peaks["source"])
+    di = stage_info[dom]
+    if di["bound"] == "tensor":
+        roof = dict(kernel=dom, bound="tensor", achieved=di["tflops"], peak=di["tc_peak_tflops"], unit="TFLOP/s",
+                    frac=di["frac"], traffic=di["traffic"], algorithmic_flops=di["flops"],
+                    algorithmic_bytes=di["bytes"], peak_source=peaks["source"] + " (" + (
+                        "fp8 = 2x bf16" if dom == "indexer" else "bf16") + ")")
+    else:
+        roof = dict(kernel=dom, bound="hbm", achieved=di["gbs"], peak=peaks["hbm_gbs"], unit="GB/s",
+                    frac=di["frac"], traffic=di["traffic"], algorithmic_bytes=di["bytes"],
+                    peak_source=peaks["source"])
 
     rows_total = wl.R * world
     line = dict(metric=METRIC, value=round(replica_throughput(wl.R, world, ms_step), 1), unit="tokens/s", n_gpus=world,
                 steps=args.steps, warmup=args.warmup, ms_per_step=round(ms_step, 5), higher_is_better=True,
-                scaling="weak", vs_baseline=None, dtype="bf16+e4m3 (f32 accumulate)",
+                scaling="weak", vs_baseline=None,
+                dtype="f32" if wl.kv_dtype == W.DT_F32 else
+                ("bf16+e4m3 (f32 accumulate)" if wl.kv_dtype == W.DT_BF16 else "e4m3 KV + bf16 (f32 accumulate)"),
                 data="synthetic (seeded; random pages; see workloads/)",
-                config=dict(workload=WORKLOAD_DESC, global_batch=rows_total,
+                config=dict(workload=name, description=WORKLOADS[name], global_batch=rows_total,
                             seq_len=int(np.mean(wl.seq_lens)), parallelism=f"replicas x{world}",
                             l2="flushed between steps (512 MB write, then a 256 MB read that retires its dirty lines, outside the timed events)",
                             timing="step replayed as one CUDA graph timed by events around the replay; stage "
@@ -420,64 +488,145 @@ def run_ours(args, rank, world, local_rank):
                               "KV / indexer-K caches and the req_to_token pool stay resident"),
                 gpu_launches=launches_per_step * args.steps,
                 clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"]))
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows)
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     return line
 
 
 # ---------------------------------------------------------------- CPU baseline (the oracle)
 
-def oracle_rows_time(wl, rows):
-    """Seconds for the oracle to run metadata (whole batch) plus indexer,
-    top-k and sparse MLA for the given rows."""
+def host_cpu() -> dict:
+    """Core count and CPU model of this host (lscpu, else /proc/cpuinfo)."""
+    n = os.cpu_count() or 1
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith(("model name", "cpu part")):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return dict(cores=n, model=model or "unknown")
+
+
+def cpu_sample_rows(wl, full: bool) -> list:
+    """Rows of the oracle's CPU sample.  Full: every row, except the chunked extend,
+    whose fp64 work (~6 TFLOP) is sampled at every 32nd row of each sequence plus its
+    first and last rows.  Bounded: all rows in a seeded random order (the caller stops
+    at its time budget)."""
+    if full and wl.mode == W.MODE_EXTEND:
+        rows, start = set(), 0
+        for n in wl.extend_lens:
+            n = int(n)
+            rows.update(range(start, start + n, 32))
+            rows.update([start, start + n - 1])
+            start += n
+        return sorted(rows)
+    if full:
+        return list(range(wl.R))
+    return [int(r) for r in np.random.default_rng(12345).permutation(wl.R)]
+
+
+def oracle_metadata_time(wl):
     import oracle
+    oracle.num_rows(wl.mode, wl.B, wl.extend_lens, wl.n_draft)  # the library is built and loaded outside the timing
     t0 = time.perf_counter()
     md = oracle.metadata(wl.mode, wl.seq_lens, wl.req_to_token, wl.req_pool_indices, W=wl.W, topk=wl.topk,
                          page_size=wl.page_size, extend_lens=wl.extend_lens, n_draft=wl.n_draft)
-    t_md = time.perf_counter() - t0
-    t1 = time.perf_counter()
+    return md, time.perf_counter() - t0
+
+
+def oracle_row_time(wl, md, r: int) -> float:
+    """Seconds for the oracle's indexer, top-k and sparse MLA of one query row."""
+    import oracle
+    t0 = time.perf_counter()
     lg = oracle.indexer_logits(wl.idx_dtype, wl.q_idx, wl.weights, wl.k_cache, wl.k_scale, md["real_page_table"],
-                               md["row_to_req"], md["seqlens_expanded"], rows=rows, width=wl.W)
+                               md["row_to_req"], md["seqlens_expanded"], rows=[r], width=wl.W)
     idx = oracle.topk_transform(lg, md["seqlens_expanded"], md["row_to_req"], md["page_table_1"], wl.topk,
-                                rows=rows, logits_rows_are_subset=True)
-    oracle.sparse_mla(wl.q_dtype, wl.kv_dtype, wl.q_nope, wl.q_rope, wl.kv, idx, wl.sm_scale, rows=rows,
+                                rows=[r], logits_rows_are_subset=True)
+    oracle.sparse_mla(wl.q_dtype, wl.kv_dtype, wl.q_nope, wl.q_rope, wl.kv, idx, wl.sm_scale, rows=[r],
                       indices_rows_are_subset=True)
-    t_rows = time.perf_counter() - t1
-    return t_md, t_rows
+    return time.perf_counter() - t0
 
 
-def cpu_baseline(wl, nrows):
-    rows = list(range(min(nrows, wl.R)))
-    t_md, t_rows = oracle_rows_time(wl, rows)
-    # whole-step time extrapolated from the sampled rows; metadata timed in full
-    per_row = t_rows / len(rows)
+def cpu_baseline(wl, full: bool = False, budget_s: float = 12.0) -> dict:
+    """The oracle as it stands (single-threaded C, fp64): metadata for the whole
+    batch, then indexer + top-k + sparse MLA row by row.  Bounded (default): rows in a
+    seeded random order until `budget_s` of row work, the mean row time scaled to all
+    rows.  Full: the whole CPU sample of the workload, its rows spread over one worker
+    thread per host core (each row runs single-threaded on one core; the oracle's C
+    code releases the interpreter lock), the per-row times summed as one core's time."""
+    from concurrent.futures import ThreadPoolExecutor
+    host = host_cpu()
+    md, t_md = oracle_metadata_time(wl)
+    rows = cpu_sample_rows(wl, full)
+    wall0 = time.perf_counter()
+    if full:
+        threads = max(1, host["cores"])
+        with ThreadPoolExecutor(threads) as ex:
+            times = list(ex.map(lambda r: oracle_row_time(wl, md, r), rows))
+    else:
+        threads = 1
+        times = []
+        for r in rows:
+            times.append(oracle_row_time(wl, md, r))
+            if sum(times) >= budget_s:
+                break
+        rows = rows[: len(times)]
+    wall = time.perf_counter() - wall0
+    per_row = float(np.sum(times)) / len(times)
     step_s = t_md + per_row * wl.R
-    return dict(value=round(wl.R / step_s, 3), unit="tokens/s", cores=1, kind="oracle",
-                sample=f"metadata for all {wl.B} requests + indexer/top-k/sparse MLA for rows {rows[0]}..{rows[-1]} "
-                       f"({len(rows)} of {wl.R}); per-row time scaled to the full step; single-threaded C, fp64")
+    scaled = len(times) < wl.R
+    what = ("the workload's full CPU sample" if full else f"a bounded sample (~{budget_s:.0f} s of row work)")
+    return dict(value=round(wl.R / step_s, 4), unit="tokens/s", cores=1, kind="oracle",
+                host=f"1 of {host['cores']} cores, {host['model']}",
+                sample=f"{what}: metadata for all {wl.B} requests ({t_md:.3f} s) + indexer/top-k/sparse MLA for "
+                       f"{len(times)} of {wl.R} rows, {per_row:.3f} s per row on one core"
+                       + (f" (rows run concurrently on {threads} threads, one core each; {wall:.1f} s wall)"
+                          if threads > 1 else "")
+                       + ("; per-row time scaled to the full step (extrapolated)" if scaled else "; every row")
+                       + "; single-threaded C, fp64",
+                step_seconds_one_core=round(step_s, 3), extrapolated=scaled)
 
 
 def run_reference(args, rank, world):
+    """The oracle as the reference implementation: each step its metadata for the
+    whole batch plus indexer/top-k/sparse MLA for one query row (cycling through
+    the rows), single-threaded on one host core."""
     if rank != 0:
         return None
-    wl = W.config(WORKLOAD, seed=2)
-    rows_per_step = 1
+    name = args.config
+    wl = W.config(name, seed=DEFAULT_SEED[name])
+    rows = cpu_sample_rows(wl, full=False)
     for k in range(args.warmup):
-        oracle_rows_time(wl, [k % wl.R])
+        md, _ = oracle_metadata_time(wl)
+        oracle_row_time(wl, md, rows[k % len(rows)])
     t = []
     for k in range(args.steps):
-        t_md, t_rows = oracle_rows_time(wl, [(args.warmup + k) % wl.R])
-        t.append(t_md + t_rows)
+        md, t_md = oracle_metadata_time(wl)
+        t.append(t_md + oracle_row_time(wl, md, rows[(args.warmup + k) % len(rows)]))
     s = float(np.mean(t))
-    v = round(rows_per_step / s, 4)
+    v = round(1 / s, 4)
+    host = host_cpu()
     sample = (f"each step: oracle metadata for the whole batch + indexer/top-k/sparse MLA for 1 of {wl.R} rows "
               "(single-threaded C, fp64)")
     return dict(impl="reference", metric=METRIC, value=v, unit="tokens/s", n_gpus=world, steps=args.steps,
                 warmup=args.warmup, ms_per_step=round(s * 1e3, 3), higher_is_better=True, scaling="weak",
                 vs_baseline=None, dtype="f64", data="synthetic (seeded; random pages; see workloads/)",
-                config=dict(workload=WORKLOAD_DESC, global_batch=wl.R, seq_len=int(np.mean(wl.seq_lens)),
-                            parallelism="oracle on rank 0"),
-                cpu_baseline=dict(value=v, unit="tokens/s", cores=1, kind="oracle", sample=sample),
+                config=dict(workload=name, description=WORKLOADS[name], global_batch=wl.R,
+                            seq_len=int(np.mean(wl.seq_lens)), parallelism="oracle on rank 0"),
+                cpu_baseline=dict(value=v, unit="tokens/s", cores=1, kind="oracle",
+                                  host=f"1 of {host['cores']} cores, {host['model']}", sample=sample),
                 e2e=dict(value=v, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
 
 
@@ -493,7 +642,7 @@ def run_kv_write(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     nsa.load()
-    wl = W.config(WORKLOAD, seed=replica_seed(0))
+    wl = W.config(WORKLOAD, seed=DEFAULT_SEED[WORKLOAD])
     rng = np.random.default_rng(7)
     n_slots = wl.kv.shape[0]
     kv_bf16 = torch.from_numpy(wl.kv.view(np.int16)).to(dev)
@@ -705,7 +854,7 @@ def run_local_attention(args):
                             seq_len=int(np.mean(wl.seq_lens)), visible_keys=local_visible_keys(cu, sk),
                             parallelism="replicas x1", l2="flushed before each launch (512 MB write, then a 256 MB read that retires its dirty lines, outside the events)"),
                 roofline=dict(kernel="local_attention", bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"],
-                              unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4), traffic=ncu_traffic("local_attention"),
+                              unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4), traffic=ncu_traffic(LOCAL_WORKLOAD, "local_attention"),
                               algorithmic_bytes=int(nbytes), peak_source=peaks["source"]),
                 e2e=dict(value=round(wl.total_q / e2e_s, 1), unit="query tokens/s", h2d_bytes_per_step=int(h2d),
                          d2h_bytes_per_step=int(d2h),
@@ -725,7 +874,10 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=3)
+    ap.add_argument("--config", default=WORKLOAD, choices=list(WORKLOADS),
+                    help="which of the five workloads to run (default: the one the metric is quoted on)")
+    ap.add_argument("--cpu-full", action="store_true",
+                    help="time the oracle on the workload's full CPU sample instead of a bounded one")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv-write", action="store_true",
                     help="measure the KV-cache write-side kernels instead of the attention step")

@@ -19,7 +19,7 @@ from . import _build
 
 __all__ = [
     "NsaError", "load", "MODE_DECODE", "MODE_EXTEND", "MODE_TARGET_VERIFY", "DT_F32", "DT_BF16",
-    "DT_E4M3", "nsa_metadata", "alloc_metadata", "nsa_local_virtual_batches", "nsa_effective_chunk_size",
+    "DT_E4M3", "nsa_metadata", "alloc_metadata", "alloc_score_hist", "nsa_local_virtual_batches", "nsa_effective_chunk_size",
     "nsa_indexer_logits", "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes",
     "nsa_sparse_mla_plan", "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged",
     "nsa_set_index_k", "nsa_topk_transform_ragged", "nsa_flatten_page_table", "nsa_copy_buffers",
@@ -34,8 +34,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_BOUNDS, ERR_TIMEOUT = range(
 EXPORTED_SYMBOLS = [
     "nsa_status_string", "nsa_abi_version", "nsa_status_read", "nsa_metadata",
     "nsa_effective_chunk_size", "nsa_local_virtual_batches", "nsa_indexer_logits",
-    "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes", "nsa_sparse_mla_plan",
-    "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged", "nsa_set_index_k",
+    "nsa_topk_transform", "nsa_topk_workspace_bytes", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes",
+    "nsa_sparse_mla_plan", "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged", "nsa_set_index_k",
     "nsa_topk_transform_ragged", "nsa_flatten_page_table", "nsa_copy_buffers",
     "nsa_check_bounded_wait", "nsa_local_attention",
 ]
@@ -68,8 +68,9 @@ def load(build_if_missing: bool = True):
         "nsa_metadata": ([I, I, I, I, I, I, I, P, P, P, L, L, P, P, P, P], I),
         "nsa_effective_chunk_size": ([I, I, I], I),
         "nsa_local_virtual_batches": ([I, I, I, P, P, P, L, L, I, P, P, P, P, P, P], I),
-        "nsa_indexer_logits": ([I, P, P, P, P, L, I, I, I, P, L, P, P, I, I, I, P, L, P, P], I),
-        "nsa_topk_transform": ([P, L, P, P, P, L, I, I, I, P, L, P, P], I),
+        "nsa_indexer_logits": ([I, P, P, P, P, L, I, I, I, P, L, P, P, I, I, I, P, L, P, P, P], I),
+        "nsa_topk_transform": ([P, L, P, P, P, L, I, I, I, P, L, P, P, S, P, P], I),
+        "nsa_topk_workspace_bytes": ([I, I, I], S),
         "nsa_sparse_mla": ([I, I, P, L, L, P, L, L, P, L, P, L, I, I, I, I, I, F, P, P, P, S, P, P], I),
         "nsa_sparse_mla_workspace_bytes": ([I, I, I, I, I, I, I], S),
         "nsa_sparse_mla_plan": ([I, I, I, I, I, I, I, P, P], I),
@@ -77,7 +78,7 @@ def load(build_if_missing: bool = True):
         "nsa_quantize_kv_cache": ([P, L, I, I, P, P], I),
         "nsa_dequantize_kv_paged": ([P, L, I, I, P, L, P, P, P], I),
         "nsa_set_index_k": ([P, L, P, I, I, P, P, L, P, P], I),
-        "nsa_topk_transform_ragged": ([P, L, P, P, P, I, I, I, P, L, P, P], I),
+        "nsa_topk_transform_ragged": ([P, L, P, P, P, I, I, I, P, L, P, P, S, P, P], I),
         "nsa_flatten_page_table": ([I, P, L, P, P, P, L, P, P], I),
         "nsa_copy_buffers": ([I, P, P, P, P], I),
         "nsa_check_bounded_wait": ([P, C.c_longlong, P], I),
@@ -107,8 +108,19 @@ def _ptr(t: Optional[torch.Tensor]):
 
 def _ld(t: torch.Tensor) -> int:
     """Leading dimension of a row-major 2D tensor: its row stride, or for a single
-    row (whose stride is arbitrary, 0 for a broadcast view) its row length."""
+    row (whose stride is arbitrary, 0 for a broadcast view) its row length.  The
+    library reads every row as packed, so elements of a row must be adjacent."""
+    if t.dim() != 2:
+        raise ValueError(f"expected a 2D tensor, got shape {tuple(t.shape)}")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError("the elements of each row must be adjacent (stride 1 in the last dimension)")
     return t.stride(0) if t.shape[0] > 1 else t.shape[1]
+
+
+def alloc_score_hist(R: int, device="cuda") -> torch.Tensor:
+    """A zeroed [R, 2048] uint32 (stored as int32) digit-count buffer shared by
+    nsa_indexer_logits and nsa_topk_transform (the top-k leaves it zeroed)."""
+    return torch.zeros((max(R, 1), 2048), dtype=torch.int32, device=device)
 
 
 def _stream(stream) -> C.c_void_p:
@@ -208,24 +220,50 @@ def nsa_local_virtual_batches(attn_chunk_size: int, page_size: int, cu_seqlens_q
 def nsa_indexer_logits(dtype: int, q_idx: torch.Tensor, weights: torch.Tensor, k_cache: torch.Tensor,
                        k_scale: torch.Tensor, real_page_table: torch.Tensor, row_to_req: torch.Tensor,
                        row_len: torch.Tensor, max_row_len: int, logits: torch.Tensor,
-                       status: Optional[torch.Tensor] = None, stream=None, rows_per_group: int = 1) -> None:
+                       status: Optional[torch.Tensor] = None, stream=None, rows_per_group: int = 1,
+                       score_hist: Optional[torch.Tensor] = None) -> None:
     R, Hi, Di = q_idx.shape
     num_pages, ps = k_cache.shape[0], k_cache.shape[1]
     assert q_idx.is_contiguous() and k_cache.is_contiguous() and weights.is_contiguous() and k_scale.is_contiguous()
     rc = load().nsa_indexer_logits(dtype, _ptr(q_idx), _ptr(weights), _ptr(k_cache), _ptr(k_scale), num_pages,
                                    ps, Hi, Di, _ptr(real_page_table), _ld(real_page_table),
                                    _ptr(row_to_req), _ptr(row_len), R, rows_per_group, max_row_len, _ptr(logits),
-                                   _ld(logits), _ptr(status), _stream(stream))
+                                   _ld(logits), _ptr(_hist(score_hist, R)), _ptr(status), _stream(stream))
     _check("nsa_indexer_logits", rc)
+
+
+def _hist(h: Optional[torch.Tensor], R: int) -> Optional[torch.Tensor]:
+    if h is not None:
+        assert h.is_contiguous() and h.element_size() == 4 and h.shape[-1] == 2048 and h.numel() >= R * 2048
+    return h
+
+
+def nsa_topk_workspace_bytes(R: int, max_row_len: int, with_score_hist: bool) -> int:
+    return int(load().nsa_topk_workspace_bytes(R, max_row_len, 1 if with_score_hist else 0))
+
+
+def alloc_topk_workspace(R: int, max_row_len: int, with_score_hist: bool, device="cuda") -> torch.Tensor:
+    """A zeroed top-k workspace (the calls leave it zeroed for the next one)."""
+    n = max(256, nsa_topk_workspace_bytes(R, max_row_len, with_score_hist))
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def _topk_ws(ws: Optional[torch.Tensor], R: int, max_row_len: int, score_hist, device):
+    if ws is None:  # a fresh zeroed one (a caller running many steps keeps its own)
+        ws = alloc_topk_workspace(R, max_row_len, score_hist is not None, device)
+    return ws, ws.numel() * ws.element_size()
 
 
 def nsa_topk_transform(logits: torch.Tensor, row_len: torch.Tensor, row_to_req: torch.Tensor,
                        page_table_1: torch.Tensor, topk: int, max_row_len: int, indices: torch.Tensor,
-                       status: Optional[torch.Tensor] = None, stream=None) -> None:
+                       status: Optional[torch.Tensor] = None, stream=None,
+                       score_hist: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None) -> None:
     R = row_len.shape[0]
+    ws, ws_bytes = _topk_ws(workspace, R, max_row_len, score_hist, logits.device)
     rc = load().nsa_topk_transform(_ptr(logits), _ld(logits), _ptr(row_len), _ptr(row_to_req),
                                    _ptr(page_table_1), _ld(page_table_1), R, topk, max_row_len,
-                                   _ptr(indices), _ld(indices), _ptr(status), _stream(stream))
+                                   _ptr(indices), _ld(indices), _ptr(_hist(score_hist, R)), _ptr(ws), ws_bytes,
+                                   _ptr(status), _stream(stream))
     _check("nsa_topk_transform", rc)
 
 
@@ -303,11 +341,15 @@ def nsa_set_index_k(k: torch.Tensor, loc: torch.Tensor, k_cache: torch.Tensor, k
 
 def nsa_topk_transform_ragged(logits: torch.Tensor, row_len: torch.Tensor, row_to_req: torch.Tensor,
                               req_offset: torch.Tensor, topk: int, max_row_len: int, indices: torch.Tensor,
-                              status: Optional[torch.Tensor] = None, stream=None) -> None:
+                              status: Optional[torch.Tensor] = None, stream=None,
+                              score_hist: Optional[torch.Tensor] = None,
+                              workspace: Optional[torch.Tensor] = None) -> None:
     R = row_len.shape[0]
+    ws, ws_bytes = _topk_ws(workspace, R, max_row_len, score_hist, logits.device)
     rc = load().nsa_topk_transform_ragged(_ptr(logits), _ld(logits), _ptr(row_len), _ptr(row_to_req),
                                           _ptr(req_offset), R, topk, max_row_len, _ptr(indices), _ld(indices),
-                                          _ptr(status), _stream(stream))
+                                          _ptr(_hist(score_hist, R)), _ptr(ws), ws_bytes, _ptr(status),
+                                          _stream(stream))
     _check("nsa_topk_transform_ragged", rc)
 
 

@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(kThreads)
 indexer_simt_kernel(const void *q, const float *w, const void *k_cache, const float *k_scale,
                     int64_t num_pages, int ps, int Hi, int Di, const int32_t *rpt, int64_t rpt_ld,
                     const int32_t *row_to_req, const int32_t *row_len, int max_row_len, float *logits,
-                    int64_t logits_ld, int32_t *status)
+                    int64_t logits_ld, uint32_t *score_hist, int32_t *status)
 {
     extern __shared__ float smem[];
     const int r = blockIdx.y;
@@ -90,7 +90,9 @@ indexer_simt_kernel(const void *q, const float *w, const void *k_cache, const fl
     const int s = s0 + t;
     if (part == 0 && s < L) {
         const float scale = sc[t];
-        logits[(int64_t)r * logits_ld + s] = isnan(scale) ? -INFINITY : acc * scale;
+        const float v = isnan(scale) ? -INFINITY : acc * scale;
+        logits[(int64_t)r * logits_ld + s] = v;
+        if (score_hist) atomicAdd(&score_hist[(int64_t)r * kScoreBins + (order_key(v) >> kScoreDigitShift)], 1u);
     }
 }
 
@@ -103,7 +105,8 @@ extern "C" nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, con
                                          const int32_t *real_page_table_dev, int64_t rpt_ld,
                                          const int32_t *row_to_req_dev, const int32_t *row_len_dev,
                                          int R, int rows_per_group, int max_row_len, float *logits_dev,
-                                         int64_t logits_ld, int32_t *status_dev, nsa_stream_t stream)
+                                         int64_t logits_ld, uint32_t *score_hist_dev, int32_t *status_dev,
+                                         nsa_stream_t stream)
 {
     using namespace nsa;
     if (dtype != NSA_DT_E4M3 && dtype != NSA_DT_F32) return NSA_ERR_UNSUPPORTED;
@@ -120,7 +123,8 @@ extern "C" nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, con
     nsa_status st = indexer_tc_try_launch(dtype, q_dev, weights_dev, k_cache_dev, k_scale_dev,
                                           num_pages, page_size, Hi, Di, real_page_table_dev, rpt_ld,
                                           row_to_req_dev, row_len_dev, R, max_row_len, logits_dev,
-                                          logits_ld, status_dev, (cudaStream_t)stream, rows_per_group);
+                                          logits_ld, score_hist_dev, status_dev, (cudaStream_t)stream,
+                                          rows_per_group);
     if (st != NSA_ERR_UNSUPPORTED) return st;
 
     const size_t smem = sizeof(float) * ((size_t)(Hi + kTok) * (Di + 1) + Hi + kTok);
@@ -131,14 +135,14 @@ extern "C" nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, con
         k<<<grid, kThreads, smem, (cudaStream_t)stream>>>(q_dev, weights_dev, k_cache_dev, k_scale_dev,
                                                           num_pages, page_size, Hi, Di, real_page_table_dev,
                                                           rpt_ld, row_to_req_dev, row_len_dev, max_row_len,
-                                                          logits_dev, logits_ld, status_dev);
+                                                          logits_dev, logits_ld, score_hist_dev, status_dev);
     } else {
         auto k = indexer_simt_kernel<NSA_DT_F32>;
         NSA_CUDA_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         k<<<grid, kThreads, smem, (cudaStream_t)stream>>>(q_dev, weights_dev, k_cache_dev, k_scale_dev,
                                                           num_pages, page_size, Hi, Di, real_page_table_dev,
                                                           rpt_ld, row_to_req_dev, row_len_dev, max_row_len,
-                                                          logits_dev, logits_ld, status_dev);
+                                                          logits_dev, logits_ld, score_hist_dev, status_dev);
     }
     return launch_status();
 }

@@ -49,6 +49,12 @@ constexpr uint32_t kTileBytes = kTileTok * kDi;    // 16 KB of e4m3
 constexpr uint32_t kHalfBytes = kHalf * kDi;       // 8 KB
 constexpr uint32_t kQRowBytes = kHi * kDi;         // 8 KB per query row
 constexpr long long kWaitBudget = 2000000000LL;    // ~1 s at 2 GHz
+// Digit counts per row in shared memory: two 16-bit counters per word, flushed to
+// the global histogram at the end of each segment and at least every kHistFlushTiles
+// tiles (each adds at most 128 to a counter, so none passes 65535).
+constexpr int kHistWords = kScoreBins / 2;
+constexpr int kHistFlushTiles = 256;
+static_assert(kHistFlushTiles * kTileTok < 65536, "16-bit digit counters");
 
 struct TcParams {
     const float *w;
@@ -61,6 +67,7 @@ struct TcParams {
     int64_t num_pages;
     float *logits;
     int64_t logits_ld;
+    uint32_t *hist;       // optional [R][kScoreBins] counts of the logits' leading digits
     int32_t *status;
     uint32_t acc_stride;  // TMEM columns per accumulator buffer
     uint32_t tmem_cols;
@@ -167,6 +174,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     uint8_t *a_ring = smem;                              // stages x 16 KB
     uint8_t *q_smem = a_ring + p.stages * kTileBytes;    // G x 8 KB
     Bars *bars = (Bars *)(q_smem + p.G * kQRowBytes);
+    uint32_t *hist_smem = (uint32_t *)(bars + 1);  // [G][kHistWords] when p.hist is set
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
@@ -360,6 +368,22 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const int et = threadIdx.x - 64;          // 0..127
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
         const int tok = quad * 32 + lane;         // token within the tile
+        uint32_t *hs = p.hist ? hist_smem : nullptr;
+        if (hs)
+            for (int j = et; j < p.G * kHistWords; j += 128) hs[j] = 0u;
+        // the per-CTA digit counts of a segment's rows go to the global histogram
+        auto flush_hist = [&](const SubGroup &sg) {
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // every epilogue thread's counts are in
+            for (int j = et; j < sg.c * kHistWords; j += 128) {
+                const uint32_t v = hs[j];
+                if (v == 0u) continue;
+                hs[j] = 0u;
+                uint32_t *g = p.hist + (int64_t)(sg.r0 + j / kHistWords) * kScoreBins + 2 * (j % kHistWords);
+                if (v & 0xFFFFu) atomicAdd(g, v & 0xFFFFu);
+                if (v >> 16) atomicAdd(g + 1, v >> 16);
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // cleared before anyone counts again
+        };
         uint32_t ai = 0, it = 0;
         for_each_segment(p, bars, [&](const SubGroup &sg, int tb, int te) -> bool {
             asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -368,6 +392,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             int Lrow[kMaxG];
 #pragma unroll
             for (int i = 0; i < kMaxG; ++i) Lrow[i] = i < sg.c ? clamp_len(p, sg.r0 + i) : 0;
+            int since_flush = 0;
             for (int t = tb; t < te; ++t, ++ai, ++it) {
                 const int ab = ai & 1;
                 const uint32_t aph = (ai >> 1) & 1;
@@ -392,12 +417,22 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     for (int h = 0; h < 32; ++h) acc = fmaf(wr[h], fmaxf(__uint_as_float(v0[h]), 0.f), acc);
 #pragma unroll
                     for (int h = 0; h < 32; ++h) acc = fmaf(wr[32 + h], fmaxf(__uint_as_float(v1[h]), 0.f), acc);
-                    if (s < Lrow[i])
-                        p.logits[(int64_t)(sg.r0 + i) * p.logits_ld + s] = valid_page ? acc * scale : -INFINITY;
+                    const bool in = s < Lrow[i];
+                    const float logit = valid_page ? acc * scale : -INFINITY;
+                    if (in) p.logits[(int64_t)(sg.r0 + i) * p.logits_ld + s] = logit;
+                    if (hs && in) {
+                        const uint32_t d = order_key(logit) >> kScoreDigitShift;
+                        atomicAdd(&hs[i * kHistWords + (d >> 1)], 1u << ((d & 1u) * 16));
+                    }
                 }
                 tc_fence_before();
                 mbar_arrive(&bars->acc_empty[ab]);
+                if (hs && ++since_flush == kHistFlushTiles) {
+                    flush_hist(sg);
+                    since_flush = 0;
+                }
             }
+            if (hs && since_flush > 0) flush_hist(sg);
             return true;
         });
     }
@@ -416,7 +451,8 @@ nsa_status indexer_tc_try_launch(nsa_dtype dtype, const void *q, const float *w,
                                  const float *k_scale, int64_t num_pages, int page_size, int Hi, int Di,
                                  const int32_t *rpt, int64_t rpt_ld, const int32_t *row_to_req,
                                  const int32_t *row_len, int R, int max_row_len, float *logits,
-                                 int64_t logits_ld, int32_t *status, cudaStream_t stream, int rows_per_group)
+                                 int64_t logits_ld, uint32_t *score_hist, int32_t *status, cudaStream_t stream,
+                                 int rows_per_group)
 {
     if (dtype != NSA_DT_E4M3 || Hi != kHi || Di != kDi || page_size % kHalf != 0) return NSA_ERR_UNSUPPORTED;
     if (((uintptr_t)q & 15) || ((uintptr_t)k_cache & 15) || ((uintptr_t)k_scale & 15)) return NSA_ERR_UNSUPPORTED;
@@ -434,14 +470,15 @@ nsa_status indexer_tc_try_launch(nsa_dtype dtype, const void *q, const float *w,
     TcParams p;
     p.w = w; p.k_scale = k_scale; p.rpt = rpt; p.rpt_ld = rpt_ld; p.row_to_req = row_to_req; p.row_len = row_len;
     p.R = R; p.G = G; p.max_row_len = max_row_len; p.ps = page_size; p.num_pages = num_pages;
-    p.logits = logits; p.logits_ld = logits_ld; p.status = status;
+    p.logits = logits; p.logits_ld = logits_ld; p.hist = score_hist; p.status = status;
     p.acc_stride = (uint32_t)(kHi * G);
     uint32_t cols = 32;
     while (cols < 2 * p.acc_stride) cols <<= 1;
     p.tmem_cols = cols;
 
     // one CTA per SM; the ring takes what the q rows and barriers leave of 227 KB
-    const size_t fixed = 1024 + (size_t)G * kQRowBytes + sizeof(Bars);
+    const size_t fixed = 1024 + (size_t)G * kQRowBytes + sizeof(Bars) +
+                         (score_hist ? (size_t)G * kHistWords * sizeof(uint32_t) : 0);
     p.stages = (int)std::min<size_t>(kMaxStages, (232448 - fixed) / kTileBytes);
     const size_t smem = fixed + (size_t)p.stages * kTileBytes;
     auto kern = indexer_tc_kernel;

@@ -33,6 +33,23 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b)
     return __uint_as_float(((uint32_t)b) << 16);
 }
 
+// Order-preserving 32-bit key of a score: larger scores give larger keys, -0
+// folds onto +0 and NaN ranks below every number.  The top-k selects on these
+// keys; the indexer histograms their top kScoreDigitBits bits per row.
+__device__ __forceinline__ uint32_t order_key(float x)
+{
+    uint32_t u = __float_as_uint(x);
+    if (x != x) return 0u;       // NaN ranks lowest
+    if ((u << 1) == 0u) u = 0u;  // -0 == +0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The per-row score histogram shared by the indexer and the top-k: counts of the
+// keys' leading kScoreDigitBits bits (kScoreBins uint32 bins per row).
+constexpr int kScoreDigitBits = 11;
+constexpr int kScoreBins = 1 << kScoreDigitBits;
+constexpr int kScoreDigitShift = 32 - kScoreDigitBits;
+
 __host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Python floor division for the page-table transform (ids are non-negative

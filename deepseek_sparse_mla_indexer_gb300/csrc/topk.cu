@@ -3,23 +3,33 @@
 // [NSA] NSAIndexerMetadata.topk_transform (the fused variant that emits KV
 // slots of the page table instead of positions), [DSA]
 // transform_index_page_table_* with page size 1 and _pad_topk_indices (-1
-// padding).
+// padding); the long-row multi-CTA plan and the indexer-to-top-k fusion follow
+// [DSA]'s top-k v2 plan and its fused top-k switch.
 //
-// Rows up to kCacheCap scores: one block of 1024 threads per row, the scores
-// read from HBM once and kept in shared memory; longer rows: a cluster of up
-// to 8 blocks per row (below).  Scores become order-preserving 32-bit keys
-// (-0 folded onto +0, NaN below every number).  The k-th largest key is
-// located by a most-significant-digit radix select with 11/11/10-bit digits:
-// each pass histograms the keys that still match the chosen prefix (eight
-// replicated shared-memory histograms spread the atomic traffic of the few
-// crowded bins), and a block scan over the bins, largest
-// digit first, picks the digit holding the k-th key.  A pass stops the search
-// early when the whole bin is selected.  A final ordered pass keeps every key
-// above the threshold and the first (k - #above) keys equal to it, in
-// position order, so ties go to the lower position and the output comes out
-// sorted without a sort: each thread owns a run of consecutive positions and
-// one block scan of its (#above, #equal) counts places them; the page-table
-// gathers of all output slots then go out together.
+// Scores become order-preserving 32-bit keys (-0 folded onto +0, NaN below
+// every number).  The selection is a most-significant-digit radix select whose
+// first 11-bit digit comes from a per-row histogram of the keys' leading bits,
+// counted either by the indexer as it writes the scores (fused) or by
+// topk_hist_kernel below, over all SMs.
+//
+// topk_row_kernel (rows up to kRowCap positions): one CTA per row.  The row's
+// keys are read once into shared memory; each thread classifies its run of
+// consecutive positions against d1 (from the histogram when it describes the
+// scores, else from one shared-memory histogram pass), the positions in the
+// threshold bin are compacted in order and resolved on their remaining 21 bits,
+// and one scan of the selected counts places every position in order.
+//
+// topk_chunk_kernel (longer rows): one CTA per 4096-position chunk of a row.  Each CTA picks
+// the threshold digit d1 from the row's histogram, reads its chunk once and
+// writes, in position order, every position whose digit is above d1 (selected)
+// or equal to it (a candidate) to a per-chunk list, with its counts.  The last
+// CTA of the row to finish (a per-row arrival counter; nobody waits) checks the
+// counts against the histogram, resolves the remaining 21 key bits on the
+// candidates alone, and writes the ordered output: one scan over the
+// concatenated lists gives every selected position its slot.  Ties go to the
+// lower position.  A histogram that does not describe the scores (the counts
+// disagree) makes that CTA select the row from the scores directly, so the
+// result never depends on the histogram's contents.
 #include <algorithm>
 
 #include "nsa_internal.cuh"
@@ -27,22 +37,44 @@
 namespace nsa {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kBins = 2048;
-constexpr int kCopies = 8;             // replicated histograms (warp w adds into copy w % 8)
-constexpr int kCacheCap = 40 * 1024;  // 160 KB of keys (+ 64 KB of histograms)
-// Dynamic shared memory of topk_transform_kernel: the histograms, then `cap` cached keys.
-constexpr size_t row_kernel_smem_bytes(int cap) { return (size_t)(kCopies * kBins + cap) * sizeof(uint32_t); }
-static_assert(row_kernel_smem_bytes(kCacheCap) <= 232448, "shared memory per block");
-constexpr int kItems = 4;             // consecutive elements per thread in the cluster's ordered pass
+constexpr int kThreads = 512;
+constexpr int kChunk = 4096;                       // positions per chunk CTA
+constexpr int kHalfChunk = kChunk / 2;             // thread t reads 4t..4t+3 of each half
+static_assert(kHalfChunk == 4 * kThreads, "two float4 per thread cover a chunk");
+constexpr int kBins = kScoreBins;                  // 11-bit digits
+constexpr int kBinsPerThread = kBins / kThreads;   // 4, largest digit first
+constexpr int kCandCap = 6144;                     // candidates of the threshold bin held in shared memory
+constexpr int kMaxChunks = kThreads;               // rows up to 2 M positions
+constexpr int kRowCap = 16384;                     // rows the one-CTA kernel caches whole
+constexpr int kRowCand = 4096;                     // its threshold-bin capacity
+constexpr int kRun = (4096 + kCandCap + kThreads - 1) / kThreads;  // list entries a thread of the assembling CTA holds
+constexpr uint32_t kFlag = 0x80000000u;            // list entry: candidate (digit == d1); candidate: selected
+constexpr uint32_t kNoDigit = 0xFFFFFFFFu;
 
-__device__ __forceinline__ uint32_t order_key(float x)
-{
-    uint32_t u = __float_as_uint(x);
-    if (x != x) return 0u;       // NaN ranks lowest
-    if ((u << 1) == 0u) u = 0u;  // -0 == +0
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
+// Dynamic shared memory of topk_assemble_kernel.
+struct ChunkSmem {
+    uint32_t hist[kBins];
+    uint32_t cand_key[kCandCap];
+    uint32_t cand_pos[kCandCap];
+    uint32_t chunk_off[kMaxChunks + 1];
+};
+
+struct TopkArgs {
+    const float *logits;
+    int64_t logits_ld;
+    const int32_t *row_len;
+    const int32_t *row_to_req;
+    const int32_t *pt;           // paged: page_table_1
+    int64_t pt_ld;
+    const int32_t *req_offset;   // ragged: per-request offset
+    int topk, max_row_len, nch_max;
+    int32_t *indices;
+    int64_t indices_ld;
+    uint32_t *hist;              // [R][kBins] digit counts (cleared after use)
+    uint32_t *counts;            // [R][nch_max] (#above | #candidates << 16) per chunk
+    uint2 *lists;                // [R][nch_max * kChunk] (position | kFlag on candidates, slot or key)
+    int32_t *status;
+};
 
 // Inclusive block scan of one value per thread; *total receives the block sum.
 __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *warp_buf, uint32_t *total)
@@ -72,496 +104,690 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *warp_b
     return incl;
 }
 
-// Keys of lg[s0 .. s0 + n) into cache[0 .. n): 16-byte loads, all in flight at once.
-template <int NT, int MAXV>
-__device__ __forceinline__ void fill_keys(const float *lg, int s0, int n, uint32_t *cache)
+// The digit of a radix pass that holds the need-th largest key.  Thread t holds
+// the counts c[j] of digits kBins-1-4t-j (largest first).  On return pick[0] = the
+// digit, pick[1] = how many of its keys are still needed, pick[2] = its count
+// (kNoDigit if the counts hold fewer than `need` keys); *total = all counts.
+__device__ __forceinline__ void pick_digit(const uint32_t (&c)[kBinsPerThread], uint32_t need, uint32_t *warp_buf,
+                                           uint32_t *total, uint32_t *pick)
 {
-    const float *src = lg + s0;
-    if ((((uintptr_t)src) & 15) == 0) {
-        const int nv = n >> 2;
-        for (int base = 0; base < nv; base += NT * MAXV) {
-            float4 v[MAXV];
+    uint32_t sum = 0u;
 #pragma unroll
-            for (int u = 0; u < MAXV; ++u) {
-                const int j = base + u * NT + (int)threadIdx.x;
-                if (j < nv) v[u] = __ldg(reinterpret_cast<const float4 *>(src) + j);
-            }
+    for (int j = 0; j < kBinsPerThread; ++j) sum += c[j];
+    if (threadIdx.x == 0) pick[2] = kNoDigit;  // ordered before every write below by the scan's barriers
+    const uint32_t incl = block_incl_scan(sum, warp_buf, total);
+    uint32_t cum = incl - sum;
+    if (cum < need && need <= incl) {
 #pragma unroll
-            for (int u = 0; u < MAXV; ++u) {
-                const int j = base + u * NT + (int)threadIdx.x;
-                if (j < nv)
-                    reinterpret_cast<uint4 *>(cache)[j] =
-                        make_uint4(order_key(v[u].x), order_key(v[u].y), order_key(v[u].z), order_key(v[u].w));
+        for (int j = 0; j < kBinsPerThread; ++j) {
+            if (cum + c[j] >= need) {
+                pick[0] = (uint32_t)(kBins - 1 - kBinsPerThread * (int)threadIdx.x - j);
+                pick[1] = need - cum;
+                pick[2] = c[j];
+                break;
             }
+            cum += c[j];
         }
-        for (int i = (nv << 2) + (int)threadIdx.x; i < n; i += NT) cache[i] = order_key(src[i]);
-    } else {
-        for (int i = threadIdx.x; i < n; i += NT) cache[i] = order_key(src[i]);
+    }
+    __syncthreads();
+}
+
+// The counts of a kBins-bin shared-memory histogram this thread owns, largest digit first.
+__device__ __forceinline__ void own_bins(const uint32_t *h, uint32_t (&c)[kBinsPerThread], uint32_t dmask)
+{
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) {
+        const int d = kBins - 1 - kBinsPerThread * (int)threadIdx.x - j;
+        c[j] = d <= (int)dmask ? h[d] : 0u;
     }
 }
 
-__global__ void __launch_bounds__(kThreads)
-topk_transform_kernel(const float *logits, int64_t logits_ld, const int32_t *row_len,
-                      const int32_t *row_to_req, const int32_t *pt, int64_t pt_ld, const int32_t *req_offset,
-                      int topk, int max_row_len, int cache_cap, int32_t *indices, int64_t indices_ld,
-                      int32_t *status)
+// The whole block resolves the low 21 key bits on nc candidates whose leading
+// digit is d1, `need` of which are to be selected (two radix passes, 11 + 10
+// bits, over a kBins shared-memory histogram), then marks the selected ones:
+// key above the threshold, or equal to it and among the first `need` such in
+// candidate (position) order.  key_of(j) reads candidate j's key, mark(j) flags it.
+template <class KeyOf, class Mark>
+__device__ __forceinline__ void resolve_candidates(KeyOf key_of, Mark mark, int nc, uint32_t d1, uint32_t need1,
+                                                   uint32_t *h, uint32_t *warp_buf, uint32_t *total, uint32_t *pick)
 {
-    extern __shared__ uint32_t dyn[];
-    uint32_t *hist = dyn;                     // [kCopies][kBins]; then the selected positions
-    uint32_t *cache = dyn + kCopies * kBins;  // [cache_cap]
-    __shared__ uint32_t warp_buf[32];
-    __shared__ uint32_t total;
-    __shared__ uint32_t sel_digit, sel_need, sel_exact;
+    const int tid = threadIdx.x;
+    uint32_t prefix = d1, need = need1;
+    int S = kScoreDigitShift;
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+        const int width = pass == 0 ? 11 : 10;
+        const int shift = S - width;
+        const uint32_t dmask = (1u << width) - 1u;
+        __syncthreads();  // the candidates are written; earlier readers of h are done
+        for (int i = tid; i < kBins; i += kThreads) h[i] = 0u;
+        __syncthreads();
+        for (int j = tid; j < nc; j += kThreads) {
+            const uint32_t k = key_of(j);
+            if ((k >> S) == prefix) atomicAdd(&h[(k >> shift) & dmask], 1u);
+        }
+        __syncthreads();
+        uint32_t c[kBinsPerThread];
+        own_bins(h, c, dmask);
+        pick_digit(c, need, warp_buf, total, pick);
+        prefix = (prefix << width) | pick[0];
+        need = pick[1];
+        S = shift;
+        if (pick[2] == need) break;  // the whole bin is selected
+    }
+    const int per = (nc + kThreads - 1) / kThreads;
+    const int j0 = min(nc, tid * per), j1 = min(nc, j0 + per);
+    uint32_t ties = 0u;
+    for (int j = j0; j < j1; ++j) ties += (key_of(j) >> S) == prefix;
+    uint32_t tie_before = block_incl_scan(ties, warp_buf, total) - ties;
+    for (int j = j0; j < j1; ++j) {
+        const uint32_t kv = key_of(j) >> S;
+        bool s = kv > prefix;
+        if (kv == prefix) s = tie_before++ < need;
+        if (s) mark(j);
+    }
+    __syncthreads();
+}
 
+// ---------------------------------------------------------------- histogram pass
+// Counts of the leading digits of every row longer than topk, one CTA per chunk:
+// a shared-memory histogram of the chunk, its occupied bins added to the row's.
+__global__ void __launch_bounds__(kThreads)
+topk_hist_kernel(const float *logits, int64_t logits_ld, const int32_t *row_len, int topk, int max_row_len,
+                 uint32_t *hist)
+{
+    __shared__ uint32_t h[kBins];
     pdl_trigger();
     pdl_wait();  // the scores come from the indexer
     const int r = blockIdx.x;
     const int L = row_len[r];
-    const int b = row_to_req[r];
-    int32_t *out = indices + (int64_t)r * indices_ld;
-    // paged: the KV slot page_table_1[b, s]; ragged: s + the request's offset
-    const int32_t *ptr = pt ? pt + (int64_t)b * pt_ld : nullptr;
-    const int32_t off = req_offset ? req_offset[b] : 0;
-    auto slot_of = [&](int s) -> int32_t { return ptr ? ptr[s] : off + s; };
-    const float *lg = logits + (int64_t)r * logits_ld;
-    const int tid = threadIdx.x;
-
-    if (L < 0 || L > max_row_len) {
-        if (tid == 0) set_status(status, NSA_ERR_BOUNDS);
-        for (int i = tid; i < topk; i += kThreads) out[i] = -1;
-        return;
-    }
-    if (L <= topk) {
-        for (int i = tid; i < topk; i += kThreads) out[i] = i < L ? slot_of(i) : -1;
-        return;
-    }
-
-    const bool cached = L <= cache_cap;
-    if (cached) fill_keys<kThreads, 8>(lg, 0, L, cache);
-    auto key_at = [&](int i) -> uint32_t { return cached ? cache[i] : order_key(lg[i]); };
-
-    // radix select: find the resolution shift S, value V and count `need`
-    // such that keys with (key >> S) > V are all selected and `need` of the
-    // keys with (key >> S) == V are selected (the lowest positions).
-    uint32_t prefix = 0u, need = (uint32_t)topk;
-    int S = 32;
-    uint32_t *myhist = hist + (size_t)((tid >> 5) % kCopies) * kBins;
-#pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-        const int width = pass < 2 ? 11 : 10;
-        const int shift = S - width;
-        const uint32_t dmask = (1u << width) - 1u;
-        for (int i = tid; i < kCopies * kBins; i += kThreads) hist[i] = 0u;
-        __syncthreads();
-        auto count_key = [&](uint32_t k) {
-            if (S == 32 || (k >> S) == prefix) atomicAdd(&myhist[(k >> shift) & dmask], 1u);
-        };
-        if (cached) {  // 16-byte reads of four consecutive keys
-            for (int i4 = tid; i4 < (L >> 2); i4 += kThreads) {
-                const uint4 k = reinterpret_cast<const uint4 *>(cache)[i4];
-                count_key(k.x); count_key(k.y); count_key(k.z); count_key(k.w);
-            }
-            for (int i = (L & ~3) + tid; i < L; i += kThreads) count_key(cache[i]);
-        } else {
-            for (int i = tid; i < L; i += kThreads) count_key(key_at(i));
-        }
-        __syncthreads();
-        // thread t owns digits (2047 - 2t) and (2046 - 2t): largest digits first
-        const int d_hi = kBins - 1 - 2 * tid, d_lo = d_hi - 1;
-        uint32_t c_hi = 0u, c_lo = 0u;
-        if (d_hi <= (int)dmask) {
-#pragma unroll
-            for (int c = 0; c < kCopies; ++c) c_hi += hist[c * kBins + d_hi];
-        }
-        if (d_lo >= 0 && d_lo <= (int)dmask) {
-#pragma unroll
-            for (int c = 0; c < kCopies; ++c) c_lo += hist[c * kBins + d_lo];
-        }
-        const uint32_t incl = block_incl_scan(c_hi + c_lo, warp_buf, &total);
-        const uint32_t excl = incl - c_hi - c_lo;
-        if (excl < need && need <= incl) {
-            if (excl + c_hi >= need) {
-                sel_digit = (uint32_t)d_hi;
-                sel_need = need - excl;
-                sel_exact = (c_hi == need - excl);
-            } else {
-                sel_digit = (uint32_t)d_lo;
-                sel_need = need - excl - c_hi;
-                sel_exact = (c_lo == need - excl - c_hi);
-            }
-        }
-        __syncthreads();
-        prefix = (S == 32 ? 0u : (prefix << width)) | sel_digit;
-        need = sel_need;
-        S = shift;
-        const bool exact = sel_exact != 0u;
-        __syncthreads();
-        if (exact) break;
-    }
-
-    // ordered selection: thread t owns the C consecutive positions from t*C (C = 4 x an
-    // odd number: 16-byte reads, and the threads of a warp hit different bank groups);
-    // one block scan of (#above, #equal) places every selected position in order
-    const int C = 4 * (((L + 4 * kThreads - 1) / (4 * kThreads)) | 1);
-    const int p0 = min(L, tid * C), p1 = min(L, p0 + C);
-    uint32_t *sel = hist;  // output slot -> position (the histograms are dead)
-    auto place = [&](uint32_t n_gt, uint32_t n_eq, uint32_t &gt_before, uint32_t &eq_before) {
-        if (L < 65536) {  // both counts fit 16 bits
-            const uint32_t packed = n_gt | (n_eq << 16);
-            const uint32_t ex = block_incl_scan(packed, warp_buf, &total) - packed;
-            gt_before = ex & 0xFFFFu;
-            eq_before = ex >> 16;
-        } else {
-            gt_before = block_incl_scan(n_gt, warp_buf, &total) - n_gt;
-            eq_before = block_incl_scan(n_eq, warp_buf, &total) - n_eq;
-        }
-    };
-    auto record = [&](bool above, int pos, uint32_t &gt_before, uint32_t &eq_before) {
-        if (above) {
-            sel[gt_before + (eq_before < need ? eq_before : need)] = (uint32_t)pos;
-            ++gt_before;
-        } else {
-            if (eq_before < need) sel[gt_before + eq_before] = (uint32_t)pos;
-            ++eq_before;
-        }
-    };
-    if (cached && C <= 64) {
-        // one read of the run: its classes kept as two 64-bit masks (above, equal)
-        uint64_t mgt = 0ull, meq = 0ull;
-        for (int i = p0; i < p1; i += 4) {
-            uint32_t k[4];
-            if (i + 4 <= p1) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(cache + i);
-                k[0] = v.x; k[1] = v.y; k[2] = v.z; k[3] = v.w;
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) k[j] = i + j < p1 ? cache[i + j] : 0u;
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (i + j >= p1) continue;
-                const uint32_t v = k[j] >> S;
-                const uint64_t bit = 1ull << (i + j - p0);
-                if (v > prefix) mgt |= bit;
-                else if (v == prefix) meq |= bit;
-            }
-        }
-        uint32_t gt_before, eq_before;
-        place((uint32_t)__popcll(mgt), (uint32_t)__popcll(meq), gt_before, eq_before);
-        for (uint64_t m = mgt | meq; m; m &= m - 1) {
-            const int bit = __ffsll((long long)m) - 1;
-            record(((mgt >> bit) & 1ull) != 0ull, p0 + bit, gt_before, eq_before);
-        }
-    } else {
-        auto cls_of = [&](int i) -> uint32_t {
-            const uint32_t v = key_at(i) >> S;
-            return v > prefix ? 2u : (v == prefix ? 1u : 0u);
-        };
-        uint32_t n_gt = 0u, n_eq = 0u;
-        for (int i = p0; i < p1; ++i) {
-            const uint32_t c = cls_of(i);
-            n_gt += c == 2u;
-            n_eq += c == 1u;
-        }
-        uint32_t gt_before, eq_before;
-        place(n_gt, n_eq, gt_before, eq_before);
-        for (int i = p0; i < p1; ++i) {
-            const uint32_t c = cls_of(i);
-            if (c != 0u) record(c == 2u, i, gt_before, eq_before);
-        }
-    }
+    if (L <= topk || L > max_row_len) return;
+    const int s0 = blockIdx.y * kChunk;
+    if (s0 >= L) return;
+    const int n = min(kChunk, L - s0);
+    for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = 0u;
     __syncthreads();
-    for (int j = tid; j < topk; j += kThreads) out[j] = slot_of((int)sel[j]);
+    const float *lg = logits + (int64_t)r * logits_ld + s0;
+    for (int i = threadIdx.x; i < n; i += kThreads) atomicAdd(&h[order_key(lg[i]) >> kScoreDigitShift], 1u);
+    __syncthreads();
+    uint32_t *hrow = hist + (int64_t)r * kBins;
+    for (int i = threadIdx.x; i < kBins; i += kThreads)
+        if (h[i]) atomicAdd(&hrow[i], h[i]);
 }
 
-
-// ---------------------------------------------------------------- cluster variant
-// Long rows: a thread-block cluster of C CTAs per row, each owning a slice of
-// the row.  Histograms and selection counts are combined through distributed
-// shared memory between hardware cluster barriers (no spin-waits); every CTA
-// reaches the same decisions from the same merged data, so control flow stays
-// uniform across the cluster.
-constexpr int kCThreads = 512;
-constexpr int kCCopies = 4;
-constexpr int kCMaxCluster = 8;
-constexpr int kCSliceCap = 16 * 1024;  // keys of one slice cached in shared memory
-
-__device__ __forceinline__ uint32_t cluster_rank()
+// ---------------------------------------------------------------- whole-row selection
+// One CTA selects row r from its scores alone (up to three radix passes over
+// global memory, then one ordered pass).  Used when the histogram does not
+// describe the scores or the threshold bin holds more than kCandCap keys.
+__device__ void select_row_directly(const float *lg, int L, int topk, int32_t *out, uint32_t *h,
+                                    uint32_t *warp_buf, uint32_t *total, uint32_t *pick,
+                                    const int32_t *ptr, int32_t off)
 {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// 32-bit load from the same shared-memory variable of CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t ld_cluster(const uint32_t *local, uint32_t rank)
-{
-    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local)), ra, v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
-    return v;
-}
-
-// 16-byte load from CTA `rank` of the cluster (address 16-byte aligned).
-__device__ __forceinline__ uint4 ld_cluster4(const uint32_t *local, uint32_t rank)
-{
-    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local)), ra;
-    uint4 v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(ra)
-                 : "memory");
-    return v;
-}
-
-__global__ void __launch_bounds__(kCThreads)
-topk_cluster_kernel(const float *logits, int64_t logits_ld, const int32_t *row_len, const int32_t *row_to_req,
-                    const int32_t *pt, int64_t pt_ld, const int32_t *req_offset, int topk, int max_row_len,
-                    int32_t *indices, int64_t indices_ld, int32_t *status)
-{
-    extern __shared__ uint32_t cache[];           // [kCSliceCap] keys of this slice
-    __shared__ uint32_t hist[kCCopies * kBins];  // replicated local histogram
-    __shared__ __align__(16) uint32_t merged[kBins];  // this CTA's combined copy (read by the peers)
-    __shared__ uint32_t warp_buf[32];
-    __shared__ uint32_t total;
-    __shared__ uint32_t sel_digit, sel_need, sel_exact;
-    __shared__ uint32_t counts[2];               // (#above, #equal) in this slice
-
-    pdl_trigger();
-    pdl_wait();  // the scores come from the indexer
-    const uint32_t rank = cluster_rank();
-    uint32_t csize;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
-    const int r = blockIdx.x / (int)csize;
-    const int tid = threadIdx.x;
-    int L = row_len[r];
-    const int b = row_to_req[r];
-    int32_t *out = indices + (int64_t)r * indices_ld;
-    // paged: the KV slot page_table_1[b, s]; ragged: s + the request's offset
-    const int32_t *ptr = pt ? pt + (int64_t)b * pt_ld : nullptr;
-    const int32_t off = req_offset ? req_offset[b] : 0;
     auto slot_of = [&](int s) -> int32_t { return ptr ? ptr[s] : off + s; };
-    const float *lg = logits + (int64_t)r * logits_ld;
-
-    if (L < 0 || L > max_row_len) {  // same decision in every CTA of the cluster
-        if (rank == 0) {
-            if (tid == 0) set_status(status, NSA_ERR_BOUNDS);
-            for (int i = tid; i < topk; i += kCThreads) out[i] = -1;
-        }
-        return;
-    }
-    if (L <= topk) {
-        if (rank == 0)
-            for (int i = tid; i < topk; i += kCThreads) out[i] = i < L ? slot_of(i) : -1;
-        return;
-    }
-
-    // this CTA's slice of the row (a multiple of 4 positions)
-    const int seg = ((L + (int)csize - 1) / (int)csize + 3) & ~3;
-    const int s0 = min(L, (int)rank * seg), s1 = min(L, s0 + seg);
-    const int n = s1 - s0;
-    const bool cached = n <= kCSliceCap;
-    if (cached) fill_keys<kCThreads, 8>(lg, s0, n, cache);
-    auto key_at = [&](int i) -> uint32_t { return cached ? cache[i] : order_key(lg[s0 + i]); };
-
+    const int tid = threadIdx.x;
     uint32_t prefix = 0u, need = (uint32_t)topk;
     int S = 32;
-    uint32_t *myhist = hist + (size_t)((tid >> 5) % kCCopies) * kBins;
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
         const int width = pass < 2 ? 11 : 10;
         const int shift = S - width;
         const uint32_t dmask = (1u << width) - 1u;
-        for (int i = tid; i < kCCopies * kBins; i += kCThreads) hist[i] = 0u;
         __syncthreads();
-        for (int i = tid; i < n; i += kCThreads) {
-            const uint32_t k = key_at(i);
-            if (S == 32 || (k >> S) == prefix) atomicAdd(&myhist[(k >> shift) & dmask], 1u);
+        for (int i = tid; i < kBins; i += kThreads) h[i] = 0u;
+        __syncthreads();
+        for (int i = tid; i < L; i += kThreads) {
+            const uint32_t k = order_key(__ldcg(lg + i));
+            if (S == 32 || (k >> S) == prefix) atomicAdd(&h[(k >> shift) & dmask], 1u);
         }
         __syncthreads();
-        for (int d = tid; d < kBins; d += kCThreads) {
-            uint32_t v = 0u;
-#pragma unroll
-            for (int c = 0; c < kCCopies; ++c) v += hist[c * kBins + d];
-            merged[d] = v;
-        }
-        if (tid == 0) {  // a decision every CTA agrees on even if no bin were chosen
-            sel_digit = 0u;
-            sel_need = need;
-            sel_exact = 1u;
-        }
-        cluster_sync();  // every slice histogram is complete
-        // thread t owns digits 2047-4t .. 2044-4t (largest first); sum them over the cluster
-        const int dlo = kBins - 4 - 4 * tid;  // digits dlo .. dlo+3, one 16-byte vector
-        uint4 acc = make_uint4(0u, 0u, 0u, 0u);
-        if (dlo <= (int)dmask) {
-            for (uint32_t q = 0; q < csize; ++q) {
-                const uint4 v = ld_cluster4(&merged[dlo], q);
-                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-            }
-        }
-        const uint32_t c4[4] = {acc.w, acc.z, acc.y, acc.x};  // digit dlo+3 first
-        const uint32_t sum = acc.x + acc.y + acc.z + acc.w;
-        const uint32_t incl = block_incl_scan(sum, warp_buf, &total);
-        uint32_t excl = incl - sum;
-        if (excl < need && need <= incl) {
-            uint32_t cum = excl;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (cum + c4[j] >= need) {
-                    sel_digit = (uint32_t)(kBins - 1 - 4 * tid - j);
-                    sel_need = need - cum;
-                    sel_exact = (c4[j] == need - cum);
-                    break;
-                }
-                cum += c4[j];
-            }
-        }
-        cluster_sync();  // peers are done reading `merged`; sel_* written
-        prefix = (S == 32 ? 0u : (prefix << width)) | sel_digit;
-        need = sel_need;
+        uint32_t c[kBinsPerThread];
+        own_bins(h, c, dmask);
+        pick_digit(c, need, warp_buf, total, pick);
+        prefix = (S == 32 ? 0u : (prefix << width)) | pick[0];
+        need = pick[1];
         S = shift;
-        const bool exact = sel_exact != 0u;
-        __syncthreads();
-        if (exact) break;
+        if (pick[2] == need) break;  // the whole bin is selected
     }
-
-    // counts of this slice, then the offsets of the lower-ranked slices
-    uint32_t n_gt = 0u, n_eq = 0u;
-    for (int i = tid; i < n; i += kCThreads) {
-        const uint32_t v = key_at(i) >> S;
-        n_gt += v > prefix;
-        n_eq += v == prefix;
-    }
-    block_incl_scan(n_gt, warp_buf, &total);
-    if (tid == 0) counts[0] = total;
-    block_incl_scan(n_eq, warp_buf, &total);
-    if (tid == 0) counts[1] = total;
-    cluster_sync();
+    // ordered pass: every key above the threshold, and the first `need` equal to it
     uint32_t gt_run = 0u, eq_run = 0u;
-    for (uint32_t q = 0; q < rank; ++q) {
-        gt_run += ld_cluster(&counts[0], q);
-        eq_run += ld_cluster(&counts[1], q);
-    }
-
-    for (int base = 0; base < n; base += kCThreads * kItems) {
-        const int i0 = base + tid * kItems;
-        uint32_t cls[kItems];
-        uint32_t a_gt = 0u, a_eq = 0u;
+    for (int base = 0; base < L; base += 4 * kThreads) {
+        const int i0 = base + 4 * tid;
+        uint32_t cls[4], a_gt = 0u, a_eq = 0u;
 #pragma unroll
-        for (int j = 0; j < kItems; ++j) {
+        for (int j = 0; j < 4; ++j) {
             cls[j] = 0u;
-            if (i0 + j < n) {
-                const uint32_t v = key_at(i0 + j) >> S;
+            if (i0 + j < L) {
+                const uint32_t v = order_key(__ldcg(lg + i0 + j)) >> S;
                 cls[j] = v > prefix ? 2u : (v == prefix ? 1u : 0u);
             }
             a_gt += cls[j] == 2u;
             a_eq += cls[j] == 1u;
         }
         const uint32_t packed = a_gt | (a_eq << 16);
-        const uint32_t incl = block_incl_scan(packed, warp_buf, &total);
+        const uint32_t incl = block_incl_scan(packed, warp_buf, total);
         uint32_t gt_before = gt_run + ((incl - packed) & 0xFFFFu);
         uint32_t eq_before = eq_run + ((incl - packed) >> 16);
 #pragma unroll
-        for (int j = 0; j < kItems; ++j) {
+        for (int j = 0; j < 4; ++j) {
             if (cls[j] == 2u) {
-                out[gt_before + (eq_before < need ? eq_before : need)] = slot_of(s0 + i0 + j);
+                out[gt_before + (eq_before < need ? eq_before : need)] = slot_of(i0 + j);
                 ++gt_before;
             } else if (cls[j] == 1u) {
-                if (eq_before < need) out[gt_before + eq_before] = slot_of(s0 + i0 + j);
+                if (eq_before < need) out[gt_before + eq_before] = slot_of(i0 + j);
                 ++eq_before;
             }
         }
-        gt_run += total & 0xFFFFu;
-        eq_run += total >> 16;
+        gt_run += *total & 0xFFFFu;
+        eq_run += *total >> 16;
+        __syncthreads();  // *total is read before the next scan writes it
     }
-    cluster_sync();  // no CTA leaves while a peer may still read its shared memory
 }
 
-}  // namespace
-}  // namespace nsa
+// Keys of lg[0 .. n) into cache[0 .. n): 16-byte loads when aligned, all in flight at once.
+__device__ __forceinline__ void fill_keys(const float *lg, int n, uint32_t *cache)
+{
+    constexpr int kV = kRowCap / (4 * kThreads);  // float4 per thread for a full row
+    if ((((uintptr_t)lg) & 15) == 0) {
+        const int nv = n >> 2;
+        float4 v[kV];
+#pragma unroll
+        for (int u = 0; u < kV; ++u) {
+            const int j = u * kThreads + (int)threadIdx.x;
+            if (j < nv) v[u] = __ldg(reinterpret_cast<const float4 *>(lg) + j);
+        }
+#pragma unroll
+        for (int u = 0; u < kV; ++u) {
+            const int j = u * kThreads + (int)threadIdx.x;
+            if (j < nv)
+                reinterpret_cast<uint4 *>(cache)[j] =
+                    make_uint4(order_key(v[u].x), order_key(v[u].y), order_key(v[u].z), order_key(v[u].w));
+        }
+        for (int i = (nv << 2) + (int)threadIdx.x; i < n; i += kThreads) cache[i] = order_key(lg[i]);
+    } else {
+        for (int i = threadIdx.x; i < n; i += kThreads) cache[i] = order_key(lg[i]);
+    }
+}
 
-namespace nsa {
-namespace {
+// Output slots of the selected positions sel[0 .. topk): the page-table reads of
+// four slots per thread go out together.
+template <class SlotOf>
+__device__ __forceinline__ void write_slots(const uint32_t *sel, int topk, int32_t *out, SlotOf slot_of)
+{
+    for (int j0 = 0; j0 < topk; j0 += 4 * kThreads) {
+        int32_t s[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = j0 + u * kThreads + (int)threadIdx.x;
+            s[u] = j < topk ? slot_of((int)sel[j]) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = j0 + u * kThreads + (int)threadIdx.x;
+            if (j < topk) out[j] = s[u];
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+topk_row_kernel(const TopkArgs a)
+{
+    extern __shared__ __align__(16) uint32_t dyn[];
+    uint32_t *h1 = dyn;                 // [kBins]; then, with cand, the selected positions
+    uint32_t *cand = dyn + kBins;       // [kRowCand] positions in the threshold bin (kFlag: selected)
+    uint32_t *cache = cand + kRowCand;  // [max_row_len] keys
+    __shared__ uint32_t warp_buf[32];
+    __shared__ uint32_t total;
+    __shared__ uint32_t pick[3];
+
+    pdl_trigger();
+    pdl_wait();  // the scores (and the digit counts) come from the indexer
+    const int r = blockIdx.x, tid = threadIdx.x;
+    const int L = a.row_len[r];
+    const int b = a.row_to_req[r];
+    int32_t *out = a.indices + (int64_t)r * a.indices_ld;
+    const int32_t *ptr = a.pt ? a.pt + (int64_t)b * a.pt_ld : nullptr;
+    const int32_t off = a.req_offset ? a.req_offset[b] : 0;
+    auto slot_of = [&](int s) -> int32_t { return ptr ? ptr[s] : off + s; };
+    const float *lg = a.logits + (int64_t)r * a.logits_ld;
+
+    // the indexer's digit counts of this row (a hint), read and cleared
+    uint32_t *hrow = a.hist ? a.hist + (int64_t)r * kBins : nullptr;
+    uint32_t hc[kBinsPerThread];
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) {
+        const int d = kBins - 1 - kBinsPerThread * tid - j;
+        hc[j] = hrow ? hrow[d] : 0u;
+        if (hrow) hrow[d] = 0u;
+    }
+    if (L < 0 || L > a.max_row_len || L <= a.topk) {
+        const bool bad = L < 0 || L > a.max_row_len;
+        if (bad && tid == 0) set_status(a.status, NSA_ERR_BOUNDS);
+        for (int i = tid; i < a.topk; i += kThreads) out[i] = (!bad && i < L) ? slot_of(i) : -1;
+        return;
+    }
+    fill_keys(lg, L, cache);
+
+    const int C = 4 * (((L + 4 * kThreads - 1) / (4 * kThreads)) | 1);  // <= 36 positions a thread
+    const int p0 = min(L, tid * C), p1 = min(L, p0 + C);
+    bool have = false;
+    if (hrow) {
+        pick_digit(hc, (uint32_t)a.topk, warp_buf, &total, pick);
+        have = total == (uint32_t)L && pick[2] != kNoDigit;  // uniform: shared values
+    } else {
+        __syncthreads();  // the cached keys are complete
+    }
+    bool done = false;
+#pragma unroll 1
+    for (int attempt = 0; attempt < 2 && !done; ++attempt) {
+        if (!have) {
+            for (int i = tid; i < kBins; i += kThreads) h1[i] = 0u;
+            __syncthreads();
+            for (int i4 = tid; i4 < (L >> 2); i4 += kThreads) {
+                const uint4 k = reinterpret_cast<const uint4 *>(cache)[i4];
+                atomicAdd(&h1[k.x >> kScoreDigitShift], 1u);
+                atomicAdd(&h1[k.y >> kScoreDigitShift], 1u);
+                atomicAdd(&h1[k.z >> kScoreDigitShift], 1u);
+                atomicAdd(&h1[k.w >> kScoreDigitShift], 1u);
+            }
+            if (tid < (L & 3)) atomicAdd(&h1[cache[(L & ~3) + tid] >> kScoreDigitShift], 1u);
+            __syncthreads();
+            own_bins(h1, hc, kBins - 1);
+            pick_digit(hc, (uint32_t)a.topk, warp_buf, &total, pick);
+            have = true;
+        }
+        const uint32_t d1 = pick[0], need1 = pick[1], cnt1 = pick[2];
+        // classify my run
+        uint64_t mgt = 0ull, meq = 0ull;
+        for (int i = p0; i < p1; i += 4) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(cache + i);  // p1 - i >= 4 unless at the row's end
+            const uint32_t k[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (i + j >= p1) continue;
+                const uint32_t d = k[j] >> kScoreDigitShift;
+                const uint64_t bit = 1ull << (i + j - p0);
+                if (d > d1) mgt |= bit;
+                else if (d == d1) meq |= bit;
+            }
+        }
+        const uint32_t n_gt = (uint32_t)__popcll(mgt), n_eq = (uint32_t)__popcll(meq);
+        const uint32_t packed = n_gt | (n_eq << 16);  // L <= kRowCap: both fit 16 bits
+        const uint32_t ex = block_incl_scan(packed, warp_buf, &total) - packed;
+        const uint32_t tot_gt = total & 0xFFFFu, tot_eq = total >> 16;
+        if (cnt1 == kNoDigit || tot_gt != (uint32_t)a.topk - need1 || tot_eq != cnt1) {
+            have = false;  // the hint does not describe these scores: count them here
+            continue;
+        }
+        uint64_t msel;
+        if (tot_eq == need1) {
+            msel = mgt | meq;  // the whole bin is selected
+        } else if (tot_eq > (uint32_t)kRowCand) {
+            break;  // a crowded bin: selected from the scores directly below
+        } else {
+            const uint32_t eq_before = ex >> 16;
+            {
+                uint32_t j = eq_before;
+                for (uint64_t m = meq; m; m &= m - 1, ++j) cand[j] = (uint32_t)(p0 + __ffsll((long long)m) - 1);
+            }
+            resolve_candidates([&](int j) -> uint32_t { return cache[cand[j] & ~kFlag]; },
+                               [&](int j) { cand[j] |= kFlag; }, (int)tot_eq, d1, need1, h1, warp_buf, &total, pick);
+            uint64_t seq = 0ull;
+            {
+                uint32_t j = eq_before;
+                for (uint64_t m = meq; m; m &= m - 1, ++j)
+                    if (cand[j] & kFlag) seq |= m & (~m + 1ull);
+            }
+            msel = mgt | seq;
+        }
+        // ordered output: every selected position gets its slot in one scan
+        const uint32_t n_sel = (uint32_t)__popcll(msel);
+        uint32_t before = block_incl_scan(n_sel, warp_buf, &total) - n_sel;  // its barriers retire the reads above
+        uint32_t *sel = dyn;  // [topk] over h1 and cand
+        for (uint64_t m = msel; m; m &= m - 1) sel[before++] = (uint32_t)(p0 + __ffsll((long long)m) - 1);
+        __syncthreads();
+        write_slots(sel, a.topk, out, slot_of);
+        done = true;
+    }
+    if (!done) select_row_directly(lg, L, a.topk, out, h1, warp_buf, &total, pick, ptr, off);
+}
+
+// ---------------------------------------------------------------- chunks
+// One CTA per 4096-position chunk: the threshold digit d1 from the row's counts,
+// then every position of the chunk whose digit is above d1 (with its KV slot) or
+// equal to it (a candidate, with its key) goes to the chunk's list, in order.
+__global__ void __launch_bounds__(kThreads, 4)
+topk_chunk_kernel(const TopkArgs a)
+{
+    __shared__ uint32_t warp_buf[32];
+    __shared__ uint32_t total;
+    __shared__ uint32_t pick[3];
+    __shared__ uint32_t n_gt_s, n_eq_s;
+
+    pdl_trigger();
+    pdl_wait();  // the scores and the digit counts come from the previous kernels
+    const int r = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
+    const int L = a.row_len[r];
+    if (L < 0 || L > a.max_row_len || L <= a.topk) return;  // written by the assemble kernel
+    const int nch = (L + kChunk - 1) / kChunk;
+    if (c >= nch) return;
+    const int b = a.row_to_req[r];
+    const int32_t *ptr = a.pt ? a.pt + (int64_t)b * a.pt_ld : nullptr;
+    const int32_t off = a.req_offset ? a.req_offset[b] : 0;
+    auto slot_of = [&](int s) -> int32_t { return ptr ? ptr[s] : off + s; };
+    const float *lg = a.logits + (int64_t)r * a.logits_ld;
+    const uint32_t *hrow = a.hist + (int64_t)r * kBins;
+
+    const int s0 = c * kChunk, n = min(kChunk, L - s0);
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int i = (j >> 2) * kHalfChunk + 4 * tid + (j & 3);
+        v[j] = i < n ? lg[s0 + i] : 0.f;
+    }
+    uint32_t hc[kBinsPerThread];
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) hc[j] = hrow[kBins - 1 - kBinsPerThread * tid - j];
+    if (tid == 0) n_gt_s = n_eq_s = 0u;
+    pick_digit(hc, (uint32_t)a.topk, warp_buf, &total, pick);
+    const bool pick_ok = pick[2] != kNoDigit;
+    const uint32_t d1 = pick[0];
+
+    // classify: bit j of gt / eq for my key j (keys 0-3: first half, 4-7: second half)
+    uint32_t gt = 0u, eq = 0u, key[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int i = (j >> 2) * kHalfChunk + 4 * tid + (j & 3);
+        key[j] = order_key(v[j]);
+        if (i < n && pick_ok) {
+            const uint32_t d = key[j] >> kScoreDigitShift;
+            if (d > d1) gt |= 1u << j;
+            else if (d == d1) eq |= 1u << j;
+        }
+    }
+    const uint32_t sel = gt | eq;
+    // the KV slots of the positions selected for sure: their page-table reads go out together
+    uint32_t w1[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int i = (j >> 2) * kHalfChunk + 4 * tid + (j & 3);
+        w1[j] = ((gt >> j) & 1u) ? (uint32_t)slot_of(s0 + i) : key[j];
+    }
+    const uint32_t nA = (uint32_t)__popc(sel & 0xFu), nB = (uint32_t)__popc(sel >> 4);
+    const uint32_t packed = nA | (nB << 16);
+    const uint32_t ex = block_incl_scan(packed, warp_buf, &total) - packed;
+    const uint32_t totA = total & 0xFFFFu;
+    uint2 *list = a.lists + ((int64_t)r * a.nch_max + c) * kChunk;
+    {
+        uint32_t oA = ex & 0xFFFFu, oB = totA + (ex >> 16);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (!((sel >> j) & 1u)) continue;
+            const int i = (j >> 2) * kHalfChunk + 4 * tid + (j & 3);
+            const uint2 e = make_uint2((uint32_t)(s0 + i) | (((eq >> j) & 1u) ? kFlag : 0u), w1[j]);
+            if (j < 4) list[oA++] = e;
+            else list[oB++] = e;
+        }
+    }
+    {
+        uint32_t g = (uint32_t)__popc(gt), q = (uint32_t)__popc(eq);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            g += __shfl_xor_sync(0xffffffffu, g, o);
+            q += __shfl_xor_sync(0xffffffffu, q, o);
+        }
+        if ((tid & 31) == 0 && (g | q)) {
+            atomicAdd(&n_gt_s, g);
+            atomicAdd(&n_eq_s, q);
+        }
+    }
+    __syncthreads();
+    if (tid == 0) a.counts[(int64_t)r * a.nch_max + c] = n_gt_s | (n_eq_s << 16);
+}
+
+// ---------------------------------------------------------------- assemble
+// One CTA per row: checks the chunks' counts against the digit counts, resolves
+// the threshold bin on the candidates (one warp), and writes the ordered output
+// from one scan over the concatenated lists, each thread holding its run of
+// entries in registers.  Rows of at most topk positions are written here too.
+__global__ void __launch_bounds__(kThreads, 1)
+topk_assemble_kernel(const TopkArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    ChunkSmem &sm = *reinterpret_cast<ChunkSmem *>(smem_raw);
+    __shared__ uint32_t warp_buf[32];
+    __shared__ uint32_t total;
+    __shared__ uint32_t pick[3];
+
+    pdl_trigger();
+    pdl_wait();  // the chunk lists come from the previous kernel
+    const int r = blockIdx.x, tid = threadIdx.x;
+    const int L = a.row_len[r];
+    const int b = a.row_to_req[r];
+    int32_t *out = a.indices + (int64_t)r * a.indices_ld;
+    const int32_t *ptr = a.pt ? a.pt + (int64_t)b * a.pt_ld : nullptr;
+    const int32_t off = a.req_offset ? a.req_offset[b] : 0;
+    auto slot_of = [&](int s) -> int32_t { return ptr ? ptr[s] : off + s; };
+    const float *lg = a.logits + (int64_t)r * a.logits_ld;
+
+    // the row's digit counts, read and cleared for the next call
+    uint32_t *hrow = a.hist + (int64_t)r * kBins;
+    uint32_t hc[kBinsPerThread];
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) {
+        const int d = kBins - 1 - kBinsPerThread * tid - j;
+        hc[j] = hrow[d];
+        hrow[d] = 0u;
+    }
+    if (L < 0 || L > a.max_row_len || L <= a.topk) {
+        const bool bad = L < 0 || L > a.max_row_len;
+        if (bad && tid == 0) set_status(a.status, NSA_ERR_BOUNDS);
+        for (int i = tid; i < a.topk; i += kThreads) out[i] = (!bad && i < L) ? slot_of(i) : -1;
+        return;
+    }
+    const int nch = (L + kChunk - 1) / kChunk;
+    uint32_t cg = 0u, cq = 0u;
+    if (tid < nch) {
+        const uint32_t w = a.counts[(int64_t)r * a.nch_max + tid];
+        cg = w & 0xFFFFu;
+        cq = w >> 16;
+    }
+    pick_digit(hc, (uint32_t)a.topk, warp_buf, &total, pick);
+    const bool pick_ok = pick[2] != kNoDigit;
+    const uint32_t d1 = pick[0], need1 = pick[1], cnt1 = pick[2];
+    // chunk offsets of the concatenated lists (chunk t's list after those of chunks < t)
+    const uint32_t incl_len = block_incl_scan(cg + cq, warp_buf, &total);
+    if (tid < nch) sm.chunk_off[tid] = incl_len - cg - cq;
+    const uint32_t list_len = total;
+    if (tid == 0) sm.chunk_off[nch] = list_len;
+    block_incl_scan(cq, warp_buf, &total);
+    const uint32_t tot_eq = total, tot_gt = list_len - tot_eq;
+    const bool counts_ok = pick_ok && tot_gt == (uint32_t)a.topk - need1 && tot_eq == cnt1;
+    if (!counts_ok || (tot_eq != need1 && tot_eq > (uint32_t)kCandCap)) {
+        select_row_directly(lg, L, a.topk, out, sm.hist, warp_buf, &total, pick, ptr, off);
+        return;
+    }
+    // my contiguous run [i0, i1) of the concatenated list, in registers
+    const uint32_t per = (list_len + kThreads - 1) / kThreads;  // <= kRun: list_len <= topk + kCandCap
+    const uint32_t i0 = min(list_len, (uint32_t)tid * per), i1 = min(list_len, i0 + per);
+    uint2 e[kRun];
+    {
+        int lo_c = 0, hi_c = nch - 1;  // the last chunk whose offset is <= i0
+        while (lo_c < hi_c) {
+            const int mid = (lo_c + hi_c + 1) >> 1;
+            if (sm.chunk_off[mid] <= i0) lo_c = mid;
+            else hi_c = mid - 1;
+        }
+        int chc = lo_c;
+        const uint2 *lists_r = a.lists + (int64_t)r * a.nch_max * kChunk;
+#pragma unroll
+        for (int u = 0; u < kRun; ++u) {
+            const uint32_t k = i0 + (uint32_t)u;
+            e[u] = make_uint2(0u, 0u);
+            if (k < i1) {
+                while (k >= sm.chunk_off[chc + 1]) ++chc;
+                e[u] = lists_r[(int64_t)chc * kChunk + (k - sm.chunk_off[chc])];
+            }
+        }
+    }
+    const int cnt = (int)(i1 - i0);
+    if (tot_eq == need1) {
+        // the whole threshold bin is selected: the lists are the output, in order
+        int32_t v[kRun];
+#pragma unroll
+        for (int u = 0; u < kRun; ++u)
+            v[u] = u < cnt ? ((e[u].x & kFlag) ? slot_of((int)(e[u].x & ~kFlag)) : (int32_t)e[u].y) : 0;
+#pragma unroll
+        for (int u = 0; u < kRun; ++u)
+            if (u < cnt) out[i0 + u] = v[u];
+        return;
+    }
+    // candidates, compacted in position order with their keys
+    uint32_t nf = 0u;
+#pragma unroll
+    for (int u = 0; u < kRun; ++u) nf += (u < cnt) ? (e[u].x >> 31) : 0u;
+    const uint32_t my_first = block_incl_scan(nf, warp_buf, &total) - nf;
+    {
+        uint32_t cb = my_first;
+#pragma unroll
+        for (int u = 0; u < kRun; ++u) {
+            if (u < cnt && (e[u].x & kFlag)) {
+                sm.cand_pos[cb] = e[u].x & ~kFlag;
+                sm.cand_key[cb] = e[u].y;
+                ++cb;
+            }
+        }
+    }
+    resolve_candidates([&](int j) -> uint32_t { return sm.cand_key[j]; }, [&](int j) { sm.cand_pos[j] |= kFlag; },
+                       (int)tot_eq, d1, need1, sm.hist, warp_buf, &total, pick);
+    // ordered output: above-d1 entries, and the selected candidates
+    bool s[kRun];
+    uint32_t nsel = 0u;
+    {
+        uint32_t cj = my_first;
+#pragma unroll
+        for (int u = 0; u < kRun; ++u) {
+            s[u] = u < cnt;
+            if (s[u] && (e[u].x & kFlag)) s[u] = (sm.cand_pos[cj++] >> 31) != 0u;
+            nsel += s[u];
+        }
+    }
+    uint32_t o = block_incl_scan(nsel, warp_buf, &total) - nsel;
+    int32_t v[kRun];
+#pragma unroll
+    for (int u = 0; u < kRun; ++u)
+        v[u] = s[u] ? ((e[u].x & kFlag) ? slot_of((int)(e[u].x & ~kFlag)) : (int32_t)e[u].y) : 0;
+#pragma unroll
+    for (int u = 0; u < kRun; ++u)
+        if (s[u]) out[o++] = v[u];
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct WsLayout {
+    size_t hist, counts, lists, bytes;
+};
+
+// Workspace of the chunked path: the digit counts [R][kBins] when the caller gives
+// none, per-chunk counts [R][nch] and lists [R][nch * kChunk] of (position, slot|key).
+WsLayout ws_layout(int R, int max_row_len, bool own_hist)
+{
+    const int64_t nch = std::max<int64_t>(1, ceil_div(max_row_len, kChunk));
+    WsLayout w;
+    w.hist = 0;
+    w.counts = own_hist ? align256((size_t)R * kBins * sizeof(uint32_t)) : 0;
+    w.lists = w.counts + align256((size_t)R * nch * sizeof(uint32_t));
+    w.bytes = w.lists + align256((size_t)R * nch * kChunk * sizeof(uint2));
+    return w;
+}
 
 nsa_status topk_launch(const float *logits_dev, int64_t logits_ld, const int32_t *row_len_dev,
                        const int32_t *row_to_req_dev, const int32_t *page_table_1_dev, int64_t pt_ld,
                        const int32_t *req_offset_dev, int R, int topk, int max_row_len, int32_t *indices_dev,
-                       int64_t indices_ld, int32_t *status_dev, nsa_stream_t stream)
+                       int64_t indices_ld, uint32_t *score_hist_dev, void *ws, size_t ws_bytes, int32_t *status_dev,
+                       nsa_stream_t stream)
 {
-    using namespace nsa;
     if (R < 0 || topk < 1 || topk > 4096 || max_row_len < 0) return NSA_ERR_INVALID_ARG;
     if (indices_ld < topk || logits_ld < max_row_len || (page_table_1_dev && pt_ld < max_row_len))
         return NSA_ERR_INVALID_ARG;
+    if (ceil_div(max_row_len, kChunk) > kMaxChunks) return NSA_ERR_UNSUPPORTED;
     if (R == 0) return NSA_OK;
     if (!logits_dev || !row_len_dev || !row_to_req_dev || !indices_dev || (!page_table_1_dev && !req_offset_dev))
         return NSA_ERR_INVALID_ARG;
-    // rows beyond the single-block key cache: one cluster of up to 8 CTAs per row
-    const int csize = max_row_len > kCacheCap ? (int)std::min<int64_t>(kCMaxCluster, ceil_div(max_row_len, kCSliceCap)) : 1;
-    if (csize > 1 && (int64_t)R * csize <= 2147483647LL) {
-        NSA_CUDA_TRY(cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)(kCSliceCap * sizeof(uint32_t))));
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(R * csize));
-        cfg.blockDim = dim3(kCThreads);
-        cfg.dynamicSmemBytes = kCSliceCap * sizeof(uint32_t);
-        cfg.stream = (cudaStream_t)stream;
-        cudaLaunchAttribute attr[2];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)csize;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        attr[1] = pdl_attribute();
-        cfg.attrs = attr;
-        cfg.numAttrs = 2;
-        NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, topk_cluster_kernel, logits_dev, logits_ld, row_len_dev,
-                                        row_to_req_dev, page_table_1_dev, pt_ld, req_offset_dev, topk, max_row_len,
-                                        indices_dev, indices_ld, status_dev));
-        return NSA_OK;
-    }
-    const int cap = max_row_len > topk ? (max_row_len < kCacheCap ? max_row_len : kCacheCap) : 0;
-    const size_t smem = row_kernel_smem_bytes(cap);
-    NSA_CUDA_TRY(cudaFuncSetAttribute(topk_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem));
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)R);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = (cudaStream_t)stream;
+    const int nch = (int)std::max<int64_t>(1, ceil_div(max_row_len, kChunk));
+    TopkArgs a;
+    a.logits = logits_dev; a.logits_ld = logits_ld; a.row_len = row_len_dev; a.row_to_req = row_to_req_dev;
+    a.pt = page_table_1_dev; a.pt_ld = pt_ld; a.req_offset = req_offset_dev;
+    a.topk = topk; a.max_row_len = max_row_len; a.nch_max = nch;
+    a.indices = indices_dev; a.indices_ld = indices_ld;
+    a.hist = score_hist_dev;
+    a.counts = nullptr; a.lists = nullptr;
+    a.status = status_dev;
+
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = (cudaStream_t)stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, topk_transform_kernel, logits_dev, logits_ld, row_len_dev, row_to_req_dev,
-                                    page_table_1_dev, pt_ld, req_offset_dev, topk, max_row_len, cap, indices_dev,
-                                    indices_ld, status_dev));
+    if (max_row_len <= kRowCap) {
+        // one CTA per row, the row cached whole (no workspace)
+        const size_t smem = (size_t)(kBins + kRowCand + ((max_row_len + 3) & ~3)) * sizeof(uint32_t);
+        NSA_CUDA_TRY(cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        cfg.gridDim = dim3((unsigned)R);
+        cfg.dynamicSmemBytes = smem;
+        NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, topk_row_kernel, a));
+        return NSA_OK;
+    }
+    const bool own_hist = score_hist_dev == nullptr;
+    const WsLayout w = ws_layout(R, max_row_len, own_hist);
+    if (!ws || ws_bytes < w.bytes || ((uintptr_t)ws & 255)) return NSA_ERR_INVALID_ARG;
+    uint8_t *base = (uint8_t *)ws;
+    if (own_hist) a.hist = (uint32_t *)(base + w.hist);
+    a.counts = (uint32_t *)(base + w.counts);
+    a.lists = (uint2 *)(base + w.lists);
+    cfg.gridDim = dim3((unsigned)R, (unsigned)nch);
+    cfg.dynamicSmemBytes = 0;
+    if (own_hist)
+        NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, topk_hist_kernel, logits_dev, logits_ld, row_len_dev, topk, max_row_len,
+                                        a.hist));
+    NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, topk_chunk_kernel, a));
+    NSA_CUDA_TRY(cudaFuncSetAttribute(topk_assemble_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)sizeof(ChunkSmem)));
+    cfg.gridDim = dim3((unsigned)R);
+    cfg.dynamicSmemBytes = sizeof(ChunkSmem);
+    NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, topk_assemble_kernel, a));
     return NSA_OK;
 }
 
 }  // namespace
 }  // namespace nsa
 
+extern "C" size_t nsa_topk_workspace_bytes(int R, int max_row_len, int with_score_hist)
+{
+    if (R <= 0 || max_row_len <= nsa::kRowCap) return 0;
+    return nsa::ws_layout(R, max_row_len, with_score_hist == 0).bytes;
+}
+
 extern "C" nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits_ld,
                                          const int32_t *row_len_dev, const int32_t *row_to_req_dev,
                                          const int32_t *page_table_1_dev, int64_t pt_ld, int R,
                                          int topk, int max_row_len, int32_t *indices_dev,
-                                         int64_t indices_ld, int32_t *status_dev, nsa_stream_t stream)
+                                         int64_t indices_ld, uint32_t *score_hist_dev, void *ws, size_t ws_bytes,
+                                         int32_t *status_dev, nsa_stream_t stream)
 {
     if (!page_table_1_dev && R > 0) return NSA_ERR_INVALID_ARG;
     return nsa::topk_launch(logits_dev, logits_ld, row_len_dev, row_to_req_dev, page_table_1_dev, pt_ld, nullptr, R,
-                            topk, max_row_len, indices_dev, indices_ld, status_dev, stream);
+                            topk, max_row_len, indices_dev, indices_ld, score_hist_dev, ws, ws_bytes, status_dev,
+                            stream);
 }
 
 extern "C" nsa_status nsa_topk_transform_ragged(const float *logits_dev, int64_t logits_ld,
                                                 const int32_t *row_len_dev, const int32_t *row_to_req_dev,
                                                 const int32_t *req_offset_dev, int R, int topk, int max_row_len,
-                                                int32_t *indices_dev, int64_t indices_ld, int32_t *status_dev,
-                                                nsa_stream_t stream)
+                                                int32_t *indices_dev, int64_t indices_ld, uint32_t *score_hist_dev,
+                                                void *ws, size_t ws_bytes, int32_t *status_dev, nsa_stream_t stream)
 {
     if (!req_offset_dev && R > 0) return NSA_ERR_INVALID_ARG;
     return nsa::topk_launch(logits_dev, logits_ld, row_len_dev, row_to_req_dev, nullptr, 0, req_offset_dev, R, topk,
-                            max_row_len, indices_dev, indices_ld, status_dev, stream);
+                            max_row_len, indices_dev, indices_ld, score_hist_dev, ws, ws_bytes, status_dev, stream);
 }

@@ -13,8 +13,9 @@ from typing import Optional
 import numpy as np
 import torch
 
-from . import (DT_BF16, DT_E4M3, DT_F32, MODE_EXTEND, alloc_metadata, nsa_indexer_logits, nsa_metadata,
-               nsa_sparse_mla, nsa_sparse_mla_workspace_bytes, nsa_status_read, nsa_topk_transform)
+from . import (DT_BF16, DT_E4M3, DT_F32, MODE_DECODE, MODE_EXTEND, alloc_metadata, alloc_score_hist,
+               alloc_topk_workspace, nsa_indexer_logits, nsa_metadata, nsa_sparse_mla, nsa_sparse_mla_workspace_bytes,
+               nsa_status_read, nsa_topk_transform)
 
 
 def _dev(a: np.ndarray, device, dtype=None) -> torch.Tensor:
@@ -35,7 +36,12 @@ class SparseAttentionStep:
       kv [slots, row] (bf16 bits / e4m3 row bytes / float32), sm_scale.
     """
 
-    def __init__(self, host, device="cuda"):
+    def __init__(self, host, device="cuda", fuse_topk: Optional[bool] = None):
+        """fuse_topk: the indexer counts each row's leading score digits for the top-k
+        (the indexer-to-top-k fusion); False: the top-k counts them in a pass of its
+        own.  Default: fused for decode (one row per request), where the indexer's
+        epilogue has room for it; unfused for extend / verify, where its epilogue
+        already handles several rows per key tile and the separate pass is cheaper."""
         self.h = host
         self.device = torch.device(device)
         d = self.device
@@ -63,6 +69,10 @@ class SparseAttentionStep:
         self.logits_ld = max(4, (self.W + 3) // 4 * 4)
         self.logits = torch.empty((self.R, self.logits_ld), dtype=torch.float32, device=d)
         self.indices = torch.empty((self.R, self.topk), dtype=torch.int32, device=d)
+        if fuse_topk is None:
+            fuse_topk = self.mode == MODE_DECODE
+        self.score_hist = alloc_score_hist(self.R, d) if fuse_topk else None
+        self.topk_ws = alloc_topk_workspace(self.R, self.W, fuse_topk, d)
         odt = torch.bfloat16 if self.q_dtype == DT_BF16 else torch.float32
         self.out = torch.empty((self.R, self.H, self.d_latent), dtype=odt, device=d)
         self.lse = torch.empty((self.R, self.H), dtype=torch.float32, device=d)
@@ -73,23 +83,27 @@ class SparseAttentionStep:
 
     # ---------------------------------------------------------- stages
     def metadata(self, stream=None, seq_lens: Optional[torch.Tensor] = None,
-                 req_pool_indices: Optional[torch.Tensor] = None):
-        """seq_lens / req_pool_indices default to the step's device copies; pinned host
-        tensors (mapped into the device's address space) are read directly."""
+                 req_pool_indices: Optional[torch.Tensor] = None, extend_lens: Optional[torch.Tensor] = None):
+        """seq_lens / req_pool_indices / extend_lens default to the step's device copies;
+        pinned host tensors (mapped into the device's address space) are read directly."""
         nsa_metadata(self.mode, self.B, self.R, self.W, self.n_draft, self.topk, self.ps,
-                     self.seq_lens if seq_lens is None else seq_lens, self.extend_lens, self.req_to_token,
+                     self.seq_lens if seq_lens is None else seq_lens,
+                     self.extend_lens if extend_lens is None else extend_lens, self.req_to_token,
                      self.req_pool_indices if req_pool_indices is None else req_pool_indices, self.md,
                      self.status, stream)
 
     def indexer(self, stream=None):
         nsa_indexer_logits(self.idx_dtype, self.q_idx, self.weights, self.k_cache, self.k_scale,
                            self.md["real_page_table"], self.md["row_to_req"], self.md["seqlens_expanded"],
-                           self.W, self.logits, self.status, stream, rows_per_group=self.rows_per_group)
+                           self.W, self.logits, self.status, stream, rows_per_group=self.rows_per_group,
+                           score_hist=self.score_hist)
 
     def topk_transform(self, stream=None, logits: Optional[torch.Tensor] = None):
+        """With other `logits` than the indexer's the histogram does not describe them:
+        the top-k then counts the digits itself (and still clears the buffer)."""
         nsa_topk_transform(self.logits if logits is None else logits, self.md["seqlens_expanded"],
                            self.md["row_to_req"], self.md["page_table_1"], self.topk, self.W, self.indices,
-                           self.status, stream)
+                           self.status, stream, score_hist=self.score_hist, workspace=self.topk_ws)
 
     def attention(self, stream=None, indices: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                   lse: Optional[torch.Tensor] = None):

@@ -198,6 +198,16 @@ nsa_status nsa_local_virtual_batches(int attn_chunk_size, int page_size, int B,
  *                      requests are handled separately, so any value is correct.
  *   max_row_len        host-known upper bound of row_len (sizes the grid)
  *   logits_dev         [R, logits_ld] float32, logits_ld >= max_row_len
+ *   score_hist_dev     optional (NULL: none) [R, 2048] uint32, caller-owned: the
+ *                      call adds, for every logit it writes, 1 to bin
+ *                      key >> 21 of its row, where key is the score's order-
+ *                      preserving 32-bit key (the top-k's first 11-bit radix
+ *                      digit; see nsa_topk_transform).  Allocate it zeroed once;
+ *                      nsa_topk_transform given the same buffer clears every row it
+ *                      reads, so the next step starts from zero.  This is the
+ *                      indexer-to-top-k fusion of the pages' fused top-k switch
+ *                      ([DSA] SGLANG_DSA_FUSE_TOPK / the top-k v2 plan): the top-k
+ *                      starts from these counts instead of a pass over the scores.
  * Supported: Hi*Di <= 8192, Di % 16 == 0.  e4m3 with Hi == 64, Di == 128 and
  * page_size % 64 == 0 runs on the tensor cores (tcgen05, fp8); every other
  * shape runs on the CUDA cores.
@@ -212,8 +222,8 @@ nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, const float *w
                               int page_size, int Hi, int Di, const int32_t *real_page_table_dev,
                               int64_t rpt_ld, const int32_t *row_to_req_dev,
                               const int32_t *row_len_dev, int R, int rows_per_group, int max_row_len,
-                              float *logits_dev, int64_t logits_ld, int32_t *status_dev,
-                              nsa_stream_t stream);
+                              float *logits_dev, int64_t logits_ld, uint32_t *score_hist_dev,
+                              int32_t *status_dev, nsa_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* nsa_topk_transform                                                       */
@@ -223,7 +233,8 @@ nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, const float *w
  * Per-row top-k of the indexer scores, transformed to KV slots
  * ([NSA] NSAIndexerMetadata.topk_transform, fused variant that "returns a
  * transformed page table directly"; [DSA] transform_index_page_table_decode /
- * _prefill with page size 1 and _pad_topk_indices):
+ * _prefill with page size 1 and _pad_topk_indices; rows split over several
+ * CTAs as in [DSA]'s top-k v2 plan):
  *   row r with L = row_len[r]:
  *     L <= topk : every position 0..L-1
  *     L >  topk : the topk positions with the largest logits; equal logits
@@ -234,17 +245,41 @@ nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, const float *w
  *   logits_dev       [R, logits_ld] float32 (only s < row_len[r] is read)
  *   row_len_dev      [R] (seqlens_expanded), row_to_req_dev [R]
  *   page_table_1_dev [*, pt_ld] token slots per request (from nsa_metadata)
- *   max_row_len      host-known upper bound of row_len
+ *   max_row_len      host-known upper bound of row_len (at most 2,097,152)
  *   indices_dev      [R, indices_ld] int32, indices_ld >= topk
+ *   score_hist_dev   optional (NULL: none) [R, 2048] uint32 digit counts from
+ *                    nsa_indexer_logits (its score_hist_dev).  The counts are a
+ *                    hint: a row whose counts disagree with its scores (the
+ *                    numbers of keys above and in the chosen digit) is selected
+ *                    from the scores directly, so the indices never depend on the
+ *                    buffer's contents.  Every row r < R is left zero.  NULL: the
+ *                    call counts the digits itself (one more kernel) into ws.
+ *   ws, ws_bytes     caller-owned device workspace of at least
+ *                    nsa_topk_workspace_bytes(R, max_row_len, score_hist_dev != NULL)
+ *                    bytes, 256-byte aligned (0 bytes, and ws may be NULL, when
+ *                    max_row_len <= 16384: those rows are selected one CTA per row
+ *                    in shared memory).  Longer rows go through per-chunk lists in
+ *                    ws.  Without score_hist_dev the workspace also holds the call's
+ *                    own digit counts, which must be ZERO before the first call;
+ *                    every call leaves them zero again.  A workspace serves calls of
+ *                    one (R, max_row_len, with/without score_hist) shape; zero it
+ *                    again before using it for another.  Calls sharing a workspace
+ *                    or a score_hist buffer must not overlap on the GPU.
  * Supported: 1 <= topk <= 4096.
- * Device errors: row_len[r] > max_row_len sets NSA_ERR_BOUNDS and that row is
- * written as all -1.  Not checked on the device (nsa_metadata's arrays always
- * satisfy it): row_to_req[r] names a row of page_table_1.
+ * Device errors: row_len[r] < 0 or > max_row_len sets NSA_ERR_BOUNDS and that
+ * row is written as all -1.  Not checked on the device (nsa_metadata's arrays
+ * always satisfy it): row_to_req[r] names a row of page_table_1.
  */
 nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits_ld, const int32_t *row_len_dev,
                               const int32_t *row_to_req_dev, const int32_t *page_table_1_dev,
                               int64_t pt_ld, int R, int topk, int max_row_len, int32_t *indices_dev,
-                              int64_t indices_ld, int32_t *status_dev, nsa_stream_t stream);
+                              int64_t indices_ld, uint32_t *score_hist_dev, void *ws, size_t ws_bytes,
+                              int32_t *status_dev, nsa_stream_t stream);
+
+/* Workspace bytes nsa_topk_transform / nsa_topk_transform_ragged need for R rows
+ * of at most max_row_len scores; with_score_hist != 0 when the caller passes the
+ * indexer's digit counts (the workspace then holds none of its own).  0 for R <= 0. */
+size_t nsa_topk_workspace_bytes(int R, int max_row_len, int with_score_hist);
 
 /* ------------------------------------------------------------------------ */
 /* nsa_sparse_mla                                                           */
@@ -337,14 +372,15 @@ nsa_status nsa_copy_buffers(int n, const void *const *src, void *const *dst, con
  * (topk_indices_offset = repeat_interleave(cu_seqlens_k[:-1], extend_lens)).
  * ------------------------------------------------------------------------ */
 
-/* As nsa_topk_transform, but row r's selected positions s become
+/* As nsa_topk_transform (same workspace), but row r's selected positions s become
  * s + req_offset_dev[row_to_req[r]] instead of page-table slots (-1 padding
  * kept).  req_offset_dev is typically the metadata's cu_seqlens_k; the sums
  * must fit int32. */
 nsa_status nsa_topk_transform_ragged(const float *logits_dev, int64_t logits_ld, const int32_t *row_len_dev,
                                      const int32_t *row_to_req_dev, const int32_t *req_offset_dev, int R,
                                      int topk, int max_row_len, int32_t *indices_dev, int64_t indices_ld,
-                                     int32_t *status_dev, nsa_stream_t stream);
+                                     uint32_t *score_hist_dev, void *ws, size_t ws_bytes, int32_t *status_dev,
+                                     nsa_stream_t stream);
 
 /* page_table_1_flattened: out_dev[kv_start_dev[b] + t] = page_table_1_dev[b *
  * pt_ld + t] for t < kv_len_dev[b] (typically cache_seqlens and cu_seqlens_k of

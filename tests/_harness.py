@@ -62,6 +62,31 @@ def check_attention(out_g: np.ndarray, lse_g: np.ndarray, out_o: np.ndarray, lse
     assert not bad.any(), f"lse: {bad.sum()} beyond tol, max err {np.abs(lse_g[fin] - lse_o[fin]).max():.3e}"
 
 
+def host_digit_hist(lg_rows: np.ndarray, lens) -> np.ndarray:
+    """Per row, counts of the leading 11 bits of each score's order-preserving
+    32-bit key (NaN lowest, -0 == +0, negative scores bit-reversed below the
+    positive ones): the digit histogram nsa_indexer_logits accumulates."""
+    out = np.zeros((len(lens), 2048), np.int64)
+    for i, L in enumerate(lens):
+        x = np.ascontiguousarray(lg_rows[i, :L], dtype=np.float32)
+        u = x.view(np.uint32).astype(np.uint64)
+        key = np.where(u & 0x80000000, (~u) & 0xFFFFFFFF, u | 0x80000000)
+        key = np.where(((u << 1) & 0xFFFFFFFF) == 0, 0x80000000, key)
+        key = np.where(np.isnan(x), 0, key)
+        out[i] = np.bincount((key >> 21).astype(np.int64), minlength=2048)
+    return out
+
+
+def check_digit_hist(step, rows, lg_rows: np.ndarray, lens):
+    """The indexer's digit counts equal those of the logits it wrote."""
+    if getattr(step, "score_hist", None) is None:
+        return
+    hg = step.score_hist.cpu().numpy().view(np.uint32)[rows].astype(np.int64)
+    exp = host_digit_hist(lg_rows, lens)
+    bad = np.nonzero((hg != exp).any(axis=1))[0]
+    assert len(bad) == 0, f"indexer digit counts differ from its logits in rows {[rows[i] for i in bad[:5]]}"
+
+
 def out_to_np(t: torch.Tensor) -> np.ndarray:
     return t.float().cpu().numpy()
 
@@ -75,10 +100,13 @@ def sample_rows(wl, n: int, seed: int = 0) -> list:
     return sorted(set([0, wl.R - 1] + [int(x) for x in mid]))
 
 
-def full_parity(step, wl, rows: Optional[Sequence[int]] = None, e2e: bool = True):
+def full_parity(step, wl, rows: Optional[Sequence[int]] = None, e2e: bool = True,
+                e2e_topk_rows: Optional[Sequence[int]] = None):
     """Stage-by-stage parity on `rows` (all rows by default) plus the end-to-end
-    check.  Returns nothing; asserts on any mismatch."""
+    check; the end-to-end top-k check (GPU indices == exact top-k of the GPU
+    logits) runs on `e2e_topk_rows` (default: `rows`).  Asserts on any mismatch."""
     rows = list(range(wl.R)) if rows is None else list(rows)
+    e2e_topk_rows = rows if e2e_topk_rows is None else list(e2e_topk_rows)
     md_o = oracle_metadata(wl)
     step.metadata()
     torch.cuda.synchronize()
@@ -93,6 +121,7 @@ def full_parity(step, wl, rows: Optional[Sequence[int]] = None, e2e: bool = True
                                rows=rows, width=wl.W)
     lg = step.logits.cpu().numpy()[rows]
     check_logits(lg, lo, lens)
+    check_digit_hist(step, rows, lg, lens)
 
     # top-k fed the oracle's logits (bit-exact)
     feed = torch.full_like(step.logits, float("nan"))
@@ -120,12 +149,19 @@ def full_parity(step, wl, rows: Optional[Sequence[int]] = None, e2e: bool = True
         # the GPU's logits, and attention over them must match the oracle.
         step.run()
         torch.cuda.synchronize()
-        lg = step.logits.cpu().numpy()[rows]
+        lg_all = step.logits.cpu().numpy()
+        lg = lg_all[rows]
         check_logits(lg, lo, lens)
-        ig = step.indices.cpu().numpy()[rows]
-        io2 = oracle.topk_transform(lg, md_o["seqlens_expanded"], md_o["row_to_req"], md_o["page_table_1"],
-                                    wl.topk, rows=rows, logits_rows_are_subset=True)
-        assert np.array_equal(ig, io2), "end-to-end indices are not the top-k of the GPU logits"
+        ig_all = step.indices.cpu().numpy()
+        lg_t = lg_all[e2e_topk_rows]
+        io2 = oracle.topk_transform(lg_t, md_o["seqlens_expanded"], md_o["row_to_req"], md_o["page_table_1"],
+                                    wl.topk, rows=e2e_topk_rows, logits_rows_are_subset=True)
+        bad = np.nonzero((ig_all[e2e_topk_rows] != io2).any(axis=1))[0]
+        assert len(bad) == 0, (f"end-to-end indices are not the top-k of the GPU logits in rows "
+                               f"{[e2e_topk_rows[i] for i in bad[:5]]}")
+        if getattr(step, "score_hist", None) is not None:
+            assert not step.score_hist.any().item(), "the top-k left digit counts behind"
+        ig = ig_all[rows]
         oo2, lso2 = oracle.sparse_mla(wl.q_dtype, wl.kv_dtype, wl.q_nope, wl.q_rope, wl.kv, ig, wl.sm_scale,
                                       rows=rows, indices_rows_are_subset=True)
         check_attention(out_to_np(step.out)[rows], step.lse.cpu().numpy()[rows], oo2, lso2, attn_tol(wl))

@@ -66,12 +66,27 @@ def test_small_case_all_rows(case):
     H.full_parity(step, wl, rows=rows)
 
 
-@pytest.mark.parametrize("name,nrows", [("v32_decode_bf16", 3), ("fp8kv_decode_h16", 3),
-                                        ("chunked_extend", 3), ("verify_long_fp8kv", 3)])
+@pytest.mark.parametrize("case", ["decode_bf16_ragged", "decode_fp8kv_h16", "extend_bf16", "verify_fp8kv",
+                                  "decode_small_heads_ps16"])
+def test_small_case_other_topk_path(case):
+    """The top-k path each mode does not take by default: decode with the top-k
+    counting the digits itself, extend / verify with the indexer counting them."""
+    from deepseek_sparse_mla_indexer_gb300.step import SparseAttentionStep
+    wl = SMALL[case]()
+    step = SparseAttentionStep(wl, "cuda", fuse_topk=wl.mode != W.MODE_DECODE)
+    rows = None if wl.R <= 8 else H.sample_rows(wl, 8, seed=3)
+    H.full_parity(step, wl, rows=rows)
+
+
+@pytest.mark.parametrize("name,nrows", [("v32_decode_bf16", 8), ("fp8kv_decode_h16", 6),
+                                        ("chunked_extend", 4), ("verify_long_fp8kv", 4)])
 def test_named_workload_full_size_sampled(name, nrows):
+    """Every stage on sampled rows (the first and last rows among them; each row
+    covers all its heads and every split of its top-k list), and the end-to-end
+    top-k (GPU indices == the exact top-k of the GPU logits) on every row."""
     wl = W.config(name)
     step = _step(wl)
-    H.full_parity(step, wl, rows=H.sample_rows(wl, nrows, seed=2))
+    H.full_parity(step, wl, rows=H.sample_rows(wl, nrows, seed=2), e2e_topk_rows=list(range(wl.R)))
 
 
 def test_empty_batch_is_a_no_op():
