@@ -393,7 +393,11 @@ def nsa_local_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
     assert k_cache.is_contiguous() and v_cache.is_contiguous() and block_table.stride(1) == 1
     assert out.is_contiguous() and lse.is_contiguous()
     nvb = seqused_k.shape[0]
-    bt_ld = _ld(block_table)  # the row stride, which is also the row's capacity
+    # the library reads bt_ld as the row stride and as the row's capacity: a column
+    # slice of a wider table (stride beyond the row length) would overstate it
+    if block_table.shape[0] > 1 and block_table.stride(0) != block_table.shape[1]:
+        raise ValueError("block_table rows must be packed (row stride == row length)")
+    bt_ld = _ld(block_table)
     rc = load().nsa_local_attention(_ptr(q), q.stride(0), _ptr(k_cache), _ptr(v_cache), num_pages, ps,
                                     _ptr(block_table), bt_ld, _ptr(cu_seqlens_q), _ptr(seqused_k),
                                     nvb, total_q, Hq, Hkv, D, float(sm_scale), _ptr(out), _ptr(lse), _ptr(status),

@@ -101,8 +101,8 @@ extern "C" nsa_status nsa_copy_buffers(int n, const void *const *src, void *cons
     }
     const int64_t total = c.start[n];
     if (total == 0) return NSA_OK;
-    int dev = 0, sms = 152;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = current_sm_count();
+    if (sms <= 0) return NSA_ERR_CUDA;
     const int64_t units = c.vec ? ceil_div(total, 16) : total;
     int64_t blocks = ceil_div(units, 256);
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;

@@ -204,8 +204,8 @@ set_index_k_kernel(const uint16_t *k, int64_t k_ld, const int32_t *loc, int n, u
 
 unsigned rows_grid(int64_t rows)
 {
-    int dev = 0, sms = 152;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = current_sm_count();
+    if (sms <= 0) return NSA_ERR_CUDA;
     const int64_t blocks = ceil_div(rows, kWarpsPerBlock);
     const int64_t cap = (int64_t)sms * 8;  // 8 blocks of 8 warps per SM, grid-stride beyond
     return (unsigned)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);

@@ -297,9 +297,11 @@ extern "C" nsa_status nsa_metadata(nsa_mode mode, int B, int R, int W, int n_dra
     p.rpi = req_pool_indices_dev; p.r2t_ld = req_to_token_ld; p.pool_rows = pool_rows;
     p.out = *out; p.status = status_dev;
 
+    const int sms = current_sm_count();
+    if (sms <= 0) return NSA_ERR_CUDA;
     const int64_t segs = (int64_t)B * ceil_div(W, kSeg);
     int64_t copy_blocks = segs;
-    if (copy_blocks > 152 * 4) copy_blocks = 152 * 4;
+    if (copy_blocks > (int64_t)sms * 4) copy_blocks = (int64_t)sms * 4;
     if (copy_blocks < 1) copy_blocks = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(1 + copy_blocks));
@@ -349,8 +351,10 @@ extern "C" nsa_status nsa_flatten_page_table(int B, const int32_t *page_table_1_
     if (B == 0 || pt_ld == 0) return NSA_OK;
     if (!page_table_1_dev || !kv_len_dev || !kv_start_dev || (!out_dev && out_len > 0)) return NSA_ERR_INVALID_ARG;
     const int segs = (int)ceil_div(pt_ld, kSeg);
+    const int sms = current_sm_count();
+    if (sms <= 0) return NSA_ERR_CUDA;
     int64_t blocks = (int64_t)B * segs;
-    if (blocks > 152 * 8) blocks = 152 * 8;
+    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     flatten_page_table_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
         B, page_table_1_dev, pt_ld, kv_len_dev, kv_start_dev, out_dev, out_len, segs, status_dev);
     return launch_status();

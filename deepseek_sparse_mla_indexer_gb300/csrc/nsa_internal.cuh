@@ -78,6 +78,16 @@ inline cudaLaunchAttribute pdl_attribute()
     return a;
 }
 
+// Number of SMs of the current device (0 if it cannot be queried): grids are
+// sized from it, never from a fixed count.
+inline int current_sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n > 0 ? n : 0;
+}
+
 inline nsa_status launch_status()
 {
     return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;

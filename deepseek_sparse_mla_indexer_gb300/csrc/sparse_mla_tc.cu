@@ -57,7 +57,6 @@ constexpr uint32_t kColL = 256;   // ones . P^T: every lane holds the running he
 constexpr uint32_t kColS = 320;   // S^T accumulator
 constexpr float kRescale = 8.0f;      // log2 units
 constexpr long long kWaitBudget = 2000000000LL;
-constexpr int kNumSms = 152;
 constexpr int kBf16RowBytes = (kDl + kDr) * 2;        // 1152
 constexpr int kFp8RowBytes = kDl + 4 * (kDl / 128) + 2 * kDr;  // 656
 constexpr int kMaxClusterSplit = 8;   // portable cluster size
@@ -687,14 +686,6 @@ sparse_mla_combine_kernel(const float *o_part, int nsplit, int64_t rows, __nv_bf
     if (threadIdx.x == 0) lse[row] = wsum > 0.f ? mrun + logf(wsum) : -INFINITY;
 }
 
-int num_sms()
-{
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return kNumSms;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return kNumSms;
-    return n;
-}
-
 // Splits of the top-k list per (row, head group), one CTA per SM: minimise
 // waves x (tiles per split + per-CTA overhead), the overhead (Q load, TMEM
 // set-up, epilogue, partial write) counted as about one and a half tiles.
@@ -702,7 +693,7 @@ void choose_split(int R, int H, int topk, int &nsplit, int &tiles_per_split)
 {
     const int tiles = (topk + kTok - 1) / kTok;
     const int64_t base = (int64_t)R * ((H + kHc - 1) / kHc);
-    const int sms = num_sms();
+    const int sms = current_sm_count() > 0 ? current_sm_count() : 1;
     int best_ns = 1;
     double best_cost = -1.0;
     for (int ns = 1; ns <= 16 && ns <= tiles; ++ns) {

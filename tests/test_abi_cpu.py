@@ -125,3 +125,25 @@ def test_leading_dimension_of_one_row_views(nsa):
     assert _ld(torch.zeros(5).expand(1, 5)) == 5        # broadcast row: stride 0, length 5
     assert _ld(torch.arange(5)[None, :]) == 5
     assert _ld(torch.zeros(1, 8)[:, :5]) == 5           # one row: only its length matters
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_local_virtual_batches_product_against_brute_force(nsa, seed):
+    """The library's host builder checked directly against grouping every query
+    token by the attention chunk of its own position (not against the oracle's
+    restatement of the same algorithm)."""
+    from tests.test_oracle_formats_metadata import _brute_force_local
+    rng = np.random.default_rng(100 + seed)
+    ps = int(rng.choice([1, 2, 4, 16]))
+    c = ps * int(rng.integers(1, 5))
+    B = int(rng.integers(1, 7))
+    kv = rng.integers(1, 60, size=B)
+    q = np.array([int(rng.integers(1, k + 1)) for k in kv])
+    cq = np.concatenate([[0], np.cumsum(q)]).astype(np.int32)
+    cols = (int(kv.max()) + c) // ps + 2
+    bt = rng.integers(0, 1000, size=(B, cols)).astype(np.int32)
+    sq, cu, sk, st, btl = nsa.nsa_local_virtual_batches(c, ps, cq, kv, bt)
+    e_sq, e_sk, e_st, e_btl = _brute_force_local(c, ps, q, kv, bt)
+    assert np.array_equal(sq, e_sq) and np.array_equal(sk, e_sk) and np.array_equal(st, e_st)
+    assert np.array_equal(btl, e_btl)
+    assert np.array_equal(cu, np.concatenate([[0], np.cumsum(e_sq)]))
