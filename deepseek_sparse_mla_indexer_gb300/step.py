@@ -13,9 +13,9 @@ from typing import Optional
 import numpy as np
 import torch
 
-from . import (DT_BF16, DT_E4M3, DT_F32, MODE_DECODE, MODE_EXTEND, alloc_metadata, alloc_score_hist,
-               alloc_topk_workspace, nsa_indexer_logits, nsa_metadata, nsa_sparse_mla, nsa_sparse_mla_workspace_bytes,
-               nsa_status_read, nsa_topk_transform)
+from . import (DT_BF16, DT_E4M3, DT_F32, MODE_EXTEND, alloc_metadata, alloc_score_hist, alloc_topk_workspace,
+               nsa_indexer_logits, nsa_metadata, nsa_sparse_mla, nsa_sparse_mla_workspace_bytes, nsa_status_read,
+               nsa_topk_transform, nsa_topk_workspace_bytes)
 
 
 def _dev(a: np.ndarray, device, dtype=None) -> torch.Tensor:
@@ -38,10 +38,11 @@ class SparseAttentionStep:
 
     def __init__(self, host, device="cuda", fuse_topk: Optional[bool] = None):
         """fuse_topk: the indexer counts each row's leading score digits for the top-k
-        (the indexer-to-top-k fusion); False: the top-k counts them in a pass of its
-        own.  Default: fused for decode (one row per request), where the indexer's
-        epilogue has room for it; unfused for extend / verify, where its epilogue
-        already handles several rows per key tile and the separate pass is cheaper."""
+        (the indexer-to-top-k fusion); False: the top-k counts them itself.  Default:
+        fused when the rows are long enough for the top-k to select them in chunks over
+        several CTAs (it then needs a workspace), where the counts save it a pass over
+        the scores; unfused when every row fits one CTA, which counts its cached row
+        more cheaply than the indexer's epilogue can."""
         self.h = host
         self.device = torch.device(device)
         d = self.device
@@ -70,7 +71,7 @@ class SparseAttentionStep:
         self.logits = torch.empty((self.R, self.logits_ld), dtype=torch.float32, device=d)
         self.indices = torch.empty((self.R, self.topk), dtype=torch.int32, device=d)
         if fuse_topk is None:
-            fuse_topk = self.mode == MODE_DECODE
+            fuse_topk = nsa_topk_workspace_bytes(self.R, self.W, False) > 0
         self.score_hist = alloc_score_hist(self.R, d) if fuse_topk else None
         self.topk_ws = alloc_topk_workspace(self.R, self.W, fuse_topk, d)
         odt = torch.bfloat16 if self.q_dtype == DT_BF16 else torch.float32

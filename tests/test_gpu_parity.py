@@ -69,11 +69,11 @@ def test_small_case_all_rows(case):
 @pytest.mark.parametrize("case", ["decode_bf16_ragged", "decode_fp8kv_h16", "extend_bf16", "verify_fp8kv",
                                   "decode_small_heads_ps16"])
 def test_small_case_other_topk_path(case):
-    """The top-k path each mode does not take by default: decode with the top-k
-    counting the digits itself, extend / verify with the indexer counting them."""
+    """The top-k path these rows (all within one CTA's reach) do not take by
+    default: the indexer counting the digits for the top-k."""
     from deepseek_sparse_mla_indexer_gb300.step import SparseAttentionStep
     wl = SMALL[case]()
-    step = SparseAttentionStep(wl, "cuda", fuse_topk=wl.mode != W.MODE_DECODE)
+    step = SparseAttentionStep(wl, "cuda", fuse_topk=True)
     rows = None if wl.R <= 8 else H.sample_rows(wl, 8, seed=3)
     H.full_parity(step, wl, rows=rows)
 
