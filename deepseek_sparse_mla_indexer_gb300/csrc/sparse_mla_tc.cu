@@ -660,30 +660,49 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 }
 
 // Several splits without a cluster: out[r, h, :] = sum_s exp(lse_s - lse) O_s / l_s,
-// lse = ln sum_s exp(lse_s), folded in split order (partial rows: raw O | lse, l).
+// lse = ln sum_s exp(lse_s) (partial rows: raw O | lse, l).  Every split's header and
+// 16-byte slice are loaded at once (all in flight), then weighed against the largest
+// lse and summed in split order.
+constexpr int kMaxSplit = 16;
+
 __global__ void __launch_bounds__(128)
 sparse_mla_combine_kernel(const float *o_part, int nsplit, int64_t rows, __nv_bfloat16 *out, float *lse)
 {
     const int64_t row = blockIdx.x;
     const int d = threadIdx.x * 4;
+    float ls[kMaxSplit], l[kMaxSplit];
+    float4 v[kMaxSplit];
+#pragma unroll
+    for (int s = 0; s < kMaxSplit; ++s) {
+        ls[s] = -INFINITY;
+        l[s] = 0.f;
+        v[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s < nsplit) {
+            const float *pr = o_part + (s * rows + row) * kPartRow;
+            const float2 hd = *reinterpret_cast<const float2 *>(pr + kDl);
+            ls[s] = hd.x;
+            l[s] = hd.y;
+            v[s] = *reinterpret_cast<const float4 *>(pr + d);
+        }
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kMaxSplit; ++s)
+        if (l[s] > 0.f) mx = fmaxf(mx, ls[s]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float mrun = -INFINITY, wsum = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-        const float *pr = o_part + (s * rows + row) * kPartRow;
-        const float2 hd = *reinterpret_cast<const float2 *>(pr + kDl);
-        if (hd.x == -INFINITY || !(hd.y > 0.f)) continue;
-        const float4 v = *reinterpret_cast<const float4 *>(pr + d);
-        const float mn = fmaxf(mrun, hd.x);
-        const float a = __expf(mrun - mn), b = __expf(hd.x - mn) / hd.y;
-        acc = make_float4(acc.x * a + v.x * b, acc.y * a + v.y * b, acc.z * a + v.z * b, acc.w * a + v.w * b);
-        wsum = wsum * a + __expf(hd.x - mn);
-        mrun = mn;
+    float wsum = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMaxSplit; ++s) {
+        if (!(l[s] > 0.f) || ls[s] == -INFINITY) continue;
+        const float e = __expf(ls[s] - mx), w = e / l[s];
+        acc = make_float4(acc.x + w * v[s].x, acc.y + w * v[s].y, acc.z + w * v[s].z, acc.w + w * v[s].w);
+        wsum += e;
     }
     const float iw = wsum > 0.f ? 1.f / wsum : 0.f;
     __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * iw, acc.y * iw), hi = __floats2bfloat162_rn(acc.z * iw, acc.w * iw);
     *reinterpret_cast<__nv_bfloat162 *>(out + row * kDl + d) = lo;
     *reinterpret_cast<__nv_bfloat162 *>(out + row * kDl + d + 2) = hi;
-    if (threadIdx.x == 0) lse[row] = wsum > 0.f ? mrun + logf(wsum) : -INFINITY;
+    if (threadIdx.x == 0) lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
 // Splits of the top-k list per (row, head group), one CTA per SM: minimise
@@ -696,7 +715,7 @@ void choose_split(int R, int H, int topk, int &nsplit, int &tiles_per_split)
     const int sms = current_sm_count() > 0 ? current_sm_count() : 1;
     int best_ns = 1;
     double best_cost = -1.0;
-    for (int ns = 1; ns <= 16 && ns <= tiles; ++ns) {
+    for (int ns = 1; ns <= kMaxSplit && ns <= tiles; ++ns) {
         const int tps = (tiles + ns - 1) / ns;
         if ((tiles + tps - 1) / tps != ns) continue;
         const int64_t units = base * ns;
