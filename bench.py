@@ -123,8 +123,14 @@ def load_peaks():
 
 # ---------------------------------------------------------------- algorithmic work per stage
 
-def algorithmic_work(wl, seqlens_expanded: np.ndarray):
-    """Bytes each stage must move and flops it must do, from the shapes alone."""
+def algorithmic_work(wl, seqlens_expanded: np.ndarray, row_to_req=None, indices=None):
+    """Bytes each stage must move and flops it must do, from the shapes alone.
+
+    Data that rows of one request share is counted once: the indexer reads each
+    request's key rows once (its longest row's worth) however many of its rows are
+    scored against them, and the sparse MLA reads each distinct selected KV row once
+    (`indices`, all rows; without it every row's selection is counted).  Flops count
+    every row's own products."""
     L = seqlens_expanded.astype(np.int64)
     Lsum = int(L.sum())
     nsel = np.minimum(L, wl.topk)
@@ -133,12 +139,21 @@ def algorithmic_work(wl, seqlens_expanded: np.ndarray):
     row_bytes = wl.kv_row_bytes
     qb = 2 if wl.q_dtype == W.DT_BF16 else 4
     dq = wl.d_latent + wl.d_rope
+    r2q = np.arange(wl.R) if row_to_req is None else np.asarray(row_to_req)
+    req_len = np.zeros(int(r2q.max()) + 1 if len(r2q) else 0, np.int64)
+    np.maximum.at(req_len, r2q, L)
+    if indices is not None:
+        sel = np.asarray(indices).reshape(-1)
+        kv_rows = int(np.unique(sel[sel >= 0]).size)
+    else:
+        kv_rows = int(nsel.sum())
     w = {}
     w["metadata"] = dict(bytes=wl.B * wl.W * 4 * 2 + wl.B * ((wl.W + ps - 1) // ps) * 4 + 40 * (wl.B + wl.R), flops=0)
-    w["indexer"] = dict(bytes=Lsum * (wl.Di * idx_elem + 4 + 4) + wl.R * wl.Hi * (wl.Di * idx_elem + 4)
-                        + int(((L + ps - 1) // ps).sum()) * 4, flops=2 * wl.Hi * wl.Di * Lsum)
+    w["indexer"] = dict(bytes=int(req_len.sum()) * (wl.Di * idx_elem + 4) + Lsum * 4
+                        + wl.R * wl.Hi * (wl.Di * idx_elem + 4) + int(((req_len + ps - 1) // ps).sum()) * 4,
+                        flops=2 * wl.Hi * wl.Di * Lsum)
     w["topk"] = dict(bytes=Lsum * 4 + wl.R * wl.topk * 4 + int(nsel.sum()) * 4, flops=0)
-    w["sparse_mla"] = dict(bytes=int(nsel.sum()) * row_bytes + wl.R * wl.H * (dq + wl.d_latent) * qb
+    w["sparse_mla"] = dict(bytes=kv_rows * row_bytes + wl.R * wl.H * (dq + wl.d_latent) * qb
                            + wl.R * wl.H * 4 + wl.R * wl.topk * 4,
                            flops=2 * wl.H * int(nsel.sum()) * (dq + wl.d_latent))
     return w
@@ -447,7 +462,7 @@ def run_ours(args, rank, world, local_rank):
                                               wl.topk)
     launches_per_step = len(calls) - 1 + mla_launches  # one launch per other stage
     md_len = step.md["seqlens_expanded"].cpu().numpy()
-    work = algorithmic_work(wl, md_len)
+    work = algorithmic_work(wl, md_len, step.md["row_to_req"].cpu().numpy(), step.indices.cpu().numpy())
     peaks = load_peaks()
     stage_ms = {s: float(np.mean(v)) for s, v in per_stage.items()}
     stage_info = {s: stage_roofline(wl, s, work[s], stage_ms[s] * 1e-3, peaks) for s in stages}

@@ -19,9 +19,10 @@
 // flattened in (group, subgroup, tile) order, are cut into equal shares, one
 // per CTA (each CTA finds its start with one block-wide pass over the row
 // lengths), so no SM idles while another works through a long row.
-// Roles (192 threads): warp 0 issues TMA loads of K pages and q rows into
+// Roles (320 threads): warp 0 issues TMA loads of K pages and q rows into
 // 128B-swizzled shared memory; warp 1 owns TMEM and issues the MMAs; warps
-// 2..5 are the epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
+// 2..9 are the epilogue in two sets of four (warp w reads TMEM lanes
+// 32*(w%4) .. +31), set k reducing the tiles accumulated in TMEM buffer k.
 // Stages are tracked with mbarriers; every wait is bounded and reports
 // NSA_ERR_TIMEOUT instead of hanging.
 #include <algorithm>
@@ -41,7 +42,8 @@ constexpr int kHalf = 64;
 constexpr int kDi = 128;
 constexpr int kHi = 64;
 constexpr int kMaxStages = 12;      // TMA ring depth: as many 16 KB stages as fit one CTA per SM
-constexpr int kThreadsTc = 192;
+constexpr int kThreadsTc = 320;     // TMA warp, MMA warp, two sets of four epilogue warps
+constexpr int kEpi = kThreadsTc - 64;  // epilogue threads (both sets)
 constexpr int kMaxG = 4;
 constexpr int kPieceTiles = 16;  // tiles whose page ids the producer warp fetches at once (one half-tile per lane)
 static_assert(kPieceTiles * 2 == 32, "the producer warp owns one half-tile per lane");
@@ -365,16 +367,19 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
     } else {
         // ---------------------------------------------------------- epilogue
-        const int et = threadIdx.x - 64;          // 0..127
+        // Two sets of four warps (one per TMEM lane quadrant each): set k takes the tiles
+        // whose accumulator is buffer k, so consecutive tiles are reduced concurrently.
+        const int et = threadIdx.x - 64;          // 0 .. kEpi-1
+        const int set = et >> 7;                  // 0: warps 2..5, 1: warps 6..9
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
         const int tok = quad * 32 + lane;         // token within the tile
         uint32_t *hs = p.hist ? hist_smem : nullptr;
         if (hs)
-            for (int j = et; j < p.G * kHistWords; j += 128) hs[j] = 0u;
+            for (int j = et; j < p.G * kHistWords; j += kEpi) hs[j] = 0u;
         // the per-CTA digit counts of a segment's rows go to the global histogram
         auto flush_hist = [&](const SubGroup &sg) {
-            asm volatile("bar.sync 1, 128;" ::: "memory");  // every epilogue thread's counts are in
-            for (int j = et; j < sg.c * kHistWords; j += 128) {
+            asm volatile("bar.sync 1, %0;" ::"n"(kEpi) : "memory");  // every epilogue thread's counts are in
+            for (int j = et; j < sg.c * kHistWords; j += kEpi) {
                 const uint32_t v = hs[j];
                 if (v == 0u) continue;
                 hs[j] = 0u;
@@ -382,52 +387,56 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 if (v & 0xFFFFu) atomicAdd(g, v & 0xFFFFu);
                 if (v >> 16) atomicAdd(g + 1, v >> 16);
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");  // cleared before anyone counts again
+            asm volatile("bar.sync 1, %0;" ::"n"(kEpi) : "memory");  // cleared before anyone counts again
         };
         uint32_t ai = 0, it = 0;
         for_each_segment(p, bars, [&](const SubGroup &sg, int tb, int te) -> bool {
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            for (int i = et; i < sg.c * kHi; i += 128) bars->w[i] = p.w[(int64_t)sg.r0 * kHi + i];
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            asm volatile("bar.sync 1, %0;" ::"n"(kEpi) : "memory");
+            for (int i = et; i < sg.c * kHi; i += kEpi) bars->w[i] = p.w[(int64_t)sg.r0 * kHi + i];
+            asm volatile("bar.sync 1, %0;" ::"n"(kEpi) : "memory");
             int Lrow[kMaxG];
 #pragma unroll
             for (int i = 0; i < kMaxG; ++i) Lrow[i] = i < sg.c ? clamp_len(p, sg.r0 + i) : 0;
             int since_flush = 0;
             for (int t = tb; t < te; ++t, ++ai, ++it) {
                 const int ab = ai & 1;
-                const uint32_t aph = (ai >> 1) & 1;
-                const int s = t * kTileTok + tok;
-                // my token's key scale arrived with the tile; then the stage is released
-                const int st = it % p.stages;
-                if (!mbar_wait(&bars->full[st], (it / p.stages) & 1, kWaitBudget)) { fail(bars, p.status); return false; }
-                const float scale = bars->scale[st][tok];
-                const bool valid_page = bars->half_ok[st][tok >> 6] != 0;
-                mbar_arrive(&bars->empty[st]);
-                if (!mbar_wait(&bars->acc_full[ab], aph, kWaitBudget)) { fail(bars, p.status); return false; }
-                tc_fence_after();
-                const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + ab * p.acc_stride;
-                for (int i = 0; i < sg.c; ++i) {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32(tbase + i * kHi, v0);
-                    tmem_ld32(tbase + i * kHi + 32, v1);
-                    tmem_ld_wait();
-                    const float *wr = bars->w + i * kHi;
-                    float acc = 0.f;
+                if (ab == set) {
+                    const uint32_t aph = (ai >> 1) & 1;
+                    const int s = t * kTileTok + tok;
+                    // my token's key scale arrived with the tile; then the stage is released
+                    const int st = it % p.stages;
+                    if (!mbar_wait(&bars->full[st], (it / p.stages) & 1, kWaitBudget)) { fail(bars, p.status); return false; }
+                    const float scale = bars->scale[st][tok];
+                    const bool valid_page = bars->half_ok[st][tok >> 6] != 0;
+                    mbar_arrive(&bars->empty[st]);
+                    if (!mbar_wait(&bars->acc_full[ab], aph, kWaitBudget)) { fail(bars, p.status); return false; }
+                    tc_fence_after();
+                    const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + ab * p.acc_stride;
+                    for (int i = 0; i < sg.c; ++i) {
+                        uint32_t v0[32], v1[32];
+                        tmem_ld32(tbase + i * kHi, v0);
+                        tmem_ld32(tbase + i * kHi + 32, v1);
+                        tmem_ld_wait();
+                        const float *wr = bars->w + i * kHi;
+                        // four independent partial sums over the 64 heads (short dependency chains)
+                        float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) acc = fmaf(wr[h], fmaxf(__uint_as_float(v0[h]), 0.f), acc);
+                        for (int h = 0; h < 32; ++h) a[h & 3] = fmaf(wr[h], fmaxf(__uint_as_float(v0[h]), 0.f), a[h & 3]);
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) acc = fmaf(wr[32 + h], fmaxf(__uint_as_float(v1[h]), 0.f), acc);
-                    const bool in = s < Lrow[i];
-                    const float logit = valid_page ? acc * scale : -INFINITY;
-                    if (in) p.logits[(int64_t)(sg.r0 + i) * p.logits_ld + s] = logit;
-                    if (hs && in) {
-                        const uint32_t d = order_key(logit) >> kScoreDigitShift;
-                        atomicAdd(&hs[i * kHistWords + (d >> 1)], 1u << ((d & 1u) * 16));
+                        for (int h = 0; h < 32; ++h) a[h & 3] = fmaf(wr[32 + h], fmaxf(__uint_as_float(v1[h]), 0.f), a[h & 3]);
+                        const float acc = (a[0] + a[1]) + (a[2] + a[3]);
+                        const bool in = s < Lrow[i];
+                        const float logit = valid_page ? acc * scale : -INFINITY;
+                        if (in) p.logits[(int64_t)(sg.r0 + i) * p.logits_ld + s] = logit;
+                        if (hs && in) {
+                            const uint32_t d = order_key(logit) >> kScoreDigitShift;
+                            atomicAdd(&hs[i * kHistWords + (d >> 1)], 1u << ((d & 1u) * 16));
+                        }
                     }
+                    tc_fence_before();
+                    mbar_arrive(&bars->acc_empty[ab]);
                 }
-                tc_fence_before();
-                mbar_arrive(&bars->acc_empty[ab]);
-                if (hs && ++since_flush == kHistFlushTiles) {
+                if (hs && ++since_flush == kHistFlushTiles) {  // both sets count every tile: uniform
                     flush_hist(sg);
                     since_flush = 0;
                 }

@@ -44,3 +44,28 @@ def test_local_bytes_decode_workload():
     pages = int(((sk + wl.page_size - 1) // wl.page_size).sum())
     expect = (keys * wl.Hkv * wl.D * 4 + wl.total_q * wl.Hq * (wl.D * 4 + 4) + pages * 4 + len(sk) * 8 + 4)
     assert bench.local_algorithmic_bytes(wl, cu, sk) == expect
+
+
+def test_step_work_counts_shared_data_once():
+    """Rows of one request share its key rows (indexer) and their selected KV rows
+    (attention): the algorithmic bytes count them once, the flops per row."""
+    wl = W.make_workload("acct", mode=W.MODE_VERIFY, seq_lens=[100, 300], n_draft=4, topk=64, page_size=16, Hi=4,
+                         Di=32, idx_dtype=W.DT_E4M3, H=16, d_latent=512, d_rope=64, q_dtype=W.DT_BF16,
+                         kv_dtype=W.DT_BF16, sm_scale=0.1, seed=3)
+    md = oracle.metadata(wl.mode, wl.seq_lens, wl.req_to_token, wl.req_pool_indices, W=wl.W, topk=wl.topk,
+                         page_size=wl.page_size, n_draft=wl.n_draft)
+    L = md["seqlens_expanded"]
+    r2q = md["row_to_req"]
+    # every row of a request selects the same 64 slots
+    idx = np.stack([np.arange(64, dtype=np.int32) + 1000 * int(b) for b in r2q])
+    w = bench.algorithmic_work(wl, L, r2q, idx)
+    longest = [int(L[r2q == b].max()) for b in range(2)]
+    assert longest == [104, 304]
+    k_bytes = sum(longest) * (32 + 4)
+    pages = sum((x + 15) // 16 for x in longest) * 4
+    assert w["indexer"]["bytes"] == k_bytes + int(L.sum()) * 4 + wl.R * 4 * (32 + 4) + pages
+    assert w["indexer"]["flops"] == 2 * 4 * 32 * int(L.sum())
+    assert w["sparse_mla"]["bytes"] == 2 * 64 * 1152 + wl.R * 16 * (576 + 512) * 2 + wl.R * 16 * 4 + wl.R * 64 * 4
+    # without the indices every row's selection counts
+    w2 = bench.algorithmic_work(wl, L, r2q)
+    assert w2["sparse_mla"]["bytes"] - w["sparse_mla"]["bytes"] == (wl.R - 2) * 64 * 1152
