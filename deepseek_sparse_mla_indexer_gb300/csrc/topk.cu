@@ -12,7 +12,8 @@
 // counted either by the indexer as it writes the scores (fused) or by
 // topk_hist_kernel below, over all SMs.
 //
-// topk_row_kernel (rows up to kRowCap positions): one CTA per row.  The row's
+// topk_row_kernel (rows up to 16 K positions: 512 threads; up to 40 K positions
+// when the rows fit one wave of CTAs: 1024 threads): one CTA per row.  The row's
 // keys are read once into shared memory; each thread classifies its run of
 // consecutive positions against d1 (from the histogram when it describes the
 // scores, else from one shared-memory histogram pass), the positions in the
@@ -45,7 +46,8 @@ constexpr int kBins = kScoreBins;                  // 11-bit digits
 constexpr int kBinsPerThread = kBins / kThreads;   // 4, largest digit first
 constexpr int kCandCap = 6144;                     // candidates of the threshold bin held in shared memory
 constexpr int kMaxChunks = kThreads;               // rows up to 2 M positions
-constexpr int kRowCap = 16384;                     // rows the one-CTA kernel caches whole
+constexpr int kRowCap = 16384;                     // rows the 512-thread one-CTA kernel caches whole
+constexpr int kLongRowCap = 40960;                 // rows the 1024-thread one-CTA kernel caches whole
 constexpr int kRowCand = 4096;                     // its threshold-bin capacity
 constexpr int kRun = (4096 + kCandCap + kThreads - 1) / kThreads;  // list entries a thread of the assembling CTA holds
 constexpr uint32_t kFlag = 0x80000000u;            // list entry: candidate (digit == d1); candidate: selected
@@ -104,24 +106,26 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *warp_b
     return incl;
 }
 
-// The digit of a radix pass that holds the need-th largest key.  Thread t holds
-// the counts c[j] of digits kBins-1-4t-j (largest first).  On return pick[0] = the
+// The digit of a radix pass that holds the need-th largest key.  Thread t of the NT
+// holds the counts c[j] of digits kBins-1-(kBins/NT)t-j (largest first).  On return pick[0] = the
 // digit, pick[1] = how many of its keys are still needed, pick[2] = its count
 // (kNoDigit if the counts hold fewer than `need` keys); *total = all counts.
-__device__ __forceinline__ void pick_digit(const uint32_t (&c)[kBinsPerThread], uint32_t need, uint32_t *warp_buf,
+template <int NT>
+__device__ __forceinline__ void pick_digit(const uint32_t (&c)[kBins / NT], uint32_t need, uint32_t *warp_buf,
                                            uint32_t *total, uint32_t *pick)
 {
+    constexpr int BPT = kBins / NT;
     uint32_t sum = 0u;
 #pragma unroll
-    for (int j = 0; j < kBinsPerThread; ++j) sum += c[j];
+    for (int j = 0; j < BPT; ++j) sum += c[j];
     if (threadIdx.x == 0) pick[2] = kNoDigit;  // ordered before every write below by the scan's barriers
     const uint32_t incl = block_incl_scan(sum, warp_buf, total);
     uint32_t cum = incl - sum;
     if (cum < need && need <= incl) {
 #pragma unroll
-        for (int j = 0; j < kBinsPerThread; ++j) {
+        for (int j = 0; j < BPT; ++j) {
             if (cum + c[j] >= need) {
-                pick[0] = (uint32_t)(kBins - 1 - kBinsPerThread * (int)threadIdx.x - j);
+                pick[0] = (uint32_t)(kBins - 1 - BPT * (int)threadIdx.x - j);
                 pick[1] = need - cum;
                 pick[2] = c[j];
                 break;
@@ -133,11 +137,12 @@ __device__ __forceinline__ void pick_digit(const uint32_t (&c)[kBinsPerThread], 
 }
 
 // The counts of a kBins-bin shared-memory histogram this thread owns, largest digit first.
-__device__ __forceinline__ void own_bins(const uint32_t *h, uint32_t (&c)[kBinsPerThread], uint32_t dmask)
+template <int NT>
+__device__ __forceinline__ void own_bins(const uint32_t *h, uint32_t (&c)[kBins / NT], uint32_t dmask)
 {
 #pragma unroll
-    for (int j = 0; j < kBinsPerThread; ++j) {
-        const int d = kBins - 1 - kBinsPerThread * (int)threadIdx.x - j;
+    for (int j = 0; j < kBins / NT; ++j) {
+        const int d = kBins - 1 - (kBins / NT) * (int)threadIdx.x - j;
         c[j] = d <= (int)dmask ? h[d] : 0u;
     }
 }
@@ -147,7 +152,7 @@ __device__ __forceinline__ void own_bins(const uint32_t *h, uint32_t (&c)[kBinsP
 // bits, over a kBins shared-memory histogram), then marks the selected ones:
 // key above the threshold, or equal to it and among the first `need` such in
 // candidate (position) order.  key_of(j) reads candidate j's key, mark(j) flags it.
-template <class KeyOf, class Mark>
+template <int NT, class KeyOf, class Mark>
 __device__ __forceinline__ void resolve_candidates(KeyOf key_of, Mark mark, int nc, uint32_t d1, uint32_t need1,
                                                    uint32_t *h, uint32_t *warp_buf, uint32_t *total, uint32_t *pick)
 {
@@ -160,22 +165,22 @@ __device__ __forceinline__ void resolve_candidates(KeyOf key_of, Mark mark, int 
         const int shift = S - width;
         const uint32_t dmask = (1u << width) - 1u;
         __syncthreads();  // the candidates are written; earlier readers of h are done
-        for (int i = tid; i < kBins; i += kThreads) h[i] = 0u;
+        for (int i = tid; i < kBins; i += NT) h[i] = 0u;
         __syncthreads();
-        for (int j = tid; j < nc; j += kThreads) {
+        for (int j = tid; j < nc; j += NT) {
             const uint32_t k = key_of(j);
             if ((k >> S) == prefix) atomicAdd(&h[(k >> shift) & dmask], 1u);
         }
         __syncthreads();
-        uint32_t c[kBinsPerThread];
-        own_bins(h, c, dmask);
-        pick_digit(c, need, warp_buf, total, pick);
+        uint32_t c[kBins / NT];
+        own_bins<NT>(h, c, dmask);
+        pick_digit<NT>(c, need, warp_buf, total, pick);
         prefix = (prefix << width) | pick[0];
         need = pick[1];
         S = shift;
         if (pick[2] == need) break;  // the whole bin is selected
     }
-    const int per = (nc + kThreads - 1) / kThreads;
+    const int per = (nc + NT - 1) / NT;
     const int j0 = min(nc, tid * per), j1 = min(nc, j0 + per);
     uint32_t ties = 0u;
     for (int j = j0; j < j1; ++j) ties += (key_of(j) >> S) == prefix;
@@ -219,6 +224,7 @@ topk_hist_kernel(const float *logits, int64_t logits_ld, const int32_t *row_len,
 // One CTA selects row r from its scores alone (up to three radix passes over
 // global memory, then one ordered pass).  Used when the histogram does not
 // describe the scores or the threshold bin holds more than kCandCap keys.
+template <int NT>
 __device__ void select_row_directly(const float *lg, int L, int topk, int32_t *out, uint32_t *h,
                                     uint32_t *warp_buf, uint32_t *total, uint32_t *pick,
                                     const int32_t *ptr, int32_t off)
@@ -233,16 +239,16 @@ __device__ void select_row_directly(const float *lg, int L, int topk, int32_t *o
         const int shift = S - width;
         const uint32_t dmask = (1u << width) - 1u;
         __syncthreads();
-        for (int i = tid; i < kBins; i += kThreads) h[i] = 0u;
+        for (int i = tid; i < kBins; i += NT) h[i] = 0u;
         __syncthreads();
-        for (int i = tid; i < L; i += kThreads) {
+        for (int i = tid; i < L; i += NT) {
             const uint32_t k = order_key(__ldcg(lg + i));
             if (S == 32 || (k >> S) == prefix) atomicAdd(&h[(k >> shift) & dmask], 1u);
         }
         __syncthreads();
-        uint32_t c[kBinsPerThread];
-        own_bins(h, c, dmask);
-        pick_digit(c, need, warp_buf, total, pick);
+        uint32_t c[kBins / NT];
+        own_bins<NT>(h, c, dmask);
+        pick_digit<NT>(c, need, warp_buf, total, pick);
         prefix = (S == 32 ? 0u : (prefix << width)) | pick[0];
         need = pick[1];
         S = shift;
@@ -250,7 +256,7 @@ __device__ void select_row_directly(const float *lg, int L, int topk, int32_t *o
     }
     // ordered pass: every key above the threshold, and the first `need` equal to it
     uint32_t gt_run = 0u, eq_run = 0u;
-    for (int base = 0; base < L; base += 4 * kThreads) {
+    for (int base = 0; base < L; base += 4 * NT) {
         const int i0 = base + 4 * tid;
         uint32_t cls[4], a_gt = 0u, a_eq = 0u;
 #pragma unroll
@@ -284,51 +290,53 @@ __device__ void select_row_directly(const float *lg, int L, int topk, int32_t *o
 }
 
 // Keys of lg[0 .. n) into cache[0 .. n): 16-byte loads when aligned, all in flight at once.
+template <int NT, int CAP>
 __device__ __forceinline__ void fill_keys(const float *lg, int n, uint32_t *cache)
 {
-    constexpr int kV = kRowCap / (4 * kThreads);  // float4 per thread for a full row
+    constexpr int kV = CAP / (4 * NT);  // float4 per thread for a full row
     if ((((uintptr_t)lg) & 15) == 0) {
         const int nv = n >> 2;
         float4 v[kV];
 #pragma unroll
         for (int u = 0; u < kV; ++u) {
-            const int j = u * kThreads + (int)threadIdx.x;
+            const int j = u * NT + (int)threadIdx.x;
             if (j < nv) v[u] = __ldg(reinterpret_cast<const float4 *>(lg) + j);
         }
 #pragma unroll
         for (int u = 0; u < kV; ++u) {
-            const int j = u * kThreads + (int)threadIdx.x;
+            const int j = u * NT + (int)threadIdx.x;
             if (j < nv)
                 reinterpret_cast<uint4 *>(cache)[j] =
                     make_uint4(order_key(v[u].x), order_key(v[u].y), order_key(v[u].z), order_key(v[u].w));
         }
-        for (int i = (nv << 2) + (int)threadIdx.x; i < n; i += kThreads) cache[i] = order_key(lg[i]);
+        for (int i = (nv << 2) + (int)threadIdx.x; i < n; i += NT) cache[i] = order_key(lg[i]);
     } else {
-        for (int i = threadIdx.x; i < n; i += kThreads) cache[i] = order_key(lg[i]);
+        for (int i = threadIdx.x; i < n; i += NT) cache[i] = order_key(lg[i]);
     }
 }
 
 // Output slots of the selected positions sel[0 .. topk): the page-table reads of
 // four slots per thread go out together.
-template <class SlotOf>
+template <int NT, class SlotOf>
 __device__ __forceinline__ void write_slots(const uint32_t *sel, int topk, int32_t *out, SlotOf slot_of)
 {
-    for (int j0 = 0; j0 < topk; j0 += 4 * kThreads) {
+    for (int j0 = 0; j0 < topk; j0 += 4 * NT) {
         int32_t s[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int j = j0 + u * kThreads + (int)threadIdx.x;
+            const int j = j0 + u * NT + (int)threadIdx.x;
             s[u] = j < topk ? slot_of((int)sel[j]) : 0;
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int j = j0 + u * kThreads + (int)threadIdx.x;
+            const int j = j0 + u * NT + (int)threadIdx.x;
             if (j < topk) out[j] = s[u];
         }
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+template <int NT, int CAP>
+__global__ void __launch_bounds__(NT, (NT < 1024 ? 2 : 1))
 topk_row_kernel(const TopkArgs a)
 {
     extern __shared__ __align__(16) uint32_t dyn[];
@@ -352,26 +360,26 @@ topk_row_kernel(const TopkArgs a)
 
     // the indexer's digit counts of this row (a hint), read and cleared
     uint32_t *hrow = a.hist ? a.hist + (int64_t)r * kBins : nullptr;
-    uint32_t hc[kBinsPerThread];
+    uint32_t hc[(kBins / NT)];
 #pragma unroll
-    for (int j = 0; j < kBinsPerThread; ++j) {
-        const int d = kBins - 1 - kBinsPerThread * tid - j;
+    for (int j = 0; j < (kBins / NT); ++j) {
+        const int d = kBins - 1 - (kBins / NT) * tid - j;
         hc[j] = hrow ? hrow[d] : 0u;
         if (hrow) hrow[d] = 0u;
     }
     if (L < 0 || L > a.max_row_len || L <= a.topk) {
         const bool bad = L < 0 || L > a.max_row_len;
         if (bad && tid == 0) set_status(a.status, NSA_ERR_BOUNDS);
-        for (int i = tid; i < a.topk; i += kThreads) out[i] = (!bad && i < L) ? slot_of(i) : -1;
+        for (int i = tid; i < a.topk; i += NT) out[i] = (!bad && i < L) ? slot_of(i) : -1;
         return;
     }
-    fill_keys(lg, L, cache);
+    fill_keys<NT, CAP>(lg, L, cache);
 
-    const int C = 4 * (((L + 4 * kThreads - 1) / (4 * kThreads)) | 1);  // <= 36 positions a thread
+    const int C = 4 * (((L + 4 * NT - 1) / (4 * NT)) | 1);  // <= 44 positions a thread (CAP / NT <= 40)
     const int p0 = min(L, tid * C), p1 = min(L, p0 + C);
     bool have = false;
     if (hrow) {
-        pick_digit(hc, (uint32_t)a.topk, warp_buf, &total, pick);
+        pick_digit<NT>(hc, (uint32_t)a.topk, warp_buf, &total, pick);
         have = total == (uint32_t)L && pick[2] != kNoDigit;  // uniform: shared values
     } else {
         __syncthreads();  // the cached keys are complete
@@ -380,9 +388,9 @@ topk_row_kernel(const TopkArgs a)
 #pragma unroll 1
     for (int attempt = 0; attempt < 2 && !done; ++attempt) {
         if (!have) {
-            for (int i = tid; i < kBins; i += kThreads) h1[i] = 0u;
+            for (int i = tid; i < kBins; i += NT) h1[i] = 0u;
             __syncthreads();
-            for (int i4 = tid; i4 < (L >> 2); i4 += kThreads) {
+            for (int i4 = tid; i4 < (L >> 2); i4 += NT) {
                 const uint4 k = reinterpret_cast<const uint4 *>(cache)[i4];
                 atomicAdd(&h1[k.x >> kScoreDigitShift], 1u);
                 atomicAdd(&h1[k.y >> kScoreDigitShift], 1u);
@@ -391,8 +399,8 @@ topk_row_kernel(const TopkArgs a)
             }
             if (tid < (L & 3)) atomicAdd(&h1[cache[(L & ~3) + tid] >> kScoreDigitShift], 1u);
             __syncthreads();
-            own_bins(h1, hc, kBins - 1);
-            pick_digit(hc, (uint32_t)a.topk, warp_buf, &total, pick);
+            own_bins<NT>(h1, hc, kBins - 1);
+            pick_digit<NT>(hc, (uint32_t)a.topk, warp_buf, &total, pick);
             have = true;
         }
         const uint32_t d1 = pick[0], need1 = pick[1], cnt1 = pick[2];
@@ -429,7 +437,7 @@ topk_row_kernel(const TopkArgs a)
                 uint32_t j = eq_before;
                 for (uint64_t m = meq; m; m &= m - 1, ++j) cand[j] = (uint32_t)(p0 + __ffsll((long long)m) - 1);
             }
-            resolve_candidates([&](int j) -> uint32_t { return cache[cand[j] & ~kFlag]; },
+            resolve_candidates<NT>([&](int j) -> uint32_t { return cache[cand[j] & ~kFlag]; },
                                [&](int j) { cand[j] |= kFlag; }, (int)tot_eq, d1, need1, h1, warp_buf, &total, pick);
             uint64_t seq = 0ull;
             {
@@ -445,10 +453,10 @@ topk_row_kernel(const TopkArgs a)
         uint32_t *sel = dyn;  // [topk] over h1 and cand
         for (uint64_t m = msel; m; m &= m - 1) sel[before++] = (uint32_t)(p0 + __ffsll((long long)m) - 1);
         __syncthreads();
-        write_slots(sel, a.topk, out, slot_of);
+        write_slots<NT>(sel, a.topk, out, slot_of);
         done = true;
     }
-    if (!done) select_row_directly(lg, L, a.topk, out, h1, warp_buf, &total, pick, ptr, off);
+    if (!done) select_row_directly<NT>(lg, L, a.topk, out, h1, warp_buf, &total, pick, ptr, off);
 }
 
 // ---------------------------------------------------------------- chunks
@@ -488,7 +496,7 @@ topk_chunk_kernel(const TopkArgs a)
 #pragma unroll
     for (int j = 0; j < kBinsPerThread; ++j) hc[j] = hrow[kBins - 1 - kBinsPerThread * tid - j];
     if (tid == 0) n_gt_s = n_eq_s = 0u;
-    pick_digit(hc, (uint32_t)a.topk, warp_buf, &total, pick);
+    pick_digit<kThreads>(hc, (uint32_t)a.topk, warp_buf, &total, pick);
     const bool pick_ok = pick[2] != kNoDigit;
     const uint32_t d1 = pick[0];
 
@@ -591,7 +599,7 @@ topk_assemble_kernel(const TopkArgs a)
         cg = w & 0xFFFFu;
         cq = w >> 16;
     }
-    pick_digit(hc, (uint32_t)a.topk, warp_buf, &total, pick);
+    pick_digit<kThreads>(hc, (uint32_t)a.topk, warp_buf, &total, pick);
     const bool pick_ok = pick[2] != kNoDigit;
     const uint32_t d1 = pick[0], need1 = pick[1], cnt1 = pick[2];
     // chunk offsets of the concatenated lists (chunk t's list after those of chunks < t)
@@ -603,7 +611,7 @@ topk_assemble_kernel(const TopkArgs a)
     const uint32_t tot_eq = total, tot_gt = list_len - tot_eq;
     const bool counts_ok = pick_ok && tot_gt == (uint32_t)a.topk - need1 && tot_eq == cnt1;
     if (!counts_ok || (tot_eq != need1 && tot_eq > (uint32_t)kCandCap)) {
-        select_row_directly(lg, L, a.topk, out, sm.hist, warp_buf, &total, pick, ptr, off);
+        select_row_directly<kThreads>(lg, L, a.topk, out, sm.hist, warp_buf, &total, pick, ptr, off);
         return;
     }
     // my contiguous run [i0, i1) of the concatenated list, in registers
@@ -657,7 +665,7 @@ topk_assemble_kernel(const TopkArgs a)
             }
         }
     }
-    resolve_candidates([&](int j) -> uint32_t { return sm.cand_key[j]; }, [&](int j) { sm.cand_pos[j] |= kFlag; },
+    resolve_candidates<kThreads>([&](int j) -> uint32_t { return sm.cand_key[j]; }, [&](int j) { sm.cand_pos[j] |= kFlag; },
                        (int)tot_eq, d1, need1, sm.hist, warp_buf, &total, pick);
     // ordered output: above-d1 entries, and the selected candidates
     bool s[kRun];
@@ -682,6 +690,19 @@ topk_assemble_kernel(const TopkArgs a)
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Which kernels select the rows: one 512-thread CTA per row up to kRowCap positions;
+// one 1024-thread CTA per row up to kLongRowCap positions while the rows fit one wave
+// (few long rows: the other SMs stay free for the next kernel's start); else chunks.
+enum { kPathRow, kPathLongRow, kPathChunks };
+
+int topk_path(int R, int max_row_len)
+{
+    if (max_row_len <= kRowCap) return kPathRow;
+    const int sms = current_sm_count();
+    if (max_row_len <= kLongRowCap && sms > 0 && R <= sms) return kPathLongRow;
+    return kPathChunks;
+}
 
 struct WsLayout {
     size_t hist, counts, lists, bytes;
@@ -729,13 +750,16 @@ nsa_status topk_launch(const float *logits_dev, int64_t logits_ld, const int32_t
     cfg.stream = (cudaStream_t)stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (max_row_len <= kRowCap) {
+    const int path = topk_path(R, max_row_len);
+    if (path != kPathChunks) {
         // one CTA per row, the row cached whole (no workspace)
         const size_t smem = (size_t)(kBins + kRowCand + ((max_row_len + 3) & ~3)) * sizeof(uint32_t);
-        NSA_CUDA_TRY(cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        auto kern = path == kPathRow ? topk_row_kernel<kThreads, kRowCap> : topk_row_kernel<1024, kLongRowCap>;
+        NSA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         cfg.gridDim = dim3((unsigned)R);
+        cfg.blockDim = dim3(path == kPathRow ? kThreads : 1024);
         cfg.dynamicSmemBytes = smem;
-        NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, topk_row_kernel, a));
+        NSA_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, a));
         return NSA_OK;
     }
     const bool own_hist = score_hist_dev == nullptr;
@@ -764,7 +788,7 @@ nsa_status topk_launch(const float *logits_dev, int64_t logits_ld, const int32_t
 
 extern "C" size_t nsa_topk_workspace_bytes(int R, int max_row_len, int with_score_hist)
 {
-    if (R <= 0 || max_row_len <= nsa::kRowCap) return 0;
+    if (R <= 0 || nsa::topk_path(R, max_row_len) != nsa::kPathChunks) return 0;
     return nsa::ws_layout(R, max_row_len, with_score_hist == 0).bytes;
 }
 
