@@ -360,14 +360,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                         }
                     }
                 }
-                if (i > 0 && !mbar_wait(&sm->o_done[4], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
-                issue_pair(4);
-                cp_async_commit();
                 if (nxt >= 0 && nxt < p.num_slots) prefetch_l2_bulk(p.kv + (int64_t)nxt * row_bytes, (uint32_t)row_bytes);
                 if (i == 0) {
-                    cp_async_wait_group<1>();
+                    cp_async_wait_group<0>();  // the Q rows (the only group in flight)
                     release_q();
                 }
+                // latent pairs first, each as soon as the previous tile's O^T block that reads
+                // its buffer is done; the rope rows last (their block holds P^T until every O^T
+                // block of the previous tile is done)
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     if (m > 0 && i > 0 && !mbar_wait(&sm->o_done[m], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
@@ -384,6 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                     }
                     release_pair(m);
                 }
+                if (i > 0 && !mbar_wait(&sm->o_done[4], (i - 1) & 1, kWaitBudget)) fail(sm, p.status);
+                issue_pair(4);
+                cp_async_commit();
                 cp_async_wait_group<0>();
                 release_pair(4);
             }
