@@ -78,15 +78,21 @@ class L2Flush:
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
 # stage's kernel from one ncu capture of a workload (profiles/ names the command),
-# keyed by (workload, stage); valid only while the kernel sources hash as they did
-# at capture.
+# keyed by (workload, stage); a stage of two launches (the chunked top-k) sums them.
+# Valid only while the kernel sources hash as they did at capture.
 NCU_TRAFFIC = {
-    ("v32_decode_bf16", "sparse_mla"): dict(bytes=int((81.316864 + 2.461440) * 1e6),
-                                            sources=["sparse_mla_tc.cu", "sm100.cuh"], sha="149ce04c4033598b"),
-    ("v32_decode_bf16", "indexer"): dict(bytes=int((79.633664 + 1.633536) * 1e6), sources=["indexer_tc.cu", "sm100.cuh"],
-                                         sha="4b3b2f1c3334e74e"),
-    ("v32_decode_bf16", "topk"): dict(bytes=int(4.731648e6), sources=["topk.cu"], sha="2f5262ea063997bf"),
-    ("v32_decode_bf16", "metadata"): dict(bytes=int(5.872640e6), sources=["metadata.cu"], sha="6d9df76679a4256d"),
+    ("v32_decode_bf16", "sparse_mla"): dict(bytes=int((81.315328 + 3.140608) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="f11030136a60f0b9"),
+    ("v32_decode_bf16", "indexer"): dict(bytes=int((79.635200 + 2.103296) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="d3f7864375dd2de5"),
+    ("v32_decode_bf16", "topk"): dict(bytes=int((4.736000) * 1e6), sources=['topk.cu'], sha="01d713834ebc52ae"),
+    ("v32_decode_bf16", "metadata"): dict(bytes=int((5.871616) * 1e6), sources=['metadata.cu'], sha="2fffb050bc91059b"),
+    ("fp8kv_decode_h16", "sparse_mla"): dict(bytes=int((197.524736 + 3.421184) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="f11030136a60f0b9"),
+    ("fp8kv_decode_h16", "indexer"): dict(bytes=int((140.058368 + 4.949504) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="d3f7864375dd2de5"),
+    ("fp8kv_decode_h16", "topk"): dict(bytes=int((8.448256) * 1e6), sources=['topk.cu'], sha="01d713834ebc52ae"),
+    ("chunked_extend", "indexer"): dict(bytes=int((79.842304 + 246.227968) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="d3f7864375dd2de5"),
+    ("chunked_extend", "topk"): dict(bytes=int((302.822912 + 51.784960) * 1e6), sources=['topk.cu'], sha="01d713834ebc52ae"),
+    ("verify_long_fp8kv", "sparse_mla"): dict(bytes=int((406.267648 + 83.962112) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="f11030136a60f0b9"),
+    ("verify_long_fp8kv", "indexer"): dict(bytes=int((468.792576 + 47.905280) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="d3f7864375dd2de5"),
+    ("verify_long_fp8kv", "topk"): dict(bytes=int((70.559488 + 1.497856 + 17.346816) * 1e6), sources=['topk.cu'], sha="01d713834ebc52ae"),
     ("local_decode_c8192", "local_attention"): dict(bytes=int((642.419968 + 3.919616) * 1e6),
                                                     sources=["local_attention.cu", "sm100.cuh"], sha="bf69a294053f9ee8"),
 }
@@ -460,7 +466,8 @@ def run_ours(args, rank, world, local_rank):
 
     _, mla_launches = nsa.nsa_sparse_mla_plan(wl.q_dtype, wl.kv_dtype, wl.R, wl.H, wl.d_latent, wl.d_rope,
                                               wl.topk)
-    launches_per_step = len(calls) - 1 + mla_launches  # one launch per other stage
+    topk_launches = nsa.nsa_topk_launches(wl.R, step.W, step.score_hist is not None)
+    launches_per_step = len(calls) - 2 + topk_launches + mla_launches  # metadata and indexer: one each
     md_len = step.md["seqlens_expanded"].cpu().numpy()
     work = algorithmic_work(wl, md_len, step.md["row_to_req"].cpu().numpy(), step.indices.cpu().numpy())
     peaks = load_peaks()

@@ -20,8 +20,8 @@ from . import _build
 __all__ = [
     "NsaError", "load", "MODE_DECODE", "MODE_EXTEND", "MODE_TARGET_VERIFY", "DT_F32", "DT_BF16",
     "DT_E4M3", "nsa_metadata", "alloc_metadata", "alloc_score_hist", "nsa_local_virtual_batches", "nsa_effective_chunk_size",
-    "nsa_indexer_logits", "nsa_topk_transform", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes",
-    "nsa_sparse_mla_plan", "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged",
+    "nsa_indexer_logits", "nsa_topk_transform", "nsa_topk_launches", "nsa_sparse_mla",
+    "nsa_sparse_mla_workspace_bytes", "nsa_sparse_mla_plan", "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged",
     "nsa_set_index_k", "nsa_topk_transform_ragged", "nsa_flatten_page_table", "nsa_copy_buffers",
     "nsa_check_bounded_wait", "nsa_local_attention", "nsa_status_read", "nsa_status_string", "nsa_abi_version",
     "EXPORTED_SYMBOLS",
@@ -34,7 +34,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_BOUNDS, ERR_TIMEOUT = range(
 EXPORTED_SYMBOLS = [
     "nsa_status_string", "nsa_abi_version", "nsa_status_read", "nsa_metadata",
     "nsa_effective_chunk_size", "nsa_local_virtual_batches", "nsa_indexer_logits",
-    "nsa_topk_transform", "nsa_topk_workspace_bytes", "nsa_sparse_mla", "nsa_sparse_mla_workspace_bytes",
+    "nsa_topk_transform", "nsa_topk_workspace_bytes", "nsa_topk_launches", "nsa_sparse_mla",
+    "nsa_sparse_mla_workspace_bytes",
     "nsa_sparse_mla_plan", "nsa_set_mla_kv", "nsa_quantize_kv_cache", "nsa_dequantize_kv_paged", "nsa_set_index_k",
     "nsa_topk_transform_ragged", "nsa_flatten_page_table", "nsa_copy_buffers",
     "nsa_check_bounded_wait", "nsa_local_attention",
@@ -71,6 +72,7 @@ def load(build_if_missing: bool = True):
         "nsa_indexer_logits": ([I, P, P, P, P, L, I, I, I, P, L, P, P, I, I, I, P, L, P, P, P], I),
         "nsa_topk_transform": ([P, L, P, P, P, L, I, I, I, P, L, P, P, S, P, P], I),
         "nsa_topk_workspace_bytes": ([I, I, I], S),
+        "nsa_topk_launches": ([I, I, I], I),
         "nsa_sparse_mla": ([I, I, P, L, L, P, L, L, P, L, P, L, I, I, I, I, I, F, P, P, P, S, P, P], I),
         "nsa_sparse_mla_workspace_bytes": ([I, I, I, I, I, I, I], S),
         "nsa_sparse_mla_plan": ([I, I, I, I, I, I, I, P, P], I),
@@ -240,6 +242,10 @@ def _hist(h: Optional[torch.Tensor], R: int) -> Optional[torch.Tensor]:
 
 def nsa_topk_workspace_bytes(R: int, max_row_len: int, with_score_hist: bool) -> int:
     return int(load().nsa_topk_workspace_bytes(R, max_row_len, 1 if with_score_hist else 0))
+
+
+def nsa_topk_launches(R: int, max_row_len: int, with_score_hist: bool) -> int:
+    return int(load().nsa_topk_launches(R, max_row_len, 1 if with_score_hist else 0))
 
 
 def alloc_topk_workspace(R: int, max_row_len: int, with_score_hist: bool, device="cuda") -> torch.Tensor:

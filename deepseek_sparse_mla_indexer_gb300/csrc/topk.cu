@@ -792,6 +792,13 @@ extern "C" size_t nsa_topk_workspace_bytes(int R, int max_row_len, int with_scor
     return nsa::ws_layout(R, max_row_len, with_score_hist == 0).bytes;
 }
 
+extern "C" int nsa_topk_launches(int R, int max_row_len, int with_score_hist)
+{
+    if (R <= 0) return 0;
+    if (nsa::topk_path(R, max_row_len) != nsa::kPathChunks) return 1;
+    return with_score_hist ? 2 : 3;
+}
+
 extern "C" nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits_ld,
                                          const int32_t *row_len_dev, const int32_t *row_to_req_dev,
                                          const int32_t *page_table_1_dev, int64_t pt_ld, int R,

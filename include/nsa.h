@@ -281,6 +281,12 @@ nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits_ld, const 
  * indexer's digit counts (the workspace then holds none of its own).  0 for R <= 0. */
 size_t nsa_topk_workspace_bytes(int R, int max_row_len, int with_score_hist);
 
+/* Kernel launches one nsa_topk_transform / nsa_topk_transform_ragged call makes
+ * for that shape: 0 for R <= 0; 1 when every row fits one CTA's shared memory;
+ * otherwise 2 with the indexer's digit counts (per-chunk candidates, then one
+ * assembly per row) or 3 without them (the call counts the digits first). */
+int nsa_topk_launches(int R, int max_row_len, int with_score_hist);
+
 /* ------------------------------------------------------------------------ */
 /* nsa_sparse_mla                                                           */
 /* ------------------------------------------------------------------------ */

@@ -40,6 +40,19 @@ def test_library_exports_every_declared_entry_point(nsa):
         assert hasattr(lib, name), f"{name} declared in include/ but not exported"
 
 
+def test_topk_launch_plan(nsa):
+    """The top-k's launch count and workspace agree: rows one CTA caches whole take
+    one launch and no workspace; longer rows take per-chunk candidates plus one
+    assembly, and one more launch when the indexer's digit counts are absent."""
+    assert nsa.nsa_topk_launches(0, 100, False) == 0
+    assert nsa.nsa_topk_launches(32, 16384, False) == 1
+    assert nsa.nsa_topk_workspace_bytes(32, 16384, False) == 0
+    big = 1 << 20  # rows longer than any one-CTA path
+    assert nsa.nsa_topk_launches(1024, big, True) == 2
+    assert nsa.nsa_topk_launches(1024, big, False) == 3
+    assert nsa.nsa_topk_workspace_bytes(1024, big, False) > nsa.nsa_topk_workspace_bytes(1024, big, True) > 0
+
+
 def test_status_strings(nsa):
     assert nsa.nsa_status_string(0) == "ok"
     assert "out of range" in nsa.nsa_status_string(4)
