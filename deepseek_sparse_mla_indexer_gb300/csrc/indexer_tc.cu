@@ -141,14 +141,16 @@ __device__ __forceinline__ int group_units(const TcParams &p, int g)
 }
 
 // Walks the CTA's share of the work: calls seg(sg, tb, te) for each run of tiles
-// [tb, te) of one subgroup, in (row group, subgroup, tile) order.
+// [tb, te) of one subgroup, in (row group, subgroup, tile) order, until seg returns
+// false.  check_abort: stop between row groups once the CTA has aborted (roles whose
+// threads must agree on every segment pass false and decide inside seg, together).
 template <class F>
-__device__ __forceinline__ void for_each_segment(const TcParams &p, const Bars *bars, F seg)
+__device__ __forceinline__ void for_each_segment(const TcParams &p, const Bars *bars, F seg, bool check_abort = true)
 {
     int g = bars->g0, uo = bars->uo0;
     long long left = bars->u_end - bars->u_begin;
     const int ngroups = (int)ceil_div(p.R, p.G);
-    while (left > 0 && g < ngroups && !bars->abort) {
+    while (left > 0 && g < ngroups && !(check_abort && bars->abort)) {
         int r = g * p.G;
         const int g_end = min(r + p.G, p.R);
         SubGroup sg;
@@ -389,52 +391,64 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kEpi) : "memory");  // cleared before anyone counts again
         };
+        // Both sets take every decision that guards a barrier together: after a failed wait a
+        // set skips its work but keeps every barrier of the segment, and the segment's end
+        // tells both sets whether to go on.
         uint32_t ai = 0, it = 0;
         for_each_segment(p, bars, [&](const SubGroup &sg, int tb, int te) -> bool {
-            asm volatile("bar.sync 1, %0;" ::"n"(kEpi) : "memory");
+            if (bar_red_or(1, kEpi, bars->abort != 0)) return false;  // the weights' buffer is free
             for (int i = et; i < sg.c * kHi; i += kEpi) bars->w[i] = p.w[(int64_t)sg.r0 * kHi + i];
             asm volatile("bar.sync 1, %0;" ::"n"(kEpi) : "memory");
             int Lrow[kMaxG];
 #pragma unroll
             for (int i = 0; i < kMaxG; ++i) Lrow[i] = i < sg.c ? clamp_len(p, sg.r0 + i) : 0;
             int since_flush = 0;
+            bool bad = false;
             for (int t = tb; t < te; ++t, ++ai, ++it) {
                 const int ab = ai & 1;
-                if (ab == set) {
+                if (ab == set && !bad) {
                     const uint32_t aph = (ai >> 1) & 1;
                     const int s = t * kTileTok + tok;
                     // my token's key scale arrived with the tile; then the stage is released
                     const int st = it % p.stages;
-                    if (!mbar_wait(&bars->full[st], (it / p.stages) & 1, kWaitBudget)) { fail(bars, p.status); return false; }
+                    if (!mbar_wait(&bars->full[st], (it / p.stages) & 1, kWaitBudget)) {
+                        fail(bars, p.status);
+                        bad = true;
+                    }
                     const float scale = bars->scale[st][tok];
                     const bool valid_page = bars->half_ok[st][tok >> 6] != 0;
                     mbar_arrive(&bars->empty[st]);
-                    if (!mbar_wait(&bars->acc_full[ab], aph, kWaitBudget)) { fail(bars, p.status); return false; }
-                    tc_fence_after();
-                    const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + ab * p.acc_stride;
-                    for (int i = 0; i < sg.c; ++i) {
-                        uint32_t v0[32], v1[32];
-                        tmem_ld32(tbase + i * kHi, v0);
-                        tmem_ld32(tbase + i * kHi + 32, v1);
-                        tmem_ld_wait();
-                        const float *wr = bars->w + i * kHi;
-                        // four independent partial sums over the 64 heads (short dependency chains)
-                        float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int h = 0; h < 32; ++h) a[h & 3] = fmaf(wr[h], fmaxf(__uint_as_float(v0[h]), 0.f), a[h & 3]);
-#pragma unroll
-                        for (int h = 0; h < 32; ++h) a[h & 3] = fmaf(wr[32 + h], fmaxf(__uint_as_float(v1[h]), 0.f), a[h & 3]);
-                        const float acc = (a[0] + a[1]) + (a[2] + a[3]);
-                        const bool in = s < Lrow[i];
-                        const float logit = valid_page ? acc * scale : -INFINITY;
-                        if (in) p.logits[(int64_t)(sg.r0 + i) * p.logits_ld + s] = logit;
-                        if (hs && in) {
-                            const uint32_t d = order_key(logit) >> kScoreDigitShift;
-                            atomicAdd(&hs[i * kHistWords + (d >> 1)], 1u << ((d & 1u) * 16));
-                        }
+                    if (!bad && !mbar_wait(&bars->acc_full[ab], aph, kWaitBudget)) {
+                        fail(bars, p.status);
+                        bad = true;
                     }
-                    tc_fence_before();
-                    mbar_arrive(&bars->acc_empty[ab]);
+                    if (!bad) {  // after a failed wait the set only keeps the barriers
+                        tc_fence_after();
+                        const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + ab * p.acc_stride;
+                        for (int i = 0; i < sg.c; ++i) {
+                            uint32_t v0[32], v1[32];
+                            tmem_ld32(tbase + i * kHi, v0);
+                            tmem_ld32(tbase + i * kHi + 32, v1);
+                            tmem_ld_wait();
+                            const float *wr = bars->w + i * kHi;
+                            // four independent partial sums over the 64 heads (short dependency chains)
+                            float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                            for (int h = 0; h < 32; ++h) a[h & 3] = fmaf(wr[h], fmaxf(__uint_as_float(v0[h]), 0.f), a[h & 3]);
+#pragma unroll
+                            for (int h = 0; h < 32; ++h) a[h & 3] = fmaf(wr[32 + h], fmaxf(__uint_as_float(v1[h]), 0.f), a[h & 3]);
+                            const float acc = (a[0] + a[1]) + (a[2] + a[3]);
+                            const bool in = s < Lrow[i];
+                            const float logit = valid_page ? acc * scale : -INFINITY;
+                            if (in) p.logits[(int64_t)(sg.r0 + i) * p.logits_ld + s] = logit;
+                            if (hs && in) {
+                                const uint32_t d = order_key(logit) >> kScoreDigitShift;
+                                atomicAdd(&hs[i * kHistWords + (d >> 1)], 1u << ((d & 1u) * 16));
+                            }
+                        }
+                        tc_fence_before();
+                        mbar_arrive(&bars->acc_empty[ab]);
+                    }
                 }
                 if (hs && ++since_flush == kHistFlushTiles) {  // both sets count every tile: uniform
                     flush_hist(sg);
@@ -442,8 +456,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 }
             }
             if (hs && since_flush > 0) flush_hist(sg);
-            return true;
-        });
+            return !bar_red_or(1, kEpi, bad);
+        }, false);
     }
 
     tc_fence_before();
