@@ -82,17 +82,17 @@ class L2Flush:
 # Valid only while the kernel sources hash as they did at capture.
 NCU_TRAFFIC = {
     ("v32_decode_bf16", "sparse_mla"): dict(bytes=int((81.315328 + 3.140608) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="f11030136a60f0b9"),
-    ("v32_decode_bf16", "indexer"): dict(bytes=int((79.635200 + 2.103296) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="d3f7864375dd2de5"),
-    ("v32_decode_bf16", "topk"): dict(bytes=int((4.736000) * 1e6), sources=['topk.cu'], sha="01d713834ebc52ae"),
-    ("v32_decode_bf16", "metadata"): dict(bytes=int((5.871616) * 1e6), sources=['metadata.cu'], sha="2fffb050bc91059b"),
+    ("v32_decode_bf16", "indexer"): dict(bytes=int((79.640064 + 2.080256) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5e9fed8939eaa343"),
+    ("v32_decode_bf16", "topk"): dict(bytes=int((4.745728) * 1e6), sources=['topk.cu'], sha="fc5ae750c9b1ccdd"),
+    ("v32_decode_bf16", "metadata"): dict(bytes=int((2.001152) * 1e6), sources=['metadata.cu'], sha="92d768faefc867e5"),
     ("fp8kv_decode_h16", "sparse_mla"): dict(bytes=int((197.524736 + 3.421184) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="f11030136a60f0b9"),
-    ("fp8kv_decode_h16", "indexer"): dict(bytes=int((140.058368 + 4.949504) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="d3f7864375dd2de5"),
-    ("fp8kv_decode_h16", "topk"): dict(bytes=int((8.448256) * 1e6), sources=['topk.cu'], sha="01d713834ebc52ae"),
-    ("chunked_extend", "indexer"): dict(bytes=int((79.842304 + 246.227968) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="d3f7864375dd2de5"),
-    ("chunked_extend", "topk"): dict(bytes=int((302.822912 + 51.784960) * 1e6), sources=['topk.cu'], sha="01d713834ebc52ae"),
+    ("fp8kv_decode_h16", "indexer"): dict(bytes=int((140.076800 + 5.263616) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5e9fed8939eaa343"),
+    ("fp8kv_decode_h16", "topk"): dict(bytes=int((8.453120) * 1e6), sources=['topk.cu'], sha="fc5ae750c9b1ccdd"),
+    ("chunked_extend", "indexer"): dict(bytes=int((79.826176 + 245.732608) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5e9fed8939eaa343"),
+    ("chunked_extend", "topk"): dict(bytes=int((302.844670 + 52.015616) * 1e6), sources=['topk.cu'], sha="fc5ae750c9b1ccdd"),
     ("verify_long_fp8kv", "sparse_mla"): dict(bytes=int((406.267648 + 83.962112) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="f11030136a60f0b9"),
-    ("verify_long_fp8kv", "indexer"): dict(bytes=int((468.792576 + 47.905280) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="d3f7864375dd2de5"),
-    ("verify_long_fp8kv", "topk"): dict(bytes=int((70.559488 + 1.497856 + 17.346816) * 1e6), sources=['topk.cu'], sha="01d713834ebc52ae"),
+    ("verify_long_fp8kv", "indexer"): dict(bytes=int((468.653820 + 47.570176) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5e9fed8939eaa343"),
+    ("verify_long_fp8kv", "topk"): dict(bytes=int((70.561280 + 1.348352 + 17.348096) * 1e6), sources=['topk.cu'], sha="fc5ae750c9b1ccdd"),
     ("local_decode_c8192", "local_attention"): dict(bytes=int((642.419968 + 3.919616) * 1e6),
                                                     sources=["local_attention.cu", "sm100.cuh"], sha="bf69a294053f9ee8"),
 }
@@ -154,7 +154,10 @@ def algorithmic_work(wl, seqlens_expanded: np.ndarray, row_to_req=None, indices=
     else:
         kv_rows = int(nsel.sum())
     w = {}
-    w["metadata"] = dict(bytes=wl.B * wl.W * 4 * 2 + wl.B * ((wl.W + ps - 1) // ps) * 4 + 40 * (wl.B + wl.R), flops=0)
+    # the step's metadata reads each page's first slot and writes its page id (no copied
+    # page_table_1: the top-k reads req_to_token through req_rows), plus the per-request
+    # and per-row fields
+    w["metadata"] = dict(bytes=wl.B * ((wl.W + ps - 1) // ps) * 4 * 2 + 40 * (wl.B + wl.R) + 4 * wl.B, flops=0)
     w["indexer"] = dict(bytes=int(req_len.sum()) * (wl.Di * idx_elem + 4) + Lsum * 4
                         + wl.R * wl.Hi * (wl.Di * idx_elem + 4) + int(((req_len + ps - 1) // ps).sum()) * 4,
                         flops=2 * wl.Hi * wl.Di * Lsum)

@@ -70,7 +70,7 @@ def load(build_if_missing: bool = True):
         "nsa_effective_chunk_size": ([I, I, I], I),
         "nsa_local_virtual_batches": ([I, I, I, P, P, P, L, L, I, P, P, P, P, P, P], I),
         "nsa_indexer_logits": ([I, P, P, P, P, L, I, I, I, P, L, P, P, I, I, I, P, L, P, P, P], I),
-        "nsa_topk_transform": ([P, L, P, P, P, L, I, I, I, P, L, P, P, S, P, P], I),
+        "nsa_topk_transform": ([P, L, P, P, P, L, P, L, I, I, I, P, L, P, P, S, P, P], I),
         "nsa_topk_workspace_bytes": ([I, I, I], S),
         "nsa_topk_launches": ([I, I, I], I),
         "nsa_sparse_mla": ([I, I, P, L, L, P, L, L, P, L, P, L, I, I, I, I, I, F, P, P, P, S, P, P], I),
@@ -99,7 +99,7 @@ class _MetadataOut(C.Structure):
                 ("nsa_cu_seqlens_k", C.c_void_p), ("nsa_cu_seqlens_q", C.c_void_p),
                 ("row_to_req", C.c_void_p), ("page_table_1", C.c_void_p), ("page_table_1_ld", C.c_int64),
                 ("real_page_table", C.c_void_p), ("real_page_table_ld", C.c_int64),
-                ("indexer_ks", C.c_void_p), ("indexer_ke", C.c_void_p)]
+                ("indexer_ks", C.c_void_p), ("indexer_ke", C.c_void_p), ("req_rows", C.c_void_p)]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -154,8 +154,10 @@ def nsa_status_read(status: torch.Tensor, stream=None) -> int:
 # ------------------------------------------------------------------ metadata
 
 def alloc_metadata(mode: int, B: int, R: int, W: int, page_size: int, device="cuda",
-                   with_ks_ke: bool = False) -> Dict[str, torch.Tensor]:
-    """Device buffers for nsa_metadata's outputs."""
+                   with_ks_ke: bool = False, with_page_table_1: bool = True,
+                   with_req_rows: bool = False) -> Dict[str, torch.Tensor]:
+    """Device buffers for nsa_metadata's outputs (page_table_1 left out, and so not
+    written, when with_page_table_1 is False; req_rows added with with_req_rows)."""
     i32 = dict(dtype=torch.int32, device=device)
     nq = R + 1 if mode == MODE_TARGET_VERIFY else B + 1
     npg = (W + page_size - 1) // page_size
@@ -163,8 +165,11 @@ def alloc_metadata(mode: int, B: int, R: int, W: int, page_size: int, device="cu
                cu_seqlens_q=torch.empty(nq, **i32), seqlens_expanded=torch.empty(R, **i32),
                nsa_cache_seqlens=torch.empty(R, **i32), nsa_cu_seqlens_k=torch.empty(R + 1, **i32),
                nsa_cu_seqlens_q=torch.empty(R + 1, **i32), row_to_req=torch.empty(R, **i32),
-               page_table_1=torch.empty((B, max(W, 1)), **i32),
                real_page_table=torch.empty((B, max(npg, 1)), **i32))
+    if with_page_table_1:
+        out["page_table_1"] = torch.empty((B, max(W, 1)), **i32)
+    if with_req_rows:
+        out["req_rows"] = torch.empty(B, **i32)
     if with_ks_ke:
         out["indexer_ks"] = torch.empty(R, **i32)
         out["indexer_ke"] = torch.empty(R, **i32)
@@ -175,11 +180,13 @@ def nsa_metadata(mode: int, B: int, R: int, W: int, n_draft: int, topk: int, pag
                  seq_lens: torch.Tensor, extend_lens: Optional[torch.Tensor], req_to_token: torch.Tensor,
                  req_pool_indices: torch.Tensor, out: Dict[str, torch.Tensor],
                  status: Optional[torch.Tensor] = None, stream=None) -> None:
+    pt1 = out.get("page_table_1")
     o = _MetadataOut(*(_ptr(out[k]) for k in ["cache_seqlens", "cu_seqlens_k", "cu_seqlens_q",
                                               "seqlens_expanded", "nsa_cache_seqlens", "nsa_cu_seqlens_k",
-                                              "nsa_cu_seqlens_q", "row_to_req", "page_table_1"]),
-                     _ld(out["page_table_1"]), _ptr(out["real_page_table"]),
-                     _ld(out["real_page_table"]), _ptr(out.get("indexer_ks")), _ptr(out.get("indexer_ke")))
+                                              "nsa_cu_seqlens_q", "row_to_req"]),
+                     _ptr(pt1), _ld(pt1) if pt1 is not None else 0, _ptr(out["real_page_table"]),
+                     _ld(out["real_page_table"]), _ptr(out.get("indexer_ks")), _ptr(out.get("indexer_ke")),
+                     _ptr(out.get("req_rows")))
     rc = load().nsa_metadata(mode, B, R, W, n_draft, topk, page_size, _ptr(seq_lens), _ptr(extend_lens),
                              _ptr(req_to_token), _ld(req_to_token), req_to_token.shape[0],
                              _ptr(req_pool_indices), C.byref(o), _ptr(status), _stream(stream))
@@ -263,11 +270,15 @@ def _topk_ws(ws: Optional[torch.Tensor], R: int, max_row_len: int, score_hist, d
 def nsa_topk_transform(logits: torch.Tensor, row_len: torch.Tensor, row_to_req: torch.Tensor,
                        page_table_1: torch.Tensor, topk: int, max_row_len: int, indices: torch.Tensor,
                        status: Optional[torch.Tensor] = None, stream=None,
-                       score_hist: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None) -> None:
+                       score_hist: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                       pt_rows: Optional[torch.Tensor] = None) -> None:
+    """pt_rows: request b's slots are row pt_rows[b] of page_table_1 (e.g. req_to_token
+    with nsa_metadata's req_rows); None: row b."""
     R = row_len.shape[0]
     ws, ws_bytes = _topk_ws(workspace, R, max_row_len, score_hist, logits.device)
     rc = load().nsa_topk_transform(_ptr(logits), _ld(logits), _ptr(row_len), _ptr(row_to_req),
-                                   _ptr(page_table_1), _ld(page_table_1), R, topk, max_row_len,
+                                   _ptr(page_table_1), _ld(page_table_1), _ptr(pt_rows),
+                                   int(page_table_1.shape[0]) if pt_rows is not None else 0, R, topk, max_row_len,
                                    _ptr(indices), _ld(indices), _ptr(_hist(score_hist, R)), _ptr(ws), ws_bytes,
                                    _ptr(status), _stream(stream))
     _check("nsa_topk_transform", rc)

@@ -14,7 +14,7 @@ extern "C" const char *nsa_status_string(int status)
     }
 }
 
-extern "C" int nsa_abi_version(void) { return 101; }
+extern "C" int nsa_abi_version(void) { return 102; }
 
 extern "C" nsa_status nsa_status_read(const int32_t *status_dev, int32_t *host_value, nsa_stream_t stream)
 {

@@ -191,6 +191,23 @@ constexpr int kSeg = 4096;  // page-table entries per copy segment (one 16-byte 
 __device__ void copy_tables(const MetaParams &p, int first_seg, int seg_stride)
 {
     const nsa_metadata_out &o = p.out;
+    if (!o.page_table_1) {
+        // no copied table: only the page ids, one thread per page of each request
+        const int npg = (int)ceil_div(p.W, p.ps);
+        const int64_t total_pg = (int64_t)p.B * npg;
+        for (int64_t g = (int64_t)first_seg * blockDim.x + threadIdx.x; g < total_pg;
+             g += (int64_t)seg_stride * blockDim.x) {
+            const int b = (int)(g / npg), q = (int)(g - (int64_t)b * npg);
+            const int32_t row = p.rpi[b];
+            if (row < 0 || row >= p.pool_rows) {
+                if (q == 0) set_status(p.status, NSA_ERR_BOUNDS);
+                continue;
+            }
+            o.real_page_table[(int64_t)b * o.real_page_table_ld + q] =
+                floor_div(p.r2t[(int64_t)row * p.r2t_ld + (int64_t)q * p.ps], p.ps);
+        }
+        return;
+    }
     const int segs_per_row = (int)ceil_div(p.W, kSeg);
     const int64_t total = (int64_t)p.B * segs_per_row;
     for (int64_t g = first_seg; g < total; g += seg_stride) {
@@ -254,6 +271,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) metadata_kernel(MetaParams p)
     if (blockIdx.x == 0) {
         if (p.B <= kSmemB) build_rows_smem(p);
         else build_rows(p);
+        if (p.out.req_rows)
+            for (int b = threadIdx.x; b < p.B; b += blockDim.x) p.out.req_rows[b] = p.rpi[b];
     } else {
         copy_tables(p, (int)blockIdx.x - 1, (int)gridDim.x - 1);
     }
@@ -286,8 +305,8 @@ extern "C" nsa_status nsa_metadata(nsa_mode mode, int B, int R, int W, int n_dra
     if (B > 0 && !out->cache_seqlens) return NSA_ERR_INVALID_ARG;
     if (R > 0 && (!out->seqlens_expanded || !out->nsa_cache_seqlens || !out->row_to_req))
         return NSA_ERR_INVALID_ARG;
-    if (B > 0 && W > 0 && (!out->page_table_1 || !out->real_page_table)) return NSA_ERR_INVALID_ARG;
-    if (out->page_table_1_ld < W || out->real_page_table_ld < ceil_div(W, page_size))
+    if (B > 0 && W > 0 && !out->real_page_table) return NSA_ERR_INVALID_ARG;
+    if ((out->page_table_1 && out->page_table_1_ld < W) || out->real_page_table_ld < ceil_div(W, page_size))
         return NSA_ERR_INVALID_ARG;
     if ((out->indexer_ks == nullptr) != (out->indexer_ke == nullptr)) return NSA_ERR_INVALID_ARG;
 
@@ -299,7 +318,10 @@ extern "C" nsa_status nsa_metadata(nsa_mode mode, int B, int R, int W, int n_dra
 
     const int sms = current_sm_count();
     if (sms <= 0) return NSA_ERR_CUDA;
-    const int64_t segs = (int64_t)B * ceil_div(W, kSeg);
+    // copy blocks: one per 4096-entry segment of page_table_1, or without it one
+    // thread per page id
+    const int64_t segs = out->page_table_1 ? (int64_t)B * ceil_div(W, kSeg)
+                                           : ceil_div((int64_t)B * ceil_div(W, page_size), kRowThreads);
     int64_t copy_blocks = segs;
     if (copy_blocks > (int64_t)sms * 4) copy_blocks = (int64_t)sms * 4;
     if (copy_blocks < 1) copy_blocks = 1;

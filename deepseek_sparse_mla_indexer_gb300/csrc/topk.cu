@@ -53,6 +53,16 @@ constexpr int kRun = (4096 + kCandCap + kThreads - 1) / kThreads;  // list entri
 constexpr uint32_t kFlag = 0x80000000u;            // list entry: candidate (digit == d1); candidate: selected
 constexpr uint32_t kNoDigit = 0xFFFFFFFFu;
 
+// Token slots of request b: its row of the paged table (nullptr when the table's row
+// map names no row of it: that request's positions then map to -1, with
+// NSA_ERR_BOUNDS), or, ragged, positions offset by the request's first key.
+struct SlotMap {
+    const int32_t *row;
+    int32_t off;
+    bool ok;
+    __device__ __forceinline__ int32_t operator()(int s) const { return row ? row[s] : (ok ? off + s : -1); }
+};
+
 // Dynamic shared memory of topk_assemble_kernel.
 struct ChunkSmem {
     uint32_t hist[kBins];
@@ -66,8 +76,10 @@ struct TopkArgs {
     int64_t logits_ld;
     const int32_t *row_len;
     const int32_t *row_to_req;
-    const int32_t *pt;           // paged: page_table_1
+    const int32_t *pt;           // paged: page_table_1 (or req_to_token with pt_rows)
     int64_t pt_ld;
+    const int32_t *pt_rows;      // optional: row of pt holding request b's slots (else row b)
+    int64_t pt_rows_limit;       // rows of pt (pt_rows[b] is checked against it)
     const int32_t *req_offset;   // ragged: per-request offset
     int topk, max_row_len, nch_max;
     int32_t *indices;
@@ -77,6 +89,18 @@ struct TopkArgs {
     uint2 *lists;                // [R][nch_max * kChunk] (position | kFlag on candidates, slot or key)
     int32_t *status;
 };
+
+__device__ __forceinline__ SlotMap slot_map(const TopkArgs &a, int b)
+{
+    SlotMap m{nullptr, a.req_offset ? a.req_offset[b] : 0, true};
+    if (a.pt) {
+        const int64_t row = a.pt_rows ? (int64_t)a.pt_rows[b] : (int64_t)b;
+        m.ok = !a.pt_rows || (row >= 0 && row < a.pt_rows_limit);
+        if (m.ok) m.row = a.pt + row * a.pt_ld;
+        else if (threadIdx.x == 0) set_status(a.status, NSA_ERR_BOUNDS);
+    }
+    return m;
+}
 
 // Inclusive block scan of one value per thread; *total receives the block sum.
 __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *warp_buf, uint32_t *total)
@@ -226,10 +250,8 @@ topk_hist_kernel(const float *logits, int64_t logits_ld, const int32_t *row_len,
 // describe the scores or the threshold bin holds more than kCandCap keys.
 template <int NT>
 __device__ void select_row_directly(const float *lg, int L, int topk, int32_t *out, uint32_t *h,
-                                    uint32_t *warp_buf, uint32_t *total, uint32_t *pick,
-                                    const int32_t *ptr, int32_t off)
+                                    uint32_t *warp_buf, uint32_t *total, uint32_t *pick, const SlotMap slot_of)
 {
-    auto slot_of = [&](int s) -> int32_t { return ptr ? ptr[s] : off + s; };
     const int tid = threadIdx.x;
     uint32_t prefix = 0u, need = (uint32_t)topk;
     int S = 32;
@@ -353,9 +375,7 @@ topk_row_kernel(const TopkArgs a)
     const int L = a.row_len[r];
     const int b = a.row_to_req[r];
     int32_t *out = a.indices + (int64_t)r * a.indices_ld;
-    const int32_t *ptr = a.pt ? a.pt + (int64_t)b * a.pt_ld : nullptr;
-    const int32_t off = a.req_offset ? a.req_offset[b] : 0;
-    auto slot_of = [&](int s) -> int32_t { return ptr ? ptr[s] : off + s; };
+    const SlotMap slot_of = slot_map(a, b);
     const float *lg = a.logits + (int64_t)r * a.logits_ld;
 
     // the indexer's digit counts of this row (a hint), read and cleared
@@ -404,19 +424,23 @@ topk_row_kernel(const TopkArgs a)
             have = true;
         }
         const uint32_t d1 = pick[0], need1 = pick[1], cnt1 = pick[2];
-        // classify my run
+        // classify my run, four keys at a time (the last group may pass the row's end)
         uint64_t mgt = 0ull, meq = 0ull;
         for (int i = p0; i < p1; i += 4) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(cache + i);  // p1 - i >= 4 unless at the row's end
-            const uint32_t k[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (i + j >= p1) continue;
-                const uint32_t d = k[j] >> kScoreDigitShift;
-                const uint64_t bit = 1ull << (i + j - p0);
-                if (d > d1) mgt |= bit;
-                else if (d == d1) meq |= bit;
+            const uint4 v = *reinterpret_cast<const uint4 *>(cache + i);
+            const uint32_t e0 = v.x >> kScoreDigitShift, e1 = v.y >> kScoreDigitShift;
+            const uint32_t e2 = v.z >> kScoreDigitShift, e3 = v.w >> kScoreDigitShift;
+            uint32_t g = (uint32_t)(e0 > d1) | ((uint32_t)(e1 > d1) << 1) | ((uint32_t)(e2 > d1) << 2) |
+                         ((uint32_t)(e3 > d1) << 3);
+            uint32_t q = (uint32_t)(e0 == d1) | ((uint32_t)(e1 == d1) << 1) | ((uint32_t)(e2 == d1) << 2) |
+                         ((uint32_t)(e3 == d1) << 3);
+            if (p1 - i < 4) {
+                const uint32_t vm = (1u << (p1 - i)) - 1u;
+                g &= vm;
+                q &= vm;
             }
+            mgt |= (uint64_t)g << (i - p0);
+            meq |= (uint64_t)q << (i - p0);
         }
         const uint32_t n_gt = (uint32_t)__popcll(mgt), n_eq = (uint32_t)__popcll(meq);
         const uint32_t packed = n_gt | (n_eq << 16);  // L <= kRowCap: both fit 16 bits
@@ -456,7 +480,7 @@ topk_row_kernel(const TopkArgs a)
         write_slots<NT>(sel, a.topk, out, slot_of);
         done = true;
     }
-    if (!done) select_row_directly<NT>(lg, L, a.topk, out, h1, warp_buf, &total, pick, ptr, off);
+    if (!done) select_row_directly<NT>(lg, L, a.topk, out, h1, warp_buf, &total, pick, slot_of);
 }
 
 // ---------------------------------------------------------------- chunks
@@ -479,9 +503,7 @@ topk_chunk_kernel(const TopkArgs a)
     const int nch = (L + kChunk - 1) / kChunk;
     if (c >= nch) return;
     const int b = a.row_to_req[r];
-    const int32_t *ptr = a.pt ? a.pt + (int64_t)b * a.pt_ld : nullptr;
-    const int32_t off = a.req_offset ? a.req_offset[b] : 0;
-    auto slot_of = [&](int s) -> int32_t { return ptr ? ptr[s] : off + s; };
+    const SlotMap slot_of = slot_map(a, b);
     const float *lg = a.logits + (int64_t)r * a.logits_ld;
     const uint32_t *hrow = a.hist + (int64_t)r * kBins;
 
@@ -572,9 +594,7 @@ topk_assemble_kernel(const TopkArgs a)
     const int L = a.row_len[r];
     const int b = a.row_to_req[r];
     int32_t *out = a.indices + (int64_t)r * a.indices_ld;
-    const int32_t *ptr = a.pt ? a.pt + (int64_t)b * a.pt_ld : nullptr;
-    const int32_t off = a.req_offset ? a.req_offset[b] : 0;
-    auto slot_of = [&](int s) -> int32_t { return ptr ? ptr[s] : off + s; };
+    const SlotMap slot_of = slot_map(a, b);
     const float *lg = a.logits + (int64_t)r * a.logits_ld;
 
     // the row's digit counts, read and cleared for the next call
@@ -611,7 +631,7 @@ topk_assemble_kernel(const TopkArgs a)
     const uint32_t tot_eq = total, tot_gt = list_len - tot_eq;
     const bool counts_ok = pick_ok && tot_gt == (uint32_t)a.topk - need1 && tot_eq == cnt1;
     if (!counts_ok || (tot_eq != need1 && tot_eq > (uint32_t)kCandCap)) {
-        select_row_directly<kThreads>(lg, L, a.topk, out, sm.hist, warp_buf, &total, pick, ptr, off);
+        select_row_directly<kThreads>(lg, L, a.topk, out, sm.hist, warp_buf, &total, pick, slot_of);
         return;
     }
     // my contiguous run [i0, i1) of the concatenated list, in registers
@@ -723,13 +743,14 @@ WsLayout ws_layout(int R, int max_row_len, bool own_hist)
 
 nsa_status topk_launch(const float *logits_dev, int64_t logits_ld, const int32_t *row_len_dev,
                        const int32_t *row_to_req_dev, const int32_t *page_table_1_dev, int64_t pt_ld,
-                       const int32_t *req_offset_dev, int R, int topk, int max_row_len, int32_t *indices_dev,
+                       const int32_t *pt_rows_dev, int64_t pt_rows_limit, const int32_t *req_offset_dev, int R, int topk, int max_row_len, int32_t *indices_dev,
                        int64_t indices_ld, uint32_t *score_hist_dev, void *ws, size_t ws_bytes, int32_t *status_dev,
                        nsa_stream_t stream)
 {
     if (R < 0 || topk < 1 || topk > 4096 || max_row_len < 0) return NSA_ERR_INVALID_ARG;
     if (indices_ld < topk || logits_ld < max_row_len || (page_table_1_dev && pt_ld < max_row_len))
         return NSA_ERR_INVALID_ARG;
+    if (pt_rows_dev && (!page_table_1_dev || pt_rows_limit < 1)) return NSA_ERR_INVALID_ARG;
     if (ceil_div(max_row_len, kChunk) > kMaxChunks) return NSA_ERR_UNSUPPORTED;
     if (R == 0) return NSA_OK;
     if (!logits_dev || !row_len_dev || !row_to_req_dev || !indices_dev || (!page_table_1_dev && !req_offset_dev))
@@ -738,6 +759,7 @@ nsa_status topk_launch(const float *logits_dev, int64_t logits_ld, const int32_t
     TopkArgs a;
     a.logits = logits_dev; a.logits_ld = logits_ld; a.row_len = row_len_dev; a.row_to_req = row_to_req_dev;
     a.pt = page_table_1_dev; a.pt_ld = pt_ld; a.req_offset = req_offset_dev;
+    a.pt_rows = pt_rows_dev; a.pt_rows_limit = pt_rows_limit;
     a.topk = topk; a.max_row_len = max_row_len; a.nch_max = nch;
     a.indices = indices_dev; a.indices_ld = indices_ld;
     a.hist = score_hist_dev;
@@ -801,13 +823,15 @@ extern "C" int nsa_topk_launches(int R, int max_row_len, int with_score_hist)
 
 extern "C" nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits_ld,
                                          const int32_t *row_len_dev, const int32_t *row_to_req_dev,
-                                         const int32_t *page_table_1_dev, int64_t pt_ld, int R,
+                                         const int32_t *page_table_1_dev, int64_t pt_ld,
+                                         const int32_t *pt_rows_dev, int64_t pt_rows_limit, int R,
                                          int topk, int max_row_len, int32_t *indices_dev,
                                          int64_t indices_ld, uint32_t *score_hist_dev, void *ws, size_t ws_bytes,
                                          int32_t *status_dev, nsa_stream_t stream)
 {
     if (!page_table_1_dev && R > 0) return NSA_ERR_INVALID_ARG;
-    return nsa::topk_launch(logits_dev, logits_ld, row_len_dev, row_to_req_dev, page_table_1_dev, pt_ld, nullptr, R,
+    return nsa::topk_launch(logits_dev, logits_ld, row_len_dev, row_to_req_dev, page_table_1_dev, pt_ld, pt_rows_dev,
+                            pt_rows_limit, nullptr, R,
                             topk, max_row_len, indices_dev, indices_ld, score_hist_dev, ws, ws_bytes, status_dev,
                             stream);
 }
@@ -819,6 +843,7 @@ extern "C" nsa_status nsa_topk_transform_ragged(const float *logits_dev, int64_t
                                                 void *ws, size_t ws_bytes, int32_t *status_dev, nsa_stream_t stream)
 {
     if (!req_offset_dev && R > 0) return NSA_ERR_INVALID_ARG;
-    return nsa::topk_launch(logits_dev, logits_ld, row_len_dev, row_to_req_dev, nullptr, 0, req_offset_dev, R, topk,
+    return nsa::topk_launch(logits_dev, logits_ld, row_len_dev, row_to_req_dev, nullptr, 0, nullptr, 0, req_offset_dev,
+                            R, topk,
                             max_row_len, indices_dev, indices_ld, score_hist_dev, ws, ws_bytes, status_dev, stream);
 }

@@ -36,13 +36,16 @@ class SparseAttentionStep:
       kv [slots, row] (bf16 bits / e4m3 row bytes / float32), sm_scale.
     """
 
-    def __init__(self, host, device="cuda", fuse_topk: Optional[bool] = None):
+    def __init__(self, host, device="cuda", fuse_topk: Optional[bool] = None, page_table_1: bool = False):
         """fuse_topk: the indexer counts each row's leading score digits for the top-k
         (the indexer-to-top-k fusion); False: the top-k counts them itself.  Default:
         fused when the rows are long enough for the top-k to select them in chunks over
         several CTAs (it then needs a workspace), where the counts save it a pass over
         the scores; unfused when every row fits one CTA, which counts its cached row
-        more cheaply than the indexer's epilogue can."""
+        more cheaply than the indexer's epilogue can.
+        page_table_1: the metadata also copies the requests' req_to_token rows into
+        page_table_1 and the top-k reads the slots from there; False (default): no copy,
+        the top-k reads them from req_to_token through the metadata's req_rows."""
         self.h = host
         self.device = torch.device(device)
         d = self.device
@@ -66,7 +69,8 @@ class SparseAttentionStep:
         self.kv = _dev(host.kv.view(np.int16), d, bf) if self.kv_dtype == DT_BF16 else _dev(host.kv, d)
         self.num_slots = int(host.kv.shape[0])
         self.H, self.d_latent, self.d_rope = host.q_nope.shape[1], host.q_nope.shape[2], host.q_rope.shape[2]
-        self.md = alloc_metadata(self.mode, self.B, self.R, self.W, self.ps, d, with_ks_ke=self.mode == MODE_EXTEND)
+        self.md = alloc_metadata(self.mode, self.B, self.R, self.W, self.ps, d, with_ks_ke=self.mode == MODE_EXTEND,
+                                 with_page_table_1=page_table_1, with_req_rows=True)
         self.logits_ld = max(4, (self.W + 3) // 4 * 4)
         self.logits = torch.empty((self.R, self.logits_ld), dtype=torch.float32, device=d)
         self.indices = torch.empty((self.R, self.topk), dtype=torch.int32, device=d)
@@ -102,9 +106,11 @@ class SparseAttentionStep:
     def topk_transform(self, stream=None, logits: Optional[torch.Tensor] = None):
         """With other `logits` than the indexer's the histogram does not describe them:
         the top-k then counts the digits itself (and still clears the buffer)."""
+        copied = "page_table_1" in self.md
         nsa_topk_transform(self.logits if logits is None else logits, self.md["seqlens_expanded"],
-                           self.md["row_to_req"], self.md["page_table_1"], self.topk, self.W, self.indices,
-                           self.status, stream, score_hist=self.score_hist, workspace=self.topk_ws)
+                           self.md["row_to_req"], self.md["page_table_1"] if copied else self.req_to_token,
+                           self.topk, self.W, self.indices, self.status, stream, score_hist=self.score_hist,
+                           workspace=self.topk_ws, pt_rows=None if copied else self.md["req_rows"])
 
     def attention(self, stream=None, indices: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                   lse: Optional[torch.Tensor] = None):

@@ -93,13 +93,17 @@ typedef struct nsa_metadata_out {
     int32_t *nsa_cu_seqlens_k;  /* [R+1]  [0, cumsum(nsa_cache_seqlens)] */
     int32_t *nsa_cu_seqlens_q;  /* [R+1]  arange(R+1) */
     int32_t *row_to_req;        /* [R]    request of each row */
-    int32_t *page_table_1;      /* [B, page_table_1_ld]; columns 0..W-1 written */
-    int64_t page_table_1_ld;    /* >= W */
+    int32_t *page_table_1;      /* [B, page_table_1_ld]; columns 0..W-1 written.  May be NULL:
+                                   then not written (the top-k can read the slots from
+                                   req_to_token through req_rows instead) */
+    int64_t page_table_1_ld;    /* >= W (ignored when page_table_1 is NULL) */
     int32_t *real_page_table;   /* [B, real_page_table_ld]; columns 0..ceil(W/ps)-1 written */
     int64_t real_page_table_ld; /* >= ceil(W / page_size) */
     int32_t *indexer_ks;        /* [R] extend only (may be NULL): first key of the row's request
                                    in the ragged key space */
     int32_t *indexer_ke;        /* [R] extend only (may be NULL): indexer_ks + seqlens_expanded */
+    int32_t *req_rows;          /* [B] (may be NULL): req_pool_indices as this call read them, the
+                                   row of req_to_token holding each request's token slots */
 } nsa_metadata_out;
 
 /*
@@ -245,6 +249,11 @@ nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, const float *w
  *   logits_dev       [R, logits_ld] float32 (only s < row_len[r] is read)
  *   row_len_dev      [R] (seqlens_expanded), row_to_req_dev [R]
  *   page_table_1_dev [*, pt_ld] token slots per request (from nsa_metadata)
+ *   pt_rows_dev      optional (NULL: request b is row b): request b's slots are row
+ *                    pt_rows_dev[b] of page_table_1_dev, which may then be req_to_token
+ *                    itself with nsa_metadata's req_rows (the same positions map to the
+ *                    same slots, with no copied table).  A row outside [0, pt_rows_limit)
+ *                    sets NSA_ERR_BOUNDS and that request's rows get -1 slots.
  *   max_row_len      host-known upper bound of row_len (at most 2,097,152)
  *   indices_dev      [R, indices_ld] int32, indices_ld >= topk
  *   score_hist_dev   optional (NULL: none) [R, 2048] uint32 digit counts from
@@ -272,7 +281,8 @@ nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, const float *w
  */
 nsa_status nsa_topk_transform(const float *logits_dev, int64_t logits_ld, const int32_t *row_len_dev,
                               const int32_t *row_to_req_dev, const int32_t *page_table_1_dev,
-                              int64_t pt_ld, int R, int topk, int max_row_len, int32_t *indices_dev,
+                              int64_t pt_ld, const int32_t *pt_rows_dev, int64_t pt_rows_limit, int R,
+                              int topk, int max_row_len, int32_t *indices_dev,
                               int64_t indices_ld, uint32_t *score_hist_dev, void *ws, size_t ws_bytes,
                               int32_t *status_dev, nsa_stream_t stream);
 

@@ -36,8 +36,12 @@ def check_metadata(step, md_o):
             continue
         g = step.md[k].cpu().numpy()
         assert np.array_equal(g, md_o[k]), f"metadata {k} differs"
-    g = step.md["page_table_1"].cpu().numpy()[:, : step.W]
-    assert np.array_equal(g, md_o["page_table_1"]), "page_table_1 differs"
+    if "page_table_1" in step.md:
+        g = step.md["page_table_1"].cpu().numpy()[:, : step.W]
+        assert np.array_equal(g, md_o["page_table_1"]), "page_table_1 differs"
+    if "req_rows" in step.md:
+        assert np.array_equal(step.md["req_rows"].cpu().numpy(), step.req_pool_indices.cpu().numpy()), \
+            "req_rows differs from req_pool_indices"
     npg = md_o["real_page_table"].shape[1]
     g = step.md["real_page_table"].cpu().numpy()[:, :npg]
     assert np.array_equal(g, md_o["real_page_table"]), "real_page_table differs"

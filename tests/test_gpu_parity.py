@@ -70,10 +70,11 @@ def test_small_case_all_rows(case):
                                   "decode_small_heads_ps16"])
 def test_small_case_other_topk_path(case):
     """The top-k path these rows (all within one CTA's reach) do not take by
-    default: the indexer counting the digits for the top-k."""
+    default: the indexer counting the digits for the top-k; and the metadata's
+    copied page_table_1, from which the top-k then reads the slots."""
     from deepseek_sparse_mla_indexer_gb300.step import SparseAttentionStep
     wl = SMALL[case]()
-    step = SparseAttentionStep(wl, "cuda", fuse_topk=True)
+    step = SparseAttentionStep(wl, "cuda", fuse_topk=True, page_table_1=True)
     rows = None if wl.R <= 8 else H.sample_rows(wl, 8, seed=3)
     H.full_parity(step, wl, rows=rows)
 
@@ -157,13 +158,41 @@ def test_out_of_range_index_sets_bounds_status():
     assert torch.isfinite(step.lse).all()
 
 
+def test_topk_row_map_outside_the_table_sets_bounds_status():
+    """A request whose row map names no row of req_to_token gets -1 slots and
+    NSA_ERR_BOUNDS; the other requests' rows are unaffected."""
+    import deepseek_sparse_mla_indexer_gb300 as nsa
+    wl = SMALL["decode_bf16_ragged"]()
+    step = _step(wl)
+    step.metadata()
+    step.indexer()
+    step.topk_transform()
+    torch.cuda.synchronize()
+    good = step.indices.cpu().numpy().copy()
+    assert step.status_code() == 0
+    rows_map = step.md["req_rows"].clone()
+    rows_map[1] = step.req_to_token.shape[0] + 5  # past the pool
+    step.status.zero_()
+    nsa.nsa_topk_transform(step.logits, step.md["seqlens_expanded"], step.md["row_to_req"], step.req_to_token,
+                           wl.topk, wl.W, step.indices, step.status, pt_rows=rows_map)
+    torch.cuda.synchronize()
+    assert step.status_code() == nsa.ERR_BOUNDS
+    got = step.indices.cpu().numpy()
+    r2q = step.md["row_to_req"].cpu().numpy()
+    for r in range(wl.R):
+        if r2q[r] == 1:
+            assert (got[r] == -1).all()
+        else:
+            assert np.array_equal(got[r], good[r])
+
+
 def test_host_rejects_bad_arguments_without_launch():
     import deepseek_sparse_mla_indexer_gb300 as nsa
     wl = SMALL["tiny_fp32_decode"]()
     step = _step(wl)
     with pytest.raises(nsa.NsaError) as e:
         nsa.nsa_topk_transform(step.logits, step.md["seqlens_expanded"], step.md["row_to_req"],
-                               step.md["page_table_1"], 0, wl.W, step.indices)
+                               step.req_to_token, 0, wl.W, step.indices, pt_rows=step.md["req_rows"])
     assert e.value.code == nsa.ERR_INVALID_ARG
     with pytest.raises(nsa.NsaError) as e:  # f32 query with bf16 KV is not a supported pair
         nsa.nsa_sparse_mla(nsa.DT_F32, nsa.DT_BF16, step.q_nope, step.q_rope, step.kv, step.indices,

@@ -59,7 +59,7 @@ def test_ragged_extend_path_matches_paged_attention():
     wl = W.make_workload("ragged", mode=W.MODE_EXTEND, seq_lens=[2100, 300, 2600], extend_lens=[8, 4, 6],
                          topk=2048, page_size=64, Hi=64, Di=128, idx_dtype=W.DT_E4M3, H=64, d_latent=512,
                          d_rope=64, q_dtype=W.DT_BF16, kv_dtype=W.DT_E4M3, sm_scale=W.SM_SCALE_V32, seed=33)
-    st = SparseAttentionStep(wl, "cuda")
+    st = SparseAttentionStep(wl, "cuda", page_table_1=True)
     st.metadata()
     torch.cuda.synchronize()
     md_o = H.oracle_metadata(wl)
