@@ -89,11 +89,32 @@ struct Bars {
     int g0, uo0;                       // first row group of this CTA's share, units into it
     long long u_begin, u_end;          // this CTA's share of the flattened tiles
     long long red[kThreadsTc / 32];
-    float w[kMaxG * kHi];
+    alignas(16) float w[kMaxG * kHi];  // read as float4
     alignas(16) float scale[kMaxStages][kTileTok];  // key scales of each stage's tile (bulk-copied with it)
     int half_ok[kMaxStages][2];                     // the stage's 64-token halves hold real keys
 };
 static_assert(offsetof(Bars, scale) % 16 == 0, "bulk-copy destinations are 16-byte aligned");
+static_assert(offsetof(Bars, w) % 16 == 0, "the weights are read as float4");
+
+// Paired fp32 arithmetic: two lanes of a 64-bit register, each rounded as fmaf rounds.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ float f32x2_sum(uint64_t v)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo + hi;
+}
 static_assert(offsetof(Bars, full) % 8 == 0 && offsetof(Bars, u_begin) % 8 == 0, "mbarriers / 64-bit fields");
 
 // Sub-group n of the CTA's row group: the n-th maximal run of rows sharing a request.
@@ -430,14 +451,31 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                             tmem_ld32(tbase + i * kHi, v0);
                             tmem_ld32(tbase + i * kHi + 32, v1);
                             tmem_ld_wait();
-                            const float *wr = bars->w + i * kHi;
-                            // four independent partial sums over the 64 heads (short dependency chains)
-                            float a[4] = {0.f, 0.f, 0.f, 0.f};
+                            const float4 *w4 = reinterpret_cast<const float4 *>(bars->w + i * kHi);
+                            // four independent partial sums over the 64 heads (heads h = 0, 1, 2, 3 mod 4;
+                            // short dependency chains), as two paired accumulators
+                            uint64_t a01 = 0ull, a23 = 0ull;
 #pragma unroll
-                            for (int h = 0; h < 32; ++h) a[h & 3] = fmaf(wr[h], fmaxf(__uint_as_float(v0[h]), 0.f), a[h & 3]);
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 w = w4[q];
+                                const float r0 = fmaxf(__uint_as_float(v0[4 * q]), 0.f);
+                                const float r1 = fmaxf(__uint_as_float(v0[4 * q + 1]), 0.f);
+                                const float r2 = fmaxf(__uint_as_float(v0[4 * q + 2]), 0.f);
+                                const float r3 = fmaxf(__uint_as_float(v0[4 * q + 3]), 0.f);
+                                a01 = f32x2_fma(f32x2_pack(w.x, w.y), f32x2_pack(r0, r1), a01);
+                                a23 = f32x2_fma(f32x2_pack(w.z, w.w), f32x2_pack(r2, r3), a23);
+                            }
 #pragma unroll
-                            for (int h = 0; h < 32; ++h) a[h & 3] = fmaf(wr[32 + h], fmaxf(__uint_as_float(v1[h]), 0.f), a[h & 3]);
-                            const float acc = (a[0] + a[1]) + (a[2] + a[3]);
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 w = w4[8 + q];
+                                const float r0 = fmaxf(__uint_as_float(v1[4 * q]), 0.f);
+                                const float r1 = fmaxf(__uint_as_float(v1[4 * q + 1]), 0.f);
+                                const float r2 = fmaxf(__uint_as_float(v1[4 * q + 2]), 0.f);
+                                const float r3 = fmaxf(__uint_as_float(v1[4 * q + 3]), 0.f);
+                                a01 = f32x2_fma(f32x2_pack(w.x, w.y), f32x2_pack(r0, r1), a01);
+                                a23 = f32x2_fma(f32x2_pack(w.z, w.w), f32x2_pack(r2, r3), a23);
+                            }
+                            const float acc = f32x2_sum(a01) + f32x2_sum(a23);
                             const bool in = s < Lrow[i];
                             const float logit = valid_page ? acc * scale : -INFINITY;
                             if (in) p.logits[(int64_t)(sg.r0 + i) * p.logits_ld + s] = logit;
