@@ -130,6 +130,30 @@ def test_local_attention_host_checks(nsa):
     assert _la_call(lib, ps=0) == inval
 
 
+def test_optional_page_table_argument_checks(nsa):
+    """Host-side checks, before any launch (so they run without a device; the pointers
+    are never dereferenced): nsa_metadata accepts a NULL page_table_1 but not a NULL
+    real_page_table; nsa_topk_transform's row map needs a table and a row limit."""
+    import ctypes as C
+    lib = nsa.load()
+    fake = C.c_void_p(0x1000)
+    B, R, W, ps = 2, 2, 128, 64
+    def md_call(pt1, real):
+        o = nsa._MetadataOut(*([fake] * 8), pt1, W if pt1 else 0, real, (W + ps - 1) // ps, None, None, None)
+        return lib.nsa_metadata(nsa.MODE_DECODE, B, R, W, 0, 64, ps, fake, None, fake, W, 4, fake,
+                                C.byref(o), None, None)
+    assert md_call(None, None) == nsa.ERR_INVALID_ARG          # no page ids buffer
+    assert md_call(fake, fake) != nsa.ERR_INVALID_ARG          # passes the checks (the launch needs a device)
+    assert md_call(None, fake) != nsa.ERR_INVALID_ARG          # page_table_1 may be left out
+    def topk_call(pt, pt_rows, limit):
+        return lib.nsa_topk_transform(fake, W, fake, fake, pt, W, pt_rows, limit, R, 64, W, fake, 64,
+                                      None, None, 0, None, None)
+    assert topk_call(fake, fake, 0) == nsa.ERR_INVALID_ARG     # a row map needs its row limit
+    assert topk_call(None, fake, 4) == nsa.ERR_INVALID_ARG     # and a table
+    assert topk_call(fake, None, 0) != nsa.ERR_INVALID_ARG
+    assert topk_call(fake, fake, 4) != nsa.ERR_INVALID_ARG
+
+
 def test_leading_dimension_of_one_row_views(nsa):
     import torch
     from deepseek_sparse_mla_indexer_gb300 import _ld
