@@ -81,18 +81,18 @@ class L2Flush:
 # keyed by (workload, stage); a stage of two launches (the chunked top-k) sums them.
 # Valid only while the kernel sources hash as they did at capture.
 NCU_TRAFFIC = {
-    ("v32_decode_bf16", "sparse_mla"): dict(bytes=int((81.315328 + 3.140608) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="f11030136a60f0b9"),
+    ("v32_decode_bf16", "sparse_mla"): dict(bytes=int((81.312768 + 2.825984) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="5a3c0f125ab4c5d8"),
     ("v32_decode_bf16", "indexer"): dict(bytes=int((79.639040 + 1.755392) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5d6e9643f23bf2ca"),
-    ("v32_decode_bf16", "topk"): dict(bytes=int((4.745728) * 1e6), sources=['topk.cu'], sha="fc5ae750c9b1ccdd"),
+    ("v32_decode_bf16", "topk"): dict(bytes=int((4.744960) * 1e6), sources=['topk.cu'], sha="61d7d13096f7898c"),
     ("v32_decode_bf16", "metadata"): dict(bytes=int((2.001152) * 1e6), sources=['metadata.cu'], sha="92d768faefc867e5"),
-    ("fp8kv_decode_h16", "sparse_mla"): dict(bytes=int((197.524736 + 3.421184) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="f11030136a60f0b9"),
+    ("fp8kv_decode_h16", "sparse_mla"): dict(bytes=int((197.520640 + 3.252224) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="5a3c0f125ab4c5d8"),
     ("fp8kv_decode_h16", "indexer"): dict(bytes=int((140.075008 + 5.098752) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5d6e9643f23bf2ca"),
-    ("fp8kv_decode_h16", "topk"): dict(bytes=int((8.453120) * 1e6), sources=['topk.cu'], sha="fc5ae750c9b1ccdd"),
+    ("fp8kv_decode_h16", "topk"): dict(bytes=int((8.453888) * 1e6), sources=['topk.cu'], sha="61d7d13096f7898c"),
     ("chunked_extend", "indexer"): dict(bytes=int((79.824128 + 245.445888) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5d6e9643f23bf2ca"),
-    ("chunked_extend", "topk"): dict(bytes=int((302.844670 + 52.015616) * 1e6), sources=['topk.cu'], sha="fc5ae750c9b1ccdd"),
-    ("verify_long_fp8kv", "sparse_mla"): dict(bytes=int((406.267648 + 83.962112) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="f11030136a60f0b9"),
+    ("chunked_extend", "topk"): dict(bytes=int((302.840576 + 51.008768) * 1e6), sources=['topk.cu'], sha="61d7d13096f7898c"),
+    ("verify_long_fp8kv", "sparse_mla"): dict(bytes=int((406.372352 + 81.999872) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="5a3c0f125ab4c5d8"),
     ("verify_long_fp8kv", "indexer"): dict(bytes=int((468.660224 + 47.524608) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5d6e9643f23bf2ca"),
-    ("verify_long_fp8kv", "topk"): dict(bytes=int((70.561280 + 1.348352 + 17.348096) * 1e6), sources=['topk.cu'], sha="fc5ae750c9b1ccdd"),
+    ("verify_long_fp8kv", "topk"): dict(bytes=int((70.563584 + 1.356288 + 17.348608) * 1e6), sources=['topk.cu'], sha="61d7d13096f7898c"),
     ("local_decode_c8192", "local_attention"): dict(bytes=int((642.419968 + 3.919616) * 1e6),
                                                     sources=["local_attention.cu", "sm100.cuh"], sha="bf69a294053f9ee8"),
 }

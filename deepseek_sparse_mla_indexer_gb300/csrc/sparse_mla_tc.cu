@@ -290,8 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
             fence_proxy_async_smem();
             mbar_arrive(&sm->kvb_full[m]);
         };
-        // fp8 rows: each worker dequantises up to kF8Items groups of 8 e4m3 codes per latent block pair
-        constexpr int kF8Items = (kTok * 16 + kWorkers - 1) / kWorkers;
+        // fp8 rows: each worker dequantises up to kF8Items groups of 16 e4m3 codes per latent block pair
+        constexpr int kF8Items = (kTok * 8 + kWorkers - 1) / kWorkers;
         // softmax state: group g (warps 4+4g .. 7+4g) owns heads hb .. hb+31
         const int grp = softmax_warp ? (warp - 4) >> 2 : 0;
         const int hb = grp * kHg;
@@ -342,22 +342,25 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
                 cp_async_wait_group<0>();
                 release_pair(4);
             } else {
-                // latent codes and scales of all four pairs go into registers first; the rope
-                // rows (bf16) go by cp.async
-                uint2 w[4][kF8Items];
-                float sc[4][kF8Items];
+                // latent codes (16 a load) and the four block scales of each row (one 16-byte
+                // load) of the whole tile go into registers first; the rope rows (bf16) go by
+                // cp.async. Item q: row q / 8, codes 16k .. 16k+15 (k = q % 8) of a block pair,
+                // which expand to the pair's chunks 2k, 2k+1; threads k >= 4 store the odd chunk
+                // first, so that eight neighbouring threads store to eight distinct bank groups.
+                uint4 w[4][kF8Items];
+                float4 sc4[kF8Items];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
+                for (int u = 0; u < kF8Items; ++u) {
+                    const int q = lid + u * kWorkers;
+                    sc4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int u = 0; u < kF8Items; ++u) {
-                        const int q = lid + u * kWorkers;
-                        w[m][u] = make_uint2(0u, 0u);
-                        sc[m][u] = 0.f;
-                        if (q < kTok * 16) {
-                            const uint8_t *rowp = sm->rowbase[q >> 4];
-                            w[m][u] = __ldg(reinterpret_cast<const uint2 *>(rowp + (16 * m + (q & 15)) * 8));
-                            sc[m][u] = __ldg(reinterpret_cast<const float *>(rowp + kDl) + m);
-                        }
+                    for (int m = 0; m < 4; ++m) w[m][u] = make_uint4(0u, 0u, 0u, 0u);
+                    if (q < kTok * 8) {
+                        const uint8_t *rowp = sm->rowbase[q >> 3];
+                        sc4[u] = __ldg(reinterpret_cast<const float4 *>(rowp + kDl));
+#pragma unroll
+                        for (int m = 0; m < 4; ++m)
+                            w[m][u] = __ldg(reinterpret_cast<const uint4 *>(rowp + 128 * m + 16 * (q & 7)));
                     }
                 }
                 if (nxt >= 0 && nxt < p.num_slots) prefetch_l2_bulk(p.kv + (int64_t)nxt * row_bytes, (uint32_t)row_bytes);
@@ -374,12 +377,23 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(MlaParams p)
 #pragma unroll
                     for (int u = 0; u < kF8Items; ++u) {
                         const int q = lid + u * kWorkers;
-                        if (q < kTok * 16) {
-                            const int row = q >> 4, c = 16 * m + (q & 15);
-                            uint32_t d4[4];
-                            dequant8(w[m][u], sc[m][u], d4);
-                            *reinterpret_cast<uint4 *>(kv_s + (c >> 3) * kKvBlk + sw128_offset(row, c & 7)) =
-                                make_uint4(d4[0], d4[1], d4[2], d4[3]);
+                        if (q < kTok * 8) {
+                            const int row = q >> 3, k = q & 7;
+                            const float sc = m == 0 ? sc4[u].x : m == 1 ? sc4[u].y : m == 2 ? sc4[u].z : sc4[u].w;
+                            uint32_t lo[4], hi[4];
+                            dequant8(make_uint2(w[m][u].x, w[m][u].y), sc, lo);
+                            dequant8(make_uint2(w[m][u].z, w[m][u].w), sc, hi);
+                            uint8_t *blk = kv_s + (2 * m + (k >> 2)) * kKvBlk;
+                            const int c0 = (2 * k) & 7;  // the pair's chunk 2k inside its block
+                            const uint4 v0 = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                            const uint4 v1 = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                            if (k < 4) {
+                                *reinterpret_cast<uint4 *>(blk + sw128_offset(row, c0)) = v0;
+                                *reinterpret_cast<uint4 *>(blk + sw128_offset(row, c0 + 1)) = v1;
+                            } else {
+                                *reinterpret_cast<uint4 *>(blk + sw128_offset(row, c0 + 1)) = v1;
+                                *reinterpret_cast<uint4 *>(blk + sw128_offset(row, c0)) = v0;
+                            }
                         }
                     }
                     release_pair(m);

@@ -358,7 +358,7 @@ __device__ __forceinline__ void write_slots(const uint32_t *sel, int topk, int32
 }
 
 template <int NT, int CAP>
-__global__ void __launch_bounds__(NT, (NT < 1024 ? 2 : 1))
+__global__ void __launch_bounds__(NT, (NT < 1024 ? 3 : 1))
 topk_row_kernel(const TopkArgs a)
 {
     extern __shared__ __align__(16) uint32_t dyn[];
