@@ -90,6 +90,7 @@ NCU_TRAFFIC = {
     ("fp8kv_decode_h16", "topk"): dict(bytes=int((8.453888) * 1e6), sources=['topk.cu'], sha="61d7d13096f7898c"),
     ("chunked_extend", "indexer"): dict(bytes=int((79.824128 + 245.445888) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5d6e9643f23bf2ca"),
     ("chunked_extend", "topk"): dict(bytes=int((302.840576 + 51.008768) * 1e6), sources=['topk.cu'], sha="61d7d13096f7898c"),
+    ("chunked_extend", "sparse_mla"): dict(bytes=int((1323.398 + 1042.790) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="5a3c0f125ab4c5d8"),
     ("verify_long_fp8kv", "sparse_mla"): dict(bytes=int((406.372352 + 81.999872) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="5a3c0f125ab4c5d8"),
     ("verify_long_fp8kv", "indexer"): dict(bytes=int((468.660224 + 47.524608) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5d6e9643f23bf2ca"),
     ("verify_long_fp8kv", "topk"): dict(bytes=int((70.563584 + 1.356288 + 17.348608) * 1e6), sources=['topk.cu'], sha="61d7d13096f7898c"),
