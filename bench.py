@@ -88,12 +88,14 @@ NCU_TRAFFIC = {
     ("fp8kv_decode_h16", "sparse_mla"): dict(bytes=int((197.520640 + 3.252224) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="5a3c0f125ab4c5d8"),
     ("fp8kv_decode_h16", "indexer"): dict(bytes=int((140.075008 + 5.098752) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5d6e9643f23bf2ca"),
     ("fp8kv_decode_h16", "topk"): dict(bytes=int((8.453888) * 1e6), sources=['topk.cu'], sha="61d7d13096f7898c"),
+    ("fp8kv_decode_h16", "metadata"): dict(bytes=int((2.157568) * 1e6), sources=['metadata.cu'], sha="92d768faefc867e5"),
     ("chunked_extend", "indexer"): dict(bytes=int((79.824128 + 245.445888) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5d6e9643f23bf2ca"),
     ("chunked_extend", "topk"): dict(bytes=int((302.840576 + 51.008768) * 1e6), sources=['topk.cu'], sha="61d7d13096f7898c"),
     ("chunked_extend", "sparse_mla"): dict(bytes=int((1323.398 + 1042.790) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="5a3c0f125ab4c5d8"),
     ("verify_long_fp8kv", "sparse_mla"): dict(bytes=int((406.372352 + 81.999872) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="5a3c0f125ab4c5d8"),
     ("verify_long_fp8kv", "indexer"): dict(bytes=int((468.660224 + 47.524608) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5d6e9643f23bf2ca"),
     ("verify_long_fp8kv", "topk"): dict(bytes=int((70.563584 + 1.356288 + 17.348608) * 1e6), sources=['topk.cu'], sha="61d7d13096f7898c"),
+    ("verify_long_fp8kv", "metadata"): dict(bytes=int((16.822528) * 1e6), sources=['metadata.cu'], sha="92d768faefc867e5"),
     ("local_decode_c8192", "local_attention"): dict(bytes=int((642.419968 + 3.919616) * 1e6),
                                                     sources=["local_attention.cu", "sm100.cuh"], sha="bf69a294053f9ee8"),
 }
