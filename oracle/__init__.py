@@ -40,11 +40,18 @@ def build(force: bool = False) -> str:
     return _SO
 
 
+def _library_path() -> str:
+    """The compiled oracle to load: `NSA_ORACLE_LIB` names a prebuilt copy (the
+    mutation tests load builds with a planted mistake this way), else `build()`."""
+    alt = os.environ.get("NSA_ORACLE_LIB")
+    return alt if alt else build()
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = C.CDLL(build())
+            lib = C.CDLL(_library_path())
             P, I, L, D = C.c_void_p, C.c_int, C.c_int64, C.c_double
             lib.orc_e4m3_to_f64.argtypes, lib.orc_e4m3_to_f64.restype = [C.c_uint8], D
             lib.orc_bf16_to_f64.argtypes, lib.orc_bf16_to_f64.restype = [C.c_uint16], D
