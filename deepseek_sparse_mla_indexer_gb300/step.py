@@ -13,7 +13,7 @@ from typing import Optional
 import numpy as np
 import torch
 
-from . import (DT_BF16, DT_E4M3, DT_F32, MODE_EXTEND, alloc_metadata, alloc_score_hist, alloc_topk_workspace,
+from . import (DT_BF16, MODE_EXTEND, alloc_metadata, alloc_score_hist, alloc_topk_workspace,
                nsa_indexer_logits, nsa_metadata, nsa_sparse_mla, nsa_sparse_mla_workspace_bytes, nsa_status_read,
                nsa_topk_transform, nsa_topk_workspace_bytes)
 

@@ -6,7 +6,6 @@ Each check ties the oracle to something other than itself: the format's own
 values, PyTorch's float8 / bfloat16 casts, the workload generator's separate
 quantiser, and invariants of the rounding."""
 import numpy as np
-import pytest
 import torch
 
 import oracle
