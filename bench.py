@@ -25,6 +25,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -79,34 +80,45 @@ class L2Flush:
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
 # stage's kernel from one ncu capture of a workload (profiles/ names the command),
 # keyed by (workload, stage); a stage of two launches (the chunked top-k) sums them.
-# Valid only while the kernel sources hash as they did at capture.
+# Valid only while the kernel sources (comments aside) hash as they did at capture.
 NCU_TRAFFIC = {
-    ("v32_decode_bf16", "sparse_mla"): dict(bytes=int((81.312768 + 2.825984) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="5a3c0f125ab4c5d8"),
-    ("v32_decode_bf16", "indexer"): dict(bytes=int((79.639040 + 1.755392) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5d6e9643f23bf2ca"),
-    ("v32_decode_bf16", "topk"): dict(bytes=int((4.744960) * 1e6), sources=['topk.cu'], sha="61d7d13096f7898c"),
-    ("v32_decode_bf16", "metadata"): dict(bytes=int((2.001152) * 1e6), sources=['metadata.cu'], sha="92d768faefc867e5"),
-    ("fp8kv_decode_h16", "sparse_mla"): dict(bytes=int((197.520640 + 3.252224) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="5a3c0f125ab4c5d8"),
-    ("fp8kv_decode_h16", "indexer"): dict(bytes=int((140.075008 + 5.098752) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5d6e9643f23bf2ca"),
-    ("fp8kv_decode_h16", "topk"): dict(bytes=int((8.453888) * 1e6), sources=['topk.cu'], sha="61d7d13096f7898c"),
-    ("fp8kv_decode_h16", "metadata"): dict(bytes=int((2.157568) * 1e6), sources=['metadata.cu'], sha="92d768faefc867e5"),
-    ("chunked_extend", "indexer"): dict(bytes=int((79.824128 + 245.445888) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5d6e9643f23bf2ca"),
-    ("chunked_extend", "topk"): dict(bytes=int((302.840576 + 51.008768) * 1e6), sources=['topk.cu'], sha="61d7d13096f7898c"),
-    ("chunked_extend", "sparse_mla"): dict(bytes=int((1323.398 + 1042.790) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="5a3c0f125ab4c5d8"),
-    ("verify_long_fp8kv", "sparse_mla"): dict(bytes=int((406.372352 + 81.999872) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="5a3c0f125ab4c5d8"),
-    ("verify_long_fp8kv", "indexer"): dict(bytes=int((468.660224 + 47.524608) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="5d6e9643f23bf2ca"),
-    ("verify_long_fp8kv", "topk"): dict(bytes=int((70.563584 + 1.356288 + 17.348608) * 1e6), sources=['topk.cu'], sha="61d7d13096f7898c"),
-    ("verify_long_fp8kv", "metadata"): dict(bytes=int((16.822528) * 1e6), sources=['metadata.cu'], sha="92d768faefc867e5"),
+    ("v32_decode_bf16", "sparse_mla"): dict(bytes=int((81.312768 + 2.825984) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="a9fcea53c576bb02"),
+    ("v32_decode_bf16", "indexer"): dict(bytes=int((79.639040 + 1.755392) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="b418f8c7433f93b5"),
+    ("v32_decode_bf16", "topk"): dict(bytes=int((4.744960) * 1e6), sources=['topk.cu'], sha="4c42535136830aa5"),
+    ("v32_decode_bf16", "metadata"): dict(bytes=int((2.001152) * 1e6), sources=['metadata.cu'], sha="c41a2686c52610f5"),
+    ("fp8kv_decode_h16", "sparse_mla"): dict(bytes=int((197.520640 + 3.252224) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="a9fcea53c576bb02"),
+    ("fp8kv_decode_h16", "indexer"): dict(bytes=int((140.075008 + 5.098752) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="b418f8c7433f93b5"),
+    ("fp8kv_decode_h16", "topk"): dict(bytes=int((8.453888) * 1e6), sources=['topk.cu'], sha="4c42535136830aa5"),
+    ("fp8kv_decode_h16", "metadata"): dict(bytes=int((2.157568) * 1e6), sources=['metadata.cu'], sha="c41a2686c52610f5"),
+    ("chunked_extend", "indexer"): dict(bytes=int((79.824128 + 245.445888) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="b418f8c7433f93b5"),
+    ("chunked_extend", "topk"): dict(bytes=int((302.840576 + 51.008768) * 1e6), sources=['topk.cu'], sha="4c42535136830aa5"),
+    ("chunked_extend", "sparse_mla"): dict(bytes=int((1323.398 + 1042.790) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="a9fcea53c576bb02"),
+    ("verify_long_fp8kv", "sparse_mla"): dict(bytes=int((406.372352 + 81.999872) * 1e6), sources=['sparse_mla_tc.cu', 'sm100.cuh'], sha="a9fcea53c576bb02"),
+    ("verify_long_fp8kv", "indexer"): dict(bytes=int((468.660224 + 47.524608) * 1e6), sources=['indexer_tc.cu', 'sm100.cuh'], sha="b418f8c7433f93b5"),
+    ("verify_long_fp8kv", "topk"): dict(bytes=int((70.563584 + 1.356288 + 17.348608) * 1e6), sources=['topk.cu'], sha="4c42535136830aa5"),
+    ("verify_long_fp8kv", "metadata"): dict(bytes=int((16.822528) * 1e6), sources=['metadata.cu'], sha="c41a2686c52610f5"),
     ("local_decode_c8192", "local_attention"): dict(bytes=int((642.419968 + 3.919616) * 1e6),
-                                                    sources=["local_attention.cu", "sm100.cuh"], sha="bf69a294053f9ee8"),
+                                                    sources=["local_attention.cu", "sm100.cuh"], sha="921bc0c500fccc86"),
 }
+
+
+_COMMENT_OR_LITERAL = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'', re.S)
+
+
+def code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs folded to one space
+    (string and character literals kept as written): edits to comments alone do not
+    change what a capture measured."""
+    text = _COMMENT_OR_LITERAL.sub(lambda m: " " if m.group(0).startswith("/") else m.group(0), text)
+    return re.sub(r"\s+", " ", text).strip()
 
 
 def sources_sha(files) -> str:
     import hashlib
     m = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "deepseek_sparse_mla_indexer_gb300", "csrc", f), "rb") as fh:
-            m.update(fh.read())
+        with open(os.path.join(ROOT, "deepseek_sparse_mla_indexer_gb300", "csrc", f)) as fh:
+            m.update(code_only(fh.read()).encode())
     return m.hexdigest()[:16]
 
 

@@ -12,8 +12,9 @@
 // counted either by the indexer as it writes the scores (fused) or by
 // topk_hist_kernel below, over all SMs.
 //
-// topk_row_kernel (rows up to 16 K positions: 512 threads; up to 40 K positions
-// when the rows fit one wave of CTAs: 1024 threads): one CTA per row.  The row's
+// topk_row_kernel (rows up to 16 K positions: 512 threads at 40 registers, up to
+// three CTAs per SM where the cached rows allow; up to 40 K positions when the rows
+// fit one wave of CTAs: 1024 threads): one CTA per row.  The row's
 // keys are read once into shared memory; each thread classifies its run of
 // consecutive positions against d1 (from the histogram when it describes the
 // scores, else from one shared-memory histogram pass), the positions in the
@@ -22,12 +23,12 @@
 //
 // topk_chunk_kernel (longer rows): one CTA per 4096-position chunk of a row.  Each CTA picks
 // the threshold digit d1 from the row's histogram, reads its chunk once and
-// writes, in position order, every position whose digit is above d1 (selected)
-// or equal to it (a candidate) to a per-chunk list, with its counts.  The last
-// CTA of the row to finish (a per-row arrival counter; nobody waits) checks the
-// counts against the histogram, resolves the remaining 21 key bits on the
-// candidates alone, and writes the ordered output: one scan over the
-// concatenated lists gives every selected position its slot.  Ties go to the
+// writes, in position order, every position whose digit is above d1 (selected,
+// with its KV slot) or equal to it (a candidate, with its key) to a per-chunk
+// list, with its counts.  topk_assemble_kernel, launched behind it with one CTA
+// per row, checks the counts against the histogram, resolves the remaining 21
+// key bits on the candidates alone, and writes the ordered output: one scan over
+// the concatenated lists gives every selected position its slot.  Ties go to the
 // lower position.  A histogram that does not describe the scores (the counts
 // disagree) makes that CTA select the row from the scores directly, so the
 // result never depends on the histogram's contents.

@@ -69,3 +69,16 @@ def test_step_work_counts_shared_data_once():
     # without the indices every row's selection counts
     w2 = bench.algorithmic_work(wl, L, r2q)
     assert w2["sparse_mla"]["bytes"] - w["sparse_mla"]["bytes"] == (wl.R - 2) * 64 * 1152
+
+
+def test_capture_hash_ignores_comments_but_not_code():
+    """The measured DRAM traffic stays attached to a kernel through comment edits
+    and is dropped by any change to its code."""
+    src = ('// header\n__global__ void k(float *p) { /* body note */\n'
+           '    p[0] = 1.f;  // trailing\n    asm volatile("add.f32 %0, %0, %0; // kept in the string" : "+f"(p[1]));\n}\n')
+    same = src.replace("// header", "// a reworded header").replace("/* body note */", "/* another\n note */")
+    code = src.replace("p[0] = 1.f;", "p[0] = 2.f;")
+    lit = src.replace("// kept in the string", "// changed in the string")
+    assert bench.code_only(src) == bench.code_only(same)
+    assert bench.code_only(src) != bench.code_only(code)
+    assert bench.code_only(src) != bench.code_only(lit)
