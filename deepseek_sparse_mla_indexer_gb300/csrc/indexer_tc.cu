@@ -13,7 +13,11 @@
 // accumulates in TMEM (fp32) via tcgen05.mma kind::f8f6f4.  The epilogue
 // (one thread per token) applies ReLU, the per-head weights, the head sum and
 // the key's scale (bulk-copied into shared memory with the tile), and stores
-// one fp32 logit per (row, token).
+// one fp32 logit per (row, token).  Given a digit-count buffer, it also counts
+// each logit's leading 11-bit key digit (the top-k's first radix digit) per row
+// in shared memory and adds the counts to the row's global histogram, so that
+// the top-k can start from the threshold digit without reading the scores to
+// count them.
 //
 // Grid: one CTA per SM, persistent, with a deep TMA ring: the tiles of all row groups,
 // flattened in (group, subgroup, tile) order, are cut into equal shares, one

@@ -1,7 +1,9 @@
 // nsa_metadata: the per-step metadata of the sparse-attention backend in one
 // launch.  Block 0 builds every length / offset array (they are O(B + R)
-// and need block-wide prefix sums); the other blocks copy the page table
-// rows out of req_to_token and derive the page-granular table on the fly.
+// and need block-wide prefix sums) and records the pool rows it read
+// (req_rows); the other blocks copy the page table rows out of req_to_token
+// and derive the page-granular table on the fly, or, when no page_table_1 is
+// asked for, read only each page's first slot to derive its page id.
 //
 // Follows [DSA] DeepseekSparseAttnBackend.init_forward_metadata (decode,
 // target-verify and extend branches), _cal_indexer_k_start_end and
