@@ -117,7 +117,7 @@ def sources_sha(files) -> str:
     import hashlib
     m = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "deepseek_sparse_mla_indexer_gb300", "csrc", f)) as fh:
+        with open(os.path.join(ROOT, "deepseek_sparse_mla_indexer_gb300", "csrc", f), encoding="utf-8") as fh:
             m.update(code_only(fh.read()).encode())
     return m.hexdigest()[:16]
 
