@@ -202,10 +202,12 @@ set_index_k_kernel(const uint16_t *k, int64_t k_ld, const int32_t *loc, int n, u
     }
 }
 
+// Blocks for `rows` rows at one warp a row: up to 8 blocks of 8 warps per SM, the
+// kernels grid-striding beyond; 0 when the device's SM count cannot be read.
 unsigned rows_grid(int64_t rows)
 {
     const int sms = current_sm_count();
-    if (sms <= 0) return NSA_ERR_CUDA;
+    if (sms <= 0) return 0;
     const int64_t blocks = ceil_div(rows, kWarpsPerBlock);
     const int64_t cap = (int64_t)sms * 8;  // 8 blocks of 8 warps per SM, grid-stride beyond
     return (unsigned)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
@@ -230,7 +232,9 @@ extern "C" nsa_status nsa_set_mla_kv(nsa_dtype kv_dtype, const void *k_nope_dev,
     if (!k_nope_dev || !k_rope_dev || !loc_dev || !kv_dev) return NSA_ERR_INVALID_ARG;
     if (!aligned(k_nope_dev, 8) || !aligned(k_rope_dev, 16) || !aligned(kv_dev, 16) || nope_ld % 4 || rope_ld % 8)
         return NSA_ERR_INVALID_ARG;
-    set_mla_kv_kernel<<<rows_grid(n), 32 * kWarpsPerBlock, 0, (cudaStream_t)stream>>>(
+    const unsigned grid = rows_grid(n);
+    if (grid == 0) return NSA_ERR_CUDA;
+    set_mla_kv_kernel<<<grid, 32 * kWarpsPerBlock, 0, (cudaStream_t)stream>>>(
         kv_dtype == NSA_DT_E4M3, (const uint16_t *)k_nope_dev, nope_ld, (const uint16_t *)k_rope_dev, rope_ld, loc_dev,
         n, (uint8_t *)kv_dev, num_slots, status_dev);
     return launch_status();
@@ -244,7 +248,9 @@ extern "C" nsa_status nsa_quantize_kv_cache(const void *kv_bf16_dev, int64_t num
     if (num_slots == 0) return NSA_OK;
     if (!kv_bf16_dev || !kv_fp8_dev || !aligned(kv_bf16_dev, 16) || !aligned(kv_fp8_dev, 16))
         return NSA_ERR_INVALID_ARG;
-    quantize_kv_cache_kernel<<<rows_grid(num_slots), 32 * kWarpsPerBlock, 0, (cudaStream_t)stream>>>(
+    const unsigned grid = rows_grid(num_slots);
+    if (grid == 0) return NSA_ERR_CUDA;
+    quantize_kv_cache_kernel<<<grid, 32 * kWarpsPerBlock, 0, (cudaStream_t)stream>>>(
         (const uint16_t *)kv_bf16_dev, num_slots, (uint8_t *)kv_fp8_dev);
     return launch_status();
 }
@@ -258,7 +264,9 @@ extern "C" nsa_status nsa_dequantize_kv_paged(const void *kv_fp8_dev, int64_t nu
     if (m == 0) return NSA_OK;
     if (!kv_fp8_dev || !slots_dev || !out_bf16_dev || !aligned(kv_fp8_dev, 16) || !aligned(out_bf16_dev, 16))
         return NSA_ERR_INVALID_ARG;
-    dequantize_kv_paged_kernel<<<rows_grid(m), 32 * kWarpsPerBlock, 0, (cudaStream_t)stream>>>(
+    const unsigned grid = rows_grid(m);
+    if (grid == 0) return NSA_ERR_CUDA;
+    dequantize_kv_paged_kernel<<<grid, 32 * kWarpsPerBlock, 0, (cudaStream_t)stream>>>(
         (const uint8_t *)kv_fp8_dev, num_slots, slots_dev, m, (uint16_t *)out_bf16_dev, status_dev);
     return launch_status();
 }
@@ -272,7 +280,9 @@ extern "C" nsa_status nsa_set_index_k(const void *k_dev, int64_t k_ld, const int
     if (n == 0) return NSA_OK;
     if (!k_dev || !loc_dev || !k_cache_dev || !k_scale_dev || !aligned(k_dev, 8) || !aligned(k_cache_dev, 4) || k_ld % 4)
         return NSA_ERR_INVALID_ARG;
-    set_index_k_kernel<<<rows_grid(n), 32 * kWarpsPerBlock, 0, (cudaStream_t)stream>>>(
+    const unsigned grid = rows_grid(n);
+    if (grid == 0) return NSA_ERR_CUDA;
+    set_index_k_kernel<<<grid, 32 * kWarpsPerBlock, 0, (cudaStream_t)stream>>>(
         (const uint16_t *)k_dev, k_ld, loc_dev, n, (uint8_t *)k_cache_dev, k_scale_dev, num_slots, status_dev);
     return launch_status();
 }
