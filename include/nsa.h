@@ -266,8 +266,9 @@ nsa_status nsa_indexer_logits(nsa_dtype dtype, const void *q_dev, const float *w
  *   ws, ws_bytes     caller-owned device workspace of at least
  *                    nsa_topk_workspace_bytes(R, max_row_len, score_hist_dev != NULL)
  *                    bytes, 256-byte aligned (0 bytes, and ws may be NULL, when
- *                    max_row_len <= 16384: those rows are selected one CTA per row
- *                    in shared memory).  Longer rows go through per-chunk lists in
+ *                    every row is selected by one CTA in shared memory:
+ *                    max_row_len <= 16384, or <= 40960 with R no larger than the
+ *                    device's SM count).  Longer rows go through per-chunk lists in
  *                    ws.  Without score_hist_dev the workspace also holds the call's
  *                    own digit counts, which must be ZERO before the first call;
  *                    every call leaves them zero again.  A workspace serves calls of
